@@ -1,0 +1,444 @@
+/*
+ * KDA oracle: a plain, slow, fp64 CPU implementation of the Kimi Delta
+ * Attention (KDA) gated delta rule.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, the smoke check in
+ * __graft_entry__.py and the CPU-baseline leg of bench.py load this library.
+ * The CUDA library shares no code, header, table or helper with it.
+ *
+ * Cited page: "Kimi K3：从 3T 稀疏预训练到百万 Token Agent 的端到端扩展"
+ * (liuzhao09.github.io/papers/kimi-k3), called [K3-notes] below.
+ *
+ *  - [K3-notes §2.2, KDA state recurrence]:
+ *        S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *        o~_t = S_t^T q_t,
+ *    S_t in R^{dk x dv} per head, alpha_t in (0,1)^{dk} per channel, beta_t a
+ *    scalar.  alpha_t = exp(g_t) with g the log-decay ([K3-notes §2.2, decay
+ *    lower-bound equation (Eq. 5)]).
+ *  - [K3-notes §2.2, chunkwise form]: per chunk of C tokens, cumulative decay
+ *    gamma^{i->j} = prod_{r=i..j} alpha^r, Gamma row r = gamma^{1->r},
+ *    pseudo-value V~ = U - W S, A = Tril[(Q o Gamma)(K / Gamma)^T] with the
+ *    diagonal included, O = (Gamma o Q) S + A V~.  The page does not print U, W
+ *    or the state carry; the plainest reading consistent with the recurrence is
+ *        L  = StrictTril[diag(beta) (Gamma o K)(K / Gamma)^T],  T = (I + L)^{-1},
+ *        U  = T diag(beta) V,   W = T diag(beta) (Gamma o K),
+ *        S' = Diag(gamma_C) S + (K o gamma_C / Gamma)^T V~.
+ *  - [K3-notes §2.5, context-parallel affine pair]: a segment maps its entry
+ *    state to S_out = S~_local + M_local S_in.
+ *
+ * Layouts (all row-major, token-major like the CUDA library's inputs):
+ *   q, k, g : [T_total][H][dk] float32  (the exact values the GPU receives)
+ *   v       : [T_total][H][dv] float32
+ *   beta    : [T_total][H]     float32
+ *   states  : [N][H][dk][dv]   double   (dv contiguous)
+ *   o       : [T_total][H][dv] double
+ * Sequence n owns tokens [cu[n], cu[n+1]).  A "chain" is one (n, h) pair,
+ * numbered n*H + h.  Chains run on host threads; each chain is a plain loop.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL -1
+#define ORACLE_ENOMEM -2
+
+/* Planted mistakes for the pin-strength tests.  0 is the oracle itself; the
+ * others are deliberate errors that the tests must catch. */
+enum {
+  MUT_NONE = 0,
+  MUT_NO_DECAY = 1,          /* alpha treated as 1                               */
+  MUT_SIGN_ERASE = 2,        /* u = beta (v + x) instead of beta (v - x)          */
+  MUT_UNDECAYED_PREDICT = 3, /* prediction from S_{t-1} before the decay          */
+  MUT_READ_TRANSPOSED = 4,   /* o = S q instead of S^T q (needs dk == dv)         */
+  MUT_READ_BEFORE_WRITE = 5, /* o read from the decayed state before the write    */
+  MUT_BETA_ONLY_ON_WRITE = 6,/* erase term without beta: u = beta v - x           */
+  MUT_DECAY_BY_COLUMN = 7,   /* Diag(alpha) applied to dv index (needs dk == dv)  */
+  MUT_BETA_SQUARED = 8,      /* u = beta^2 (v - x)                                */
+  MUT_COUNT = 9
+};
+
+typedef struct {
+  int N, H, dk, dv;
+  const int64_t *cu;
+  const float *q, *k, *v, *g, *beta;
+  const double *s0;  /* nullable: zero initial state */
+  double *o;         /* nullable */
+  double *s_final;   /* nullable */
+  const int32_t *chains;
+  int nchains;
+  int mutation;
+  int chunk;         /* chunk form only */
+  int subtile_ref;   /* chunk form only */
+  int next;          /* work counter */
+  int status;
+} job_t;
+
+/* ---------------------------------------------------------------- recurrence */
+
+/* One token of [K3-notes §2.2, KDA state recurrence] applied to S (dk x dv):
+ *   S <- Diag(alpha) S                       (decay first, as the equation reads)
+ *   x  = S^T k                               (what the decayed state predicts for k)
+ *   u  = beta (v - x)                        ((I - beta k k^T) erases along k ...)
+ *   S <- S + k u^T                           (... and beta k v^T writes)
+ *   o  = S^T q
+ * The middle three lines expand (I - beta k k^T) Diag(alpha) S + beta k v^T.
+ * work: dk + dv doubles of scratch. */
+static void kda_token(int dk, int dv, double *S, const float *q, const float *k,
+                      const float *v, const float *g, double beta, double *o,
+                      double *work, int mutation) {
+  double *x = work;       /* dv */
+  double *u = work + dv;  /* dv */
+  (void)u;
+  if (mutation == MUT_UNDECAYED_PREDICT) {
+    for (int j = 0; j < dv; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += S[(size_t)i * dv + j] * (double)k[i];
+      x[j] = acc;
+    }
+  }
+  if (mutation != MUT_NO_DECAY) {
+    for (int i = 0; i < dk; ++i) {
+      for (int j = 0; j < dv; ++j) {
+        double a = exp((double)g[mutation == MUT_DECAY_BY_COLUMN ? j : i]);
+        S[(size_t)i * dv + j] *= a;
+      }
+    }
+  }
+  if (mutation != MUT_UNDECAYED_PREDICT) {
+    for (int j = 0; j < dv; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += S[(size_t)i * dv + j] * (double)k[i];
+      x[j] = acc;
+    }
+  }
+  if (mutation == MUT_READ_BEFORE_WRITE) {
+    for (int j = 0; j < dv; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += S[(size_t)i * dv + j] * (double)q[i];
+      o[j] = acc;
+    }
+  }
+  for (int j = 0; j < dv; ++j) {
+    double uj;
+    switch (mutation) {
+      case MUT_SIGN_ERASE: uj = beta * ((double)v[j] + x[j]); break;
+      case MUT_BETA_ONLY_ON_WRITE: uj = beta * (double)v[j] - x[j]; break;
+      case MUT_BETA_SQUARED: uj = beta * beta * ((double)v[j] - x[j]); break;
+      default: uj = beta * ((double)v[j] - x[j]); break;
+    }
+    for (int i = 0; i < dk; ++i) S[(size_t)i * dv + j] += (double)k[i] * uj;
+  }
+  if (mutation == MUT_READ_BEFORE_WRITE) return;
+  for (int j = 0; j < dv; ++j) {
+    double acc = 0.0;
+    if (mutation == MUT_READ_TRANSPOSED) {
+      for (int i = 0; i < dk; ++i) acc += S[(size_t)j * dv + i] * (double)q[i];
+    } else {
+      for (int i = 0; i < dk; ++i) acc += S[(size_t)i * dv + j] * (double)q[i];
+    }
+    o[j] = acc;
+  }
+}
+
+static int next_chain(job_t *J) { return __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED); }
+
+static void *recurrent_worker(void *arg) {
+  job_t *J = (job_t *)arg;
+  const int dk = J->dk, dv = J->dv, H = J->H;
+  double *S = (double *)malloc(sizeof(double) * (size_t)dk * dv);
+  double *work = (double *)malloc(sizeof(double) * (size_t)(2 * dv));
+  double *obuf = (double *)malloc(sizeof(double) * (size_t)dv);
+  if (!S || !work || !obuf) {
+    J->status = ORACLE_ENOMEM;
+    free(S); free(work); free(obuf);
+    return NULL;
+  }
+  for (;;) {
+    int w = next_chain(J);
+    if (w >= J->nchains) break;
+    int c = J->chains ? J->chains[w] : w;
+    int n = c / H, h = c % H;
+    size_t sidx = ((size_t)n * H + h) * (size_t)dk * dv;
+    if (J->s0) memcpy(S, J->s0 + sidx, sizeof(double) * (size_t)dk * dv);
+    else memset(S, 0, sizeof(double) * (size_t)dk * dv);
+    for (int64_t t = J->cu[n]; t < J->cu[n + 1]; ++t) {
+      size_t th = (size_t)t * H + h;
+      kda_token(dk, dv, S, J->q + th * dk, J->k + th * dk, J->v + th * dv, J->g + th * dk,
+                (double)J->beta[th], obuf, work, J->mutation);
+      if (J->o) memcpy(J->o + th * dv, obuf, sizeof(double) * (size_t)dv);
+    }
+    if (J->s_final) memcpy(J->s_final + sidx, S, sizeof(double) * (size_t)dk * dv);
+  }
+  free(S); free(work); free(obuf);
+  return NULL;
+}
+
+static int run_threads(job_t *J, int nthreads, void *(*fn)(void *)) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > J->nchains) nthreads = J->nchains > 0 ? J->nchains : 1;
+  J->next = 0;
+  J->status = ORACLE_OK;
+  if (nthreads == 1) {
+    fn(J);
+    return J->status;
+  }
+  pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!tid) return ORACLE_ENOMEM;
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (pthread_create(&tid[t], NULL, fn, J) != 0) break;
+    ++started;
+  }
+  if (started == 0) fn(J);
+  for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+  free(tid);
+  return J->status;
+}
+
+static int check_common(int N, int H, int dk, int dv, const int64_t *cu) {
+  if (N < 0 || H <= 0 || dk <= 0 || dv <= 0 || !cu) return ORACLE_EINVAL;
+  for (int n = 0; n < N; ++n)
+    if (cu[n + 1] < cu[n]) return ORACLE_EINVAL;
+  return ORACLE_OK;
+}
+
+/* Token-by-token recurrence over every chain listed in `chains` (all N*H
+ * chains when chains == NULL).  Rows of o that belong to other chains are
+ * left untouched. */
+int oracle_kda_recurrent(int N, int H, int dk, int dv, const int64_t *cu, const float *q,
+                         const float *k, const float *v, const float *g, const float *beta,
+                         const double *s0, double *o, double *s_final, const int32_t *chains,
+                         int nchains, int nthreads, int mutation) {
+  int st = check_common(N, H, dk, dv, cu);
+  if (st) return st;
+  if ((mutation == MUT_READ_TRANSPOSED || mutation == MUT_DECAY_BY_COLUMN) && dk != dv)
+    return ORACLE_EINVAL;
+  if (mutation < 0 || mutation >= MUT_COUNT) return ORACLE_EINVAL;
+  job_t J;
+  memset(&J, 0, sizeof(J));
+  J.N = N; J.H = H; J.dk = dk; J.dv = dv; J.cu = cu;
+  J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta;
+  J.s0 = s0; J.o = o; J.s_final = s_final;
+  J.chains = chains; J.nchains = chains ? nchains : N * H;
+  J.mutation = mutation;
+  return run_threads(&J, nthreads, recurrent_worker);
+}
+
+/* One decode step for N independent sequences: each (n, h) consumes one token
+ * (row n of q/k/v/g/beta) and updates state[n][h] in place.  This is the same
+ * recurrence with every sequence one token long. */
+int oracle_kda_decode_step(int N, int H, int dk, int dv, const float *q, const float *k,
+                           const float *v, const float *g, const float *beta, double *state,
+                           double *o, const int32_t *chains, int nchains, int nthreads) {
+  if (N <= 0) return ORACLE_EINVAL;
+  int64_t *cu = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N + 1));
+  if (!cu) return ORACLE_ENOMEM;
+  for (int n = 0; n <= N; ++n) cu[n] = n;
+  int st = oracle_kda_recurrent(N, H, dk, dv, cu, q, k, v, g, beta, state, o, state, chains,
+                                nchains, nthreads, MUT_NONE);
+  free(cu);
+  return st;
+}
+
+/* ------------------------------------------------------------- chunk form */
+
+/* The chunkwise form of [K3-notes §2.2] written out in fp64 with the U, W and
+ * carry formulas stated in the file header.  It is not blocked or fused beyond
+ * what those formulas state.  subtile_ref selects how the Gram products
+ * (Q o Gamma)(K / Gamma)^T are factored: 0 uses the chunk start as the decay
+ * reference for every pair (the page's literal form); 1 uses, for each key
+ * column s, the cumulative decay at the start of s's 16-token tile, which is
+ * the tile-range argument of [K3-notes §2.2, Fig. 3].  Both are the same
+ * number in exact arithmetic; in fp64 both stay in range for C <= 64 and
+ * g >= -5. */
+static void *chunk_worker(void *arg) {
+  job_t *J = (job_t *)arg;
+  const int dk = J->dk, dv = J->dv, H = J->H, C = J->chunk;
+  size_t need = (size_t)dk * dv          /* S */
+                + (size_t)C * dk * 2     /* G, Gamma */
+                + (size_t)C * C * 3      /* A, L, T */
+                + (size_t)C * dv * 3     /* U, Vt, O */
+                + (size_t)C * dk         /* W */
+                + (size_t)dk * dv;       /* S next */
+  double *buf = (double *)malloc(sizeof(double) * need);
+  if (!buf) { J->status = ORACLE_ENOMEM; return NULL; }
+  for (;;) {
+    int w = next_chain(J);
+    if (w >= J->nchains) break;
+    int c = J->chains ? J->chains[w] : w;
+    int n = c / H, h = c % H;
+    double *S = buf;
+    double *G = S + (size_t)dk * dv;
+    double *Gam = G + (size_t)C * dk;
+    double *A = Gam + (size_t)C * dk;
+    double *L = A + (size_t)C * C;
+    double *T = L + (size_t)C * C;
+    double *U = T + (size_t)C * C;
+    double *Vt = U + (size_t)C * dv;
+    double *O = Vt + (size_t)C * dv;
+    double *W = O + (size_t)C * dv;
+    double *Sn = W + (size_t)C * dk;
+    size_t sidx = ((size_t)n * H + h) * (size_t)dk * dv;
+    if (J->s0) memcpy(S, J->s0 + sidx, sizeof(double) * (size_t)dk * dv);
+    else memset(S, 0, sizeof(double) * (size_t)dk * dv);
+    for (int64_t t0 = J->cu[n]; t0 < J->cu[n + 1]; t0 += C) {
+      int len = (int)((J->cu[n + 1] - t0) < C ? (J->cu[n + 1] - t0) : C);
+#define IDX(t, d) (((size_t)(t0 + (t)) * H + h) * (size_t)(d))
+      /* cumulative log-decay within the chunk, G[r] = sum_{t<=r} g_t */
+      for (int i = 0; i < dk; ++i) {
+        double acc = 0.0;
+        for (int r = 0; r < len; ++r) {
+          acc += (double)J->g[IDX(r, dk) + i];
+          G[(size_t)r * dk + i] = acc;
+          Gam[(size_t)r * dk + i] = exp(acc);
+        }
+      }
+      /* A (diagonal included) and L (strict) */
+      for (int r = 0; r < len; ++r) {
+        for (int s = 0; s < len; ++s) {
+          double a = 0.0, l = 0.0;
+          if (s <= r) {
+            int s0 = J->subtile_ref ? (s / 16) * 16 : 0;
+            for (int i = 0; i < dk; ++i) {
+              double ref = s0 > 0 ? G[(size_t)(s0 - 1) * dk + i] : 0.0;
+              double qb = (double)J->q[IDX(r, dk) + i] * exp(G[(size_t)r * dk + i] - ref);
+              double gk = (double)J->k[IDX(r, dk) + i] * exp(G[(size_t)r * dk + i] - ref);
+              double kb = (double)J->k[IDX(s, dk) + i] * exp(ref - G[(size_t)s * dk + i]);
+              a += qb * kb;
+              l += gk * kb;
+            }
+          }
+          A[(size_t)r * C + s] = a;
+          L[(size_t)r * C + s] = (s < r) ? (double)J->beta[IDX(r, 1)] * l : 0.0;
+        }
+      }
+      /* T = (I + L)^{-1}, forward substitution row by row */
+      for (int r = 0; r < len; ++r) {
+        for (int s = 0; s < len; ++s) {
+          double acc = (r == s) ? 1.0 : 0.0;
+          for (int m = 0; m < r; ++m) acc -= L[(size_t)r * C + m] * T[(size_t)m * C + s];
+          T[(size_t)r * C + s] = acc;
+        }
+      }
+      /* U = T diag(beta) V ; W = T diag(beta) (Gamma o K) */
+      for (int r = 0; r < len; ++r) {
+        for (int j = 0; j < dv; ++j) {
+          double acc = 0.0;
+          for (int s = 0; s < len; ++s)
+            acc += T[(size_t)r * C + s] * (double)J->beta[IDX(s, 1)] * (double)J->v[IDX(s, dv) + j];
+          U[(size_t)r * dv + j] = acc;
+        }
+        for (int i = 0; i < dk; ++i) {
+          double acc = 0.0;
+          for (int s = 0; s < len; ++s)
+            acc += T[(size_t)r * C + s] * (double)J->beta[IDX(s, 1)] * Gam[(size_t)s * dk + i] *
+                   (double)J->k[IDX(s, dk) + i];
+          W[(size_t)r * dk + i] = acc;
+        }
+      }
+      /* V~ = U - W S */
+      for (int r = 0; r < len; ++r)
+        for (int j = 0; j < dv; ++j) {
+          double acc = U[(size_t)r * dv + j];
+          for (int i = 0; i < dk; ++i) acc -= W[(size_t)r * dk + i] * S[(size_t)i * dv + j];
+          Vt[(size_t)r * dv + j] = acc;
+        }
+      /* O = (Gamma o Q) S + A V~ */
+      for (int r = 0; r < len; ++r)
+        for (int j = 0; j < dv; ++j) {
+          double acc = 0.0;
+          for (int i = 0; i < dk; ++i)
+            acc += Gam[(size_t)r * dk + i] * (double)J->q[IDX(r, dk) + i] * S[(size_t)i * dv + j];
+          for (int s = 0; s <= r; ++s) acc += A[(size_t)r * C + s] * Vt[(size_t)s * dv + j];
+          O[(size_t)r * dv + j] = acc;
+        }
+      /* S' = Diag(gamma_C) S + (K o gamma_C / Gamma)^T V~ */
+      for (int i = 0; i < dk; ++i) {
+        double GC = G[(size_t)(len - 1) * dk + i];
+        for (int j = 0; j < dv; ++j) {
+          double acc = exp(GC) * S[(size_t)i * dv + j];
+          for (int r = 0; r < len; ++r)
+            acc += (double)J->k[IDX(r, dk) + i] * exp(GC - G[(size_t)r * dk + i]) *
+                   Vt[(size_t)r * dv + j];
+          Sn[(size_t)i * dv + j] = acc;
+        }
+      }
+      memcpy(S, Sn, sizeof(double) * (size_t)dk * dv);
+      if (J->o)
+        for (int r = 0; r < len; ++r)
+          memcpy(J->o + IDX(r, dv), O + (size_t)r * dv, sizeof(double) * (size_t)dv);
+#undef IDX
+    }
+    if (J->s_final) memcpy(J->s_final + sidx, S, sizeof(double) * (size_t)dk * dv);
+  }
+  free(buf);
+  return NULL;
+}
+
+int oracle_kda_chunked(int N, int H, int dk, int dv, const int64_t *cu, const float *q,
+                       const float *k, const float *v, const float *g, const float *beta,
+                       const double *s0, double *o, double *s_final, const int32_t *chains,
+                       int nchains, int nthreads, int chunk, int subtile_ref) {
+  int st = check_common(N, H, dk, dv, cu);
+  if (st) return st;
+  if (chunk <= 0 || chunk > 256) return ORACLE_EINVAL;
+  job_t J;
+  memset(&J, 0, sizeof(J));
+  J.N = N; J.H = H; J.dk = dk; J.dv = dv; J.cu = cu;
+  J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta;
+  J.s0 = s0; J.o = o; J.s_final = s_final;
+  J.chains = chains; J.nchains = chains ? nchains : N * H;
+  J.chunk = chunk; J.subtile_ref = subtile_ref;
+  return run_threads(&J, nthreads, chunk_worker);
+}
+
+/* ------------------------------------------------------------ affine pair */
+
+/* [K3-notes §2.5, context-parallel affine pair] for tokens [t0, t1) of head h:
+ * the segment maps any entry state S_in to S_out = S~ + M S_in.  M (dk x dk)
+ * is the ordered product of the per-token transitions
+ * (I - beta_t k_t k_t^T) Diag(alpha_t); S~ (dk x dv) is the segment's state when
+ * it starts from zero.  Both follow from the recurrence by carrying M as extra
+ * state columns that receive no write. */
+int oracle_kda_affine_pair(int H, int dk, int dv, int h, int64_t t0, int64_t t1, const float *k,
+                           const float *v, const float *g, const float *beta, double *M,
+                           double *St) {
+  if (H <= 0 || dk <= 0 || dv <= 0 || h < 0 || h >= H || t1 < t0) return ORACLE_EINVAL;
+  double *x = (double *)malloc(sizeof(double) * (size_t)(dk + dv));
+  if (!x) return ORACLE_ENOMEM;
+  for (int i = 0; i < dk; ++i)
+    for (int m = 0; m < dk; ++m) M[(size_t)i * dk + m] = (i == m) ? 1.0 : 0.0;
+  memset(St, 0, sizeof(double) * (size_t)dk * dv);
+  for (int64_t t = t0; t < t1; ++t) {
+    size_t th = (size_t)t * H + h;
+    const float *kt = k + th * dk, *vt = v + th * dv, *gt = g + th * dk;
+    double b = (double)beta[th];
+    for (int i = 0; i < dk; ++i) {
+      double a = exp((double)gt[i]);
+      for (int m = 0; m < dk; ++m) M[(size_t)i * dk + m] *= a;
+      for (int j = 0; j < dv; ++j) St[(size_t)i * dv + j] *= a;
+    }
+    /* M <- M - beta k (k^T M);   S~ <- S~ + k beta (v - S~^T k)^T */
+    for (int m = 0; m < dk; ++m) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += (double)kt[i] * M[(size_t)i * dk + m];
+      x[m] = acc;
+    }
+    for (int i = 0; i < dk; ++i)
+      for (int m = 0; m < dk; ++m) M[(size_t)i * dk + m] -= b * (double)kt[i] * x[m];
+    for (int j = 0; j < dv; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += (double)kt[i] * St[(size_t)i * dv + j];
+      x[j] = b * ((double)vt[j] - acc);
+    }
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) St[(size_t)i * dv + j] += (double)kt[i] * x[j];
+  }
+  free(x);
+  return ORACLE_OK;
+}
+
+int oracle_mutation_count(void) { return MUT_COUNT; }
