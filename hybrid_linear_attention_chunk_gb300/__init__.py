@@ -1,0 +1,13 @@
+"""KDA (Kimi Delta Attention) chunked prefill and decode step on one GB300.
+
+The compute path is libkda.so, a C-ABI library of hand-written sm_103a CUDA
+kernels (declared in include/kda.h).  This package holds its build script,
+its ctypes binding (same names as the C entry points) and the seeded
+synthetic input generator.  Importing the package does not load the library;
+the first call does, and raises if it is missing.
+"""
+from ._lib import (KdaChunkDesc, KdaDecodeDesc, KdaError, chunk_desc, kda_chunk_fwd,  # noqa: F401
+                   kda_chunk_fwd_workspace_size, kda_decode_step, load, LIB_PATH)
+
+__all__ = ["kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size", "load", "KdaError",
+           "KdaChunkDesc", "KdaDecodeDesc", "chunk_desc", "LIB_PATH"]

@@ -1,0 +1,198 @@
+"""ctypes binding of libkda.so (include/kda.h).  Argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels.  PyTorch
+supplies device memory and the current stream.  There is no fallback: if
+libkda.so is missing or cannot load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_F32, KDA_BF16 = 0, 1
+KERNELS = {"auto": 0, "simt": 1, "tc": 2}
+STATUS = {
+    0: "KDA_OK", -1: "KDA_ERR_NULL", -2: "KDA_ERR_SHAPE", -3: "KDA_ERR_DTYPE",
+    -4: "KDA_ERR_ALIGN", -5: "KDA_ERR_RANGE", -6: "KDA_ERR_CUDA", -7: "KDA_ERR_UNSUPPORTED",
+    -8: "KDA_ERR_ALIAS",
+}
+
+
+class KdaChunkDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("chunk", ctypes.c_int),
+                ("num_seqs", ctypes.c_int), ("qkv_dtype", ctypes.c_int),
+                ("out_dtype", ctypes.c_int), ("gate_dtype", ctypes.c_int),
+                ("validate", ctypes.c_int), ("kernel", ctypes.c_int), ("segments", ctypes.c_int)]
+
+
+class KdaDecodeDesc(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int), ("H", ctypes.c_int), ("dk", ctypes.c_int),
+                ("dv", ctypes.c_int), ("qkv_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("gate_dtype", ctypes.c_int), ("validate", ctypes.c_int)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, fn: str, detail: str = ""):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        super().__init__(f"{fn} returned {name}" + (f": {detail}" if detail else ""))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libkda.so (raises if it is absent: there is no CPU path)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkda.so is not built ({LIB_PATH}); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        lib.kda_chunk_fwd.argtypes = [ctypes.POINTER(KdaChunkDesc), P, P, P, P, P, P, P, P, P, P]
+        lib.kda_chunk_fwd.restype = ctypes.c_int
+        lib.kda_chunk_fwd_ex.argtypes = [ctypes.POINTER(KdaChunkDesc), P, P, P, P, P, P, P, P, P,
+                                         P, ctypes.c_size_t, P]
+        lib.kda_chunk_fwd_ex.restype = ctypes.c_int
+        lib.kda_chunk_fwd_workspace_size.argtypes = [ctypes.POINTER(KdaChunkDesc),
+                                                     ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [ctypes.POINTER(KdaDecodeDesc), P, P, P, P, P, P, P, P]
+        lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_last_cuda_error.argtypes = []
+        lib.kda_last_cuda_error.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, fn: str):
+    if status != 0:
+        lib = load()
+        detail = lib.kda_status_string(status).decode()
+        if status == -6:
+            detail += " (" + lib.kda_last_cuda_error().decode() + ")"
+        raise KdaError(status, fn, detail)
+
+
+def chunk_desc(q, v, *, chunk=64, cu_seqlens=None, out_dtype=None, gate_dtype=None, validate=False,
+               kernel="auto", segments=0, B=None) -> KdaChunkDesc:
+    if q.dim() == 4:
+        B_, T, H, dk = q.shape
+    else:
+        T, H, dk = q.shape
+        B_ = 1
+    if B is not None and q.dim() == 3:
+        B_ = B
+        T = T // B
+    dv = v.shape[-1]
+    d = KdaChunkDesc()
+    d.B, d.T, d.H, d.dk, d.dv, d.chunk = B_, T, H, dk, dv, chunk
+    d.num_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    d.qkv_dtype = _dt(q)
+    d.out_dtype = KDA_BF16 if out_dtype == torch.bfloat16 else (
+        KDA_F32 if out_dtype == torch.float32 else _dt(q))
+    d.gate_dtype = gate_dtype if gate_dtype is not None else KDA_F32
+    d.validate = int(bool(validate))
+    d.kernel = KERNELS[kernel]
+    d.segments = int(segments)
+    return d
+
+
+def kda_chunk_fwd(q, k, v, log_alpha, beta, initial_state=None, cu_seqlens=None, out=None,
+                  final_state=None, *, chunk=64, kernel="auto", segments=0, validate=False,
+                  out_dtype=None, want_final_state=True, B=None, stream=None, workspace=None):
+    """Chunked KDA prefill through the C ABI.
+
+    q, k, log_alpha: [B*T, H, dk] (or [B, T, H, dk]); v: [.., H, dv];
+    beta: [B*T, H]; initial_state: [N, H, dk, dv] fp32 or None;
+    cu_seqlens: int32 [N+1] on the device or None.  Returns (out, final_state).
+    """
+    lib = load()
+    dev = q.device
+    d = chunk_desc(q, v, chunk=chunk, cu_seqlens=cu_seqlens, out_dtype=out_dtype or q.dtype,
+                   gate_dtype=_dt(log_alpha), validate=validate, kernel=kernel, segments=segments, B=B)
+    if beta.dtype != log_alpha.dtype:
+        raise TypeError("log_alpha and beta must share a dtype")
+    Nseq = d.num_seqs if cu_seqlens is not None else d.B
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (d.dv,), dtype=out_dtype or q.dtype, device=dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(Nseq, d.H, d.dk, d.dv, dtype=torch.float32, device=dev)
+    args = [ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+            _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state)]
+    if workspace is not None:
+        st = lib.kda_chunk_fwd_ex(*args, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream, dev))
+        _check(st, "kda_chunk_fwd_ex")
+    else:
+        st = lib.kda_chunk_fwd(*args, _stream_handle(stream, dev))
+        _check(st, "kda_chunk_fwd")
+    return out, final_state
+
+
+def kda_chunk_fwd_workspace_size(desc: KdaChunkDesc) -> int:
+    lib = load()
+    n = ctypes.c_size_t(0)
+    _check(lib.kda_chunk_fwd_workspace_size(ctypes.byref(desc), ctypes.byref(n)),
+           "kda_chunk_fwd_workspace_size")
+    return n.value
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, state_inout, out=None, *, validate=False,
+                    out_dtype=None, stream=None):
+    """One decode step through the C ABI: q,k,log_alpha [N,H,dk], v [N,H,dv],
+    beta [N,H], state_inout [N,H,dk,dv] fp32 (updated in place).  Returns out."""
+    lib = load()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    d = KdaDecodeDesc()
+    d.N, d.H, d.dk, d.dv = N, H, dk, dv
+    d.qkv_dtype = _dt(q)
+    od = out_dtype or q.dtype
+    d.out_dtype = _dt(torch.empty(0, dtype=od))
+    d.gate_dtype = _dt(log_alpha)
+    d.validate = int(bool(validate))
+    if out is None:
+        out = torch.empty(N, H, dv, dtype=od, device=q.device)
+    st = lib.kda_decode_step(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                             _ptr(state_inout), _ptr(out), _stream_handle(stream, q.device))
+    _check(st, "kda_decode_step")
+    return out

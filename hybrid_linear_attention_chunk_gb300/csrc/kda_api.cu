@@ -1,0 +1,260 @@
+// Host side of the C ABI declared in include/kda.h: argument checks, kernel
+// choice, launch.  Every compute step runs in the kernels of the other
+// translation units; nothing here touches tensor data.
+#include <stdio.h>
+#include <string.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+kda_status cuda_fail(cudaError_t e) {
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return KDA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+bool dtype_ok(kda_dtype t) { return t == KDA_F32 || t == KDA_BF16; }
+
+size_t esize(kda_dtype t) { return t == KDA_BF16 ? 2 : 4; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+
+Range span(const void *p, size_t bytes) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + bytes};
+}
+
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
+
+// --------------------------------------------------------------- validation
+
+__global__ void validate_prefill_kernel(PrefillArgs a, int *flag) {
+  const size_t nk = (size_t)a.T_total * a.H * a.dk;
+  const size_t nb = (size_t)a.T_total * a.H;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  int bad = 0;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nk; i += stride) {
+    float g = ld_elem(a.g, i, a.gate);
+    if (!(g >= kLogDecayFloor && g <= 0.f)) bad |= 1;
+  }
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nb; i += stride) {
+    float b = ld_elem(a.beta, i, a.gate);
+    if (!(b >= 0.f && b <= 1.f)) bad |= 2;
+  }
+  if (a.cu && blockIdx.x == 0) {
+    for (int n = threadIdx.x; n <= a.N; n += blockDim.x) {
+      int c = a.cu[n];
+      if (n == 0 && c != 0) bad |= 4;
+      if (n == a.N && c != a.T_total) bad |= 4;
+      if (n > 0 && c < a.cu[n - 1]) bad |= 4;
+    }
+  }
+  if (bad) atomicOr(flag, bad);
+}
+
+__global__ void validate_decode_kernel(DecodeArgs a, int *flag) {
+  const size_t nk = (size_t)a.N * a.H * a.dk;
+  const size_t nb = (size_t)a.N * a.H;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  int bad = 0;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nk; i += stride) {
+    float g = ld_elem(a.g, i, a.gate);
+    if (!(g >= kLogDecayFloor && g <= 0.f)) bad |= 1;
+  }
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nb; i += stride) {
+    float b = ld_elem(a.beta, i, a.gate);
+    if (!(b >= 0.f && b <= 1.f)) bad |= 2;
+  }
+  if (bad) atomicOr(flag, bad);
+}
+
+// Runs a check kernel, waits for it and reports KDA_ERR_RANGE on a bad value.
+template <class Launch>
+kda_status run_validation(cudaStream_t s, Launch launch) {
+  int *d_flag = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&d_flag), sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int h_flag = 0;
+  e = cudaMemsetAsync(d_flag, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = launch(d_flag);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h_flag, d_flag, sizeof(int), cudaMemcpyDeviceToHost, s);
+  cudaError_t ef = cudaFreeAsync(d_flag, s);
+  if (e == cudaSuccess) e = ef;
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return h_flag ? KDA_ERR_RANGE : KDA_OK;
+}
+
+kda_status check_prefill(const kda_chunk_desc *d, const void *q, const void *k, const void *v,
+                         const void *g, const void *beta, const float *s0, const int32_t *cu,
+                         void *out, float *sT, PrefillArgs *a) {
+  if (!d || !q || !k || !v || !g || !beta || !out) return KDA_ERR_NULL;
+  if (!dtype_ok(d->qkv_dtype) || !dtype_ok(d->out_dtype) || !dtype_ok(d->gate_dtype))
+    return KDA_ERR_DTYPE;
+  if (d->H <= 0 || !dim_ok(d->dk) || !dim_ok(d->dv) || d->T < 0 || d->B <= 0) return KDA_ERR_SHAPE;
+  if (!(d->chunk == 16 || d->chunk == 32 || d->chunk == 64)) return KDA_ERR_SHAPE;
+  if (d->segments < 0) return KDA_ERR_SHAPE;
+  if (cu) {
+    if (d->B != 1 || d->num_seqs <= 0) return KDA_ERR_SHAPE;
+  } else if (d->num_seqs != 0) {
+    return KDA_ERR_SHAPE;
+  }
+  const long long T_total = cu ? (long long)d->T : (long long)d->B * d->T;
+  if (T_total * d->H * (d->dk > d->dv ? d->dk : d->dv) >= (1LL << 40)) return KDA_ERR_SHAPE;
+  const void *ptrs[] = {q, k, v, g, beta, s0, cu, out, sT};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+  const int Nseq = cu ? d->num_seqs : d->B;
+  const size_t th = (size_t)T_total * d->H;
+  Range r_out = span(out, th * d->dv * esize(d->out_dtype));
+  Range ins[] = {span(q, th * d->dk * esize(d->qkv_dtype)), span(k, th * d->dk * esize(d->qkv_dtype)),
+                 span(v, th * d->dv * esize(d->qkv_dtype)), span(g, th * d->dk * esize(d->gate_dtype)),
+                 span(beta, th * esize(d->gate_dtype)),
+                 span(s0, s0 ? (size_t)Nseq * d->H * d->dk * d->dv * 4 : 0),
+                 span(cu, cu ? (size_t)(Nseq + 1) * 4 : 0),
+                 span(sT, sT ? (size_t)Nseq * d->H * d->dk * d->dv * 4 : 0)};
+  for (const Range &r : ins)
+    if (overlap(r_out, r)) return KDA_ERR_ALIAS;
+  if (sT) {
+    Range r_sT = span(sT, (size_t)Nseq * d->H * d->dk * d->dv * 4);
+    for (int i = 0; i < 5; ++i)
+      if (overlap(r_sT, ins[i])) return KDA_ERR_ALIAS;
+    if (s0 && s0 != sT && overlap(r_sT, ins[5])) return KDA_ERR_ALIAS;
+  }
+  a->N = Nseq;
+  a->T_total = (int)T_total;
+  a->T_seq = cu ? 0 : d->T;
+  a->H = d->H;
+  a->dk = d->dk;
+  a->dv = d->dv;
+  a->chunk = d->chunk;
+  a->qkv = d->qkv_dtype;
+  a->out = d->out_dtype;
+  a->gate = d->gate_dtype;
+  a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta;
+  a->s0 = s0; a->cu = cu; a->o = out; a->sT = sT;
+  return KDA_OK;
+}
+
+kda_status run_prefill(const kda_chunk_desc *d, const PrefillArgs &a, cudaStream_t s) {
+  if (d->validate) {
+    kda_status st = run_validation(s, [&](int *flag) { return launch_validate_prefill(a, flag, s); });
+    if (st != KDA_OK) return st;
+  }
+  bool tc = chunk_tc_supports(a);
+  if (d->kernel == KDA_KERNEL_TC && !tc) return KDA_ERR_UNSUPPORTED;
+  cudaError_t e = (d->kernel != KDA_KERNEL_SIMT && tc) ? launch_chunk_tc(a, s) : launch_chunk_simt(a, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KDA_OK;
+}
+
+}  // namespace
+
+cudaError_t launch_validate_prefill(const PrefillArgs &a, int *d_flag, cudaStream_t s) {
+  validate_prefill_kernel<<<1024, 256, 0, s>>>(a, d_flag);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate_decode(const DecodeArgs &a, int *d_flag, cudaStream_t s) {
+  validate_decode_kernel<<<256, 256, 0, s>>>(a, d_flag);
+  return cudaGetLastError();
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+kda_status kda_chunk_fwd(const kda_chunk_desc *desc, const void *q, const void *k, const void *v,
+                         const void *log_alpha, const void *beta, const float *initial_state,
+                         const int32_t *cu_seqlens, void *out, float *final_state,
+                         kda_stream_t stream) {
+  PrefillArgs a;
+  kda_status st = check_prefill(desc, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                                final_state, &a);
+  if (st != KDA_OK) return st;
+  return run_prefill(desc, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kda_status kda_chunk_fwd_workspace_size(const kda_chunk_desc *desc, size_t *bytes) {
+  if (!desc || !bytes) return KDA_ERR_NULL;
+  *bytes = 0;
+  return KDA_OK;
+}
+
+kda_status kda_chunk_fwd_ex(const kda_chunk_desc *desc, const void *q, const void *k,
+                            const void *v, const void *log_alpha, const void *beta,
+                            const float *initial_state, const int32_t *cu_seqlens, void *out,
+                            float *final_state, void *workspace, size_t workspace_bytes,
+                            kda_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  return kda_chunk_fwd(desc, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                       final_state, stream);
+}
+
+kda_status kda_decode_step(const kda_decode_desc *d, const void *q, const void *k, const void *v,
+                           const void *log_alpha, const void *beta, float *state_inout, void *out,
+                           kda_stream_t stream) {
+  if (!d || !q || !k || !v || !log_alpha || !beta || !state_inout || !out) return KDA_ERR_NULL;
+  if (!dtype_ok(d->qkv_dtype) || !dtype_ok(d->out_dtype) || !dtype_ok(d->gate_dtype))
+    return KDA_ERR_DTYPE;
+  if (d->N <= 0 || d->H <= 0 || !dim_ok(d->dk) || !dim_ok(d->dv)) return KDA_ERR_SHAPE;
+  if ((long long)d->N * d->H >= (1LL << 31)) return KDA_ERR_SHAPE;
+  const void *ptrs[] = {q, k, v, log_alpha, beta, state_inout, out};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return KDA_ERR_ALIGN;
+  const size_t nh = (size_t)d->N * d->H;
+  Range r_s = span(state_inout, nh * d->dk * d->dv * 4);
+  Range r_o = span(out, nh * d->dv * esize(d->out_dtype));
+  Range ins[] = {span(q, nh * d->dk * esize(d->qkv_dtype)), span(k, nh * d->dk * esize(d->qkv_dtype)),
+                 span(v, nh * d->dv * esize(d->qkv_dtype)),
+                 span(log_alpha, nh * d->dk * esize(d->gate_dtype)),
+                 span(beta, nh * esize(d->gate_dtype))};
+  if (overlap(r_s, r_o)) return KDA_ERR_ALIAS;
+  for (const Range &r : ins)
+    if (overlap(r_s, r) || overlap(r_o, r)) return KDA_ERR_ALIAS;
+  DecodeArgs a;
+  a.N = d->N; a.H = d->H; a.dk = d->dk; a.dv = d->dv;
+  a.qkv = d->qkv_dtype; a.out = d->out_dtype; a.gate = d->gate_dtype;
+  a.q = q; a.k = k; a.v = v; a.g = log_alpha; a.beta = beta;
+  a.state = state_inout; a.o = out;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d->validate) {
+    kda_status st = run_validation(s, [&](int *flag) { return launch_validate_decode(a, flag, s); });
+    if (st != KDA_OK) return st;
+  }
+  cudaError_t e = launch_decode(a, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KDA_OK;
+}
+
+const char *kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_NULL: return "a required pointer is NULL";
+    case KDA_ERR_SHAPE: return "unsupported or inconsistent size";
+    case KDA_ERR_DTYPE: return "unsupported dtype";
+    case KDA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case KDA_ERR_RANGE: return "input value outside its range (validate mode)";
+    case KDA_ERR_CUDA: return "CUDA error (see kda_last_cuda_error)";
+    case KDA_ERR_UNSUPPORTED: return "the requested kernel does not cover these arguments";
+    case KDA_ERR_ALIAS: return "forbidden aliasing between arguments";
+  }
+  return "unknown status";
+}
+
+const char *kda_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

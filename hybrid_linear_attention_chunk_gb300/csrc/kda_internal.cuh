@@ -1,0 +1,75 @@
+// Internal declarations shared by the libkda.so translation units.
+//
+// Cited page: "Kimi K3：从 3T 稀疏预训练到百万 Token Agent 的端到端扩展"
+// (liuzhao09.github.io/papers/kimi-k3), [K3-notes] below.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Log-decay floor of [K3-notes §2.2, Eq. 5] (g_min = -5).  The kernels'
+// range guard relies on it: 16 tokens at the floor sum to -80, and e^80 is
+// still a finite fp32/bf16 value.
+constexpr float kLogDecayFloor = -5.0f;
+// A chunk whose per-channel cumulative log-decay stays at or above this uses
+// one decay reference for the whole chunk; below it the Gram products are
+// factored per 16-token tile ([K3-notes §2.2, Fig. 3]).
+constexpr float kSingleRefBound = -80.0f;
+
+struct PrefillArgs {
+  int N;        // sequences
+  int T_total;  // tokens in the packed buffer
+  int T_seq;    // tokens per sequence when cu_seqlens == nullptr
+  int H, dk, dv, chunk;
+  kda_dtype qkv, out, gate;
+  const void *q, *k, *v, *g, *beta;
+  const float *s0;           // nullable
+  const int32_t *cu;         // nullable
+  void *o;
+  float *sT;                 // nullable
+};
+
+struct DecodeArgs {
+  int N, H, dk, dv;
+  kda_dtype qkv, out, gate;
+  const void *q, *k, *v, *g, *beta;
+  float *state;
+  void *o;
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_chunk_simt(const PrefillArgs &a, cudaStream_t s);
+bool chunk_tc_supports(const PrefillArgs &a);
+cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_validate_prefill(const PrefillArgs &a, int *d_flag, cudaStream_t s);
+cudaError_t launch_validate_decode(const DecodeArgs &a, int *d_flag, cudaStream_t s);
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ float ld_elem(const void *p, size_t i, kda_dtype t) {
+  if (t == KDA_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+  return reinterpret_cast<const float *>(p)[i];
+}
+
+__device__ __forceinline__ void st_elem(void *p, size_t i, float x, kda_dtype t) {
+  if (t == KDA_BF16) reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
+  else reinterpret_cast<float *>(p)[i] = x;
+}
+
+// Token range of sequence n.
+__device__ __forceinline__ void seq_range(const PrefillArgs &a, int n, int &bos, int &eos) {
+  if (a.cu) {
+    bos = a.cu[n];
+    eos = a.cu[n + 1];
+  } else {
+    bos = n * a.T_seq;
+    eos = bos + a.T_seq;
+  }
+}
+
+}  // namespace kda

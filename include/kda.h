@@ -1,0 +1,160 @@
+/*
+ * kda.h - C ABI of libkda.so: Kimi Delta Attention (KDA) chunked prefill and
+ * decode step on one GB300 (sm_103a).
+ *
+ * Cited page: "Kimi K3：从 3T 稀疏预训练到百万 Token Agent 的端到端扩展"
+ * (liuzhao09.github.io/papers/kimi-k3), [K3-notes] below.
+ *
+ * The operation ([K3-notes §2.2, KDA state recurrence]), per sequence n and
+ * head h, over that sequence's tokens t in order:
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t,            alpha_t = exp(log_alpha_t)  (per channel)
+ * with S in R^{dk x dv}.  The library does not scale or normalise q or k.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    keeps no pointer after the call returns.  Every pointer must be 16-byte
+ *    aligned (KDA_ERR_ALIGN otherwise).  Tensors are dense and row-major in
+ *    the shapes written below (last index contiguous).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without waiting, except in validate mode.
+ *  - Argument errors are reported synchronously, before anything is launched,
+ *    as a negative kda_status.  A launch failure returns KDA_ERR_CUDA.
+ *    Asynchronous device faults surface at the caller's next synchronisation.
+ *  - Preconditions on values ([K3-notes §2.2, Eq. 5] bounds the log-decay
+ *    below by g_min = -5): log_alpha in [-5, 0], beta in [0, 1], cu_seqlens
+ *    non-decreasing from 0 to T.  The kernels rely on the log-decay floor for
+ *    their range guard.  They are checked only in validate mode (desc.validate
+ *    = 1), which runs a check kernel first, synchronises the stream and
+ *    returns KDA_ERR_RANGE without computing anything if a value is outside.
+ *  - Results are deterministic: the same inputs give bitwise the same outputs.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *kda_stream_t; /* the same type as cudaStream_t */
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_NULL = -1,        /* a required pointer (or the descriptor) is NULL      */
+  KDA_ERR_SHAPE = -2,       /* a size is out of the supported set                  */
+  KDA_ERR_DTYPE = -3,       /* unsupported dtype combination                       */
+  KDA_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned                    */
+  KDA_ERR_RANGE = -5,       /* validate mode found a value outside its range       */
+  KDA_ERR_CUDA = -6,        /* a CUDA call or kernel launch failed                 */
+  KDA_ERR_UNSUPPORTED = -7, /* a kernel choice that does not cover these arguments */
+  KDA_ERR_ALIAS = -8        /* forbidden aliasing between arguments                */
+} kda_status;
+
+/* Which prefill kernel runs.  AUTO picks the tensor-core kernel when it covers
+ * the arguments (bf16 q/k/v, bf16 out, dk = dv = 128, chunk = 64) and the
+ * CUDA-core kernel otherwise.  Asking for TC on arguments it does not cover
+ * returns KDA_ERR_UNSUPPORTED. */
+typedef enum { KDA_KERNEL_AUTO = 0, KDA_KERNEL_SIMT = 1, KDA_KERNEL_TC = 2 } kda_kernel;
+
+typedef struct {
+  int B;          /* batch; must be 1 when cu_seqlens is given                */
+  int T;          /* tokens per sequence, or total tokens when varlen          */
+  int H;          /* heads                                                    */
+  int dk, dv;     /* key and value head dims: each one of 16, 32, 64, 128      */
+  int chunk;      /* chunk length C: 16, 32 or 64 (outputs do not depend on it
+                     beyond rounding)                                          */
+  int num_seqs;   /* varlen: number of sequences N (cu_seqlens has N+1 entries);
+                     0 when cu_seqlens is NULL                                 */
+  kda_dtype qkv_dtype;  /* q, k, v                                             */
+  kda_dtype out_dtype;  /* out                                                 */
+  kda_dtype gate_dtype; /* log_alpha and beta                                  */
+  int validate;   /* 1: range-check inputs first (synchronises the stream)     */
+  kda_kernel kernel;
+  int segments;   /* long sequences: split each sequence into this many
+                     segments that run in parallel and are joined through
+                     their affine pairs; 0 = choose automatically, 1 = never  */
+} kda_chunk_desc;
+
+/*
+ * kda_chunk_fwd - chunked prefill ([K3-notes §2.2, chunkwise form];
+ * initial/final state for prefix-cache resume, [K3-notes §2.5, Fig. 12]).
+ *
+ *   q, k        [B*T, H, dk]  qkv_dtype   (token-major; B sequences of T
+ *                                          tokens, or N packed sequences)
+ *   v           [B*T, H, dv]  qkv_dtype
+ *   log_alpha   [B*T, H, dk]  gate_dtype  (g = ln alpha, per channel)
+ *   beta        [B*T, H]      gate_dtype
+ *   initial_state [Nseq, H, dk, dv] fp32, or NULL for zeros
+ *   cu_seqlens  [N+1] int32 (varlen: sequence n is tokens
+ *               [cu_seqlens[n], cu_seqlens[n+1]) ), or NULL for B x T
+ *   out         [B*T, H, dv]  out_dtype   (written)
+ *   final_state [Nseq, H, dk, dv] fp32, or NULL (written)
+ * Nseq = num_seqs when varlen, else B.  An empty sequence leaves its
+ * final state equal to its initial state.  initial_state may equal
+ * final_state (in-place resume); out may not alias any input.
+ * When the planner splits long sequences into segments it allocates a
+ * stream-ordered workspace (cudaMallocAsync/cudaFreeAsync on `stream`); use
+ * kda_chunk_fwd_ex to pass one instead.
+ */
+kda_status kda_chunk_fwd(const kda_chunk_desc *desc, const void *q, const void *k, const void *v,
+                         const void *log_alpha, const void *beta, const float *initial_state,
+                         const int32_t *cu_seqlens, void *out, float *final_state,
+                         kda_stream_t stream);
+
+/* Bytes of device workspace kda_chunk_fwd_ex needs for these arguments (0 when
+ * no sequence is split).  Host-only; launches nothing. */
+kda_status kda_chunk_fwd_workspace_size(const kda_chunk_desc *desc, size_t *bytes);
+
+/* kda_chunk_fwd with a caller-owned device workspace of at least
+ * kda_chunk_fwd_workspace_size bytes (16-byte aligned; NULL allowed when that
+ * size is 0).  The workspace must not be in use by another call in flight. */
+kda_status kda_chunk_fwd_ex(const kda_chunk_desc *desc, const void *q, const void *k,
+                            const void *v, const void *log_alpha, const void *beta,
+                            const float *initial_state, const int32_t *cu_seqlens, void *out,
+                            float *final_state, void *workspace, size_t workspace_bytes,
+                            kda_stream_t stream);
+
+typedef struct {
+  int N;          /* independent sequences, one token each                    */
+  int H;          /* heads                                                    */
+  int dk, dv;     /* each one of 16, 32, 64, 128                              */
+  kda_dtype qkv_dtype, out_dtype, gate_dtype;
+  int validate;   /* 1: range-check inputs first (synchronises the stream)     */
+} kda_decode_desc;
+
+/*
+ * kda_decode_step - one token of the recurrence for N sequences, updating
+ * their states in place ([K3-notes §2.2, KDA state recurrence]; the decode
+ * regime of [K3-notes §2.5]).
+ *
+ *   q, k        [N, H, dk]  qkv_dtype
+ *   v           [N, H, dv]  qkv_dtype
+ *   log_alpha   [N, H, dk]  gate_dtype
+ *   beta        [N, H]      gate_dtype
+ *   state_inout [N, H, dk, dv] fp32, read and overwritten
+ *   out         [N, H, dv]  out_dtype, written
+ * state_inout may not alias out or any input.
+ */
+kda_status kda_decode_step(const kda_decode_desc *desc, const void *q, const void *k,
+                           const void *v, const void *log_alpha, const void *beta,
+                           float *state_inout, void *out, kda_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char *kda_status_string(kda_status status);
+
+/* The last CUDA error string seen by this thread's most recent failing call,
+ * or "" (never NULL). */
+const char *kda_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,110 @@
+"""The C ABI on the CPU: the library loads, exports every declared symbol, and
+rejects bad arguments synchronously (before any CUDA call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from hybrid_linear_attention_chunk_gb300 import _lib
+    return _lib.load()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("kda_chunk_fwd", "kda_decode_step", "kda_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_symbols():
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for s in range(-8, 1):
+        assert lib.kda_status_string(s)
+    assert lib.kda_last_cuda_error() is not None
+
+
+def _desc(**kw):
+    from hybrid_linear_attention_chunk_gb300._lib import KdaChunkDesc
+    d = KdaChunkDesc()
+    vals = dict(B=1, T=128, H=2, dk=64, dv=64, chunk=64, num_seqs=0, qkv_dtype=1, out_dtype=1,
+                gate_dtype=0, validate=0, kernel=0, segments=0)
+    vals.update(kw)
+    for k, v in vals.items():
+        setattr(d, k, v)
+    return d
+
+
+FAKE = 1 << 20  # a 16-byte aligned fake device address: never dereferenced
+
+
+def _call(lib, d, **ptrs):
+    p = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, g=FAKE * 4, b=FAKE * 5, s0=None, cu=None, o=FAKE * 6,
+             sT=None)
+    p.update(ptrs)
+    P = ctypes.c_void_p
+    return lib.kda_chunk_fwd(ctypes.byref(d), P(p["q"]), P(p["k"]), P(p["v"]), P(p["g"]), P(p["b"]),
+                             P(p["s0"]), P(p["cu"]), P(p["o"]), P(p["sT"]), None)
+
+
+def test_argument_errors_are_synchronous(lib):
+    assert lib.kda_chunk_fwd(None, None, None, None, None, None, None, None, None, None, None) == -1
+    assert _call(lib, _desc(), q=None) == -1
+    assert _call(lib, _desc(dk=48)) == -2
+    assert _call(lib, _desc(chunk=128)) == -2
+    assert _call(lib, _desc(H=0)) == -2
+    assert _call(lib, _desc(qkv_dtype=7)) == -3
+    assert _call(lib, _desc(), k=FAKE * 2 + 4) == -4
+    assert _call(lib, _desc(B=2), cu=FAKE * 9) == -2          # varlen needs B == 1
+    assert _call(lib, _desc(num_seqs=3)) == -2                # num_seqs without cu_seqlens
+    assert _call(lib, _desc(), o=FAKE * 3) == -8              # out aliases v
+    assert _call(lib, _desc(segments=-1)) == -2
+
+
+def test_decode_argument_errors(lib):
+    from hybrid_linear_attention_chunk_gb300._lib import KdaDecodeDesc
+    d = KdaDecodeDesc()
+    d.N, d.H, d.dk, d.dv, d.qkv_dtype, d.out_dtype, d.gate_dtype, d.validate = 4, 2, 128, 128, 1, 1, 0, 0
+    P = ctypes.c_void_p
+    ok = [P(FAKE * i) for i in range(1, 8)]
+    assert lib.kda_decode_step(ctypes.byref(d), *ok[:6], None, None) == -1
+    bad = list(ok)
+    bad[5] = P(FAKE * 1)  # state aliases q
+    assert lib.kda_decode_step(ctypes.byref(d), *bad, None) == -8
+    d.dv = 100
+    assert lib.kda_decode_step(ctypes.byref(d), *ok, None) == -2
+
+
+def test_workspace_size_is_host_only(lib):
+    n = ctypes.c_size_t(123)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(_desc()), ctypes.byref(n)) == 0
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "hybrid_linear_attention_chunk_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in src and "from oracle" not in src, fn
+                assert "kda_oracle" not in src, fn
