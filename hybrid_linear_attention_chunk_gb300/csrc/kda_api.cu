@@ -19,6 +19,8 @@ kda_status cuda_fail(cudaError_t e) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool aligned_to(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
 bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 bool dtype_ok(kda_dtype t) { return t == KDA_F32 || t == KDA_BF16; }
@@ -111,9 +113,14 @@ kda_status check_prefill(const kda_chunk_desc *d, const void *q, const void *k, 
   }
   const long long T_total = cu ? (long long)d->T : (long long)d->B * d->T;
   if (T_total * d->H * (d->dk > d->dv ? d->dk : d->dv) >= (1LL << 40)) return KDA_ERR_SHAPE;
-  const void *ptrs[] = {q, k, v, g, beta, s0, cu, out, sT};
-  for (const void *p : ptrs)
-    if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+  // q, k, v, log_alpha and out are tiled with bulk copies / 16-byte vectors;
+  // beta, the states and cu_seqlens only need their element alignment.
+  const void *ptrs16[] = {q, k, v, g, out};
+  for (const void *p : ptrs16)
+    if (!aligned16(p)) return KDA_ERR_ALIGN;
+  const void *ptrs4[] = {beta, s0, cu, sT};
+  for (const void *p : ptrs4)
+    if (p && !aligned_to(p, 4)) return KDA_ERR_ALIGN;
   const int Nseq = cu ? d->num_seqs : d->B;
   const size_t th = (size_t)T_total * d->H;
   Range r_out = span(out, th * d->dv * esize(d->out_dtype));
@@ -212,9 +219,12 @@ kda_status kda_decode_step(const kda_decode_desc *d, const void *q, const void *
     return KDA_ERR_DTYPE;
   if (d->N <= 0 || d->H <= 0 || !dim_ok(d->dk) || !dim_ok(d->dv)) return KDA_ERR_SHAPE;
   if ((long long)d->N * d->H >= (1LL << 31)) return KDA_ERR_SHAPE;
-  const void *ptrs[] = {q, k, v, log_alpha, beta, state_inout, out};
-  for (const void *p : ptrs)
-    if (!aligned16(p)) return KDA_ERR_ALIGN;
+  // the state is streamed as 16-byte vectors; the rest needs element alignment
+  if (!aligned16(state_inout)) return KDA_ERR_ALIGN;
+  if (!aligned_to(q, esize(d->qkv_dtype)) || !aligned_to(k, esize(d->qkv_dtype)) ||
+      !aligned_to(v, esize(d->qkv_dtype)) || !aligned_to(out, esize(d->out_dtype)) ||
+      !aligned_to(log_alpha, esize(d->gate_dtype)) || !aligned_to(beta, esize(d->gate_dtype)))
+    return KDA_ERR_ALIGN;
   const size_t nh = (size_t)d->N * d->H;
   Range r_s = span(state_inout, nh * d->dk * d->dv * 4);
   Range r_o = span(out, nh * d->dv * esize(d->out_dtype));
@@ -256,5 +266,13 @@ const char *kda_status_string(kda_status s) {
 }
 
 const char *kda_last_cuda_error(void) { return g_last_cuda_error; }
+
+kda_status kda_device_watchdog(unsigned int *flags, int clear) {
+  if (!flags) return KDA_ERR_NULL;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = read_tc_watchdog(flags, clear != 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KDA_OK;
+}
 
 }  // extern "C"

@@ -46,6 +46,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_chunk_simt(const PrefillArgs &a, cudaStream_t s);
 bool chunk_tc_supports(const PrefillArgs &a);
 cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s);
+cudaError_t read_tc_watchdog(unsigned int *flags, bool clear);
 cudaError_t launch_validate_prefill(const PrefillArgs &a, int *d_flag, cudaStream_t s);
 cudaError_t launch_validate_decode(const DecodeArgs &a, int *d_flag, cudaStream_t s);
 

@@ -14,9 +14,12 @@
  * Conventions shared by every call
  * --------------------------------
  *  - All tensor pointers are DEVICE pointers owned by the caller; the library
- *    keeps no pointer after the call returns.  Every pointer must be 16-byte
- *    aligned (KDA_ERR_ALIGN otherwise).  Tensors are dense and row-major in
- *    the shapes written below (last index contiguous).
+ *    keeps no pointer after the call returns.  Alignment (KDA_ERR_ALIGN
+ *    otherwise): kda_chunk_fwd needs q, k, v, log_alpha and out 16-byte
+ *    aligned and the other pointers 4-byte aligned; kda_decode_step needs
+ *    state_inout 16-byte aligned and the other pointers aligned to their
+ *    element size.  Tensors are dense and row-major in the shapes written
+ *    below (last index contiguous).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and the call returns without waiting, except in validate mode.
  *  - Argument errors are reported synchronously, before anything is launched,
@@ -152,6 +155,14 @@ const char *kda_status_string(kda_status status);
 /* The last CUDA error string seen by this thread's most recent failing call,
  * or "" (never NULL). */
 const char *kda_last_cuda_error(void);
+
+/* The tensor-core prefill bounds every wait on its internal barriers (2 s).
+ * A wait that runs out makes the kernel abandon its work, release what it
+ * holds and OR a bit into a per-device word; the outputs of that call are
+ * then undefined.  This call waits for the current device to go idle
+ * (cudaDeviceSynchronize), stores that word in *flags (0 = no time-out since
+ * it was last cleared) and clears it when `clear` is non-zero. */
+kda_status kda_device_watchdog(unsigned int *flags, int clear);
 
 #ifdef __cplusplus
 }
