@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on GB300: chunked prefill and decode step.
+
+Prints ONE JSON line (rank 0).  The headline workload is the bf16 batch
+prefill B=4, H=32, T=8192, d=128, C=64 (fp32 log-decay and beta, zero initial
+state): `value` is prefill tokens/s over all ranks.  One step = one
+kda_chunk_fwd call over the whole batch.  The decode workload (N=256, H=32,
+d=128, fp32 state, 1000 consecutive steps) is reported beside it in
+`decode` as state GB/s and sequence-steps/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the correctness reference, not a
+tuned CPU implementation) on the host cores, on a bounded sample of the same
+workload, and prints the same line with "impl": "reference".
+
+Under torchrun each rank runs its own copy of the workload (independent
+problems: weak scaling, no collective in the data path); the step time is the
+maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=32,d=128) & decode state GB/s vs roofline, 1×GB300"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_SRC = os.path.join(ROOT, "hybrid_linear_attention_chunk_gb300", "csrc", "kda_chunk_tc.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kda_chunk_tc_prefill_B4_H32_T8192.traffic.txt")
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def source_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the prefill kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if "=" in line and not line.startswith("#"):
+                    k, v = line.strip().split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha") != source_sha(PREFILL_SRC):
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while work runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ workload sizes
+
+def prefill_bytes(B, T, H, dk, dv, qkv_bytes=2, gate_bytes=4, out_bytes=2, state_in=False):
+    tok = B * T * H
+    b = tok * (2 * dk + dv) * qkv_bytes + tok * dk * gate_bytes + tok * gate_bytes + tok * dv * out_bytes
+    b += B * H * dk * dv * 4 * (2 if state_in else 1)
+    return b
+
+
+def prefill_flops(B, T, H, d, C):
+    # 6 d^2 + 10 C d per (token, head): the dense contractions of the chunk form
+    return B * T * H * (6 * d * d + 10 * C * d)
+
+
+def decode_bytes(N, H, dk, dv):
+    nh = N * H
+    return nh * dk * dv * 4 * 2 + nh * (2 * dk + dv) * 2 + nh * dk * 4 + nh * 4 + nh * dv * 2
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import hybrid_linear_attention_chunk_gb300 as kda
+    from hybrid_linear_attention_chunk_gb300 import inputs
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    kda.load()
+    hbm_peak, tc_peak, peak_kind = load_peaks()
+
+    w = inputs.PREFILL_B4_T8K
+    x = inputs.make_prefill(w, device=dev, seed=inputs.SEED_BASE + w.seed_index + 1000 * rank)
+    q, k, v, g, beta = x["q"], x["k"], x["v"], x["log_alpha"], x["beta"]
+    out = torch.empty(w.B * w.T, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    sT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.kda_chunk_fwd(q, k, v, g, beta, None, None, out, sT, B=w.B, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    ms_local = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    ms = reduce_max(ms_local, world, dev)
+    ms_step = ms / args.steps
+    tokens = w.B * w.T
+    value = world * tokens / (ms_step * 1e-3)
+
+    # roofline of the prefill kernel (one launch per step, events on its stream)
+    alg_bytes = prefill_bytes(w.B, w.T, w.H, w.dk, w.dv)
+    achieved = alg_bytes / (ms_local / args.steps * 1e-3) / 1e9
+    traffic = profiled_traffic()
+    flops = prefill_flops(w.B, w.T, w.H, w.dk, w.chunk)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} hbm_gbs",
+                "kernel": "chunk_tc_kernel", "algorithmic_bytes_per_launch": alg_bytes,
+                "tensor_tflops": round(flops / (ms_local / args.steps * 1e-3) / 1e12, 1),
+                "tensor_frac_of_bf16_peak": round(flops / (ms_local / args.steps * 1e-3) / 1e12 / tc_peak, 4)}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hg, hb = (t.cpu().pin_memory() for t in (q, k, v, g, beta))
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hs = torch.empty(sT.shape, dtype=sT.dtype).pin_memory()
+        dq, dk_, dv_, dg, db = (torch.empty_like(t) for t in (q, k, v, g, beta))
+        e2e_steps = max(3, min(20, args.steps // 20))
+
+        def e2e_step():
+            for d_, h_ in ((dq, hq), (dk_, hk), (dv_, hv), (dg, hg), (db, hb)):
+                d_.copy_(h_, non_blocking=True)
+            kda.kda_chunk_fwd(dq, dk_, dv_, dg, db, None, None, out, sT, B=w.B, stream=stream)
+            ho.copy_(out, non_blocking=True)
+            hs.copy_(sT, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        t0 = time.perf_counter()
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = reduce_max(ev0.elapsed_time(ev1), world, dev) / e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in (q, k, v, g, beta))
+        d2h = out.numel() * out.element_size() + sT.numel() * sT.element_size()
+        e2e = {"value": round(world * tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps, "api": "kda_chunk_fwd via ctypes, pinned host buffers"}
+        del hq, hk, hv, hg, hb, dq, dk_, dv_, dg, db
+
+    # decode: 1000 consecutive steps of the N=256 workload
+    dw = inputs.DECODE_N256
+    dsteps = args.decode_steps
+    dec = None
+    if dsteps > 0:
+        dx = inputs.make_decode(dw, steps=dsteps, device=dev, seed=inputs.SEED_BASE + dw.seed_index + 1000 * rank)
+        state = dx["state"]
+        dout = torch.empty(dsteps, dw.N, dw.H, dw.dv, dtype=torch.bfloat16, device=dev)
+        views = [tuple(dx[n][t] for n in ("q", "k", "v", "log_alpha", "beta")) for t in range(dsteps)]
+
+        def dstep(t):
+            kda.kda_decode_step(*views[t], state, dout[t], stream=stream)
+
+        for t in range(min(3, dsteps)):
+            dstep(t)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        ev0.record(stream)
+        for t in range(dsteps):
+            dstep(t)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        dms_local = ev0.elapsed_time(ev1)
+        dms = reduce_max(dms_local, world, dev)
+        per = dms / dsteps
+        db_ = decode_bytes(dw.N, dw.H, dw.dk, dw.dv)
+        gbs = db_ / (dms_local / dsteps * 1e-3) / 1e9
+        dec = {"workload": dw.name, "steps": dsteps, "us_per_step": round(per * 1e3, 2),
+               "state_gbs": round(world * db_ / (per * 1e-3) / 1e9, 1),
+               "seq_steps_per_s": round(world * dw.N / (per * 1e-3), 1),
+               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                            "frac": round(gbs / hbm_peak, 4), "kernel": "decode_d128_kernel",
+                            "algorithmic_bytes_per_launch": db_},
+               "launches": dsteps}
+        del dx, views
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), log_alpha U[ln0.5,-1e-3], beta sigmoid(N(0,1)))",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk, "qkv": "bf16", "gates": "fp32", "state": "fp32, zero initial",
+                       "out": "bf16", "kernel": "tcgen05 chunk_tc_kernel",
+                       "l2": "inputs 1.62 GB per step > 129 MB L2: no flush"},
+            "roofline": roofline,
+            "gpu_launches": args.steps,
+            "e2e": e2e,
+            "decode": dec,
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, x, seconds=args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------- oracle on the host
+
+def cpu_baseline(w, x, seconds=12.0):
+    """The fp64 oracle (as it stands) on host cores over a bounded sample of the
+    workload: whole (sequence, head) chains of T tokens."""
+    import numpy as np
+    import oracle
+    from hybrid_linear_attention_chunk_gb300 import inputs
+
+    cores = os.cpu_count() or 1
+    T = w.T
+
+    def run_chains(nchains):
+        # chains 0..nchains-1 in (sequence, head) order; host copies of just those
+        nh = min(w.H, nchains)
+        ns = (nchains + w.H - 1) // w.H
+        hs = {name: inputs.host_f32(x[name][: ns * T, :nh].contiguous())
+              for name in ("q", "k", "v", "log_alpha", "beta")}
+        cu = np.arange(ns + 1, dtype=np.int64) * T
+        t0 = time.perf_counter()
+        oracle.recurrent(hs["q"], hs["k"], hs["v"], hs["log_alpha"], hs["beta"], None, cu,
+                         chains=list(range(nchains)), nthreads=cores, want_o=True)
+        return time.perf_counter() - t0
+
+    # calibrate with one chain, then fill ~`seconds` across all cores
+    t1 = run_chains(1)
+    nchains = int(max(1, min(w.B * w.H, round(seconds / max(t1, 1e-3) * cores))))
+    if nchains > w.H:
+        nchains = (nchains // w.H) * w.H
+    dt = run_chains(nchains)
+    tok_equiv = nchains * T / w.H  # tokens (all heads) of work done
+    return {"value": round(tok_equiv / dt, 2), "unit": "tokens/s", "cores": min(cores, nchains),
+            "kind": "oracle",
+            "sample": f"{nchains} of {w.B * w.H} (sequence, head) chains of {w.name}, full length {T}; "
+                      f"value = chains*T/H tokens per second; {dt:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import torch
+    from hybrid_linear_attention_chunk_gb300 import inputs
+
+    w = inputs.PREFILL_B4_T8K
+    cores = os.cpu_count() or 1
+    # a bounded slice of the workload: `cores` heads of sequence 0, first L tokens
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    L0 = 512
+    xs = inputs.make_prefill(inputs.scaled(w, B=1, H=min(cores, w.H)), device=dev)
+    hs = {n: inputs.host_f32(xs[n]) for n in ("q", "k", "v", "log_alpha", "beta")}
+
+    def one(L):
+        cu = np.array([0, L], dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.recurrent(hs["q"][:L], hs["k"][:L], hs["v"][:L], hs["log_alpha"][:L], hs["beta"][:L],
+                         None, cu, nthreads=cores)
+        return time.perf_counter() - t0
+
+    t_cal = one(L0)
+    budget = 90.0 / max(1, args.steps + args.warmup)  # whole run within ~2 minutes
+    L = int(min(w.T, max(16, L0 * budget / max(t_cal, 1e-4))))
+    for _ in range(args.warmup):
+        one(L)
+    times = [one(L) for _ in range(args.steps)]
+    dt = sum(times)
+    heads = hs["q"].shape[1]
+    tokens = args.steps * L * heads / w.H
+    value = tokens / dt
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"per step: {heads} heads x {L} tokens of sequence 0 "
+                                       f"(value = tokens*heads/H per second)"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
