@@ -12,14 +12,22 @@
 //   M1  [A ; L''] = [Q o Gamma ; Gamma o K] (K / Gamma)^T      (M=128 N=64 K=128)
 //   A  = Tril_incl(A), L = StrictTril(diag(beta) L'')
 //   T_b = (I + L)^{-1} diag(beta)   blocked forward substitution on CUDA cores
-//   M2  [0 | U^T] = V^T [0 ; T_b]^T                              (M=128 N=128 K=64)
+//   M2  U^T = V^T T_b^T                                          (M=128 N=64 K=64)
 //   M3  W^T = (Gamma o K)^T T_b^T                                (M=128 N=64 K=64)
-//   M4  [O^T | V~^T] += S^T [Q o Gamma ; -W]^T                   (M=128 N=128 K=128)
+//   M4  V~^T = U^T - S^T W^T ;  O^T = S^T (Q o Gamma)^T          (M=128 N=64 K=128, twice)
 //   M5  O^T += V~^T A^T                                          (M=128 N=64 K=64)
-//   M6  D = V~^T (K o gamma_C / Gamma)                           (M=128 N=128 K=64)
-//   S^T <- S^T Diag(gamma_C) + D     (fp32 master state kept in TMEM)
+//   S^T <- S^T Diag(gamma_C)           (fp32 master state in TMEM, scaled in place)
+//   M6  S^T += V~^T (K o gamma_C / Gamma)                        (M=128 N=128 K=64)
 // Every product is computed transposed so that M = 128 (dv or dk) and the
 // tensor core runs at full width; TMEM lane j holds row j of the result.
+//
+// Two warp groups overlap consecutive chunks.  The chunk group (warps 0-7)
+// runs one chunk ahead: decay prologue, M1, the UT solve, M2/M3.  The state
+// group (warps 8-11) runs the serial state chain: -W staging, M4, V~ staging,
+// the gamma scaling, M5/M6, the bf16 state copy and the output.  Operands the
+// state group still reads while the chunk group prepares the next chunk are
+// double-buffered by chunk parity.  Thread 0 of each group issues that
+// group's MMAs and the chunk group's thread 0 issues the TMA loads of V.
 //
 // Range guard ([K3-notes §2.2, Eq. 5 and Fig. 3]): with log-decay >= -5 a
 // 16-token tile sums to >= -80.  If every channel's chunk total G_C is >= -80
@@ -29,12 +37,9 @@
 // query-side factors are <= 1 (rows before the tile are zeroed) and key-side
 // factors are <= e^{80}.
 //
-// Warp roles: warps 0-7 (256 threads) do the decay prologue, the solve and
-// the TMEM epilogues; warp 8 allocates TMEM and issues the TMA loads of V;
-// warp 9 issues the MMAs.  Hand-offs go through mbarriers; every wait is
-// bounded (a 2 s watchdog), and on a time-out all roles leave their loops,
-// drain outstanding copies and MMAs, free TMEM and return with an error bit
-// set in a device word the host can read.
+// Every wait on an mbarrier is bounded (2 s).  On a time-out both groups
+// leave their loops, drain their MMAs and copies, free TMEM and return with a
+// bit set in a device word the host can read (kda_device_watchdog).
 #include <cudaTypedefs.h>
 
 #include "kda_internal.cuh"
@@ -49,53 +54,52 @@ using namespace sm100;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 320;
-constexpr int kMathThreads = 256;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 384;
+constexpr int kChunkThreads = 256;  // warps 0-7
+constexpr int kStateThreads = 128;  // warps 8-11
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSingleRefBound2 = kSingleRefBound * kLog2e;  // the -80 bound in log2 units
 
-// Shared-memory map (byte offsets from a 1024-aligned base).
-constexpr uint32_t OFF_QG = 0;        // [Q o Gamma ; Gamma o K -> -W]: 128 rows x 128, 2 K-halves
-constexpr uint32_t OFF_KB = 32768;    // K / Gamma: 64 rows x 128
-constexpr uint32_t OFF_KH = 49152;    // K o gamma_C / Gamma: 64 rows x 128 (MN-major B of M6)
-constexpr uint32_t OFF_ZT = 65536;    // [0 ; T_b]: 128 rows x 64
-constexpr uint32_t OFF_ST = 81920;    // S^T bf16: 128 rows x 128
-constexpr uint32_t OFF_VT = 114688;   // V~^T bf16: 128 rows x 64; also the output staging tile
-constexpr uint32_t OFF_V0 = 131072;   // V tile stage 0 (TMA): 64 rows x 128
-constexpr uint32_t OFF_V1 = 147456;   // V tile stage 1
-constexpr uint32_t OFF_AM = 163840;   // A bf16: 64 rows x 64
-constexpr uint32_t OFF_LF = 172032;   // L fp32 [64][65]
-constexpr uint32_t OFF_TF = 188672;   // T fp32 [64][65]
-constexpr uint32_t OFF_XF = 205312;   // solve scratch fp32 [3][16][17]
-constexpr uint32_t OFF_CTL = 208640;  // control block (below)
+// Shared-memory map (byte offsets from a 1024-aligned base).  "x2" buffers
+// are indexed by chunk parity.
+constexpr uint32_t OFF_QG = 0;        // x2 32 KB: [Q o Gamma ; Gamma o K], 128 rows x 128, two K-halves;
+                                      //   rows 64..127 later hold -W^T (MN-major) for the state group
+constexpr uint32_t OFF_KB = 65536;    // 16 KB: K / Gamma, 64 rows x 128; then L (fp32 64x64) in the solve
+constexpr uint32_t OFF_KH = 81920;    // x2 16 KB: K o gamma_C / Gamma (MN-major B of M6)
+constexpr uint32_t OFF_AM = 114688;   // x2 8 KB: A bf16, 64 rows x 64
+constexpr uint32_t OFF_ZT = 131072;   // 8 KB: T_b bf16, 64 rows x 64
+constexpr uint32_t OFF_TF = 139264;   // 16 KB: T fp32 64x64
+constexpr uint32_t OFF_XF = 155648;   // 4 KB: solve scratch fp32 [3][16][17]
+constexpr uint32_t OFF_V = 159744;    // 16 KB: V tile (TMA), 64 rows x 128 as two 64-column boxes
+constexpr uint32_t OFF_ST = 176128;   // 32 KB: S^T bf16, 128 rows x 128
+constexpr uint32_t OFF_VT = 208896;   // 16 KB: V~^T bf16 128 rows x 64; also the output staging tile
+constexpr uint32_t OFF_CTL = 225280;  // 4 KB control block
 constexpr uint32_t SMEM_USED = OFF_CTL + 4096;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
-constexpr int LDF = 65;                            // fp32 row stride of L and T
 
-// TMEM columns (512 allocated; lane = row of each transposed product).
-constexpr uint32_t TM_D1 = 0;     // M1 result, later M3 (W^T)
-constexpr uint32_t TM_O = 64;     // O^T accumulator (M2 zeroes it; M4, M5 add)
-constexpr uint32_t TM_U = 128;    // U^T, then V~^T after M4
-constexpr uint32_t TM_D6 = 192;   // M6 result
-constexpr uint32_t TM_S = 320;    // fp32 master state S^T
+// TMEM columns (512 allocated).
+constexpr uint32_t TM_D1 = 0;     // M1 result (chunk group)
+constexpr uint32_t TM_W = 64;     // M3 result W^T (read by the state group)
+constexpr uint32_t TM_U = 128;    // x2 64: U^T, V~^T after M4 (by chunk parity)
+constexpr uint32_t TM_O = 256;    // O^T accumulator
+constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
-  B_PREP = 0, B_M1, B_SOLVE, B_M23, B_W, B_M4, B_E4, B_M56, B_VFULL0, B_VFULL1, B_VEMPTY0,
-  B_VEMPTY1, B_TEARDOWN, B_COUNT
+  B_M1 = 0, B_M23, B_VFULL, B_READY0, B_READY1, B_FREE0, B_FREE1, B_WFREE, B_M4, B_M56,
+  B_TD_C, B_TD_S, B_COUNT
 };
 
 struct Ctl {
   uint64_t bar[16];
+  float gam[2][128];     // gamma_C per channel, by chunk parity
   float bs[64];          // beta of the chunk's rows (0 past the end)
-  float gam[128];        // gamma_C per channel
   float tot[4][128];     // per-16-row-group log2-decay sums
   uint32_t tmem_slot;
-  int abort;             // any role gave up
+  int abort;             // any thread gave up
   int nb;                // M1 rounds for the current chunk (1 or 4)
-  int slow[2];           // range-guard vote, double-buffered by chunk parity
-  int go[2];             // math-group wait result, double-buffered
+  int slow[2];           // range-guard vote, by chunk parity
+  int go_c[2];           // chunk-group wait verdicts (double-buffered)
+  int go_s[2];           // state-group wait verdicts
 };
 static_assert(sizeof(Ctl) <= 4096, "control block");
 
@@ -120,15 +124,19 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
   return __bfloat1622float2(v);
 }
 
-// Named barrier 1 over the 256 math threads (warps reconverged first).
-__device__ __forceinline__ void math_bar() {
-  __syncwarp();
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-}
-
 // a[i] for a runtime i without spilling the array to local memory
 __device__ __forceinline__ float pick4(const float (&a)[4], int i) {
   return i == 0 ? a[0] : (i == 1 ? a[1] : (i == 2 ? a[2] : a[3]));
+}
+
+// Named barriers: 1 = chunk group (256 threads), 2 = state group (128).
+__device__ __forceinline__ void bar_chunk() {
+  __syncwarp();
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+__device__ __forceinline__ void bar_state() {
+  __syncwarp();
+  asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
 __device__ __forceinline__ void st_shared_u32(uint8_t *p, uint32_t v) {
@@ -148,7 +156,7 @@ __device__ __forceinline__ void st_row16_bf16(uint8_t *tile, uint32_t row, uint3
                pack_bf16(v[12], v[13]), pack_bf16(v[14], v[15]));
 }
 
-// Inputs of one chunk held in registers by a math thread: channel pair
+// Inputs of one chunk held in registers by a chunk-group thread: channel pair
 // (2p, 2p+1), rows [16 rg, 16 rg + 16).
 struct Prefetch {
   uint32_t q[16], k[16];
@@ -157,7 +165,7 @@ struct Prefetch {
 };
 
 __device__ __forceinline__ void prefetch_chunk(Prefetch &pf, const PrefillArgs &a, int h, int t0, int len,
-                                               int p, int rg, int mtid) {
+                                               int p, int rg, int ctid) {
   const int H = a.H;
   const uint32_t *q = reinterpret_cast<const uint32_t *>(a.q);
   const uint32_t *k = reinterpret_cast<const uint32_t *>(a.k);
@@ -177,41 +185,100 @@ __device__ __forceinline__ void prefetch_chunk(Prefetch &pf, const PrefillArgs &
     }
   }
   pf.beta = 0.f;
-  if (mtid < kC && mtid < len) pf.beta = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + mtid) * H + h);
+  if (ctid < kC && ctid < len) pf.beta = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + ctid) * H + h);
 }
 
-// The math group's view of an mbarrier wait: thread 0 waits, the group
-// synchronises, and everyone gets the same verdict (so that no thread can
-// leave while others sit in a group barrier).
-__device__ __forceinline__ bool math_wait(Ctl *ctl, int b, uint32_t &phase_bits, int mtid, int &seq,
-                                          unsigned int *err) {
-  const uint32_t parity = (phase_bits >> b) & 1u;
-  if (mtid == 0) {
+// A group-wide view of an mbarrier wait: the group's thread 0 waits, the
+// group synchronises, and every thread gets the same verdict (so no thread
+// can leave while others sit in a group barrier).
+template <bool kChunkGroup>
+__device__ __forceinline__ bool group_wait(Ctl *ctl, int b, uint32_t parity, int gtid, int &seq, unsigned int *err) {
+  int *go = kChunkGroup ? ctl->go_c : ctl->go_s;
+  if (gtid == 0) {
     const bool ok = mbar_wait(smem_u32(&ctl->bar[b]), parity, &ctl->abort, err, 1u << b);
-    ctl->go[seq & 1] = ok && !ctl->abort;
+    go[seq & 1] = ok && !ctl->abort;
   }
-  phase_bits ^= 1u << b;
-  math_bar();
-  const bool go = ctl->go[seq & 1] != 0;
+  if (kChunkGroup) bar_chunk(); else bar_state();
+  const bool r = go[seq & 1] != 0;
   ++seq;
   tc_fence_after();
-  return go;
+  return r;
 }
 
-// Publish the group's shared-memory writes to the async proxy and signal.
-__device__ __forceinline__ void math_signal(Ctl *ctl, int b, int mtid) {
-  fence_proxy_async_smem();
-  tc_fence_before();
-  math_bar();
-  if (mtid == 0) mbar_arrive(smem_u32(&ctl->bar[b]));
-}
-
-__device__ __forceinline__ bool one_wait(Ctl *ctl, int b, uint32_t &phase_bits, unsigned int *err) {
-  const uint32_t parity = (phase_bits >> b) & 1u;
-  phase_bits ^= 1u << b;
+// Single-thread wait (used by a group's thread 0 right before it issues).
+__device__ __forceinline__ bool solo_wait(Ctl *ctl, int b, uint32_t parity, unsigned int *err) {
   const bool ok = mbar_wait(smem_u32(&ctl->bar[b]), parity, &ctl->abort, err, 1u << b);
   tc_fence_after();
   return ok;
+}
+
+// The group's shared-memory writes become visible to the tensor core (async
+// proxy) and its TMEM accesses are ordered before what follows the barrier.
+template <bool kChunkGroup>
+__device__ __forceinline__ void group_publish() {
+  fence_proxy_async_smem();
+  tc_fence_before();
+  if (kChunkGroup) bar_chunk(); else bar_state();
+  tc_fence_after();
+}
+
+// ------------------------------------------------------------- MMA batches
+
+__device__ __forceinline__ void issue_m1(uint32_t tbase, uint32_t qg, uint32_t kb, bool acc_first) {
+  constexpr uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
+    const uint32_t kbo = (kk >> 2) * 8192 + (kk & 3) * 32;
+    mma_bf16_ss(tbase + TM_D1, smem_desc_sw128(qg + ka, 16, 1024), smem_desc_sw128(kb + kbo, 16, 1024), id,
+                (kk > 0 || acc_first) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void issue_m23(uint32_t tbase, uint32_t v, uint32_t qg, uint32_t zt, uint32_t tm_u) {
+  constexpr uint32_t id = idesc_bf16_f32(128, 64, 1, 0);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)  // U^T = V^T T_b^T   (A = V, MN-major: 2 blocks of 64 columns)
+    mma_bf16_ss(tbase + tm_u, smem_desc_sw128(v + kk * 2048, 8192, 1024), smem_desc_sw128(zt + kk * 32, 16, 1024),
+                id, kk > 0 ? 1u : 0u);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)  // W^T = (Gamma o K)^T T_b^T   (A = rows 64..127 of QG, MN-major)
+    mma_bf16_ss(tbase + TM_W, smem_desc_sw128(qg + 8192 + kk * 2048, 16384, 1024),
+                smem_desc_sw128(zt + kk * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
+}
+
+// -W^T lives in QG rows 64..127 as an MN-major operand: i in [0,64) in the
+// first K-half's rows 64..127, i in [64,128) in the second's.
+__device__ __forceinline__ uint32_t wt_piece(uint32_t qg, int piece) { return qg + piece * 16384 + 8192; }
+
+__device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t st, uint32_t qg, uint32_t tm_u) {
+  constexpr uint32_t id_w = idesc_bf16_f32(128, 64, 0, 1);
+  constexpr uint32_t id_q = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {  // V~^T = U^T + S^T (-W)^T
+    const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
+    mma_bf16_ss(tbase + tm_u, smem_desc_sw128(st + ka, 16, 1024),
+                smem_desc_sw128(wt_piece(qg, kk >> 2) + (kk & 3) * 2048, 8192, 1024), id_w, 1u);
+  }
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {  // O^T = S^T (Q o Gamma)^T
+    const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
+    mma_bf16_ss(tbase + TM_O, smem_desc_sw128(st + ka, 16, 1024), smem_desc_sw128(qg + ka, 16, 1024), id_q,
+                kk > 0 ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t vt, uint32_t am, uint32_t kh) {
+  constexpr uint32_t id5 = idesc_bf16_f32(128, 64, 0, 0);
+  constexpr uint32_t id6 = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)  // O^T += V~^T A^T
+    mma_bf16_ss(tbase + TM_O, smem_desc_sw128(vt + kk * 32, 16, 1024), smem_desc_sw128(am + kk * 32, 16, 1024),
+                id5, 1u);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)  // S^T += V~^T (K o gamma_C / Gamma)   (B MN-major)
+    mma_bf16_ss(tbase + TM_S, smem_desc_sw128(vt + kk * 32, 16, 1024),
+                smem_desc_sw128(kh + kk * 2048, 8192, 1024), id6, 1u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -226,178 +293,71 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
   int bos, eos;
   seq_range(a, n, bos, eos);
   const int nchunks = (eos - bos + kC - 1) / kC;
+  const size_t sbase = ((size_t)n * H + h) * kD * kD;
 
-  if (warp == kProducerWarp) {
+  if (warp == 0) {
     tmem_alloc(smem_u32(&ctl->tmem_slot), 512);
     tmem_relinquish();
   }
-  if (tid == 0) {
+  if (tid == 32) {
     for (int b = 0; b < B_COUNT; ++b) mbar_init(smem_u32(&ctl->bar[b]), 1);
     ctl->abort = 0;
     ctl->nb = 1;
     ctl->slow[0] = ctl->slow[1] = 0;
-    ctl->go[0] = ctl->go[1] = 0;
+    ctl->go_c[0] = ctl->go_c[1] = ctl->go_s[0] = ctl->go_s[1] = 0;
     fence_mbar_init();
-  }
-  if (tid < kMathThreads) {
-    // rows 0..63 of [0 ; T_b] stay zero for the whole kernel
-    for (int e = tid; e < 8192 / 16; e += kMathThreads)
-      reinterpret_cast<uint4 *>(sm + OFF_ZT)[e] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = ctl->tmem_slot;
+  const uint32_t sm_base = smem_u32(sm);
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmap_v);
-      uint32_t empty_phase = 0;
-      int issued = 0;
-      for (int c = 0; c < nchunks; ++c) {
-        const int stage = c & 1, use = c >> 1;
-        if (use > 0) {
-          const int b = B_VEMPTY0 + stage;
-          const uint32_t parity = (empty_phase >> stage) & 1u;
-          empty_phase ^= 1u << stage;
-          if (!mbar_wait(smem_u32(&ctl->bar[b]), parity, &ctl->abort, A.err, 1u << b)) break;
-        }
-        const uint32_t full = smem_u32(&ctl->bar[B_VFULL0 + stage]);
-        const uint32_t dst = smem_u32(sm + (stage ? OFF_V1 : OFF_V0));
-        mbar_arrive_expect_tx(full, 2 * kC * 64 * 2);
-        tma_load_3d(dst, &tmap_v, full, 0, h, bos + c * kC);
-        tma_load_3d(dst + 8192, &tmap_v, full, 64, h, bos + c * kC);
-        ++issued;
-      }
-      // the last load of each stage must have landed before the CTA retires
-      for (int c = issued - 2 > 0 ? issued - 2 : 0; c < issued; ++c) {
-        const int stage = c & 1, use = c >> 1;
-        volatile int no_abort = 0;
-        mbar_wait(smem_u32(&ctl->bar[B_VFULL0 + stage]), use & 1, &no_abort, A.err, 1u << 16);
-      }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // --------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      uint32_t ph = 0;
-      const uint32_t qg = smem_u32(sm + OFF_QG), kb = smem_u32(sm + OFF_KB), kh = smem_u32(sm + OFF_KH);
-      const uint32_t zt = smem_u32(sm + OFF_ZT), st = smem_u32(sm + OFF_ST), vt = smem_u32(sm + OFF_VT);
-      const uint32_t am = smem_u32(sm + OFF_AM);
-      constexpr uint32_t id_m1 = idesc_bf16_f32(128, 64, 0, 0);
-      constexpr uint32_t id_m2 = idesc_bf16_f32(128, 128, 1, 0);
-      constexpr uint32_t id_m3 = idesc_bf16_f32(128, 64, 1, 0);
-      constexpr uint32_t id_m4 = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t id_m5 = idesc_bf16_f32(128, 64, 0, 0);
-      constexpr uint32_t id_m6 = idesc_bf16_f32(128, 128, 0, 1);
-      for (int c = 0; c < nchunks; ++c) {
-        const int stage = c & 1;
-        if (!one_wait(ctl, B_PREP, ph, A.err)) break;
-        const int nb = ctl->nb;
-        bool ok = true;
-        for (int r = 0; r < nb && ok; ++r) {
-          if (r > 0) ok = one_wait(ctl, B_PREP, ph, A.err);
-          if (!ok) break;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            const uint32_t koffb = (kk >> 2) * 8192 + (kk & 3) * 32;
-            mma_bf16_ss(tbase + TM_D1, smem_desc_sw128(qg + koff, 16, 1024),
-                        smem_desc_sw128(kb + koffb, 16, 1024), id_m1, (kk > 0 || r > 0) ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&ctl->bar[B_M1]));
-        }
-        if (!ok) break;
-        if (!one_wait(ctl, B_SOLVE, ph, A.err)) break;
-        if (!one_wait(ctl, B_VFULL0 + stage, ph, A.err)) break;
-        const uint32_t vs = smem_u32(sm + (stage ? OFF_V1 : OFF_V0));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // M2: [0 | U^T] = V^T [0 ; T_b]^T    (A = V, MN-major; B = [0 ; T_b], K-major)
-          mma_bf16_ss(tbase + TM_O, smem_desc_sw128(vs + kk * 2048, 8192, 1024),
-                      smem_desc_sw128(zt + kk * 32, 16, 1024), id_m2, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // M3: W^T = (Gamma o K)^T T_b^T     (A = rows 64..127 of QG, MN-major)
-          mma_bf16_ss(tbase + TM_D1, smem_desc_sw128(qg + 8192 + kk * 2048, 16384, 1024),
-                      smem_desc_sw128(zt + 8192 + kk * 32, 16, 1024), id_m3, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&ctl->bar[B_M23]));
-        mma_commit(smem_u32(&ctl->bar[B_VEMPTY0 + stage]));
-        if (!one_wait(ctl, B_W, ph, A.err)) break;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // M4: [O^T | V~^T] += S^T [Q o Gamma ; -W]^T
-          const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tbase + TM_O, smem_desc_sw128(st + koff, 16, 1024),
-                      smem_desc_sw128(qg + koff, 16, 1024), id_m4, 1u);
-        }
-        mma_commit(smem_u32(&ctl->bar[B_M4]));
-        if (!one_wait(ctl, B_E4, ph, A.err)) break;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // M5: O^T += V~^T A^T
-          mma_bf16_ss(tbase + TM_O, smem_desc_sw128(vt + kk * 32, 16, 1024),
-                      smem_desc_sw128(am + kk * 32, 16, 1024), id_m5, 1u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // M6: D = V~^T (K o gamma_C / Gamma)   (B MN-major)
-          mma_bf16_ss(tbase + TM_D6, smem_desc_sw128(vt + kk * 32, 16, 1024),
-                      smem_desc_sw128(kh + kk * 2048, 8192, 1024), id_m6, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&ctl->bar[B_M56]));
-      }
-      // every MMA issued above has completed before TMEM is released
-      mma_commit(smem_u32(&ctl->bar[B_TEARDOWN]));
-      volatile int no_abort = 0;
-      mbar_wait(smem_u32(&ctl->bar[B_TEARDOWN]), 0, &no_abort, A.err, 1u << 17);
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------- math group
-    const int mtid = tid;                 // 0..255
+  if (tid < kChunkThreads) {
+    // =========================================================== chunk group
+    // registers: 256 x 200 + 128 x 104 = the launch's 384 x 168
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
+    const int ctid = tid;
     const int qw = warp & 3, ch = warp >> 2;
-    const int p = mtid & 63, rg = mtid >> 6;
-    uint32_t ph = 0;
+    const int p = ctid & 63, rg = ctid >> 6;
     int seq = 0;
-    const size_t sbase = ((size_t)n * H + h) * kD * kD;
-    const int jrow = 32 * qw + lane;      // TMEM lane = row j (or i) of the transposed products
-
-    // initial state -> TMEM (fp32 master) and S^T bf16 operand
-    for (int blk = 0; blk < 4; ++blk) {
-      const int i0 = 64 * ch + 16 * blk;
-      float s[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) s[c] = a.s0 ? a.s0[sbase + (size_t)(i0 + c) * kD + jrow] : 0.f;
-      tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
-      st_row16_bf16(sm + OFF_ST + ch * 16384, jrow, 16 * blk, s);
+    uint32_t ph_m1 = 0, ph_m23 = 0, ph_v = 0;
+    int issued_v = 0, landed_v = 0;
+    if (ctid == 0 && nchunks > 0) {
+      tma_prefetch_desc(&tmap_v);
+      const uint32_t full = smem_u32(&ctl->bar[B_VFULL]);
+      mbar_arrive_expect_tx(full, 2 * kC * 64 * 2);
+      tma_load_3d(sm_base + OFF_V, &tmap_v, full, 0, h, bos);
+      tma_load_3d(sm_base + OFF_V + 8192, &tmap_v, full, 64, h, bos);
+      issued_v = 1;
     }
-    tmem_wait_st();
-
     Prefetch pf;
-    if (nchunks > 0) prefetch_chunk(pf, a, h, bos, min(kC, eos - bos), p, rg, mtid);
+    if (nchunks > 0) prefetch_chunk(pf, a, h, bos, min(kC, eos - bos), p, rg, ctid);
     bool alive = true;
-    for (int c = 0; c < nchunks && alive; ++c) {
-      const int t0 = bos + c * kC;
+    for (int m = 0; m < nchunks && alive; ++m) {
+      const int par = m & 1;
+      const int t0 = bos + m * kC;
       const int len = min(kC, eos - t0);
+      uint8_t *qg = sm + OFF_QG + par * 32768;
+      uint8_t *kh = sm + OFF_KH + par * 16384;
+      if (m >= 2 && !(alive = group_wait<true>(ctl, B_FREE0 + par, ((m >> 1) - 1) & 1, ctid, seq, A.err))) break;
+
       // ---------------- decay prologue: cumulative log2-decay and scaled operands
       float G0[16], G1[16];
-      float a0 = 0.f, a1 = 0.f;
+      {
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        a0 += pf.g[r].x * kLog2e;
-        a1 += pf.g[r].y * kLog2e;
-        G0[r] = a0;
-        G1[r] = a1;
+        for (int r = 0; r < 16; ++r) {
+          a0 += pf.g[r].x * kLog2e;
+          a1 += pf.g[r].y * kLog2e;
+          G0[r] = a0;
+          G1[r] = a1;
+        }
+        ctl->tot[rg][2 * p] = a0;
+        ctl->tot[rg][2 * p + 1] = a1;
       }
-      ctl->tot[rg][2 * p] = a0;
-      ctl->tot[rg][2 * p + 1] = a1;
-      if (mtid < kC) ctl->bs[mtid] = pf.beta;
-      math_bar();
+      if (ctid < kC) ctl->bs[ctid] = pf.beta;
+      bar_chunk();
       float ref0[4], ref1[4], run0 = 0.f, run1 = 0.f;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
@@ -407,43 +367,47 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
         run1 += ctl->tot[b][2 * p + 1];
       }
       const float GC0 = run0, GC1 = run1;
-      const float own0 = pick4(ref0, rg), own1 = pick4(ref1, rg);
+      {
+        const float own0 = pick4(ref0, rg), own1 = pick4(ref1, rg);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        G0[r] += own0;
-        G1[r] += own1;
+        for (int r = 0; r < 16; ++r) {
+          G0[r] += own0;
+          G1[r] += own1;
+        }
       }
+      const float gc0 = ex2(GC0), gc1 = ex2(GC1);
       if (rg == 0) {
-        ctl->gam[2 * p] = ex2(GC0);
-        ctl->gam[2 * p + 1] = ex2(GC1);
+        ctl->gam[par][2 * p] = gc0;
+        ctl->gam[par][2 * p + 1] = gc1;
       }
-      if (GC0 < kSingleRefBound2 || GC1 < kSingleRefBound2) atomicOr(&ctl->slow[c & 1], 1);
-      math_bar();
-      const bool slow = ctl->slow[c & 1] != 0;
-      if (mtid == 0) {
-        ctl->slow[(c + 1) & 1] = 0;
-        ctl->nb = slow ? 4 : 1;
-      }
+      if (GC0 < kSingleRefBound2 || GC1 < kSingleRefBound2) atomicOr(&ctl->slow[par], 1);
+      bar_chunk();
+      const bool slow = ctl->slow[par] != 0;
+      if (ctid == 0) ctl->slow[par ^ 1] = 0;
       const uint32_t half = (uint32_t)(p >> 5), col = (uint32_t)((2 * p) & 63);
-      uint8_t *qg_q = sm + OFF_QG + half * 16384;
-      uint8_t *kb_t = sm + OFF_KB + half * 8192;
-      uint8_t *kh_t = sm + OFF_KH + half * 8192;
+      uint8_t *qg_h = qg + half * 16384;
+      uint8_t *kb_h = sm + OFF_KB + half * 8192;
+      uint8_t *kh_h = kh + half * 8192;
       if (!slow) {
-        const float gc0 = ex2(GC0), gc1 = ex2(GC1);
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
           const uint32_t row = 16 * rg + r;
           const float e0 = ex2(G0[r]), e1 = ex2(G1[r]);
           const float i0 = ex2(-G0[r]), i1 = ex2(-G1[r]);
           const float2 qv = unpack_bf16(pf.q[r]), kv = unpack_bf16(pf.k[r]);
-          st_shared_u32(qg_q + sw128_offset(row, col), pack_bf16(qv.x * e0, qv.y * e1));
-          st_shared_u32(qg_q + sw128_offset(64 + row, col), pack_bf16(kv.x * e0, kv.y * e1));
+          st_shared_u32(qg_h + sw128_offset(row, col), pack_bf16(qv.x * e0, qv.y * e1));
+          st_shared_u32(qg_h + sw128_offset(64 + row, col), pack_bf16(kv.x * e0, kv.y * e1));
           const float kb0 = kv.x * i0, kb1 = kv.y * i1;
-          st_shared_u32(kb_t + sw128_offset(row, col), pack_bf16(kb0, kb1));
-          st_shared_u32(kh_t + sw128_offset(row, col), pack_bf16(kb0 * gc0, kb1 * gc1));
+          st_shared_u32(kb_h + sw128_offset(row, col), pack_bf16(kb0, kb1));
+          st_shared_u32(kh_h + sw128_offset(row, col), pack_bf16(kb0 * gc0, kb1 * gc1));
         }
-        math_signal(ctl, B_PREP, mtid);
-        alive = math_wait(ctl, B_M1, ph, mtid, seq, A.err);
+        group_publish<true>();
+        if (ctid == 0) {
+          issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, false);
+          mma_commit(smem_u32(&ctl->bar[B_M1]));
+        }
+        alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
+        ph_m1 ^= 1u;
       } else {
         for (int b = 0; b < 4 && alive; ++b) {
           const float rb0 = pick4(ref0, b), rb1 = pick4(ref1, b);
@@ -461,12 +425,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
               ba = kv.x * ex2(rb0 - G0[r]);
               bb = kv.y * ex2(rb1 - G1[r]);
             }
-            st_shared_u32(qg_q + sw128_offset(row, col), pack_bf16(qa, qb));
-            st_shared_u32(qg_q + sw128_offset(64 + row, col), pack_bf16(ka, kbv));
-            st_shared_u32(kb_t + sw128_offset(row, col), pack_bf16(ba, bb));
+            st_shared_u32(qg_h + sw128_offset(row, col), pack_bf16(qa, qb));
+            st_shared_u32(qg_h + sw128_offset(64 + row, col), pack_bf16(ka, kbv));
+            st_shared_u32(kb_h + sw128_offset(row, col), pack_bf16(ba, bb));
           }
-          math_signal(ctl, B_PREP, mtid);
-          alive = math_wait(ctl, B_M1, ph, mtid, seq, A.err);
+          group_publish<true>();
+          if (ctid == 0) {
+            issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, b > 0);
+            mma_commit(smem_u32(&ctl->bar[B_M1]));
+          }
+          alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
+          ph_m1 ^= 1u;
         }
         if (!alive) break;
         // operands with the chunk start as reference (may underflow to 0: fine)
@@ -475,19 +444,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
           const uint32_t row = 16 * rg + r;
           const float2 qv = unpack_bf16(pf.q[r]), kv = unpack_bf16(pf.k[r]);
           const float e0 = ex2(G0[r]), e1 = ex2(G1[r]);
-          st_shared_u32(qg_q + sw128_offset(row, col), pack_bf16(qv.x * e0, qv.y * e1));
-          st_shared_u32(qg_q + sw128_offset(64 + row, col), pack_bf16(kv.x * e0, kv.y * e1));
-          st_shared_u32(kh_t + sw128_offset(row, col),
+          st_shared_u32(qg_h + sw128_offset(row, col), pack_bf16(qv.x * e0, qv.y * e1));
+          st_shared_u32(qg_h + sw128_offset(64 + row, col), pack_bf16(kv.x * e0, kv.y * e1));
+          st_shared_u32(kh_h + sw128_offset(row, col),
                         pack_bf16(kv.x * ex2(GC0 - G0[r]), kv.y * ex2(GC1 - G1[r])));
         }
       }
       if (!alive) break;
       // next chunk's inputs travel while this one computes
-      if (c + 1 < nchunks) prefetch_chunk(pf, a, h, t0 + kC, min(kC, eos - t0 - kC), p, rg, mtid);
+      if (m + 1 < nchunks) prefetch_chunk(pf, a, h, t0 + kC, min(kC, eos - t0 - kC), p, rg, ctid);
 
       // ---------------- masks, L, and T_b = (I + L)^{-1} diag(beta)
       {
-        float *Lf = reinterpret_cast<float *>(sm + OFF_LF);
+        float *Lf = reinterpret_cast<float *>(sm + OFF_KB);  // K / Gamma is dead once M1 is done
         float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
         float *Xf = reinterpret_cast<float *>(sm + OFF_XF);
         if (qw < 2) {
@@ -500,7 +469,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
             tmem_wait_ld();
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc) v[cc] = (s0 + cc <= r) ? v[cc] : 0.f;
-            st_row16_bf16(sm + OFF_AM, r, s0, v);
+            st_row16_bf16(sm + OFF_AM + par * 8192, r, s0, v);
           }
         } else {
           const int r = 32 * (qw - 2) + lane;
@@ -512,158 +481,239 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
             tmem_ld16(tmem_addr(tbase, 32 * qw, TM_D1 + s0), v);
             tmem_wait_ld();
 #pragma unroll
-            for (int cc = 0; cc < 16; ++cc) Lf[r * LDF + s0 + cc] = (s0 + cc < r) ? br * v[cc] : 0.f;
+            for (int cc = 0; cc < 16; ++cc) v[cc] = (s0 + cc < r) ? br * v[cc] : 0.f;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+              *reinterpret_cast<float4 *>(Lf + r * 64 + s0 + 4 * c4) =
+                  make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
           }
         }
-        math_bar();
-        // diagonal 16x16 blocks by forward substitution (one column per thread);
-        // the blocks above the diagonal are zero
-        if (mtid < 64) {
-          const int ab = mtid >> 4, cc = mtid & 15, base = 16 * ab;
+        bar_chunk();
+        // Diagonal 16x16 blocks by forward substitution, one column per thread:
+        // x = e_c - L_blk x with x[m] = 0 for m < c, written without branches.
+        // The blocks above the diagonal are zero.
+        if (ctid < 64) {
+          const int ab = ctid >> 4, cc = ctid & 15, base = 16 * ab;
           float x[16];
 #pragma unroll
           for (int rr = 0; rr < 16; ++rr) {
             float acc = (rr == cc) ? 1.f : 0.f;
-            if (rr > cc) {
 #pragma unroll
-              for (int m = 0; m < rr; ++m)
-                if (m >= cc) acc -= Lf[(base + rr) * LDF + base + m] * x[m];
-            }
+            for (int m = 0; m < rr; ++m) acc -= Lf[(base + rr) * 64 + base + m] * x[m];
             x[rr] = acc;
-            Tf[(base + rr) * LDF + base + cc] = acc;
+            Tf[(base + rr) * 64 + base + cc] = acc;
           }
         } else {
-          for (int e = mtid - 64; e < 6 * 256; e += 192) {
+          for (int e = ctid - 64; e < 6 * 256; e += 192) {
             const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
             const int ab = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
             const int bb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            Tf[(16 * ab + rr) * LDF + 16 * bb + cc] = 0.f;
+            Tf[(16 * ab + rr) * 64 + 16 * bb + cc] = 0.f;
           }
         }
-        math_bar();
-        // off-diagonal blocks by distance d: T_ab = -T_aa sum_{c=b}^{a-1} L_ac T_cb
+        bar_chunk();
+        // Off-diagonal blocks by distance d: T_ab = -T_aa sum_{c=b}^{a-1} L_ac T_cb
 #pragma unroll 1
         for (int d = 1; d < 4; ++d) {
           const int nblk = 4 - d;
-          for (int e = mtid; e < nblk * 256; e += 256) {
+          for (int e = ctid; e < nblk * 256; e += 256) {
             const int b = e >> 8, ab = b + d, rr = (e >> 4) & 15, cc = e & 15;
             float acc = 0.f;
             for (int cb = b; cb < ab; ++cb) {
 #pragma unroll
               for (int m = 0; m < 16; ++m)
-                acc += Lf[(16 * ab + rr) * LDF + 16 * cb + m] * Tf[(16 * cb + m) * LDF + 16 * b + cc];
+                acc += Lf[(16 * ab + rr) * 64 + 16 * cb + m] * Tf[(16 * cb + m) * 64 + 16 * b + cc];
             }
             Xf[(b * 16 + rr) * 17 + cc] = acc;
           }
-          math_bar();
-          for (int e = mtid; e < nblk * 256; e += 256) {
+          bar_chunk();
+          for (int e = ctid; e < nblk * 256; e += 256) {
             const int b = e >> 8, ab = b + d, rr = (e >> 4) & 15, cc = e & 15;
             float acc = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-              acc += Tf[(16 * ab + rr) * LDF + 16 * ab + m] * Xf[(b * 16 + m) * 17 + cc];
-            Tf[(16 * ab + rr) * LDF + 16 * b + cc] = -acc;
+            for (int m = 0; m < 16; ++m) acc += Tf[(16 * ab + rr) * 64 + 16 * ab + m] * Xf[(b * 16 + m) * 17 + cc];
+            Tf[(16 * ab + rr) * 64 + 16 * b + cc] = -acc;
           }
-          math_bar();
+          bar_chunk();
         }
         {
-          const int r = mtid >> 2, s0 = (mtid & 3) * 16;
+          const int r = ctid >> 2, s0 = (ctid & 3) * 16;
           float v[16];
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) v[cc] = Tf[r * LDF + s0 + cc] * ctl->bs[s0 + cc];
-          st_row16_bf16(sm + OFF_ZT, 64 + r, s0, v);
+          for (int cc = 0; cc < 16; ++cc) v[cc] = Tf[r * 64 + s0 + cc] * ctl->bs[s0 + cc];
+          st_row16_bf16(sm + OFF_ZT, r, s0, v);
         }
       }
-      math_signal(ctl, B_SOLVE, mtid);
+      group_publish<true>();
 
-      // ---------------- W^T (TMEM) -> -W, rows 64..127 of QG
-      if (!(alive = math_wait(ctl, B_M23, ph, mtid, seq, A.err))) break;
-      {
-        const int i = jrow;
-        uint8_t *dst = sm + OFF_QG + (i >> 6) * 16384;
+      // ---------------- U^T and W^T; then hand the chunk to the state group
+      if (ctid == 0) {
+        bool ok = solo_wait(ctl, B_VFULL, ph_v, A.err);
+        ph_v ^= 1u;
+        landed_v = ok ? issued_v : landed_v;
+        if (ok && m >= 1) ok = solo_wait(ctl, B_WFREE, (m - 1) & 1, A.err);
+        if (ok) {
+          issue_m23(tbase, sm_base + OFF_V, smem_u32(qg), sm_base + OFF_ZT, TM_U + par * 64);
+          mma_commit(smem_u32(&ctl->bar[B_M23]));
+          ok = solo_wait(ctl, B_M23, ph_m23, A.err);
+          ph_m23 ^= 1u;
+        }
+        if (ok && m + 1 < nchunks) {  // the V buffer is free again
+          const uint32_t full = smem_u32(&ctl->bar[B_VFULL]);
+          mbar_arrive_expect_tx(full, 2 * kC * 64 * 2);
+          tma_load_3d(sm_base + OFF_V, &tmap_v, full, 0, h, t0 + kC);
+          tma_load_3d(sm_base + OFF_V + 8192, &tmap_v, full, 64, h, t0 + kC);
+          ++issued_v;
+        }
+        if (ok) mbar_arrive(smem_u32(&ctl->bar[B_READY0 + par]));
+        ctl->go_c[seq & 1] = ok && !ctl->abort;
+      }
+      bar_chunk();
+      alive = ctl->go_c[seq & 1] != 0;
+      ++seq;
+    }
+    if (ctid == 0) {
+      // outstanding V copy (only after an abort) and this group's MMAs
+      volatile int no_abort = 0;
+      if (issued_v > landed_v) mbar_wait(smem_u32(&ctl->bar[B_VFULL]), ph_v, &no_abort, A.err, 1u << 20);
+      mma_commit(smem_u32(&ctl->bar[B_TD_C]));
+      mbar_wait(smem_u32(&ctl->bar[B_TD_C]), 0, &no_abort, A.err, 1u << 21);
+    }
+  } else {
+    // =========================================================== state group
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
+    const int stid = tid - kChunkThreads;  // = TMEM lane j of every state-group product
+    const int qw = warp & 3;                // lane quarter, = stid >> 5
+    const int j = stid;
+    int seq = 0;
+    uint32_t ph_m4 = 0, ph_m56 = 0;
+    // initial state -> TMEM (fp32 master) and the bf16 operand S^T
+#pragma unroll 1
+    for (int blk = 0; blk < 8; ++blk) {
+      const int i0 = 16 * blk;
+      float s[16];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+      for (int c = 0; c < 16; ++c) s[c] = a.s0 ? a.s0[sbase + (size_t)(i0 + c) * kD + j] : 0.f;
+      tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
+      st_row16_bf16(sm + OFF_ST + (blk >> 2) * 16384, j, 16 * (blk & 3), s);
+    }
+    tmem_wait_st();
+    group_publish<false>();
+    bool alive = true;
+    for (int c = 0; c < nchunks && alive; ++c) {
+      const int par = c & 1;
+      const int t0 = bos + c * kC;
+      const int len = min(kC, eos - t0);
+      uint8_t *qg = sm + OFF_QG + par * 32768;
+      const uint32_t tm_u = TM_U + par * 64;
+      if (!(alive = group_wait<false>(ctl, B_READY0 + par, (c >> 1) & 1, stid, seq, A.err))) break;
+
+      // ---------------- -W^T (TMEM) -> MN-major operand in QG rows 64..127
+      {
+        uint8_t *dst = qg + (j >> 6) * 16384 + 8192;
+        const uint32_t row = j & 63;
+#pragma unroll
+        for (int r0 = 0; r0 < 64; r0 += 16) {
           float v[16];
-          const int r0 = 32 * ch + 16 * hh;
-          tmem_ld16(tmem_addr(tbase, 32 * qw, TM_D1 + r0), v);
+          tmem_ld16(tmem_addr(tbase, 32 * qw, TM_W + r0), v);
           tmem_wait_ld();
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc)
-            *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_offset(64 + r0 + cc, i & 63)) =
-                __float2bfloat16_rn(-v[cc]);
+          for (int cc = 0; cc < 16; ++cc) v[cc] = -v[cc];
+          st_row16_bf16(dst, row, r0, v);
         }
       }
-      math_signal(ctl, B_W, mtid);
-
-      // ---------------- V~^T (TMEM) -> bf16 operand
-      if (!(alive = math_wait(ctl, B_M4, ph, mtid, seq, A.err))) break;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float v[16];
-        const int r0 = 32 * ch + 16 * hh;
-        tmem_ld16(tmem_addr(tbase, 32 * qw, TM_U + r0), v);
-        tmem_wait_ld();
-        st_row16_bf16(sm + OFF_VT, jrow, r0, v);
+      group_publish<false>();
+      if (stid == 0) {
+        mbar_arrive(smem_u32(&ctl->bar[B_WFREE]));
+        issue_m4(tbase, sm_base + OFF_ST, smem_u32(qg), tm_u);
+        mma_commit(smem_u32(&ctl->bar[B_M4]));
       }
-      math_signal(ctl, B_E4, mtid);
+      if (!(alive = group_wait<false>(ctl, B_M4, ph_m4, stid, seq, A.err))) break;
+      ph_m4 ^= 1u;
 
-      // ---------------- state update and output
-      if (!(alive = math_wait(ctl, B_M56, ph, mtid, seq, A.err))) break;
+      // ---------------- V~^T -> bf16 operand; S^T <- S^T Diag(gamma_C)
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        const int i0 = 64 * ch + 16 * blk;
-        float dd[16], s[16];
-        tmem_ld16(tmem_addr(tbase, 32 * qw, TM_D6 + i0), dd);
+      for (int r0 = 0; r0 < 64; r0 += 16) {
+        float v[16];
+        tmem_ld16(tmem_addr(tbase, 32 * qw, tm_u + r0), v);
+        tmem_wait_ld();
+        st_row16_bf16(sm + OFF_VT, j, r0, v);
+      }
+      {
+        const float *gam = ctl->gam[par];
+#pragma unroll 2
+        for (int i0 = 0; i0 < 128; i0 += 16) {
+          float s[16];
+          tmem_ld16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
+          tmem_wait_ld();
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) s[cc] *= gam[i0 + cc];
+          tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
+        }
+        tmem_wait_st();
+      }
+      group_publish<false>();
+      if (stid == 0) {
+        issue_m56(tbase, sm_base + OFF_VT, sm_base + OFF_AM + par * 8192, sm_base + OFF_KH + par * 16384);
+        mma_commit(smem_u32(&ctl->bar[B_M56]));
+      }
+      if (!(alive = group_wait<false>(ctl, B_M56, ph_m56, stid, seq, A.err))) break;
+      ph_m56 ^= 1u;
+
+      // ---------------- bf16 copy of the new state; the output rows
+#pragma unroll 2
+      for (int i0 = 0; i0 < 128; i0 += 16) {
+        float s[16];
         tmem_ld16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
         tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < 16; ++cc) s[cc] = ctl->gam[i0 + cc] * s[cc] + dd[cc];
-        tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
-        st_row16_bf16(sm + OFF_ST + ch * 16384, jrow, 16 * blk, s);
+        st_row16_bf16(sm + OFF_ST + (i0 >> 6) * 16384, j, i0 & 63, s);
       }
       {
         __nv_bfloat16 *ostage = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int r0 = 0; r0 < 64; r0 += 16) {
           float v[16];
-          const int r0 = 32 * ch + 16 * hh;
           tmem_ld16(tmem_addr(tbase, 32 * qw, TM_O + r0), v);
           tmem_wait_ld();
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) ostage[(r0 + cc) * kD + jrow] = __float2bfloat16_rn(v[cc]);
+          for (int cc = 0; cc < 16; ++cc) ostage[(r0 + cc) * kD + j] = __float2bfloat16_rn(v[cc]);
         }
       }
-      tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
-      math_bar();
+      bar_state();
       {
         const uint4 *src = reinterpret_cast<const uint4 *>(sm + OFF_VT);
         uint4 *o = reinterpret_cast<uint4 *>(a.o);
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int idx = it * kMathThreads + mtid, row = idx >> 4, c16 = idx & 15;
+        for (int it = 0; it < 8; ++it) {
+          const int idx = it * kStateThreads + stid, row = idx >> 4, c16 = idx & 15;
           if (row < len) o[((size_t)(t0 + row) * H + h) * (kD / 8) + c16] = src[idx];
         }
       }
+      group_publish<false>();
+      if (stid == 0) mbar_arrive(smem_u32(&ctl->bar[B_FREE0 + par]));
     }
-    // final state
     if (alive && a.sT) {
-      for (int blk = 0; blk < 4; ++blk) {
-        const int i0 = 64 * ch + 16 * blk;
+#pragma unroll 1
+      for (int i0 = 0; i0 < 128; i0 += 16) {
         float s[16];
         tmem_ld16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
         tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) a.sT[sbase + (size_t)(i0 + cc) * kD + jrow] = s[cc];
+        for (int cc = 0; cc < 16; ++cc) a.sT[sbase + (size_t)(i0 + cc) * kD + j] = s[cc];
       }
+    }
+    if (stid == 0) {
+      volatile int no_abort = 0;
+      mma_commit(smem_u32(&ctl->bar[B_TD_S]));
+      mbar_wait(smem_u32(&ctl->bar[B_TD_S]), 0, &no_abort, A.err, 1u << 22);
     }
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == kProducerWarp) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
