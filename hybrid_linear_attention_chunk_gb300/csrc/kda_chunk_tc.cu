@@ -158,35 +158,58 @@ __device__ __forceinline__ void st_row16_bf16(uint8_t *tile, uint32_t row, uint3
 
 // Inputs of one chunk held in registers by a chunk-group thread: channel pair
 // (2p, 2p+1), rows [16 rg, 16 rg + 16).
+// Thread layout of the prologue: channel octet o = ctid & 15 (channels
+// [8o, 8o+8)), row group rg = ctid >> 4 (rows [4rg, 4rg+4)); every global
+// load and shared store moves 16 bytes.
 struct Prefetch {
-  uint32_t q[16], k[16];
-  float2 g[16];
+  uint4 q[4], k[4];   // 8 bf16 each
+  float4 g[4][2];     // 8 fp32 each
   float beta;
 };
 
 __device__ __forceinline__ void prefetch_chunk(Prefetch &pf, const PrefillArgs &a, int h, int t0, int len,
-                                               int p, int rg, int ctid) {
+                                               int o, int rg, int ctid) {
   const int H = a.H;
-  const uint32_t *q = reinterpret_cast<const uint32_t *>(a.q);
-  const uint32_t *k = reinterpret_cast<const uint32_t *>(a.k);
-  const float2 *g = reinterpret_cast<const float2 *>(a.g);
+  const uint4 *q = reinterpret_cast<const uint4 *>(a.q);
+  const uint4 *k = reinterpret_cast<const uint4 *>(a.k);
+  const float4 *g = reinterpret_cast<const float4 *>(a.g);
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int row = 16 * rg + r;
+  for (int r = 0; r < 4; ++r) {
+    const int row = 4 * rg + r;
     if (row < len) {
-      const size_t e = ((size_t)(t0 + row) * H + h) * (kD / 2) + p;  // in element pairs
+      const size_t e = ((size_t)(t0 + row) * H + h) * (kD / 8) + o;  // in 8-element units
       pf.q[r] = __ldg(q + e);
       pf.k[r] = __ldg(k + e);
-      pf.g[r] = __ldg(g + e);
+      pf.g[r][0] = __ldg(g + 2 * e);
+      pf.g[r][1] = __ldg(g + 2 * e + 1);
     } else {
-      pf.q[r] = 0u;
-      pf.k[r] = 0u;
-      pf.g[r] = make_float2(0.f, 0.f);
+      pf.q[r] = make_uint4(0u, 0u, 0u, 0u);
+      pf.k[r] = make_uint4(0u, 0u, 0u, 0u);
+      pf.g[r][0] = pf.g[r][1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
   pf.beta = 0.f;
   if (ctid < kC && ctid < len) pf.beta = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + ctid) * H + h);
 }
+
+__device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = unpack_bf16(w[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ void st_shared_8bf16(uint8_t *p, const float (&f)[8]) {
+  st_shared_v4(p, pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+}
+
+// fp32 64x64 matrices of the solve (L, T) are stored row-major with the
+// column index XORed with 4*(row & 7): columns keep 4-float groups intact,
+// and eight consecutive rows read at one column hit eight different banks.
+__device__ __forceinline__ int swz64(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
 
 // A group-wide view of an mbarrier wait: the group's thread 0 waits, the
 // group synchronises, and every thread gets the same verdict (so no thread
@@ -319,7 +342,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     const int ctid = tid;
     const int qw = warp & 3, ch = warp >> 2;
-    const int p = ctid & 63, rg = ctid >> 6;
+    const int o = ctid & 15, rg = ctid >> 4, tile = rg >> 2;  // prologue layout (see Prefetch)
     int seq = 0;
     uint32_t ph_m1 = 0, ph_m23 = 0, ph_v = 0;
     int issued_v = 0, landed_v = 0;
@@ -332,7 +355,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
       issued_v = 1;
     }
     Prefetch pf;
-    if (nchunks > 0) prefetch_chunk(pf, a, h, bos, min(kC, eos - bos), p, rg, ctid);
+    if (nchunks > 0) prefetch_chunk(pf, a, h, bos, min(kC, eos - bos), o, rg, ctid);
+    float *tot = reinterpret_cast<float *>(sm + OFF_TF);  // [16][128] row-group sums (T is not live yet)
     bool alive = true;
     for (int m = 0; m < nchunks && alive; ++m) {
       const int par = m & 1;
@@ -343,63 +367,86 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
       if (m >= 2 && !(alive = group_wait<true>(ctl, B_FREE0 + par, ((m >> 1) - 1) & 1, ctid, seq, A.err))) break;
 
       // ---------------- decay prologue: cumulative log2-decay and scaled operands
-      float G0[16], G1[16];
+      float G[4][8];
       {
-        float a0 = 0.f, a1 = 0.f;
+        float run[8];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          a0 += pf.g[r].x * kLog2e;
-          a1 += pf.g[r].y * kLog2e;
-          G0[r] = a0;
-          G1[r] = a1;
+        for (int c = 0; c < 8; ++c) run[c] = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float gg[8] = {pf.g[r][0].x, pf.g[r][0].y, pf.g[r][0].z, pf.g[r][0].w,
+                               pf.g[r][1].x, pf.g[r][1].y, pf.g[r][1].z, pf.g[r][1].w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            run[c] += gg[c] * kLog2e;
+            G[r][c] = run[c];
+          }
         }
-        ctl->tot[rg][2 * p] = a0;
-        ctl->tot[rg][2 * p + 1] = a1;
+        *reinterpret_cast<float4 *>(tot + rg * 128 + 8 * o) = make_float4(run[0], run[1], run[2], run[3]);
+        *reinterpret_cast<float4 *>(tot + rg * 128 + 8 * o + 4) = make_float4(run[4], run[5], run[6], run[7]);
       }
       if (ctid < kC) ctl->bs[ctid] = pf.beta;
       bar_chunk();
-      float ref0[4], ref1[4], run0 = 0.f, run1 = 0.f;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        ref0[b] = run0;
-        ref1[b] = run1;
-        run0 += ctl->tot[b][2 * p];
-        run1 += ctl->tot[b][2 * p + 1];
-      }
-      const float GC0 = run0, GC1 = run1;
+      // prefix over the 16 row groups: own offset and chunk total
+      float own[8], GC[8];
       {
-        const float own0 = pick4(ref0, rg), own1 = pick4(ref1, rg);
+        float run[8];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          G0[r] += own0;
-          G1[r] += own1;
+        for (int c = 0; c < 8; ++c) run[c] = own[c] = 0.f;
+#pragma unroll
+        for (int g2 = 0; g2 < 16; ++g2) {
+          if (g2 == rg) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) own[c] = run[c];
+          }
+          const float4 t0v = *reinterpret_cast<const float4 *>(tot + g2 * 128 + 8 * o);
+          const float4 t1v = *reinterpret_cast<const float4 *>(tot + g2 * 128 + 8 * o + 4);
+          run[0] += t0v.x; run[1] += t0v.y; run[2] += t0v.z; run[3] += t0v.w;
+          run[4] += t1v.x; run[5] += t1v.y; run[6] += t1v.z; run[7] += t1v.w;
         }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) GC[c] = run[c];
       }
-      const float gc0 = ex2(GC0), gc1 = ex2(GC1);
+      float gc[8];
+      bool below = false;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) G[r][c] += own[c];
+        gc[c] = ex2(GC[c]);
+        below |= GC[c] < kSingleRefBound2;
+      }
       if (rg == 0) {
-        ctl->gam[par][2 * p] = gc0;
-        ctl->gam[par][2 * p + 1] = gc1;
+        *reinterpret_cast<float4 *>(&ctl->gam[par][8 * o]) = make_float4(gc[0], gc[1], gc[2], gc[3]);
+        *reinterpret_cast<float4 *>(&ctl->gam[par][8 * o + 4]) = make_float4(gc[4], gc[5], gc[6], gc[7]);
       }
-      if (GC0 < kSingleRefBound2 || GC1 < kSingleRefBound2) atomicOr(&ctl->slow[par], 1);
+      if (below) atomicOr(&ctl->slow[par], 1);
       bar_chunk();
       const bool slow = ctl->slow[par] != 0;
       if (ctid == 0) ctl->slow[par ^ 1] = 0;
-      const uint32_t half = (uint32_t)(p >> 5), col = (uint32_t)((2 * p) & 63);
+      const uint32_t half = (uint32_t)(o >> 3), col = (uint32_t)(8 * (o & 7));
       uint8_t *qg_h = qg + half * 16384;
       uint8_t *kb_h = sm + OFF_KB + half * 8192;
       uint8_t *kh_h = kh + half * 8192;
       if (!slow) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const uint32_t row = 16 * rg + r;
-          const float e0 = ex2(G0[r]), e1 = ex2(G1[r]);
-          const float i0 = ex2(-G0[r]), i1 = ex2(-G1[r]);
-          const float2 qv = unpack_bf16(pf.q[r]), kv = unpack_bf16(pf.k[r]);
-          st_shared_u32(qg_h + sw128_offset(row, col), pack_bf16(qv.x * e0, qv.y * e1));
-          st_shared_u32(qg_h + sw128_offset(64 + row, col), pack_bf16(kv.x * e0, kv.y * e1));
-          const float kb0 = kv.x * i0, kb1 = kv.y * i1;
-          st_shared_u32(kb_h + sw128_offset(row, col), pack_bf16(kb0, kb1));
-          st_shared_u32(kh_h + sw128_offset(row, col), pack_bf16(kb0 * gc0, kb1 * gc1));
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t row = 4 * rg + r;
+          float qv[8], kv[8], fq[8], fk[8], fb[8], fh[8];
+          unpack8_bf16(pf.q[r], qv);
+          unpack8_bf16(pf.k[r], kv);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float e = ex2(G[r][c]), i = ex2(-G[r][c]);
+            fq[c] = qv[c] * e;
+            fk[c] = kv[c] * e;
+            fb[c] = kv[c] * i;
+            fh[c] = fb[c] * gc[c];
+          }
+          st_shared_8bf16(qg_h + sw128_offset(row, col), fq);
+          st_shared_8bf16(qg_h + sw128_offset(64 + row, col), fk);
+          st_shared_8bf16(kb_h + sw128_offset(row, col), fb);
+          st_shared_8bf16(kh_h + sw128_offset(row, col), fh);
         }
         group_publish<true>();
         if (ctid == 0) {
@@ -409,25 +456,36 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
         alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
         ph_m1 ^= 1u;
       } else {
-        for (int b = 0; b < 4 && alive; ++b) {
-          const float rb0 = pick4(ref0, b), rb1 = pick4(ref1, b);
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          if (!alive) break;
+          // reference of key tile b: the cumulative decay before its first row
+          float ref[8];
 #pragma unroll
-          for (int r = 0; r < 16; ++r) {
-            const uint32_t row = 16 * rg + r;
-            const float2 qv = unpack_bf16(pf.q[r]), kv = unpack_bf16(pf.k[r]);
-            float qa = 0.f, qb = 0.f, ka = 0.f, kbv = 0.f, ba = 0.f, bb = 0.f;
-            if (rg >= b) {
-              const float e0 = ex2(G0[r] - rb0), e1 = ex2(G1[r] - rb1);
-              qa = qv.x * e0; qb = qv.y * e1;
-              ka = kv.x * e0; kbv = kv.y * e1;
+          for (int c = 0; c < 8; ++c) ref[c] = 0.f;
+          for (int g2 = 0; g2 < 4 * b; ++g2) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ref[c] += tot[g2 * 128 + 8 * o + c];
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const uint32_t row = 4 * rg + r;
+            float qv[8], kv[8], fq[8], fk[8], fb[8];
+            unpack8_bf16(pf.q[r], qv);
+            unpack8_bf16(pf.k[r], kv);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              fq[c] = fk[c] = fb[c] = 0.f;
+              if (tile >= b) {
+                const float e = ex2(G[r][c] - ref[c]);
+                fq[c] = qv[c] * e;
+                fk[c] = kv[c] * e;
+              }
+              if (tile == b) fb[c] = kv[c] * ex2(ref[c] - G[r][c]);
             }
-            if (rg == b) {
-              ba = kv.x * ex2(rb0 - G0[r]);
-              bb = kv.y * ex2(rb1 - G1[r]);
-            }
-            st_shared_u32(qg_h + sw128_offset(row, col), pack_bf16(qa, qb));
-            st_shared_u32(qg_h + sw128_offset(64 + row, col), pack_bf16(ka, kbv));
-            st_shared_u32(kb_h + sw128_offset(row, col), pack_bf16(ba, bb));
+            st_shared_8bf16(qg_h + sw128_offset(row, col), fq);
+            st_shared_8bf16(qg_h + sw128_offset(64 + row, col), fk);
+            st_shared_8bf16(kb_h + sw128_offset(row, col), fb);
           }
           group_publish<true>();
           if (ctid == 0) {
@@ -440,19 +498,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
         if (!alive) break;
         // operands with the chunk start as reference (may underflow to 0: fine)
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const uint32_t row = 16 * rg + r;
-          const float2 qv = unpack_bf16(pf.q[r]), kv = unpack_bf16(pf.k[r]);
-          const float e0 = ex2(G0[r]), e1 = ex2(G1[r]);
-          st_shared_u32(qg_h + sw128_offset(row, col), pack_bf16(qv.x * e0, qv.y * e1));
-          st_shared_u32(qg_h + sw128_offset(64 + row, col), pack_bf16(kv.x * e0, kv.y * e1));
-          st_shared_u32(kh_h + sw128_offset(row, col),
-                        pack_bf16(kv.x * ex2(GC0 - G0[r]), kv.y * ex2(GC1 - G1[r])));
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t row = 4 * rg + r;
+          float qv[8], kv[8], fq[8], fk[8], fh[8];
+          unpack8_bf16(pf.q[r], qv);
+          unpack8_bf16(pf.k[r], kv);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float e = ex2(G[r][c]);
+            fq[c] = qv[c] * e;
+            fk[c] = kv[c] * e;
+            fh[c] = kv[c] * ex2(GC[c] - G[r][c]);
+          }
+          st_shared_8bf16(qg_h + sw128_offset(row, col), fq);
+          st_shared_8bf16(qg_h + sw128_offset(64 + row, col), fk);
+          st_shared_8bf16(kh_h + sw128_offset(row, col), fh);
         }
       }
       if (!alive) break;
       // next chunk's inputs travel while this one computes
-      if (m + 1 < nchunks) prefetch_chunk(pf, a, h, t0 + kC, min(kC, eos - t0 - kC), p, rg, ctid);
+      if (m + 1 < nchunks) prefetch_chunk(pf, a, h, t0 + kC, min(kC, eos - t0 - kC), o, rg, ctid);
 
       // ---------------- masks, L, and T_b = (I + L)^{-1} diag(beta)
       {
@@ -484,14 +549,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
             for (int cc = 0; cc < 16; ++cc) v[cc] = (s0 + cc < r) ? br * v[cc] : 0.f;
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4)
-              *reinterpret_cast<float4 *>(Lf + r * 64 + s0 + 4 * c4) =
+              *reinterpret_cast<float4 *>(Lf + swz64(r, s0 + 4 * c4)) =
                   make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
           }
         }
         bar_chunk();
         // Diagonal 16x16 blocks by forward substitution, one column per thread:
         // x = e_c - L_blk x with x[m] = 0 for m < c, written without branches.
-        // The blocks above the diagonal are zero.
         if (ctid < 64) {
           const int ab = ctid >> 4, cc = ctid & 15, base = 16 * ab;
           float x[16];
@@ -499,48 +563,56 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
           for (int rr = 0; rr < 16; ++rr) {
             float acc = (rr == cc) ? 1.f : 0.f;
 #pragma unroll
-            for (int m = 0; m < rr; ++m) acc -= Lf[(base + rr) * 64 + base + m] * x[m];
+            for (int mm = 0; mm < rr; ++mm) acc -= Lf[swz64(base + rr, base + mm)] * x[mm];
             x[rr] = acc;
-            Tf[(base + rr) * 64 + base + cc] = acc;
-          }
-        } else {
-          for (int e = ctid - 64; e < 6 * 256; e += 192) {
-            const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-            const int ab = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int bb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            Tf[(16 * ab + rr) * 64 + 16 * bb + cc] = 0.f;
+            Tf[swz64(base + rr, base + cc)] = acc;
           }
         }
         bar_chunk();
-        // Off-diagonal blocks by distance d: T_ab = -T_aa sum_{c=b}^{a-1} L_ac T_cb
+        // Off-diagonal blocks by distance d: T_ab = -T_aa sum_{c=b}^{a-1} L_ac T_cb.
+        // One thread per (block, row, 4-column group); blocks above the
+        // diagonal are never read (T_b below masks them).
 #pragma unroll 1
         for (int d = 1; d < 4; ++d) {
-          const int nblk = 4 - d;
-          for (int e = ctid; e < nblk * 256; e += 256) {
-            const int b = e >> 8, ab = b + d, rr = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.f;
+          const int ntask = (4 - d) * 64;
+          const int b = ctid >> 6, ab = b + d, rr = (ctid >> 2) & 15, c0 = 16 * b + 4 * (ctid & 3);
+          if (ctid < ntask) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int cb = b; cb < ab; ++cb) {
 #pragma unroll
-              for (int m = 0; m < 16; ++m)
-                acc += Lf[(16 * ab + rr) * 64 + 16 * cb + m] * Tf[(16 * cb + m) * 64 + 16 * b + cc];
+              for (int mm = 0; mm < 16; ++mm) {
+                const float l = Lf[swz64(16 * ab + rr, 16 * cb + mm)];
+                const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(16 * cb + mm, c0));
+                acc.x += l * t.x; acc.y += l * t.y; acc.z += l * t.z; acc.w += l * t.w;
+              }
             }
-            Xf[(b * 16 + rr) * 17 + cc] = acc;
+            *reinterpret_cast<float4 *>(Xf + (b * 16 + rr) * 16 + 4 * (ctid & 3)) = acc;
           }
           bar_chunk();
-          for (int e = ctid; e < nblk * 256; e += 256) {
-            const int b = e >> 8, ab = b + d, rr = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.f;
+          if (ctid < ntask) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc += Tf[(16 * ab + rr) * 64 + 16 * ab + m] * Xf[(b * 16 + m) * 17 + cc];
-            Tf[(16 * ab + rr) * 64 + 16 * b + cc] = -acc;
+            for (int mm = 0; mm < 16; ++mm) {
+              const float l = Tf[swz64(16 * ab + rr, 16 * ab + mm)];
+              const float4 x = *reinterpret_cast<const float4 *>(Xf + (b * 16 + mm) * 16 + 4 * (ctid & 3));
+              acc.x += l * x.x; acc.y += l * x.y; acc.z += l * x.z; acc.w += l * x.w;
+            }
+            *reinterpret_cast<float4 *>(Tf + swz64(16 * ab + rr, c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
           }
           bar_chunk();
         }
         {
           const int r = ctid >> 2, s0 = (ctid & 3) * 16;
+          const bool upper = (ctid & 3) > (r >> 4);  // block above the diagonal: T is zero there
           float v[16];
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) v[cc] = Tf[r * 64 + s0 + cc] * ctl->bs[s0 + cc];
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(r, s0 + 4 * c4));
+            v[4 * c4] = upper ? 0.f : t.x * ctl->bs[s0 + 4 * c4];
+            v[4 * c4 + 1] = upper ? 0.f : t.y * ctl->bs[s0 + 4 * c4 + 1];
+            v[4 * c4 + 2] = upper ? 0.f : t.z * ctl->bs[s0 + 4 * c4 + 2];
+            v[4 * c4 + 3] = upper ? 0.f : t.w * ctl->bs[s0 + 4 * c4 + 3];
+          }
           st_row16_bf16(sm + OFF_ZT, r, s0, v);
         }
       }
