@@ -1,5 +1,5 @@
 // Chunked KDA prefill on the 5th-generation tensor cores (tcgen05 MMA with
-// TMEM accumulators, operands in 128-byte-swizzled shared memory, V tiles
+// TMEM accumulators, operands in 128-byte-swizzled shared memory, inputs
 // brought in by TMA).  bf16 q/k/v/out, fp32 log-decay and beta, fp32 state,
 // dk = dv = 128, chunk C = 64.
 //
@@ -20,14 +20,15 @@
 //   M6  S^T += V~^T (K o gamma_C / Gamma)                        (M=128 N=128 K=64)
 // Every product is computed transposed so that M = 128 (dv or dk) and the
 // tensor core runs at full width; TMEM lane j holds row j of the result.
+// M4 reads its A operand, the bf16 copy of S^T, straight from TMEM.
 //
 // Two warp groups overlap consecutive chunks.  The chunk group (warps 0-7)
-// runs one chunk ahead: decay prologue, M1, the UT solve, M2/M3.  The state
-// group (warps 8-11) runs the serial state chain: -W staging, M4, V~ staging,
-// the gamma scaling, M5/M6, the bf16 state copy and the output.  Operands the
-// state group still reads while the chunk group prepares the next chunk are
-// double-buffered by chunk parity.  Thread 0 of each group issues that
-// group's MMAs and the chunk group's thread 0 issues the TMA loads of V.
+// runs one chunk ahead: decay prologue, M1, the UT solve, M2/M3, and the TMA
+// loads of q, k, log-decay and v.  The state group (warps 8-11) runs the
+// serial state chain: -W staging, M4, V~ staging, the gamma scaling, M5/M6,
+// the bf16 state copy and the output.  Operands the state group still reads
+// while the chunk group prepares the next chunk are double-buffered by chunk
+// parity.  Thread 0 of each group issues that group's MMAs.
 //
 // Range guard ([K3-notes §2.2, Eq. 5 and Fig. 3]): with log-decay >= -5 a
 // 16-token tile sums to >= -80.  If every channel's chunk total G_C is >= -80
@@ -62,18 +63,18 @@ constexpr float kSingleRefBound2 = kSingleRefBound * kLog2e;  // the -80 bound i
 
 // Shared-memory map (byte offsets from a 1024-aligned base).  "x2" buffers
 // are indexed by chunk parity.
-constexpr uint32_t OFF_QG = 0;        // x2 32 KB: [Q o Gamma ; Gamma o K], 128 rows x 128, two K-halves;
-                                      //   rows 64..127 later hold -W^T (MN-major) for the state group
-constexpr uint32_t OFF_KB = 65536;    // 16 KB: K / Gamma, 64 rows x 128; then L (fp32 64x64) in the solve
+constexpr uint32_t OFF_QG = 0;        // 48 KB: per 64-column K-half (stride KHALF):
+                                      //   [Q o Gamma, even chunks | Gamma o K | Q o Gamma, odd chunks]
+constexpr uint32_t KHALF = 24576;
+constexpr uint32_t OFF_KB = 49152;    // 16 KB: q tile (TMA) -> K / Gamma -> L (fp32 64x64)
+constexpr uint32_t OFF_TF = 65536;    // 16 KB: k tile (TMA) -> T (fp32 64x64)
 constexpr uint32_t OFF_KH = 81920;    // x2 16 KB: K o gamma_C / Gamma (MN-major B of M6)
 constexpr uint32_t OFF_AM = 114688;   // x2 8 KB: A bf16, 64 rows x 64
-constexpr uint32_t OFF_ZT = 131072;   // 8 KB: T_b bf16, 64 rows x 64
-constexpr uint32_t OFF_TF = 139264;   // 16 KB: T fp32 64x64
-constexpr uint32_t OFF_XF = 155648;   // 4 KB: solve scratch fp32 [3][16][17]
-constexpr uint32_t OFF_V = 159744;    // 16 KB: V tile (TMA), 64 rows x 128 as two 64-column boxes
-constexpr uint32_t OFF_ST = 176128;   // 32 KB: S^T bf16, 128 rows x 128
-constexpr uint32_t OFF_VT = 208896;   // 16 KB: V~^T bf16 128 rows x 64; also the output staging tile
-constexpr uint32_t OFF_CTL = 225280;  // 4 KB control block
+constexpr uint32_t OFF_ZT = 131072;   // 8 KB: row-group sums (prologue) / solve scratch / T_b bf16
+constexpr uint32_t OFF_V = 139264;    // 16 KB: v tile (TMA), two 64-column boxes
+constexpr uint32_t OFF_GS = 155648;   // 32 KB: log-decay tile (TMA), fp32 [64][128]
+constexpr uint32_t OFF_VT = 188416;   // 16 KB: -W^T (MN-major), then V~^T, then the output tile
+constexpr uint32_t OFF_CTL = 204800;  // 4 KB control block
 constexpr uint32_t SMEM_USED = OFF_CTL + 4096;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 
@@ -82,21 +83,20 @@ constexpr uint32_t TM_D1 = 0;     // M1 result (chunk group)
 constexpr uint32_t TM_W = 64;     // M3 result W^T (read by the state group)
 constexpr uint32_t TM_U = 128;    // x2 64: U^T, V~^T after M4 (by chunk parity)
 constexpr uint32_t TM_O = 256;    // O^T accumulator
+constexpr uint32_t TM_STB = 320;  // bf16 S^T, two values per column (A operand of M4)
 constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
-  B_M1 = 0, B_M23, B_VFULL, B_READY0, B_READY1, B_FREE0, B_FREE1, B_WFREE, B_M4, B_M56,
-  B_TD_C, B_TD_S, B_COUNT
+  B_M1 = 0, B_M23, B_VFULL, B_QKFULL, B_GFULL, B_READY0, B_READY1, B_FREE0, B_FREE1, B_WFREE, B_M4,
+  B_M56, B_TD_C, B_TD_S, B_COUNT
 };
 
 struct Ctl {
   uint64_t bar[16];
   float gam[2][128];     // gamma_C per channel, by chunk parity
   float bs[64];          // beta of the chunk's rows (0 past the end)
-  float tot[4][128];     // per-16-row-group log2-decay sums
   uint32_t tmem_slot;
   int abort;             // any thread gave up
-  int nb;                // M1 rounds for the current chunk (1 or 4)
   int slow[2];           // range-guard vote, by chunk parity
   int go_c[2];           // chunk-group wait verdicts (double-buffered)
   int go_s[2];           // state-group wait verdicts
@@ -106,6 +106,10 @@ static_assert(sizeof(Ctl) <= 4096, "control block");
 struct TcArgs {
   PrefillArgs a;
   unsigned int *err;
+};
+
+struct TcMaps {
+  CUtensorMap q, k, v, g;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -124,11 +128,6 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
   return __bfloat1622float2(v);
 }
 
-// a[i] for a runtime i without spilling the array to local memory
-__device__ __forceinline__ float pick4(const float (&a)[4], int i) {
-  return i == 0 ? a[0] : (i == 1 ? a[1] : (i == 2 ? a[2] : a[3]));
-}
-
 // Named barriers: 1 = chunk group (256 threads), 2 = state group (128).
 __device__ __forceinline__ void bar_chunk() {
   __syncwarp();
@@ -139,57 +138,17 @@ __device__ __forceinline__ void bar_state() {
   asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-__device__ __forceinline__ void st_shared_u32(uint8_t *p, uint32_t v) {
-  *reinterpret_cast<uint32_t *>(p) = v;
-}
-
 __device__ __forceinline__ void st_shared_v4(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
 }
 
 // Stores 16 fp32 values as bf16 at columns [c0, c0+16) of row `row` of a
 // 128-byte-swizzled tile (c0 a multiple of 8 within one 64-column half).
-__device__ __forceinline__ void st_row16_bf16(uint8_t *tile, uint32_t row, uint32_t c0, const float (&v)[16]) {
+__device__ __forceinline__ void st_row16_bf16(uint8_t *tile, uint32_t row, uint32_t c0, const float *v) {
   st_shared_v4(tile + sw128_offset(row, c0), pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
                pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
   st_shared_v4(tile + sw128_offset(row, c0 + 8), pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]),
                pack_bf16(v[12], v[13]), pack_bf16(v[14], v[15]));
-}
-
-// Inputs of one chunk held in registers by a chunk-group thread: channel pair
-// (2p, 2p+1), rows [16 rg, 16 rg + 16).
-// Thread layout of the prologue: channel octet o = ctid & 15 (channels
-// [8o, 8o+8)), row group rg = ctid >> 4 (rows [4rg, 4rg+4)); every global
-// load and shared store moves 16 bytes.
-struct Prefetch {
-  uint4 q[4], k[4];   // 8 bf16 each
-  float4 g[4][2];     // 8 fp32 each
-  float beta;
-};
-
-__device__ __forceinline__ void prefetch_chunk(Prefetch &pf, const PrefillArgs &a, int h, int t0, int len,
-                                               int o, int rg, int ctid) {
-  const int H = a.H;
-  const uint4 *q = reinterpret_cast<const uint4 *>(a.q);
-  const uint4 *k = reinterpret_cast<const uint4 *>(a.k);
-  const float4 *g = reinterpret_cast<const float4 *>(a.g);
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int row = 4 * rg + r;
-    if (row < len) {
-      const size_t e = ((size_t)(t0 + row) * H + h) * (kD / 8) + o;  // in 8-element units
-      pf.q[r] = __ldg(q + e);
-      pf.k[r] = __ldg(k + e);
-      pf.g[r][0] = __ldg(g + 2 * e);
-      pf.g[r][1] = __ldg(g + 2 * e + 1);
-    } else {
-      pf.q[r] = make_uint4(0u, 0u, 0u, 0u);
-      pf.k[r] = make_uint4(0u, 0u, 0u, 0u);
-      pf.g[r][0] = pf.g[r][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-  pf.beta = 0.f;
-  if (ctid < kC && ctid < len) pf.beta = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + ctid) * H + h);
 }
 
 __device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&f)[8]) {
@@ -204,6 +163,15 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&f)[8]) {
 
 __device__ __forceinline__ void st_shared_8bf16(uint8_t *p, const float (&f)[8]) {
   st_shared_v4(p, pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+}
+
+// Packs 32 fp32 values into 16 bf16 pairs (even element in the low half), the
+// TMEM layout of an MMA A operand, and stores them at TMEM address taddr.
+__device__ __forceinline__ void tmem_st_bf16x32(uint32_t taddr, const float (&v)[32]) {
+  float w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = __uint_as_float(pack_bf16(v[2 * i], v[2 * i + 1]));
+  tmem_st16(taddr, w);
 }
 
 // fp32 64x64 matrices of the solve (L, T) are stored row-major with the
@@ -245,13 +213,57 @@ __device__ __forceinline__ void group_publish() {
   tc_fence_after();
 }
 
+// ------------------------------------------------------------------- loads
+
+struct Loader {
+  const TcMaps *maps;
+  Ctl *ctl;
+  uint32_t sm_base;
+  int h;
+  int issued[3];  // q/k, g, v
+  int landed[3];
+
+  __device__ void qk(int t0) {
+    const uint32_t full = smem_u32(&ctl->bar[B_QKFULL]);
+    mbar_arrive_expect_tx(full, 4 * 8192);
+    tma_load_3d(sm_base + OFF_KB, &maps->q, full, 0, h, t0);
+    tma_load_3d(sm_base + OFF_KB + 8192, &maps->q, full, 64, h, t0);
+    tma_load_3d(sm_base + OFF_TF, &maps->k, full, 0, h, t0);
+    tma_load_3d(sm_base + OFF_TF + 8192, &maps->k, full, 64, h, t0);
+    ++issued[0];
+  }
+  __device__ void g(int t0) {
+    const uint32_t full = smem_u32(&ctl->bar[B_GFULL]);
+    mbar_arrive_expect_tx(full, kC * kD * 4);
+    tma_load_3d(sm_base + OFF_GS, &maps->g, full, 0, h, t0);
+    ++issued[1];
+  }
+  __device__ void v(int t0) {
+    const uint32_t full = smem_u32(&ctl->bar[B_VFULL]);
+    mbar_arrive_expect_tx(full, 2 * 8192);
+    tma_load_3d(sm_base + OFF_V, &maps->v, full, 0, h, t0);
+    tma_load_3d(sm_base + OFF_V + 8192, &maps->v, full, 64, h, t0);
+    ++issued[2];
+  }
+  // copies still in flight after an abort must land before the CTA retires
+  __device__ void drain(unsigned int *err) {
+    const int bars[3] = {B_QKFULL, B_GFULL, B_VFULL};
+    volatile int no_abort = 0;
+    for (int i = 0; i < 3; ++i)
+      if (issued[i] > landed[i])
+        mbar_wait(smem_u32(&ctl->bar[bars[i]]), landed[i] & 1, &no_abort, err, 1u << (20 + i));
+  }
+};
+
 // ------------------------------------------------------------- MMA batches
 
-__device__ __forceinline__ void issue_m1(uint32_t tbase, uint32_t qg, uint32_t kb, bool acc_first) {
+__device__ __forceinline__ void issue_m1(uint32_t tbase, uint32_t qg, uint32_t kb, int par, bool acc_first) {
   constexpr uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+  // A = 128 consecutive rows: [Q o Gamma ; Gamma o K] for even chunks,
+  // [Gamma o K ; Q o Gamma] for odd ones (so the solve swaps lane roles)
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
+    const uint32_t ka = (kk >> 2) * KHALF + par * 8192 + (kk & 3) * 32;
     const uint32_t kbo = (kk >> 2) * 8192 + (kk & 3) * 32;
     mma_bf16_ss(tbase + TM_D1, smem_desc_sw128(qg + ka, 16, 1024), smem_desc_sw128(kb + kbo, 16, 1024), id,
                 (kk > 0 || acc_first) ? 1u : 0u);
@@ -265,29 +277,21 @@ __device__ __forceinline__ void issue_m23(uint32_t tbase, uint32_t v, uint32_t q
     mma_bf16_ss(tbase + tm_u, smem_desc_sw128(v + kk * 2048, 8192, 1024), smem_desc_sw128(zt + kk * 32, 16, 1024),
                 id, kk > 0 ? 1u : 0u);
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)  // W^T = (Gamma o K)^T T_b^T   (A = rows 64..127 of QG, MN-major)
-    mma_bf16_ss(tbase + TM_W, smem_desc_sw128(qg + 8192 + kk * 2048, 16384, 1024),
+  for (int kk = 0; kk < 4; ++kk)  // W^T = (Gamma o K)^T T_b^T   (A = the Gamma o K blocks, MN-major)
+    mma_bf16_ss(tbase + TM_W, smem_desc_sw128(qg + 8192 + kk * 2048, KHALF, 1024),
                 smem_desc_sw128(zt + kk * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
 }
 
-// -W^T lives in QG rows 64..127 as an MN-major operand: i in [0,64) in the
-// first K-half's rows 64..127, i in [64,128) in the second's.
-__device__ __forceinline__ uint32_t wt_piece(uint32_t qg, int piece) { return qg + piece * 16384 + 8192; }
-
-__device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t st, uint32_t qg, uint32_t tm_u) {
+__device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t vt, uint32_t qg, int par, uint32_t tm_u) {
   constexpr uint32_t id_w = idesc_bf16_f32(128, 64, 0, 1);
   constexpr uint32_t id_q = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {  // V~^T = U^T + S^T (-W)^T
-    const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
-    mma_bf16_ss(tbase + tm_u, smem_desc_sw128(st + ka, 16, 1024),
-                smem_desc_sw128(wt_piece(qg, kk >> 2) + (kk & 3) * 2048, 8192, 1024), id_w, 1u);
-  }
+  for (int kk = 0; kk < 8; ++kk)  // V~^T = U^T + S^T (-W)^T     (B = -W^T, MN-major, in the V~ buffer)
+    mma_bf16_ts(tbase + tm_u, tbase + TM_STB + kk * 8, smem_desc_sw128(vt + kk * 2048, 8192, 1024), id_w, 1u);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {  // O^T = S^T (Q o Gamma)^T
-    const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
-    mma_bf16_ss(tbase + TM_O, smem_desc_sw128(st + ka, 16, 1024), smem_desc_sw128(qg + ka, 16, 1024), id_q,
-                kk > 0 ? 1u : 0u);
+    const uint32_t kb = (kk >> 2) * KHALF + par * 16384 + (kk & 3) * 32;
+    mma_bf16_ts(tbase + TM_O, tbase + TM_STB + kk * 8, smem_desc_sw128(qg + kb, 16, 1024), id_q, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -305,7 +309,7 @@ __device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t vt, uint32_t 
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
+chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl *ctl = reinterpret_cast<Ctl *>(sm + OFF_CTL);
@@ -325,7 +329,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
   if (tid == 32) {
     for (int b = 0; b < B_COUNT; ++b) mbar_init(smem_u32(&ctl->bar[b]), 1);
     ctl->abort = 0;
-    ctl->nb = 1;
     ctl->slow[0] = ctl->slow[1] = 0;
     ctl->go_c[0] = ctl->go_c[1] = ctl->go_s[0] = ctl->go_s[1] = 0;
     fence_mbar_init();
@@ -342,90 +345,114 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     const int ctid = tid;
     const int qw = warp & 3, ch = warp >> 2;
-    const int o = ctid & 15, rg = ctid >> 4, tile = rg >> 2;  // prologue layout (see Prefetch)
+    // prologue layout: channel octet o (channels [8o, 8o+8)), row group rg
+    // (rows [4rg, 4rg+4)), 16-token tile of those rows
+    const int o = ctid & 15, rg = ctid >> 4, tile = rg >> 2;
     int seq = 0;
-    uint32_t ph_m1 = 0, ph_m23 = 0, ph_v = 0;
-    int issued_v = 0, landed_v = 0;
+    uint32_t ph_m1 = 0, ph_m23 = 0, ph_v = 0, ph_qk = 0, ph_g = 0;
+    Loader ld{&maps, ctl, sm_base, h, {0, 0, 0}, {0, 0, 0}};
     if (ctid == 0 && nchunks > 0) {
-      tma_prefetch_desc(&tmap_v);
-      const uint32_t full = smem_u32(&ctl->bar[B_VFULL]);
-      mbar_arrive_expect_tx(full, 2 * kC * 64 * 2);
-      tma_load_3d(sm_base + OFF_V, &tmap_v, full, 0, h, bos);
-      tma_load_3d(sm_base + OFF_V + 8192, &tmap_v, full, 64, h, bos);
-      issued_v = 1;
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      tma_prefetch_desc(&maps.g);
+      ld.g(bos);
+      ld.qk(bos);
+      ld.v(bos);
     }
-    Prefetch pf;
-    if (nchunks > 0) prefetch_chunk(pf, a, h, bos, min(kC, eos - bos), o, rg, ctid);
-    float *tot = reinterpret_cast<float *>(sm + OFF_TF);  // [16][128] row-group sums (T is not live yet)
+    float beta_next = 0.f;
+    if (ctid < kC && ctid < eos - bos) beta_next = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(bos + ctid) * H + h);
+    // prologue scratch in the T_b buffer: per-tile sums, tile references, chunk totals
+    float *tot = reinterpret_cast<float *>(sm + OFF_ZT);  // [4][128]
+    float *refs = tot + 4 * 128;                          // [4][128]
+    float *gct = refs + 4 * 128;                          // [128]
+    float *gs_w = reinterpret_cast<float *>(sm + OFF_GS);
+    const float *gs = gs_w;
+    uint8_t *qg = sm + OFF_QG;
     bool alive = true;
     for (int m = 0; m < nchunks && alive; ++m) {
       const int par = m & 1;
       const int t0 = bos + m * kC;
       const int len = min(kC, eos - t0);
-      uint8_t *qg = sm + OFF_QG + par * 32768;
       uint8_t *kh = sm + OFF_KH + par * 16384;
       if (m >= 2 && !(alive = group_wait<true>(ctl, B_FREE0 + par, ((m >> 1) - 1) & 1, ctid, seq, A.err))) break;
 
       // ---------------- decay prologue: cumulative log2-decay and scaled operands
-      float G[4][8];
+      // Cumulative sums run channel-pair-major (thread = channel pair p,
+      // 16-row tile t4) and are written back over the log-decay tile, so the
+      // operand pass below can read them in its own layout.
+      if (!(alive = group_wait<true>(ctl, B_GFULL, ph_g, ctid, seq, A.err))) break;
+      ph_g ^= 1u;
+      if (ctid == 0) ld.landed[1] = ld.issued[1];
       {
-        float run[8];
+        const int p = ctid & 63, t4 = ctid >> 6;
+        float2 Gl[16];
+        float2 run = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) run[c] = 0.f;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const float gg[8] = {pf.g[r][0].x, pf.g[r][0].y, pf.g[r][0].z, pf.g[r][0].w,
-                               pf.g[r][1].x, pf.g[r][1].y, pf.g[r][1].z, pf.g[r][1].w};
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            run[c] += gg[c] * kLog2e;
-            G[r][c] = run[c];
-          }
+        for (int r = 0; r < 16; ++r) {
+          const int row = 16 * t4 + r;
+          float2 gv = *reinterpret_cast<const float2 *>(gs + row * kD + 2 * p);
+          if (row >= len) gv = make_float2(0.f, 0.f);  // past the end: identity step
+          run.x += gv.x * kLog2e;
+          run.y += gv.y * kLog2e;
+          Gl[r] = run;
         }
-        *reinterpret_cast<float4 *>(tot + rg * 128 + 8 * o) = make_float4(run[0], run[1], run[2], run[3]);
-        *reinterpret_cast<float4 *>(tot + rg * 128 + 8 * o + 4) = make_float4(run[4], run[5], run[6], run[7]);
-      }
-      if (ctid < kC) ctl->bs[ctid] = pf.beta;
-      bar_chunk();
-      // prefix over the 16 row groups: own offset and chunk total
-      float own[8], GC[8];
-      {
-        float run[8];
+        *reinterpret_cast<float2 *>(tot + t4 * 128 + 2 * p) = run;
+        if (ctid < kC) ctl->bs[ctid] = beta_next;
+        bar_chunk();
+        float2 off = make_float2(0.f, 0.f), tc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) run[c] = own[c] = 0.f;
-#pragma unroll
-        for (int g2 = 0; g2 < 16; ++g2) {
-          if (g2 == rg) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) own[c] = run[c];
-          }
-          const float4 t0v = *reinterpret_cast<const float4 *>(tot + g2 * 128 + 8 * o);
-          const float4 t1v = *reinterpret_cast<const float4 *>(tot + g2 * 128 + 8 * o + 4);
-          run[0] += t0v.x; run[1] += t0v.y; run[2] += t0v.z; run[3] += t0v.w;
-          run[4] += t1v.x; run[5] += t1v.y; run[6] += t1v.z; run[7] += t1v.w;
+        for (int b = 0; b < 4; ++b) {
+          const float2 tb = *reinterpret_cast<const float2 *>(tot + b * 128 + 2 * p);
+          if (b < t4) { off.x += tb.x; off.y += tb.y; }
+          tc.x += tb.x;
+          tc.y += tb.y;
         }
+        *reinterpret_cast<float2 *>(refs + t4 * 128 + 2 * p) = off;  // reference of 16-token tile t4
 #pragma unroll
-        for (int c = 0; c < 8; ++c) GC[c] = run[c];
+        for (int r = 0; r < 16; ++r) {
+          const int row = 16 * t4 + r;
+          *reinterpret_cast<float2 *>(gs_w + row * kD + 2 * p) = make_float2(Gl[r].x + off.x, Gl[r].y + off.y);
+        }
+        if (t4 == 0) *reinterpret_cast<float2 *>(&ctl->gam[par][2 * p]) = make_float2(ex2(tc.x), ex2(tc.y));
+        if (t4 == 0) *reinterpret_cast<float2 *>(gct + 2 * p) = tc;
+        if (t4 == 0 && (tc.x < kSingleRefBound2 || tc.y < kSingleRefBound2)) atomicOr(&ctl->slow[par], 1);
       }
-      float gc[8];
-      bool below = false;
+      if (ctid < kC)  // beta of the next chunk's rows, 0 past the end
+        beta_next = ctid < eos - (t0 + kC)
+                        ? __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + kC + ctid) * H + h)
+                        : 0.f;
+      // q and k tiles of this chunk (the wait's barrier also closes the vote)
+      if (!(alive = group_wait<true>(ctl, B_QKFULL, ph_qk, ctid, seq, A.err))) break;
+      ph_qk ^= 1u;
+      if (ctid == 0) ld.landed[0] = ld.issued[0];
+      const uint32_t half = (uint32_t)(o >> 3), col = (uint32_t)(8 * (o & 7));
+      float G[4][8], gc[8], GC[8];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 a0 = *reinterpret_cast<const float4 *>(gs + (4 * rg + r) * kD + 8 * o);
+        const float4 a1 = *reinterpret_cast<const float4 *>(gs + (4 * rg + r) * kD + 8 * o + 4);
+        G[r][0] = a0.x; G[r][1] = a0.y; G[r][2] = a0.z; G[r][3] = a0.w;
+        G[r][4] = a1.x; G[r][5] = a1.y; G[r][6] = a1.z; G[r][7] = a1.w;
+      }
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
+        gc[c] = ctl->gam[par][8 * o + c];
+        GC[c] = gct[8 * o + c];
+      }
+      uint4 qr[4], kr[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) G[r][c] += own[c];
-        gc[c] = ex2(GC[c]);
-        below |= GC[c] < kSingleRefBound2;
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t row = 4 * rg + r;
+        qr[r] = *reinterpret_cast<const uint4 *>(sm + OFF_KB + half * 8192 + sw128_offset(row, col));
+        kr[r] = *reinterpret_cast<const uint4 *>(sm + OFF_TF + half * 8192 + sw128_offset(row, col));
+        if ((int)row >= len) qr[r] = kr[r] = make_uint4(0u, 0u, 0u, 0u);
       }
-      if (rg == 0) {
-        *reinterpret_cast<float4 *>(&ctl->gam[par][8 * o]) = make_float4(gc[0], gc[1], gc[2], gc[3]);
-        *reinterpret_cast<float4 *>(&ctl->gam[par][8 * o + 4]) = make_float4(gc[4], gc[5], gc[6], gc[7]);
-      }
-      if (below) atomicOr(&ctl->slow[par], 1);
-      bar_chunk();
       const bool slow = ctl->slow[par] != 0;
+      bar_chunk();  // the q tile is read before K / Gamma overwrites it
       if (ctid == 0) ctl->slow[par ^ 1] = 0;
-      const uint32_t half = (uint32_t)(o >> 3), col = (uint32_t)(8 * (o & 7));
-      uint8_t *qg_h = qg + half * 16384;
+      uint8_t *qb_h = qg + half * KHALF + par * 16384;   // Q o Gamma of this parity
+      uint8_t *gk_h = qg + half * KHALF + 8192;          // Gamma o K
       uint8_t *kb_h = sm + OFF_KB + half * 8192;
       uint8_t *kh_h = kh + half * 8192;
       if (!slow) {
@@ -433,8 +460,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
         for (int r = 0; r < 4; ++r) {
           const uint32_t row = 4 * rg + r;
           float qv[8], kv[8], fq[8], fk[8], fb[8], fh[8];
-          unpack8_bf16(pf.q[r], qv);
-          unpack8_bf16(pf.k[r], kv);
+          unpack8_bf16(qr[r], qv);
+          unpack8_bf16(kr[r], kv);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const float e = ex2(G[r][c]), i = ex2(-G[r][c]);
@@ -443,14 +470,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
             fb[c] = kv[c] * i;
             fh[c] = fb[c] * gc[c];
           }
-          st_shared_8bf16(qg_h + sw128_offset(row, col), fq);
-          st_shared_8bf16(qg_h + sw128_offset(64 + row, col), fk);
+          st_shared_8bf16(qb_h + sw128_offset(row, col), fq);
+          st_shared_8bf16(gk_h + sw128_offset(row, col), fk);
           st_shared_8bf16(kb_h + sw128_offset(row, col), fb);
           st_shared_8bf16(kh_h + sw128_offset(row, col), fh);
         }
         group_publish<true>();
         if (ctid == 0) {
-          issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, false);
+          issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, par, false);
           mma_commit(smem_u32(&ctl->bar[B_M1]));
         }
         alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
@@ -462,17 +489,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
           // reference of key tile b: the cumulative decay before its first row
           float ref[8];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) ref[c] = 0.f;
-          for (int g2 = 0; g2 < 4 * b; ++g2) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) ref[c] += tot[g2 * 128 + 8 * o + c];
-          }
+          for (int c = 0; c < 8; ++c) ref[c] = refs[b * 128 + 8 * o + c];
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const uint32_t row = 4 * rg + r;
             float qv[8], kv[8], fq[8], fk[8], fb[8];
-            unpack8_bf16(pf.q[r], qv);
-            unpack8_bf16(pf.k[r], kv);
+            unpack8_bf16(qr[r], qv);
+            unpack8_bf16(kr[r], kv);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               fq[c] = fk[c] = fb[c] = 0.f;
@@ -483,13 +506,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
               }
               if (tile == b) fb[c] = kv[c] * ex2(ref[c] - G[r][c]);
             }
-            st_shared_8bf16(qg_h + sw128_offset(row, col), fq);
-            st_shared_8bf16(qg_h + sw128_offset(64 + row, col), fk);
+            st_shared_8bf16(qb_h + sw128_offset(row, col), fq);
+            st_shared_8bf16(gk_h + sw128_offset(row, col), fk);
             st_shared_8bf16(kb_h + sw128_offset(row, col), fb);
           }
           group_publish<true>();
           if (ctid == 0) {
-            issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, b > 0);
+            issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, par, b > 0);
             mma_commit(smem_u32(&ctl->bar[B_M1]));
           }
           alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
@@ -501,8 +524,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
         for (int r = 0; r < 4; ++r) {
           const uint32_t row = 4 * rg + r;
           float qv[8], kv[8], fq[8], fk[8], fh[8];
-          unpack8_bf16(pf.q[r], qv);
-          unpack8_bf16(pf.k[r], kv);
+          unpack8_bf16(qr[r], qv);
+          unpack8_bf16(kr[r], kv);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const float e = ex2(G[r][c]);
@@ -510,22 +533,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
             fk[c] = kv[c] * e;
             fh[c] = kv[c] * ex2(GC[c] - G[r][c]);
           }
-          st_shared_8bf16(qg_h + sw128_offset(row, col), fq);
-          st_shared_8bf16(qg_h + sw128_offset(64 + row, col), fk);
+          st_shared_8bf16(qb_h + sw128_offset(row, col), fq);
+          st_shared_8bf16(gk_h + sw128_offset(row, col), fk);
           st_shared_8bf16(kh_h + sw128_offset(row, col), fh);
         }
       }
       if (!alive) break;
-      // next chunk's inputs travel while this one computes
-      if (m + 1 < nchunks) prefetch_chunk(pf, a, h, t0 + kC, min(kC, eos - t0 - kC), o, rg, ctid);
+      if (ctid == 0 && m + 1 < nchunks) ld.g(t0 + kC);  // the cumulative sums have been consumed
 
       // ---------------- masks, L, and T_b = (I + L)^{-1} diag(beta)
       {
         float *Lf = reinterpret_cast<float *>(sm + OFF_KB);  // K / Gamma is dead once M1 is done
         float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
-        float *Xf = reinterpret_cast<float *>(sm + OFF_XF);
-        if (qw < 2) {
-          const int r = 32 * qw + lane;
+        float *Xf = reinterpret_cast<float *>(sm + OFF_ZT);  // [3][16][16] scratch before T_b lands
+        // even chunks: TMEM lanes 0..63 hold A's rows, 64..127 L''; odd chunks the reverse
+        const bool a_rows = (qw < 2) == (par == 0);
+        const int r = 32 * (qw & 1) + lane;
+        if (a_rows) {
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             float v[16];
@@ -537,7 +561,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
             st_row16_bf16(sm + OFF_AM + par * 8192, r, s0, v);
           }
         } else {
-          const int r = 32 * (qw - 2) + lane;
           const float br = ctl->bs[r];
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
@@ -554,75 +577,105 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
           }
         }
         bar_chunk();
-        // Diagonal 16x16 blocks by forward substitution, one column per thread:
-        // x = e_c - L_blk x with x[m] = 0 for m < c, written without branches.
+        // Diagonal 16x16 blocks, one column per thread, right-looking: once
+        // x[m] is final it is subtracted from every later row, so the
+        // dependent chain is one multiply-add per row.  Entries above the
+        // diagonal come out as 0.
         if (ctid < 64) {
           const int ab = ctid >> 4, cc = ctid & 15, base = 16 * ab;
           float x[16];
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) {
-            float acc = (rr == cc) ? 1.f : 0.f;
+          for (int rr = 0; rr < 16; ++rr) x[rr] = (rr == cc) ? 1.f : 0.f;
 #pragma unroll
-            for (int mm = 0; mm < rr; ++mm) acc -= Lf[swz64(base + rr, base + mm)] * x[mm];
-            x[rr] = acc;
-            Tf[swz64(base + rr, base + cc)] = acc;
+          for (int mm = 0; mm < 16; ++mm) {
+#pragma unroll
+            for (int rr = mm + 1; rr < 16; ++rr) x[rr] -= Lf[swz64(base + rr, base + mm)] * x[mm];
           }
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) Tf[swz64(base + rr, base + cc)] = x[rr];
         }
         bar_chunk();
-        // Off-diagonal blocks by distance d: T_ab = -T_aa sum_{c=b}^{a-1} L_ac T_cb.
-        // One thread per (block, row, 4-column group); blocks above the
-        // diagonal are never read (T_b below masks them).
-#pragma unroll 1
-        for (int d = 1; d < 4; ++d) {
-          const int ntask = (4 - d) * 64;
-          const int b = ctid >> 6, ab = b + d, rr = (ctid >> 2) & 15, c0 = 16 * b + 4 * (ctid & 3);
-          if (ctid < ntask) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cb = b; cb < ab; ++cb) {
-#pragma unroll
-              for (int mm = 0; mm < 16; ++mm) {
-                const float l = Lf[swz64(16 * ab + rr, 16 * cb + mm)];
-                const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(16 * cb + mm, c0));
-                acc.x += l * t.x; acc.y += l * t.y; acc.z += l * t.z; acc.w += l * t.w;
-              }
-            }
-            *reinterpret_cast<float4 *>(Xf + (b * 16 + rr) * 16 + 4 * (ctid & 3)) = acc;
-          }
-          bar_chunk();
-          if (ctid < ntask) {
+        // Off-diagonal blocks in two levels of the 2x2 block inverse
+        // [[P, 0], [R, Q]]^{-1} = [[P^-1, 0], [-Q^-1 R P^-1, Q^-1]]:
+        //   level 1 (16-row blocks): T_10 and T_32;
+        //   level 2 (32-row blocks): T_[23][01] = -T_[23][23] L_[23][01] T_[01][01].
+        // One thread per (row, 4-column group) of each output; X is scratch.
+        // Blocks above the diagonal are never read (T_b below masks them).
+        {
+          // level 1: two 16x16 outputs, 128 tasks
+          const int blk = ctid >> 6, rr = (ctid >> 2) & 15, q4 = ctid & 3;
+          const int rb = 16 * (2 * blk + 1), cb = 16 * (2 * blk);  // output block (rb, cb)
+          if (ctid < 128) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int mm = 0; mm < 16; ++mm) {
-              const float l = Tf[swz64(16 * ab + rr, 16 * ab + mm)];
-              const float4 x = *reinterpret_cast<const float4 *>(Xf + (b * 16 + mm) * 16 + 4 * (ctid & 3));
-              acc.x += l * x.x; acc.y += l * x.y; acc.z += l * x.z; acc.w += l * x.w;
+              const float l = Lf[swz64(rb + rr, cb + mm)];
+              const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(cb + mm, cb + 4 * q4));
+              acc.x += l * t.x; acc.y += l * t.y; acc.z += l * t.z; acc.w += l * t.w;
             }
-            *reinterpret_cast<float4 *>(Tf + swz64(16 * ab + rr, c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            *reinterpret_cast<float4 *>(Xf + (blk * 16 + rr) * 16 + 4 * q4) = acc;
+          }
+          bar_chunk();
+          if (ctid < 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int mm = 0; mm < 16; ++mm) {
+              const float l = Tf[swz64(rb + rr, rb + mm)];
+              const float4 xv = *reinterpret_cast<const float4 *>(Xf + (blk * 16 + mm) * 16 + 4 * q4);
+              acc.x += l * xv.x; acc.y += l * xv.y; acc.z += l * xv.z; acc.w += l * xv.w;
+            }
+            *reinterpret_cast<float4 *>(Tf + swz64(rb + rr, cb + 4 * q4)) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
           }
           bar_chunk();
         }
         {
-          const int r = ctid >> 2, s0 = (ctid & 3) * 16;
-          const bool upper = (ctid & 3) > (r >> 4);  // block above the diagonal: T is zero there
+          // level 2: the 32x32 block below the diagonal, 256 tasks
+          const int rr = ctid >> 3, q4 = ctid & 7;  // output row 32 + rr, columns 4 q4 .. 4 q4 + 3
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int mm = 0; mm < 32; ++mm) {  // X = L_[23][01] T_[01][01]  (T lower triangular)
+            if (mm < 16 && q4 >= 4) continue;  // block (0,1) of T is zero (never stored)
+            const float l = Lf[swz64(32 + rr, mm)];
+            const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(mm, 4 * q4));
+            acc.x += l * t.x; acc.y += l * t.y; acc.z += l * t.z; acc.w += l * t.w;
+          }
+          *reinterpret_cast<float4 *>(Xf + rr * 32 + 4 * q4) = acc;
+          bar_chunk();
+          acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int mm = 0; mm < 32; ++mm) {  // -T_[23][23] X
+            if (mm >= 16 && rr < 16) continue;  // block (2,3) of T is zero (never stored)
+            const float l = Tf[swz64(32 + rr, 32 + mm)];
+            const float4 xv = *reinterpret_cast<const float4 *>(Xf + mm * 32 + 4 * q4);
+            acc.x += l * xv.x; acc.y += l * xv.y; acc.z += l * xv.z; acc.w += l * xv.w;
+          }
+          *reinterpret_cast<float4 *>(Tf + swz64(32 + rr, 4 * q4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+          bar_chunk();
+        }
+        {
+          const int rr = ctid >> 2, s0 = (ctid & 3) * 16;
+          const bool upper = (ctid & 3) > (rr >> 4);  // block above the diagonal: T is zero there
           float v[16];
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(r, s0 + 4 * c4));
+            const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(rr, s0 + 4 * c4));
             v[4 * c4] = upper ? 0.f : t.x * ctl->bs[s0 + 4 * c4];
             v[4 * c4 + 1] = upper ? 0.f : t.y * ctl->bs[s0 + 4 * c4 + 1];
             v[4 * c4 + 2] = upper ? 0.f : t.z * ctl->bs[s0 + 4 * c4 + 2];
             v[4 * c4 + 3] = upper ? 0.f : t.w * ctl->bs[s0 + 4 * c4 + 3];
           }
-          st_row16_bf16(sm + OFF_ZT, r, s0, v);
+          st_row16_bf16(sm + OFF_ZT, rr, s0, v);
         }
       }
       group_publish<true>();
 
       // ---------------- U^T and W^T; then hand the chunk to the state group
       if (ctid == 0) {
+        if (m + 1 < nchunks) ld.qk(t0 + kC);  // L and T are dead: their space takes the next q, k
         bool ok = solo_wait(ctl, B_VFULL, ph_v, A.err);
         ph_v ^= 1u;
-        landed_v = ok ? issued_v : landed_v;
+        if (ok) ld.landed[2] = ld.issued[2];
         if (ok && m >= 1) ok = solo_wait(ctl, B_WFREE, (m - 1) & 1, A.err);
         if (ok) {
           issue_m23(tbase, sm_base + OFF_V, smem_u32(qg), sm_base + OFF_ZT, TM_U + par * 64);
@@ -630,13 +683,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
           ok = solo_wait(ctl, B_M23, ph_m23, A.err);
           ph_m23 ^= 1u;
         }
-        if (ok && m + 1 < nchunks) {  // the V buffer is free again
-          const uint32_t full = smem_u32(&ctl->bar[B_VFULL]);
-          mbar_arrive_expect_tx(full, 2 * kC * 64 * 2);
-          tma_load_3d(sm_base + OFF_V, &tmap_v, full, 0, h, t0 + kC);
-          tma_load_3d(sm_base + OFF_V + 8192, &tmap_v, full, 64, h, t0 + kC);
-          ++issued_v;
-        }
+        if (ok && m + 1 < nchunks) ld.v(t0 + kC);  // the v buffer is free again
         if (ok) mbar_arrive(smem_u32(&ctl->bar[B_READY0 + par]));
         ctl->go_c[seq & 1] = ok && !ctl->abort;
       }
@@ -645,11 +692,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
       ++seq;
     }
     if (ctid == 0) {
-      // outstanding V copy (only after an abort) and this group's MMAs
+      ld.drain(A.err);
       volatile int no_abort = 0;
-      if (issued_v > landed_v) mbar_wait(smem_u32(&ctl->bar[B_VFULL]), ph_v, &no_abort, A.err, 1u << 20);
       mma_commit(smem_u32(&ctl->bar[B_TD_C]));
-      mbar_wait(smem_u32(&ctl->bar[B_TD_C]), 0, &no_abort, A.err, 1u << 21);
+      mbar_wait(smem_u32(&ctl->bar[B_TD_C]), 0, &no_abort, A.err, 1u << 23);
     }
   } else {
     // =========================================================== state group
@@ -659,15 +705,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
     const int j = stid;
     int seq = 0;
     uint32_t ph_m4 = 0, ph_m56 = 0;
-    // initial state -> TMEM (fp32 master) and the bf16 operand S^T
+    uint8_t *vt = sm + OFF_VT;
+    // initial state -> TMEM: fp32 master and the bf16 copy M4 reads
 #pragma unroll 1
-    for (int blk = 0; blk < 8; ++blk) {
-      const int i0 = 16 * blk;
-      float s[16];
+    for (int i0 = 0; i0 < kD; i0 += 32) {
+      float s[32];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) s[c] = a.s0 ? a.s0[sbase + (size_t)(i0 + c) * kD + j] : 0.f;
-      tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
-      st_row16_bf16(sm + OFF_ST + (blk >> 2) * 16384, j, 16 * (blk & 3), s);
+      for (int c = 0; c < 32; ++c) s[c] = a.s0 ? a.s0[sbase + (size_t)(i0 + c) * kD + j] : 0.f;
+      tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), *reinterpret_cast<float(*)[16]>(s));
+      tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0 + 16), *reinterpret_cast<float(*)[16]>(s + 16));
+      tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_STB + i0 / 2), s);
     }
     tmem_wait_st();
     group_publish<false>();
@@ -676,51 +723,49 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
       const int par = c & 1;
       const int t0 = bos + c * kC;
       const int len = min(kC, eos - t0);
-      uint8_t *qg = sm + OFF_QG + par * 32768;
       const uint32_t tm_u = TM_U + par * 64;
       if (!(alive = group_wait<false>(ctl, B_READY0 + par, (c >> 1) & 1, stid, seq, A.err))) break;
 
-      // ---------------- -W^T (TMEM) -> MN-major operand in QG rows 64..127
+      // ---------------- -W^T (TMEM) -> MN-major operand in the V~ buffer
       {
-        uint8_t *dst = qg + (j >> 6) * 16384 + 8192;
-        const uint32_t row = j & 63;
+        float v[64];
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_W), *reinterpret_cast<float(*)[32]>(v));
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_W + 32), *reinterpret_cast<float(*)[32]>(v + 32));
+        tmem_wait_ld();
 #pragma unroll
-        for (int r0 = 0; r0 < 64; r0 += 16) {
-          float v[16];
-          tmem_ld16(tmem_addr(tbase, 32 * qw, TM_W + r0), v);
-          tmem_wait_ld();
+        for (int cc = 0; cc < 64; ++cc) v[cc] = -v[cc];
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) v[cc] = -v[cc];
-          st_row16_bf16(dst, row, r0, v);
-        }
+        for (int r0 = 0; r0 < 64; r0 += 16) st_row16_bf16(vt, j, r0, v + r0);
       }
       group_publish<false>();
       if (stid == 0) {
         mbar_arrive(smem_u32(&ctl->bar[B_WFREE]));
-        issue_m4(tbase, sm_base + OFF_ST, smem_u32(qg), tm_u);
+        issue_m4(tbase, sm_base + OFF_VT, sm_base + OFF_QG, par, tm_u);
         mma_commit(smem_u32(&ctl->bar[B_M4]));
       }
       if (!(alive = group_wait<false>(ctl, B_M4, ph_m4, stid, seq, A.err))) break;
       ph_m4 ^= 1u;
 
       // ---------------- V~^T -> bf16 operand; S^T <- S^T Diag(gamma_C)
-#pragma unroll
-      for (int r0 = 0; r0 < 64; r0 += 16) {
-        float v[16];
-        tmem_ld16(tmem_addr(tbase, 32 * qw, tm_u + r0), v);
+      {
+        float v[64];
+        tmem_ld32(tmem_addr(tbase, 32 * qw, tm_u), *reinterpret_cast<float(*)[32]>(v));
+        tmem_ld32(tmem_addr(tbase, 32 * qw, tm_u + 32), *reinterpret_cast<float(*)[32]>(v + 32));
         tmem_wait_ld();
-        st_row16_bf16(sm + OFF_VT, j, r0, v);
+#pragma unroll
+        for (int r0 = 0; r0 < 64; r0 += 16) st_row16_bf16(vt, j, r0, v + r0);
       }
       {
         const float *gam = ctl->gam[par];
-#pragma unroll 2
-        for (int i0 = 0; i0 < 128; i0 += 16) {
-          float s[16];
-          tmem_ld16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
+#pragma unroll 1
+        for (int i0 = 0; i0 < kD; i0 += 32) {
+          float s[32];
+          tmem_ld32(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
           tmem_wait_ld();
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) s[cc] *= gam[i0 + cc];
-          tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
+          for (int cc = 0; cc < 32; ++cc) s[cc] *= gam[i0 + cc];
+          tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), *reinterpret_cast<float(*)[16]>(s));
+          tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0 + 16), *reinterpret_cast<float(*)[16]>(s + 16));
         }
         tmem_wait_st();
       }
@@ -733,28 +778,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
       ph_m56 ^= 1u;
 
       // ---------------- bf16 copy of the new state; the output rows
-#pragma unroll 2
-      for (int i0 = 0; i0 < 128; i0 += 16) {
-        float s[16];
-        tmem_ld16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
+#pragma unroll 1
+      for (int i0 = 0; i0 < kD; i0 += 32) {
+        float s[32];
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
         tmem_wait_ld();
-        st_row16_bf16(sm + OFF_ST + (i0 >> 6) * 16384, j, i0 & 63, s);
+        tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_STB + i0 / 2), s);
       }
       {
-        __nv_bfloat16 *ostage = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT);
+        __nv_bfloat16 *ostage = reinterpret_cast<__nv_bfloat16 *>(vt);
+        float v[64];
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_O), *reinterpret_cast<float(*)[32]>(v));
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_O + 32), *reinterpret_cast<float(*)[32]>(v + 32));
+        tmem_wait_ld();
 #pragma unroll
-        for (int r0 = 0; r0 < 64; r0 += 16) {
-          float v[16];
-          tmem_ld16(tmem_addr(tbase, 32 * qw, TM_O + r0), v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int cc = 0; cc < 16; ++cc) ostage[(r0 + cc) * kD + j] = __float2bfloat16_rn(v[cc]);
-        }
+        for (int cc = 0; cc < 64; ++cc) ostage[cc * kD + j] = __float2bfloat16_rn(v[cc]);
       }
+      tmem_wait_st();
       tc_fence_before();
       bar_state();
       {
-        const uint4 *src = reinterpret_cast<const uint4 *>(sm + OFF_VT);
+        const uint4 *src = reinterpret_cast<const uint4 *>(vt);
         uint4 *o = reinterpret_cast<uint4 *>(a.o);
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
@@ -767,18 +811,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, TcArgs A) {
     }
     if (alive && a.sT) {
 #pragma unroll 1
-      for (int i0 = 0; i0 < 128; i0 += 16) {
-        float s[16];
-        tmem_ld16(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
+      for (int i0 = 0; i0 < kD; i0 += 32) {
+        float s[32];
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
         tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) a.sT[sbase + (size_t)(i0 + cc) * kD + j] = s[cc];
+        for (int cc = 0; cc < 32; ++cc) a.sT[sbase + (size_t)(i0 + cc) * kD + j] = s[cc];
       }
     }
     if (stid == 0) {
       volatile int no_abort = 0;
       mma_commit(smem_u32(&ctl->bar[B_TD_S]));
-      mbar_wait(smem_u32(&ctl->bar[B_TD_S]), 0, &no_abort, A.err, 1u << 22);
+      mbar_wait(smem_u32(&ctl->bar[B_TD_S]), 0, &no_abort, A.err, 1u << 24);
     }
   }
 
@@ -804,6 +848,22 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
+// [T_total, H, 128] row-major tensor; boxes of 64 tokens of one head.
+CUresult encode_tok_head(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const void *base, int T, int H,
+                         bool fp32) {
+  const cuuint64_t esz = fp32 ? 4 : 2;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * esz, (cuuint64_t)H * kD * esz};
+  // bf16: two 64-column boxes with the 128-byte swizzle the MMA operands use;
+  // fp32: the whole 512-byte row, unswizzled
+  const cuuint32_t box[3] = {fp32 ? (cuuint32_t)kD : 64u, 1, (cuuint32_t)kC};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             fp32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 }  // namespace
 
 bool chunk_tc_supports(const PrefillArgs &a) {
@@ -815,15 +875,12 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
   if (a.N * a.H == 0) return cudaSuccess;
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
-  CUtensorMap tmap;
-  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)a.H, (cuuint64_t)(a.T_total > 0 ? a.T_total : 1)};
-  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)a.H * kD * 2};
-  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kC};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.v), dims, strides, box,
-                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcMaps maps;
+  if (encode_tok_head(encode, &maps.q, a.q, a.T_total, a.H, false) != CUDA_SUCCESS ||
+      encode_tok_head(encode, &maps.k, a.k, a.T_total, a.H, false) != CUDA_SUCCESS ||
+      encode_tok_head(encode, &maps.v, a.v, a.T_total, a.H, false) != CUDA_SUCCESS ||
+      encode_tok_head(encode, &maps.g, a.g, a.T_total, a.H, true) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -831,7 +888,7 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
   e = cudaGetSymbolAddress(&wd, g_tc_watchdog);
   if (e != cudaSuccess) return e;
   TcArgs args{a, reinterpret_cast<unsigned int *>(wd)};
-  chunk_tc_kernel<<<a.N * a.H, kThreads, SMEM_BYTES, s>>>(tmap, args);
+  chunk_tc_kernel<<<a.N * a.H, kThreads, SMEM_BYTES, s>>>(maps, args);
   return cudaGetLastError();
 }
 
