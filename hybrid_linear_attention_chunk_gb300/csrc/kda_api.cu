@@ -153,15 +153,58 @@ kda_status check_prefill(const kda_chunk_desc *d, const void *q, const void *k, 
   return KDA_OK;
 }
 
-kda_status run_prefill(const kda_chunk_desc *d, const PrefillArgs &a, cudaStream_t s) {
+// ws_mode 0: a split plan allocates its workspace stream-ordered on s;
+// ws_mode 1: the caller's (ws, ws_bytes) is used.
+kda_status run_prefill(const kda_chunk_desc *d, const PrefillArgs &a, cudaStream_t s, int ws_mode, void *ws,
+                       size_t ws_bytes) {
+  const bool tc = chunk_tc_supports(a);
+  if (d->kernel == KDA_KERNEL_TC && !tc) return KDA_ERR_UNSUPPORTED;
+  const bool use_tc = d->kernel != KDA_KERNEL_SIMT && tc;
+  if (d->segments > 1 && (!use_tc || a.cu)) return KDA_ERR_UNSUPPORTED;
+  const SegPlan pl = use_tc ? plan_segments(a, d->segments) : SegPlan{1, 0, 0};
+  if (pl.P > 1 && ws_mode == 1) {
+    if (!ws) return KDA_ERR_NULL;
+    if (ws_bytes < pl.ws_bytes) return KDA_ERR_SHAPE;
+    if (!aligned16(ws)) return KDA_ERR_ALIGN;
+  }
   if (d->validate) {
     kda_status st = run_validation(s, [&](int *flag) { return launch_validate_prefill(a, flag, s); });
     if (st != KDA_OK) return st;
   }
-  bool tc = chunk_tc_supports(a);
-  if (d->kernel == KDA_KERNEL_TC && !tc) return KDA_ERR_UNSUPPORTED;
-  cudaError_t e = (d->kernel != KDA_KERNEL_SIMT && tc) ? launch_chunk_tc(a, s) : launch_chunk_simt(a, s);
+  cudaError_t e;
+  if (pl.P <= 1) {
+    e = use_tc ? launch_chunk_tc(a, s) : launch_chunk_simt(a, s);
+  } else if (ws_mode == 1) {
+    e = launch_chunk_tc_segmented(a, pl, ws, s);
+  } else {
+    void *tmp = nullptr;
+    e = cudaMallocAsync(&tmp, pl.ws_bytes, s);
+    if (e == cudaSuccess) {
+      e = launch_chunk_tc_segmented(a, pl, tmp, s);
+      cudaError_t ef = cudaFreeAsync(tmp, s);
+      if (e == cudaSuccess) e = ef;
+    }
+  }
   if (e != cudaSuccess) return cuda_fail(e);
+  return KDA_OK;
+}
+
+// Arguments as far as sizes go (for the workspace query, which has no pointers).
+kda_status args_from_desc(const kda_chunk_desc *d, PrefillArgs *a) {
+  if (!dtype_ok(d->qkv_dtype) || !dtype_ok(d->out_dtype) || !dtype_ok(d->gate_dtype)) return KDA_ERR_DTYPE;
+  if (d->H <= 0 || !dim_ok(d->dk) || !dim_ok(d->dv) || d->T < 0 || d->B <= 0) return KDA_ERR_SHAPE;
+  if (!(d->chunk == 16 || d->chunk == 32 || d->chunk == 64) || d->segments < 0) return KDA_ERR_SHAPE;
+  const bool varlen = d->num_seqs > 0;
+  if (varlen && d->B != 1) return KDA_ERR_SHAPE;
+  a->N = varlen ? d->num_seqs : d->B;
+  a->T_total = varlen ? d->T : d->B * d->T;
+  a->T_seq = varlen ? 0 : d->T;
+  a->H = d->H; a->dk = d->dk; a->dv = d->dv; a->chunk = d->chunk;
+  a->qkv = d->qkv_dtype; a->out = d->out_dtype; a->gate = d->gate_dtype;
+  a->q = a->k = a->v = a->g = a->beta = nullptr;
+  a->s0 = nullptr; a->o = nullptr; a->sT = nullptr;
+  static const int32_t dummy = 0;
+  a->cu = varlen ? &dummy : nullptr;  // only its presence matters to the planner
   return KDA_OK;
 }
 
@@ -191,12 +234,20 @@ kda_status kda_chunk_fwd(const kda_chunk_desc *desc, const void *q, const void *
   kda_status st = check_prefill(desc, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
                                 final_state, &a);
   if (st != KDA_OK) return st;
-  return run_prefill(desc, a, reinterpret_cast<cudaStream_t>(stream));
+  return run_prefill(desc, a, reinterpret_cast<cudaStream_t>(stream), 0, nullptr, 0);
 }
 
 kda_status kda_chunk_fwd_workspace_size(const kda_chunk_desc *desc, size_t *bytes) {
   if (!desc || !bytes) return KDA_ERR_NULL;
   *bytes = 0;
+  PrefillArgs a;
+  kda_status st = args_from_desc(desc, &a);
+  if (st != KDA_OK) return st;
+  const bool tc = chunk_tc_supports(a);
+  if (desc->kernel == KDA_KERNEL_TC && !tc) return KDA_ERR_UNSUPPORTED;
+  const bool use_tc = desc->kernel != KDA_KERNEL_SIMT && tc;
+  if (desc->segments > 1 && (!use_tc || a.cu)) return KDA_ERR_UNSUPPORTED;
+  if (use_tc) *bytes = plan_segments(a, desc->segments).ws_bytes;
   return KDA_OK;
 }
 
@@ -205,10 +256,11 @@ kda_status kda_chunk_fwd_ex(const kda_chunk_desc *desc, const void *q, const voi
                             const float *initial_state, const int32_t *cu_seqlens, void *out,
                             float *final_state, void *workspace, size_t workspace_bytes,
                             kda_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
-  return kda_chunk_fwd(desc, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
-                       final_state, stream);
+  PrefillArgs a;
+  kda_status st = check_prefill(desc, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                                final_state, &a);
+  if (st != KDA_OK) return st;
+  return run_prefill(desc, a, reinterpret_cast<cudaStream_t>(stream), 1, workspace, workspace_bytes);
 }
 
 kda_status kda_decode_step(const kda_decode_desc *d, const void *q, const void *k, const void *v,

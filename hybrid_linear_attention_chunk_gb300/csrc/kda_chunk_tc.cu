@@ -316,11 +316,28 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   const PrefillArgs &a = A.a;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H;
-  const int n = blockIdx.x / H, h = blockIdx.x % H;
+  // work item: (sequence n, segment, head h, kind) -- see PrefillArgs
+  int item = blockIdx.x;
+  const int kind = item % a.kinds;
+  item /= a.kinds;
+  const int h = item % H;
+  item /= H;
+  const int seg = item % a.nseg, n = item / a.nseg;
   int bos, eos;
   seq_range(a, n, bos, eos);
+  if (a.seg_tokens > 0) {
+    const int sb = min(eos, bos + seg * a.seg_tokens);
+    eos = min(eos, sb + a.seg_tokens);
+    bos = sb;
+  }
   const int nchunks = (eos - bos + kC - 1) / kC;
-  const size_t sbase = ((size_t)n * H + h) * kD * kD;
+  const bool zero_v = kind == 1;  // transition pass: v = 0, identity entry state
+  const float *s_in = (kind == 0 && a.s0) ? a.s0 + (((size_t)n * a.nseg + seg) * H + h) * kD * kD : nullptr;
+  float *s_out = nullptr;
+  if (a.sT) {
+    if (a.kinds == 2) s_out = a.sT + ((((size_t)kind * a.N + n) * a.nseg + seg) * H + h) * kD * kD;
+    else if (seg == a.nseg - 1) s_out = a.sT + ((size_t)n * H + h) * kD * kD;
+  }
 
   if (warp == 0) {
     tmem_alloc(smem_u32(&ctl->tmem_slot), 512);
@@ -358,8 +375,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       tma_prefetch_desc(&maps.g);
       ld.g(bos);
       ld.qk(bos);
-      ld.v(bos);
+      if (!zero_v) ld.v(bos);
     }
+    if (zero_v)  // the v tile stays zero for the whole item
+      for (int e = ctid; e < 16384 / 16; e += kChunkThreads)
+        reinterpret_cast<uint4 *>(sm + OFF_V)[e] = make_uint4(0u, 0u, 0u, 0u);
     float beta_next = 0.f;
     if (ctid < kC && ctid < eos - bos) beta_next = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(bos + ctid) * H + h);
     // prologue scratch in the T_b buffer: per-tile sums, tile references, chunk totals
@@ -673,9 +693,12 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // ---------------- U^T and W^T; then hand the chunk to the state group
       if (ctid == 0) {
         if (m + 1 < nchunks) ld.qk(t0 + kC);  // L and T are dead: their space takes the next q, k
-        bool ok = solo_wait(ctl, B_VFULL, ph_v, A.err);
-        ph_v ^= 1u;
-        if (ok) ld.landed[2] = ld.issued[2];
+        bool ok = true;
+        if (!zero_v) {
+          ok = solo_wait(ctl, B_VFULL, ph_v, A.err);
+          ph_v ^= 1u;
+          if (ok) ld.landed[2] = ld.issued[2];
+        }
         if (ok && m >= 1) ok = solo_wait(ctl, B_WFREE, (m - 1) & 1, A.err);
         if (ok) {
           issue_m23(tbase, sm_base + OFF_V, smem_u32(qg), sm_base + OFF_ZT, TM_U + par * 64);
@@ -683,7 +706,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           ok = solo_wait(ctl, B_M23, ph_m23, A.err);
           ph_m23 ^= 1u;
         }
-        if (ok && m + 1 < nchunks) ld.v(t0 + kC);  // the v buffer is free again
+        if (ok && !zero_v && m + 1 < nchunks) ld.v(t0 + kC);  // the v buffer is free again
         if (ok) mbar_arrive(smem_u32(&ctl->bar[B_READY0 + par]));
         ctl->go_c[seq & 1] = ok && !ctl->abort;
       }
@@ -706,12 +729,14 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     int seq = 0;
     uint32_t ph_m4 = 0, ph_m56 = 0;
     uint8_t *vt = sm + OFF_VT;
-    // initial state -> TMEM: fp32 master and the bf16 copy M4 reads
+    // entry state -> TMEM: fp32 master and the bf16 copy M4 reads (S^T row j;
+    // the identity for a transition item, zero without an initial state)
 #pragma unroll 1
     for (int i0 = 0; i0 < kD; i0 += 32) {
       float s[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) s[c] = a.s0 ? a.s0[sbase + (size_t)(i0 + c) * kD + j] : 0.f;
+      for (int c = 0; c < 32; ++c)
+        s[c] = zero_v ? (i0 + c == j ? 1.f : 0.f) : (s_in ? s_in[(size_t)(i0 + c) * kD + j] : 0.f);
       tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), *reinterpret_cast<float(*)[16]>(s));
       tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0 + 16), *reinterpret_cast<float(*)[16]>(s + 16));
       tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_STB + i0 / 2), s);
@@ -797,7 +822,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       tmem_wait_st();
       tc_fence_before();
       bar_state();
-      {
+      if (a.o) {  // segment passes of the long-sequence plan write no output
         const uint4 *src = reinterpret_cast<const uint4 *>(vt);
         uint4 *o = reinterpret_cast<uint4 *>(a.o);
 #pragma unroll
@@ -809,14 +834,14 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       group_publish<false>();
       if (stid == 0) mbar_arrive(smem_u32(&ctl->bar[B_FREE0 + par]));
     }
-    if (alive && a.sT) {
+    if (alive && s_out) {
 #pragma unroll 1
       for (int i0 = 0; i0 < kD; i0 += 32) {
         float s[32];
         tmem_ld32(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
         tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) a.sT[sbase + (size_t)(i0 + cc) * kD + j] = s[cc];
+        for (int cc = 0; cc < 32; ++cc) s_out[(size_t)(i0 + cc) * kD + j] = s[cc];
       }
     }
     if (stid == 0) {
@@ -888,7 +913,7 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
   e = cudaGetSymbolAddress(&wd, g_tc_watchdog);
   if (e != cudaSuccess) return e;
   TcArgs args{a, reinterpret_cast<unsigned int *>(wd)};
-  chunk_tc_kernel<<<a.N * a.H, kThreads, SMEM_BYTES, s>>>(maps, args);
+  chunk_tc_kernel<<<a.N * a.nseg * a.H * a.kinds, kThreads, SMEM_BYTES, s>>>(maps, args);
   return cudaGetLastError();
 }
 

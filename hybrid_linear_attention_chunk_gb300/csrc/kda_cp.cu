@@ -1,0 +1,149 @@
+// Long sequences: in-device context parallelism through segment affine pairs.
+//
+// Cited page: "Kimi K3：从 3T 稀疏预训练到百万 Token Agent 的端到端扩展"
+// (liuzhao09.github.io/papers/kimi-k3), [K3-notes] below.
+//
+// [K3-notes §2.5, context-parallel affine pair]: a segment maps any entry
+// state to S_out = S~ + M S_in, and pairs compose.  When a batch has too few
+// (sequence, head) chains to fill the GPU, every sequence is cut into P
+// segments of whole chunks and
+//   pass 1  runs each of the first P-1 segments twice with the tensor-core
+//           kernel: from S = 0 with the real v (final state S~), and from
+//           S = I with v = 0 (final state M, the product of the segment's
+//           transitions); no outputs;
+//   pass 2  chains the entry states E_0 = S_0, E_{p+1} = S~_p + M_p E_p
+//           (fp32, one CTA per chain);
+//   pass 3  reruns every segment from its entry state, writing o, and the
+//           last segment writes the final state.
+// Every chain's segments run in parallel in passes 1 and 3.  Kernel
+// boundaries order the passes; no kernel waits on another.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kScanThreads = 256;
+
+// One CTA per (sequence n, head h).  pairs: [2][N][P-1][H][D][D] (S~ then M),
+// E: [N][P][H][D][D].  E_p lives in shared memory between steps.
+__global__ void __launch_bounds__(kScanThreads)
+cp_scan_kernel(int N, int H, int P, const float *__restrict__ s0, const float *__restrict__ pairs,
+               float *__restrict__ E) {
+  extern __shared__ float sE[];  // [2][D][D]
+  const int nh = blockIdx.x, n = nh / H, h = nh % H;
+  const int tid = threadIdx.x, j = tid & (kD - 1), half = tid >> 7;
+  const size_t DD = (size_t)kD * kD;
+  const size_t pair_stride = (size_t)N * (P - 1) * H * DD;  // S~ -> M
+  for (int e = tid; e < kD * kD; e += kScanThreads) {
+    const float v = s0 ? s0[((size_t)n * H + h) * DD + e] : 0.f;
+    sE[e] = v;
+    E[(((size_t)n * P + 0) * H + h) * DD + e] = v;
+  }
+  __syncthreads();
+  for (int p = 0; p + 1 < P; ++p) {
+    const float *Ecur = sE + (p & 1) * kD * kD;
+    float *Enext = sE + ((p + 1) & 1) * kD * kD;
+    const float *St = pairs + (((size_t)n * (P - 1) + p) * H + h) * DD;
+    const float *M = St + pair_stride;
+    float *Eg = E + (((size_t)n * P + p + 1) * H + h) * DD;
+    // rows [64 half, 64 half + 64) of column j
+    for (int i = 64 * half; i < 64 * half + 64; ++i) {
+      const float *Mi = M + (size_t)i * kD;
+      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll 8
+      for (int m = 0; m < kD; m += 4) {
+        const float4 mv = __ldg(reinterpret_cast<const float4 *>(Mi + m));
+        acc0 += mv.x * Ecur[(m + 0) * kD + j];
+        acc1 += mv.y * Ecur[(m + 1) * kD + j];
+        acc2 += mv.z * Ecur[(m + 2) * kD + j];
+        acc3 += mv.w * Ecur[(m + 3) * kD + j];
+      }
+      const float v = St[(size_t)i * kD + j] + ((acc0 + acc1) + (acc2 + acc3));
+      Enext[i * kD + j] = v;
+      Eg[(size_t)i * kD + j] = v;
+    }
+    __syncthreads();
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+}  // namespace
+
+// Chooses the number of segments per sequence.  requested: 0 = automatic,
+// 1 = never split, >1 = that many (fewer if the sequence has fewer chunks).
+SegPlan plan_segments(const PrefillArgs &a, int requested) {
+  SegPlan pl;
+  pl.P = 1;
+  pl.seg_tokens = 0;
+  pl.ws_bytes = 0;
+  if (requested == 1 || a.cu != nullptr || !chunk_tc_supports(a) || a.T_seq <= 0) return pl;
+  const long long nc = (a.T_seq + a.chunk - 1) / a.chunk;  // chunks per sequence
+  const long long chains = (long long)a.N * a.H;
+  int P = 1;
+  if (requested > 1) {
+    P = (int)(requested < nc ? requested : nc);
+  } else {
+    const long long sms = sm_count();
+    if (chains * 2 > sms || nc < 64) return pl;
+    auto waves = [&](long long ctas) { return (ctas + sms - 1) / sms; };
+    // time in chunk-steps of one CTA: the segment passes plus a scan step
+    // (about one chunk) per segment boundary
+    double best = (double)waves(chains) * nc;
+    for (int cand = 2; cand <= 64 && cand <= nc; ++cand) {
+      const long long len = (nc + cand - 1) / cand;
+      const double t = (double)(waves(2 * (cand - 1) * chains) + waves(cand * chains)) * len + (cand - 1);
+      if (t < 0.8 * best) {
+        best = t;
+        P = cand;
+      }
+    }
+  }
+  if (P <= 1) return pl;
+  const long long seg_chunks = (nc + P - 1) / P;
+  pl.seg_tokens = (int)(seg_chunks * a.chunk);
+  pl.P = (int)((a.T_seq + pl.seg_tokens - 1) / pl.seg_tokens);
+  if (pl.P <= 1) {
+    pl.P = 1;
+    pl.seg_tokens = 0;
+    return pl;
+  }
+  const size_t state = (size_t)kD * kD * sizeof(float);
+  pl.ws_bytes = (size_t)(3 * pl.P - 2) * (size_t)a.N * a.H * state;
+  return pl;
+}
+
+cudaError_t launch_chunk_tc_segmented(const PrefillArgs &a, const SegPlan &pl, void *ws, cudaStream_t s) {
+  const size_t DD = (size_t)kD * kD;
+  float *pairs = static_cast<float *>(ws);                                    // [2][N][P-1][H][D][D]
+  float *E = pairs + (size_t)2 * a.N * (pl.P - 1) * a.H * DD;                 // [N][P][H][D][D]
+  PrefillArgs p1 = a;  // pass 1: affine pairs of segments 0 .. P-2
+  p1.o = nullptr;
+  p1.s0 = nullptr;
+  p1.sT = pairs;
+  p1.seg_tokens = pl.seg_tokens;
+  p1.nseg = pl.P - 1;
+  p1.kinds = 2;
+  cudaError_t e = launch_chunk_tc(p1, s);
+  if (e != cudaSuccess) return e;
+  const size_t smem = 2 * DD * sizeof(float);
+  e = cudaFuncSetAttribute(cp_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cp_scan_kernel<<<a.N * a.H, kScanThreads, smem, s>>>(a.N, a.H, pl.P, a.s0, pairs, E);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  PrefillArgs p3 = a;  // pass 3: every segment from its entry state
+  p3.s0 = E;
+  p3.seg_tokens = pl.seg_tokens;
+  p3.nseg = pl.P;
+  p3.kinds = 1;
+  return launch_chunk_tc(p3, s);
+}
+
+}  // namespace kda

@@ -30,8 +30,19 @@ struct PrefillArgs {
   const void *q, *k, *v, *g, *beta;
   const float *s0;           // nullable
   const int32_t *cu;         // nullable
-  void *o;
+  void *o;                   // nullable only for the segment passes of the long-sequence plan
   float *sT;                 // nullable
+  // Long-sequence plan (tensor-core kernel only; the defaults mean one work
+  // item per (sequence, head)).  Sequence n is cut into segments of
+  // seg_tokens tokens (a multiple of the chunk); this launch covers segments
+  // [0, nseg).  With kinds == 2 every (n, segment, h) runs twice: kind 0
+  // from a zero state with v as given, kind 1 from the identity with v = 0,
+  // giving the segment's affine pair (S~, M); their final states go to
+  // sT[kind][n][segment][h].  With kinds == 1 segment j starts from
+  // s0[n][j][h] and only the last segment writes sT[n][h].
+  int seg_tokens = 0;        // 0: the whole sequence is one segment
+  int nseg = 1;
+  int kinds = 1;
 };
 
 struct DecodeArgs {
@@ -47,6 +58,15 @@ cudaError_t launch_chunk_simt(const PrefillArgs &a, cudaStream_t s);
 bool chunk_tc_supports(const PrefillArgs &a);
 cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s);
 cudaError_t read_tc_watchdog(unsigned int *flags, bool clear);
+
+// Segment plan for long sequences (kda_cp.cu).
+struct SegPlan {
+  int P;              // segments per sequence (1: no split)
+  int seg_tokens;     // tokens per segment (a multiple of the chunk)
+  size_t ws_bytes;    // device workspace: (3P - 2) x N x H fp32 dk x dv states
+};
+SegPlan plan_segments(const PrefillArgs &a, int requested);
+cudaError_t launch_chunk_tc_segmented(const PrefillArgs &a, const SegPlan &pl, void *ws, cudaStream_t s);
 cudaError_t launch_validate_prefill(const PrefillArgs &a, int *d_flag, cudaStream_t s);
 cudaError_t launch_validate_decode(const DecodeArgs &a, int *d_flag, cudaStream_t s);
 

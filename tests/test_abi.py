@@ -108,3 +108,21 @@ def test_product_package_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in src and "from oracle" not in src, fn
                 assert "kda_oracle" not in src, fn
+
+
+def test_segment_planner_sizes(lib):
+    """The long-sequence planner is host-only: the long-context shape (one
+    sequence of 2^20 tokens, 16 heads) gets a workspace, the batch shape
+    (4 x 8192 tokens, 32 heads) does not."""
+    n = ctypes.c_size_t(0)
+    long_ctx = _desc(B=1, T=1 << 20, H=16, dk=128, dv=128)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(long_ctx), ctypes.byref(n)) == 0
+    assert n.value > 0 and n.value % (128 * 128 * 4 * 16) == 0
+    batch = _desc(B=4, T=8192, H=32, dk=128, dv=128)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(batch), ctypes.byref(n)) == 0
+    assert n.value == 0
+    forced = _desc(B=1, T=4096, H=2, dk=128, dv=128, segments=4)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(forced), ctypes.byref(n)) == 0
+    assert n.value == (3 * 4 - 2) * 2 * 128 * 128 * 4
+    varlen_split = _desc(B=1, T=4096, H=2, dk=128, dv=128, num_seqs=2, segments=4)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(varlen_split), ctypes.byref(n)) == -7

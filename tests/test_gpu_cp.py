@@ -1,0 +1,96 @@
+"""Long sequences split into segments joined through their affine pairs
+([K3-notes §2.5, context-parallel affine pair]), against the fp64 oracle and
+against the unsplit tensor-core kernel.
+
+Cited page: "Kimi K3：从 3T 稀疏预训练到百万 Token Agent 的端到端扩展"
+(liuzhao09.github.io/papers/kimi-k3), [K3-notes] below.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _helpers import TOL_BF16_FRO, TOL_BF16_MAXN, assert_close, max_norm, oracle_prefill, rel_fro, to_np
+from hybrid_linear_attention_chunk_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def run(kda, x, B, **kw):
+    o, s = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["initial_state"], None,
+                             B=B, **kw)
+    torch.cuda.synchronize()
+    return o, s
+
+
+def long_inputs(B, T, H, seed_index=2):
+    w = inputs.scaled(inputs.LONG_T1M, B=B, T=T, H=H)
+    return w, inputs.make_prefill(w, device=DEV)
+
+
+@pytest.mark.parametrize("T,segments", [(4096, 4), (4000, 3), (1000, 7)])
+def test_segments_match_oracle(kda, T, segments):
+    w, x = long_inputs(2, T, 2)
+    o, s = run(kda, x, 2, segments=segments)
+    o_ref, s_ref = oracle_prefill(x)
+    assert_close(to_np(o), o_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="o")
+    assert_close(to_np(s), s_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="S")
+
+
+def test_segments_agree_with_unsplit(kda):
+    w, x = long_inputs(1, 8192, 3)
+    o1, s1 = run(kda, x, 1, segments=1)
+    o4, s4 = run(kda, x, 1, segments=5)
+    assert rel_fro(to_np(o4), to_np(o1)) <= 1e-2
+    assert rel_fro(to_np(s4), to_np(s1)) <= 1e-2
+
+
+def test_caller_workspace_equals_stream_ordered(kda):
+    w, x = long_inputs(1, 3000, 2)
+    d = kda.chunk_desc(x["q"], x["v"], gate_dtype=0, segments=4, B=1)
+    nbytes = kda.kda_chunk_fwd_workspace_size(d)
+    assert nbytes == (3 * 4 - 2) * 1 * 2 * 128 * 128 * 4
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    o1, s1 = run(kda, x, 1, segments=4)
+    o2, s2 = run(kda, x, 1, segments=4, workspace=ws)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    small = torch.empty(nbytes - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(kda.KdaError) as e:
+        run(kda, x, 1, segments=4, workspace=small)
+    assert e.value.status == -2
+
+
+def test_split_refused_where_unsupported(kda):
+    w = inputs.scaled(inputs.VARLEN_64, H=2)
+    x = inputs.make_prefill(w, device=DEV, lengths=np.array([300, 200]))
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["initial_state"],
+                          x["cu_seqlens"], segments=2)
+    assert e.value.status == -7
+
+
+def test_long_context_full_size(kda):
+    """The long-context workload at full size (B=1, H=16, T=1,048,576, slow
+    decay, random initial state): the automatic plan splits it; it must agree
+    with the unsplit kernel everywhere, and with the oracle on the first
+    16384 tokens of two heads."""
+    w = inputs.LONG_T1M
+    x = inputs.make_prefill(w, device=DEV)
+    d = kda.chunk_desc(x["q"], x["v"], gate_dtype=0, B=1)
+    assert kda.kda_chunk_fwd_workspace_size(d) > 0  # the planner splits this shape
+    o_cp, s_cp = run(kda, x, 1)
+    o_1, s_1 = run(kda, x, 1, segments=1)
+    assert torch.isfinite(o_cp.float()).all() and torch.isfinite(s_cp).all()
+    assert rel_fro(to_np(s_cp), to_np(s_1)) <= 1e-2
+    # outputs: compare a strided sample of rows (the whole tensor is 4 GB)
+    rows = torch.arange(0, w.T, 97, device=DEV)
+    assert rel_fro(to_np(o_cp[rows]), to_np(o_1[rows])) <= 1e-2
+    del o_1, s_1
+    # oracle on the first 16384 tokens of heads 0 and 11
+    L = 16384
+    sub = {n: x[n][:L].contiguous() for n in ("q", "k", "v", "log_alpha", "beta")}
+    sub["initial_state"] = x["initial_state"]
+    sub["cu_seqlens"] = torch.tensor([0, L], dtype=torch.int32, device=DEV)
+    o_ref, _ = oracle_prefill(sub, chains=[0, 11])
+    for h in (0, 11):
+        assert_close(to_np(o_cp[:L, h]), o_ref[:, h], TOL_BF16_FRO, TOL_BF16_MAXN, what=f"o head {h}")
