@@ -311,6 +311,13 @@ def run_gpu(args):
                "launches": dsteps}
         del dx, views
 
+    # the long-context and varlen workloads, reported beside the headline
+    extra = {}
+    for key, wl, nsteps in (("long_context", inputs.LONG_T1M, args.long_steps),
+                            ("varlen", inputs.VARLEN_64, args.varlen_steps)):
+        if nsteps > 0:
+            extra[key] = time_prefill_workload(kda, inputs, wl, nsteps, dev, stream, world, rank, hbm_peak)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -326,6 +333,7 @@ def run_gpu(args):
             "e2e": e2e,
             "decode": dec,
             "clocks": clk,
+            **extra,
         }
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, x, seconds=args.cpu_seconds)
@@ -333,6 +341,50 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def time_prefill_workload(kda, inputs, w, steps, dev, stream, world, rank, hbm_peak):
+    """Times one more prefill workload (one kda_chunk_fwd call per step)."""
+    import numpy as np
+    import torch
+    x = inputs.make_prefill(w, device=dev, seed=inputs.SEED_BASE + w.seed_index + 1000 * rank)
+    varlen = w.varlen_seqs > 0
+    cu = x["cu_seqlens"] if varlen else None
+    B = None if varlen else w.B
+    out = torch.empty(x["T_total"], w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    sT = torch.empty(x["N"], w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+    d = kda.chunk_desc(x["q"], x["v"], cu_seqlens=cu, gate_dtype=0, B=B)
+    ws_bytes = kda.kda_chunk_fwd_workspace_size(d)
+
+    def step():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["initial_state"], cu, out, sT,
+                          B=B, stream=stream)
+
+    step()
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_local = ev0.elapsed_time(ev1) / steps
+    ms = reduce_max(ms_local, world, dev)
+    tokens = x["T_total"]
+    lens = np.asarray(x["lengths"])
+    alg = prefill_bytes(1, tokens, w.H, w.dk, w.dv, state_in=x["initial_state"] is not None)
+    alg += (x["N"] - 1) * w.H * w.dk * w.dv * 4 * (2 if x["initial_state"] is not None else 1)
+    gbs = alg / (ms_local * 1e-3) / 1e9
+    res = {"workload": w.name, "steps": steps, "ms_per_step": round(ms, 3),
+           "tokens_per_s": round(world * tokens / (ms * 1e-3), 1), "tokens": int(tokens),
+           "sequences": int(x["N"]), "longest": int(lens.max()),
+           "split_workspace_bytes": int(ws_bytes),
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                        "frac": round(gbs / hbm_peak, 4), "algorithmic_bytes_per_step": int(alg)}}
+    del x, out, sT
+    torch.cuda.empty_cache()
+    return res
 
 
 # ------------------------------------------------------- oracle on the host
@@ -428,6 +480,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--long-steps", type=int, default=3, help="steps of the 2^20-token workload (0: skip)")
+    ap.add_argument("--varlen-steps", type=int, default=5, help="steps of the 64-sequence varlen workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
