@@ -21,7 +21,7 @@ KERNELS = {"auto": 0, "simt": 1, "tc": 2}
 STATUS = {
     0: "KDA_OK", -1: "KDA_ERR_NULL", -2: "KDA_ERR_SHAPE", -3: "KDA_ERR_DTYPE",
     -4: "KDA_ERR_ALIGN", -5: "KDA_ERR_RANGE", -6: "KDA_ERR_CUDA", -7: "KDA_ERR_UNSUPPORTED",
-    -8: "KDA_ERR_ALIAS",
+    -8: "KDA_ERR_ALIAS", -9: "KDA_ERR_SCRATCH_LIMIT",
 }
 
 
@@ -71,6 +71,8 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_fwd_workspace_size.argtypes = [ctypes.POINTER(KdaChunkDesc),
                                                      ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
+        lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(KdaChunkDesc), P, P, P, P, P, P, P, P, P, P]
+        lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [ctypes.POINTER(KdaDecodeDesc), P, P, P, P, P, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -165,6 +167,29 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, initial_state=None, cu_seqlens=None,
     else:
         st = lib.kda_chunk_fwd(*args, _stream_handle(stream, dev))
         _check(st, "kda_chunk_fwd")
+    return out, final_state
+
+
+def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, initial_state=None, cu_seqlens=None, out=None,
+                          final_state=None, *, chunk=64, kernel="auto", segments=0, out_dtype=None,
+                          want_final_state=True, B=None, stream=None):
+    """kda_chunk_fwd through the entry point that allocates no device memory:
+    the long-sequence workspace comes from the library's static scratch array
+    (KDA_STATIC_WORKSPACE_BYTES).  Output tensors are allocated here by torch
+    only when not given; pass `out` and `final_state` to allocate nothing."""
+    lib = load()
+    dev = q.device
+    d = chunk_desc(q, v, chunk=chunk, cu_seqlens=cu_seqlens, out_dtype=out_dtype or q.dtype,
+                   gate_dtype=_dt(log_alpha), validate=False, kernel=kernel, segments=segments, B=B)
+    Nseq = d.num_seqs if cu_seqlens is not None else d.B
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (d.dv,), dtype=out_dtype or q.dtype, device=dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(Nseq, d.H, d.dk, d.dv, dtype=torch.float32, device=dev)
+    st = lib.kda_chunk_fwd_noalloc(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                   _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                   _stream_handle(stream, dev))
+    _check(st, "kda_chunk_fwd_noalloc")
     return out, final_state
 
 

@@ -313,6 +313,7 @@ const char *kda_status_string(kda_status s) {
     case KDA_ERR_CUDA: return "CUDA error (see kda_last_cuda_error)";
     case KDA_ERR_UNSUPPORTED: return "the requested kernel does not cover these arguments";
     case KDA_ERR_ALIAS: return "forbidden aliasing between arguments";
+    case KDA_ERR_SCRATCH_LIMIT: return "the call needs more scratch than the library's static array";
   }
   return "unknown status";
 }

@@ -1,0 +1,57 @@
+// kda_chunk_fwd_noalloc: kda_chunk_fwd for callers that cannot allocate
+// device memory (see include/kda.h).  The workspace of the long-sequence
+// plan comes from a fixed array compiled into the library instead of from
+// cudaMallocAsync or from the caller.
+#include <mutex>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+// Held by every GPU that loads the library, until the process exits.
+static __device__ __align__(256) unsigned char g_static_ws[KDA_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_ws_mutex;
+void *g_ws_ptr[kMaxDevices] = {};
+
+// Device address of g_static_ws on the current device.  In host code the name
+// g_static_ws is only a host-side stand-in, so the address is looked up once
+// per device, with that device current, and cached.
+kda_status static_ws_address(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  if (!g_ws_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return KDA_ERR_CUDA;
+    g_ws_ptr[dev] = p;
+  }
+  *out = g_ws_ptr[dev];
+  return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" kda_status kda_chunk_fwd_noalloc(const kda_chunk_desc *desc, const void *q, const void *k,
+                                            const void *v, const void *log_alpha, const void *beta,
+                                            const float *initial_state, const int32_t *cu_seqlens, void *out,
+                                            float *final_state, kda_stream_t stream) {
+  if (!desc) return KDA_ERR_NULL;
+  if (desc->validate) return KDA_ERR_UNSUPPORTED;  // its range check would need an allocation
+  size_t need = 0;
+  kda_status st = kda_chunk_fwd_workspace_size(desc, &need);
+  if (st != KDA_OK) return st;
+  if (need > KDA_STATIC_WORKSPACE_BYTES) return KDA_ERR_SCRATCH_LIMIT;
+  void *ws = nullptr;
+  if (need > 0) {
+    st = kda::static_ws_address(&ws);
+    if (st != KDA_OK) return st;
+  }
+  // The segment passes write every workspace byte they later read, so the
+  // previous call's contents need no clearing.
+  return kda_chunk_fwd_ex(desc, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state, ws,
+                          need > 0 ? (size_t)KDA_STATIC_WORKSPACE_BYTES : 0, stream);
+}

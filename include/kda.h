@@ -57,7 +57,9 @@ typedef enum {
   KDA_ERR_RANGE = -5,       /* validate mode found a value outside its range       */
   KDA_ERR_CUDA = -6,        /* a CUDA call or kernel launch failed                 */
   KDA_ERR_UNSUPPORTED = -7, /* a kernel choice that does not cover these arguments */
-  KDA_ERR_ALIAS = -8        /* forbidden aliasing between arguments                */
+  KDA_ERR_ALIAS = -8,       /* forbidden aliasing between arguments                */
+  KDA_ERR_SCRATCH_LIMIT = -9 /* kda_chunk_fwd_noalloc: the call needs more scratch
+                                than KDA_STATIC_WORKSPACE_BYTES                      */
 } kda_status;
 
 /* Which prefill kernel runs.  AUTO picks the tensor-core kernel when it covers
@@ -163,6 +165,46 @@ const char *kda_last_cuda_error(void);
  * (cudaDeviceSynchronize), stores that word in *flags (0 = no time-out since
  * it was last cleared) and clears it when `clear` is non-zero. */
 kda_status kda_device_watchdog(unsigned int *flags, int clear);
+
+/* Size of the library's built-in scratch array used by kda_chunk_fwd_noalloc:
+ * 32 MiB of device memory on every GPU that loads libkda.so, held until the
+ * process exits. */
+#define KDA_STATIC_WORKSPACE_BYTES (32u << 20)
+
+/*
+ * kda_chunk_fwd_noalloc - kda_chunk_fwd for callers that cannot allocate.
+ * The paper has no counterpart: this is a property of the library, not of the
+ * method.
+ *
+ * Some callers own every byte of device memory through their own allocator
+ * (for example a serving process that reserves the GPU's memory in fixed pools
+ * at start-up), or run in code paths where a device allocation could block on
+ * or fail against memory pressure they do not control.  For them kda_chunk_fwd
+ * is unusable whenever its planner splits long sequences, because it then
+ * allocates a stream-ordered workspace, and kda_chunk_fwd_ex needs a buffer they
+ * may have no way to provide.  This entry point takes the same arguments as
+ * kda_chunk_fwd and computes the same results, but takes its workspace from a
+ * fixed array inside the library (KDA_STATIC_WORKSPACE_BYTES); it never calls
+ * cudaMalloc, cudaMallocAsync, cudaFree or any other allocating routine.  The
+ * caller still passes every input and output buffer.
+ *
+ * - A call whose plan needs more scratch than KDA_STATIC_WORKSPACE_BYTES (see
+ *   kda_chunk_fwd_workspace_size) returns KDA_ERR_SCRATCH_LIMIT before launching
+ *   anything.  Validate mode needs an allocation and is refused with
+ *   KDA_ERR_UNSUPPORTED.
+ * - The first call on a device (the current device at call time) looks up the
+ *   array's device address once for that device; make that first call before
+ *   any stream capture.
+ * - All calls in the process share the one array, and it keeps whatever the
+ *   previous call left in it (every call writes all the scratch it reads, so
+ *   nothing has to start at zero).  Calls whose work overlaps on the GPU (on
+ *   different streams, or from different threads without ordering between
+ *   them) race on that array and may return wrong results: order them.
+ */
+kda_status kda_chunk_fwd_noalloc(const kda_chunk_desc *desc, const void *q, const void *k,
+                                 const void *v, const void *log_alpha, const void *beta,
+                                 const float *initial_state, const int32_t *cu_seqlens, void *out,
+                                 float *final_state, kda_stream_t stream);
 
 #ifdef __cplusplus
 }
