@@ -311,7 +311,9 @@ __device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t vt, uint32_t 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-aligned base by pointer arithmetic on the shared array, so that the
+  // compiler keeps every access through `sm` in the shared address space
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Ctl *ctl = reinterpret_cast<Ctl *>(sm + OFF_CTL);
   const PrefillArgs &a = A.a;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -613,6 +615,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           }
 #pragma unroll
           for (int rr = 0; rr < 16; ++rr) Tf[swz64(base + rr, base + cc)] = x[rr];
+        } else if (ctid < 192) {
+          // blocks (0,1) and (2,3) of T are zero; level 2 below reads them
+          const int e = ctid - 64, blk = e >> 6, rr = (e >> 2) & 15, c4 = e & 3;
+          const int r0 = 32 * blk, c0 = 32 * blk + 16;
+          *reinterpret_cast<float4 *>(Tf + swz64(r0 + rr, c0 + 4 * c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         bar_chunk();
         // Off-diagonal blocks in two levels of the 2x2 block inverse
@@ -654,8 +661,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           const int rr = ctid >> 3, q4 = ctid & 7;  // output row 32 + rr, columns 4 q4 .. 4 q4 + 3
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int mm = 0; mm < 32; ++mm) {  // X = L_[23][01] T_[01][01]  (T lower triangular)
-            if (mm < 16 && q4 >= 4) continue;  // block (0,1) of T is zero (never stored)
+          for (int mm = 0; mm < 32; ++mm) {  // X = L_[23][01] T_[01][01]
             const float l = Lf[swz64(32 + rr, mm)];
             const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(mm, 4 * q4));
             acc.x += l * t.x; acc.y += l * t.y; acc.z += l * t.z; acc.w += l * t.w;
@@ -665,7 +671,6 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int mm = 0; mm < 32; ++mm) {  // -T_[23][23] X
-            if (mm >= 16 && rr < 16) continue;  // block (2,3) of T is zero (never stored)
             const float l = Tf[swz64(32 + rr, 32 + mm)];
             const float4 xv = *reinterpret_cast<const float4 *>(Xf + mm * 32 + 4 * q4);
             acc.x += l * xv.x; acc.y += l * xv.y; acc.z += l * xv.z; acc.w += l * xv.w;
