@@ -1,6 +1,6 @@
 // Chunked KDA prefill on the 5th-generation tensor cores (tcgen05 MMA with
-// TMEM accumulators, operands in 128-byte-swizzled shared memory, inputs
-// brought in by TMA).  bf16 q/k/v/out, fp32 log-decay and beta, fp32 state,
+// TMEM accumulators, operands in 128-byte-swizzled shared memory; log-decay
+// and v brought in by TMA, q and k prefetched into registers a chunk ahead).  bf16 q/k/v/out, fp32 log-decay and beta, fp32 state,
 // dk = dv = 128, chunk C = 64.
 //
 // Cited page: "Kimi K3：从 3T 稀疏预训练到百万 Token Agent 的端到端扩展"
@@ -23,8 +23,10 @@
 // M4 reads its A operand, the bf16 copy of S^T, straight from TMEM.
 //
 // Two warp groups overlap consecutive chunks.  The chunk group (warps 0-7)
-// runs one chunk ahead: decay prologue, M1, the UT solve, M2/M3, and the TMA
-// loads of q, k, log-decay and v.  The state group (warps 8-11) runs the
+// runs one chunk ahead: decay prologue, M1, the UT solve, M2/M3, the TMA
+// loads of log-decay and v and the register prefetch of the next q and k.
+// M2/M3 complete asynchronously: their completion is what hands the chunk to
+// the state group.  The state group (warps 8-11) runs the
 // serial state chain: -W staging, M4, V~ staging, the gamma scaling, M5/M6,
 // the bf16 state copy and the output.  Operands the state group still reads
 // while the chunk group prepares the next chunk are double-buffered by chunk
@@ -66,15 +68,16 @@ constexpr float kSingleRefBound2 = kSingleRefBound * kLog2e;  // the -80 bound i
 constexpr uint32_t OFF_QG = 0;        // 48 KB: per 64-column K-half (stride KHALF):
                                       //   [Q o Gamma, even chunks | Gamma o K | Q o Gamma, odd chunks]
 constexpr uint32_t KHALF = 24576;
-constexpr uint32_t OFF_KB = 49152;    // 16 KB: q tile (TMA) -> K / Gamma -> L (fp32 64x64)
-constexpr uint32_t OFF_TF = 65536;    // 16 KB: k tile (TMA) -> T (fp32 64x64)
+constexpr uint32_t OFF_KB = 49152;    // 16 KB: K / Gamma -> L, then T over it (fp32 64x64)
+constexpr uint32_t OFF_TF = 65536;    // 16 KB: scratch of the solve's block products
 constexpr uint32_t OFF_KH = 81920;    // x2 16 KB: K o gamma_C / Gamma (MN-major B of M6)
 constexpr uint32_t OFF_AM = 114688;   // x2 8 KB: A bf16, 64 rows x 64
-constexpr uint32_t OFF_ZT = 131072;   // 8 KB: row-group sums (prologue) / solve scratch / T_b bf16
+constexpr uint32_t OFF_ZT = 131072;   // 8 KB: T_b bf16 (read by M2/M3)
 constexpr uint32_t OFF_V = 139264;    // 16 KB: v tile (TMA), two 64-column boxes
 constexpr uint32_t OFF_GS = 155648;   // 32 KB: log-decay tile (TMA), fp32 [64][128]
 constexpr uint32_t OFF_VT = 188416;   // 16 KB: -W^T (MN-major), then V~^T, then the output tile
-constexpr uint32_t OFF_CTL = 204800;  // 4 KB control block
+constexpr uint32_t OFF_PRO = 204800;  // 5 KB: decay prologue sums (written while M2/M3 may still run)
+constexpr uint32_t OFF_CTL = 209920;  // 4 KB control block
 constexpr uint32_t SMEM_USED = OFF_CTL + 4096;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 
@@ -87,7 +90,7 @@ constexpr uint32_t TM_STB = 320;  // bf16 S^T, two values per column (A operand 
 constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
-  B_M1 = 0, B_M23, B_VFULL, B_QKFULL, B_GFULL, B_READY0, B_READY1, B_FREE0, B_FREE1, B_WFREE, B_M4,
+  B_M1 = 0, B_M23, B_VFULL, B_GFULL, B_READY0, B_READY1, B_FREE0, B_FREE1, B_WFREE, B_M4,
   B_M56, B_TD_C, B_TD_S, B_COUNT
 };
 
@@ -97,7 +100,6 @@ struct Ctl {
   float bs[64];          // beta of the chunk's rows (0 past the end)
   uint32_t tmem_slot;
   int abort;             // any thread gave up
-  int slow[2];           // range-guard vote, by chunk parity
   int go_c[2];           // chunk-group wait verdicts (double-buffered)
   int go_s[2];           // state-group wait verdicts
 };
@@ -109,7 +111,7 @@ struct TcArgs {
 };
 
 struct TcMaps {
-  CUtensorMap q, k, v, g;
+  CUtensorMap v, g;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -133,6 +135,18 @@ __device__ __forceinline__ void bar_chunk() {
   __syncwarp();
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
+// Chunk-group barrier that also returns whether any thread passed p = true.
+__device__ __forceinline__ bool bar_chunk_or(bool p) {
+  uint32_t r;
+  __syncwarp();
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, 256, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ void bar_state() {
   __syncwarp();
   asm volatile("bar.sync 2, 128;" ::: "memory");
@@ -149,6 +163,12 @@ __device__ __forceinline__ void st_row16_bf16(uint8_t *tile, uint32_t row, uint3
                pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
   st_shared_v4(tile + sw128_offset(row, c0 + 8), pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]),
                pack_bf16(v[12], v[13]), pack_bf16(v[14], v[15]));
+}
+
+// Stores 4 fp32 values as bf16 at columns [c0, c0+4) of a 128-byte-swizzled
+// tile (c0 a multiple of 4).
+__device__ __forceinline__ void st_row4_bf16(uint8_t *tile, uint32_t row, uint32_t c0, const float4 &v) {
+  *reinterpret_cast<uint2 *>(tile + sw128_offset(row, c0)) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
 }
 
 __device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&f)[8]) {
@@ -172,6 +192,58 @@ __device__ __forceinline__ void tmem_st_bf16x32(uint32_t taddr, const float (&v)
 #pragma unroll
   for (int i = 0; i < 16; ++i) w[i] = __uint_as_float(pack_bf16(v[2 * i], v[2 * i + 1]));
   tmem_st16(taddr, w);
+}
+
+// Shared-memory float4 load kept in program order with the other volatile
+// loads, so that a batch of them issues back to back.
+__device__ __forceinline__ float4 lds128(const float *p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
+
+__device__ __forceinline__ float f4c(const float4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ float4 mul4(const float4 &a, const float4 &b) {
+  return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+}
+
+__device__ __forceinline__ float4 add4(const float4 &a, const float4 &b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+// acc[i] = sum_j l[i][j] t[j] over eight k (l[i][h] holds k = 4h .. 4h + 3):
+// a 4x4 block of a product
+__device__ __forceinline__ void fma4x8(float4 (&acc)[4], const float4 (&l)[4][2], const float4 (&t)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float lv = f4c(l[i][j >> 2], j & 3);
+      acc[i].x += lv * t[j].x; acc[i].y += lv * t[j].y; acc[i].z += lv * t[j].z; acc[i].w += lv * t[j].w;
+    }
+  }
+}
+
+// acc += l[k0 + i] * t[i] for i < 8 (l: the left factor's row, four per float4)
+__device__ __forceinline__ void fma8(float4 &acc, const float4 *l, int k0, const float4 (&t)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float lv = f4c(l[(k0 + i) >> 2], (k0 + i) & 3);
+    acc.x += lv * t[i].x; acc.y += lv * t[i].y; acc.z += lv * t[i].z; acc.w += lv * t[i].w;
+  }
+}
+
+
+// Named barrier over the first n threads of the chunk group.
+__device__ __forceinline__ void bar_sync_n(int id, int n) {
+  __syncwarp();
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // fp32 64x64 matrices of the solve (L, T) are stored row-major with the
@@ -220,40 +292,59 @@ struct Loader {
   Ctl *ctl;
   uint32_t sm_base;
   int h;
-  int issued[3];  // q/k, g, v
-  int landed[3];
+  int issued[2];  // g, v
+  int landed[2];
 
-  __device__ void qk(int t0) {
-    const uint32_t full = smem_u32(&ctl->bar[B_QKFULL]);
-    mbar_arrive_expect_tx(full, 4 * 8192);
-    tma_load_3d(sm_base + OFF_KB, &maps->q, full, 0, h, t0);
-    tma_load_3d(sm_base + OFF_KB + 8192, &maps->q, full, 64, h, t0);
-    tma_load_3d(sm_base + OFF_TF, &maps->k, full, 0, h, t0);
-    tma_load_3d(sm_base + OFF_TF + 8192, &maps->k, full, 64, h, t0);
-    ++issued[0];
-  }
   __device__ void g(int t0) {
     const uint32_t full = smem_u32(&ctl->bar[B_GFULL]);
     mbar_arrive_expect_tx(full, kC * kD * 4);
     tma_load_3d(sm_base + OFF_GS, &maps->g, full, 0, h, t0);
-    ++issued[1];
+    ++issued[0];
   }
   __device__ void v(int t0) {
     const uint32_t full = smem_u32(&ctl->bar[B_VFULL]);
     mbar_arrive_expect_tx(full, 2 * 8192);
     tma_load_3d(sm_base + OFF_V, &maps->v, full, 0, h, t0);
     tma_load_3d(sm_base + OFF_V + 8192, &maps->v, full, 64, h, t0);
-    ++issued[2];
+    ++issued[1];
   }
   // copies still in flight after an abort must land before the CTA retires
   __device__ void drain(unsigned int *err) {
-    const int bars[3] = {B_QKFULL, B_GFULL, B_VFULL};
+    const int bars[2] = {B_GFULL, B_VFULL};
     volatile int no_abort = 0;
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 2; ++i)
       if (issued[i] > landed[i])
         mbar_wait(smem_u32(&ctl->bar[bars[i]]), landed[i] & 1, &no_abort, err, 1u << (20 + i));
   }
 };
+
+// 16-byte read-only global load that does not allocate in L1 (q and k are
+// read once).
+__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// q and k rows of the chunk starting at token t0, in the operand pass's
+// layout: rows 4 rg .. 4 rg + 3, channels 8 o .. 8 o + 7; rows at or past eos
+// read as 0.
+__device__ __forceinline__ void load_qk_rows(const PrefillArgs &a, int t0, int eos, int h, int rg, int o,
+                                             uint4 (&qn)[4], uint4 (&kn)[4]) {
+  const uint4 *q = reinterpret_cast<const uint4 *>(a.q), *k = reinterpret_cast<const uint4 *>(a.k);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int t = t0 + 4 * rg + r;
+    qn[r] = kn[r] = make_uint4(0u, 0u, 0u, 0u);
+    if (t < eos) {
+      const size_t idx = ((size_t)t * a.H + h) * (kD / 8) + o;
+      qn[r] = ld_stream16(q + idx);
+      kn[r] = ld_stream16(k + idx);
+    }
+  }
+}
 
 // ------------------------------------------------------------- MMA batches
 
@@ -346,9 +437,10 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     tmem_relinquish();
   }
   if (tid == 32) {
-    for (int b = 0; b < B_COUNT; ++b) mbar_init(smem_u32(&ctl->bar[b]), 1);
+    // READY: M2/M3 completion (tcgen05.commit) and the chunk group's thread 0
+    for (int b = 0; b < B_COUNT; ++b)
+      mbar_init(smem_u32(&ctl->bar[b]), (b == B_READY0 || b == B_READY1) ? 2 : 1);
     ctl->abort = 0;
-    ctl->slow[0] = ctl->slow[1] = 0;
     ctl->go_c[0] = ctl->go_c[1] = ctl->go_s[0] = ctl->go_s[1] = 0;
     fence_mbar_init();
   }
@@ -360,32 +452,33 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
 
   if (tid < kChunkThreads) {
     // =========================================================== chunk group
-    // registers: 256 x 200 + 128 x 104 = the launch's 384 x 168
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
+    // registers: 256 x 208 + 128 x 88 = the launch's 384 x 168
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
     const int ctid = tid;
     const int qw = warp & 3, ch = warp >> 2;
     // prologue layout: channel octet o (channels [8o, 8o+8)), row group rg
     // (rows [4rg, 4rg+4)), 16-token tile of those rows
     const int o = ctid & 15, rg = ctid >> 4, tile = rg >> 2;
     int seq = 0;
-    uint32_t ph_m1 = 0, ph_m23 = 0, ph_v = 0, ph_qk = 0, ph_g = 0;
-    Loader ld{&maps, ctl, sm_base, h, {0, 0, 0}, {0, 0, 0}};
+    uint32_t ph_m1 = 0, ph_m23 = 0, ph_v = 0, ph_g = 0;
+    Loader ld{&maps, ctl, sm_base, h, {0, 0}, {0, 0}};
     if (ctid == 0 && nchunks > 0) {
-      tma_prefetch_desc(&maps.q);
-      tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.g);
       ld.g(bos);
-      ld.qk(bos);
       if (!zero_v) ld.v(bos);
     }
+    uint4 qn[4], kn[4];  // q and k rows of the next chunk, in flight during the current one
+    if (nchunks > 0) load_qk_rows(a, bos, eos, h, rg, o, qn, kn);
     if (zero_v)  // the v tile stays zero for the whole item
       for (int e = ctid; e < 16384 / 16; e += kChunkThreads)
         reinterpret_cast<uint4 *>(sm + OFF_V)[e] = make_uint4(0u, 0u, 0u, 0u);
+    for (int e = ctid; e < 8192 / 16; e += kChunkThreads)  // T_b above the diagonal: zero for good
+      reinterpret_cast<uint4 *>(sm + OFF_ZT)[e] = make_uint4(0u, 0u, 0u, 0u);
     float beta_next = 0.f;
     if (ctid < kC && ctid < eos - bos) beta_next = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(bos + ctid) * H + h);
     // prologue scratch in the T_b buffer: per-tile sums, tile references, chunk totals
-    float *tot = reinterpret_cast<float *>(sm + OFF_ZT);  // [4][128]
+    float *tot = reinterpret_cast<float *>(sm + OFF_PRO);  // [4][128]
     float *refs = tot + 4 * 128;                          // [4][128]
     float *gct = refs + 4 * 128;                          // [128]
     float *gs_w = reinterpret_cast<float *>(sm + OFF_GS);
@@ -405,7 +498,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // operand pass below can read them in its own layout.
       if (!(alive = group_wait<true>(ctl, B_GFULL, ph_g, ctid, seq, A.err))) break;
       ph_g ^= 1u;
-      if (ctid == 0) ld.landed[1] = ld.issued[1];
+      if (ctid == 0) ld.landed[0] = ld.issued[0];
+      bool vote;  // a channel's chunk total is below the single-reference bound
       {
         const int p = ctid & 63, t4 = ctid >> 6;
         float2 Gl[16];
@@ -438,16 +532,28 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
         if (t4 == 0) *reinterpret_cast<float2 *>(&ctl->gam[par][2 * p]) = make_float2(ex2(tc.x), ex2(tc.y));
         if (t4 == 0) *reinterpret_cast<float2 *>(gct + 2 * p) = tc;
-        if (t4 == 0 && (tc.x < kSingleRefBound2 || tc.y < kSingleRefBound2)) atomicOr(&ctl->slow[par], 1);
+        vote = tc.x < kSingleRefBound2 || tc.y < kSingleRefBound2;
       }
       if (ctid < kC)  // beta of the next chunk's rows, 0 past the end
         beta_next = ctid < eos - (t0 + kC)
                         ? __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + kC + ctid) * H + h)
                         : 0.f;
-      // q and k tiles of this chunk (the wait's barrier also closes the vote)
-      if (!(alive = group_wait<true>(ctl, B_QKFULL, ph_qk, ctid, seq, A.err))) break;
-      ph_qk ^= 1u;
-      if (ctid == 0) ld.landed[0] = ld.issued[0];
+      // The previous chunk's M2/M3 must be done with Gamma o K, T_b and the v
+      // tile before this chunk overwrites them; then this chunk's v tile.
+      if (ctid == 0) {
+        bool ok = true;
+        if (m >= 1) {
+          ok = solo_wait(ctl, B_M23, ph_m23, A.err);
+          ph_m23 ^= 1u;
+          if (ok && !zero_v) ld.v(t0);
+        }
+        ctl->go_c[seq & 1] = ok && !ctl->abort;
+      }
+      // the barrier publishes the cumulative sums and closes the vote
+      const bool slow = bar_chunk_or(vote);
+      alive = ctl->go_c[seq & 1] != 0;
+      ++seq;
+      if (!alive) break;
       const uint32_t half = (uint32_t)(o >> 3), col = (uint32_t)(8 * (o & 7));
       float G[4][8], gc[8], GC[8];
 #pragma unroll
@@ -465,14 +571,9 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       uint4 qr[4], kr[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const uint32_t row = 4 * rg + r;
-        qr[r] = *reinterpret_cast<const uint4 *>(sm + OFF_KB + half * 8192 + sw128_offset(row, col));
-        kr[r] = *reinterpret_cast<const uint4 *>(sm + OFF_TF + half * 8192 + sw128_offset(row, col));
-        if ((int)row >= len) qr[r] = kr[r] = make_uint4(0u, 0u, 0u, 0u);
+        qr[r] = qn[r];
+        kr[r] = kn[r];
       }
-      const bool slow = ctl->slow[par] != 0;
-      bar_chunk();  // the q tile is read before K / Gamma overwrites it
-      if (ctid == 0) ctl->slow[par ^ 1] = 0;
       uint8_t *qb_h = qg + half * KHALF + par * 16384;   // Q o Gamma of this parity
       uint8_t *gk_h = qg + half * KHALF + 8192;          // Gamma o K
       uint8_t *kb_h = sm + OFF_KB + half * 8192;
@@ -497,6 +598,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           st_shared_8bf16(kb_h + sw128_offset(row, col), fb);
           st_shared_8bf16(kh_h + sw128_offset(row, col), fh);
         }
+        if (m + 1 < nchunks) load_qk_rows(a, t0 + kC, eos, h, rg, o, qn, kn);
         group_publish<true>();
         if (ctid == 0) {
           issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, par, false);
@@ -559,15 +661,18 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           st_shared_8bf16(gk_h + sw128_offset(row, col), fk);
           st_shared_8bf16(kh_h + sw128_offset(row, col), fh);
         }
+        if (m + 1 < nchunks) load_qk_rows(a, t0 + kC, eos, h, rg, o, qn, kn);
       }
       if (!alive) break;
       if (ctid == 0 && m + 1 < nchunks) ld.g(t0 + kC);  // the cumulative sums have been consumed
 
       // ---------------- masks, L, and T_b = (I + L)^{-1} diag(beta)
+      // L is stored with zeros on and above its diagonal and T is computed in
+      // place over it: T is zero above the diagonal too, so the zeros L leaves
+      // there are already T's.
       {
         float *Lf = reinterpret_cast<float *>(sm + OFF_KB);  // K / Gamma is dead once M1 is done
-        float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
-        float *Xf = reinterpret_cast<float *>(sm + OFF_ZT);  // [3][16][16] scratch before T_b lands
+        float *Xf = reinterpret_cast<float *>(sm + OFF_TF);  // scratch of the block products
         // even chunks: TMEM lanes 0..63 hold A's rows, 64..127 L''; odd chunks the reverse
         const bool a_rows = (qw < 2) == (par == 0);
         const int r = 32 * (qw & 1) + lane;
@@ -599,125 +704,164 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           }
         }
         bar_chunk();
-        // Diagonal 16x16 blocks, one column per thread, right-looking: once
-        // x[m] is final it is subtracted from every later row, so the
-        // dependent chain is one multiply-add per row.  Entries above the
-        // diagonal come out as 0.
+        // Diagonal 16x16 blocks: one column of T per thread, rows in groups of
+        // four (left-looking).  A group first takes the contributions of the
+        // rows already solved, then is solved within itself; the sum of row r
+        // adds the x[r-1] term last, so consecutive rows are one multiply-add
+        // apart on the dependent chain.
         if (ctid < 64) {
-          const int ab = ctid >> 4, cc = ctid & 15, base = 16 * ab;
+          const int base = 16 * (ctid >> 4), cc = ctid & 15;
           float x[16];
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) x[rr] = (rr == cc) ? 1.f : 0.f;
+          for (int R = 0; R < 4; ++R) {
+            float4 lr[4][4];
 #pragma unroll
-          for (int mm = 0; mm < 16; ++mm) {
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int rr = mm + 1; rr < 16; ++rr) x[rr] -= Lf[swz64(base + rr, base + mm)] * x[mm];
+              for (int q = 0; q <= R; ++q)
+                lr[i][q] = *reinterpret_cast<const float4 *>(Lf + swz64(base + 4 * R + i, base + 4 * q));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = 4 * R + i;
+              float acc = rr == cc ? 1.f : 0.f;
+#pragma unroll
+              for (int mm = 0; mm < rr; ++mm) acc -= f4c(lr[i][mm >> 2], mm & 3) * x[mm];
+              x[rr] = acc;
+            }
           }
+          bar_sync_n(3, 64);  // the block's L is read in full before T overwrites it
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) Tf[swz64(base + rr, base + cc)] = x[rr];
-        } else if (ctid < 192) {
-          // blocks (0,1) and (2,3) of T are zero; level 2 below reads them
-          const int e = ctid - 64, blk = e >> 6, rr = (e >> 2) & 15, c4 = e & 3;
-          const int r0 = 32 * blk, c0 = 32 * blk + 16;
-          *reinterpret_cast<float4 *>(Tf + swz64(r0 + rr, c0 + 4 * c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int rr = 0; rr < 16; ++rr) Lf[swz64(base + rr, base + cc)] = x[rr];
         }
         bar_chunk();
         // Off-diagonal blocks in two levels of the 2x2 block inverse
         // [[P, 0], [R, Q]]^{-1} = [[P^-1, 0], [-Q^-1 R P^-1, Q^-1]]:
         //   level 1 (16-row blocks): T_10 and T_32;
-        //   level 2 (32-row blocks): T_[23][01] = -T_[23][23] L_[23][01] T_[01][01].
-        // One thread per (row, 4-column group) of each output; X is scratch.
-        // Blocks above the diagonal are never read (T_b below masks them).
-        {
-          // level 1: two 16x16 outputs, 128 tasks
+        //   level 2 (32-row blocks): T_[23][01].
+        // Each output is X = R P^-1 into scratch, then -Q^-1 X.  Shared-memory
+        // bandwidth limits these products, so level 2 blocks 4x4 outputs per
+        // thread and splits k four ways across the warps.  Every block of
+        // T_b = T diag(beta) is written as soon as its T block is final, the
+        // product outputs straight from registers; T_b's blocks above the
+        // diagonal stay zero from the start.
+        const float4 *bs4 = reinterpret_cast<const float4 *>(ctl->bs);
+        uint8_t *zt = sm + OFF_ZT;
+        if (ctid < 128) {
+          // level 1: two 16x16 outputs, 128 tasks of (row, 4 columns)
           const int blk = ctid >> 6, rr = (ctid >> 2) & 15, q4 = ctid & 3;
           const int rb = 16 * (2 * blk + 1), cb = 16 * (2 * blk);  // output block (rb, cb)
-          if (ctid < 128) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          float *X1 = Xf + blk * 256;                              // [16][16]
+          float4 l[4], t[8];
 #pragma unroll
-            for (int mm = 0; mm < 16; ++mm) {
-              const float l = Lf[swz64(rb + rr, cb + mm)];
-              const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(cb + mm, cb + 4 * q4));
-              acc.x += l * t.x; acc.y += l * t.y; acc.z += l * t.z; acc.w += l * t.w;
-            }
-            *reinterpret_cast<float4 *>(Xf + (blk * 16 + rr) * 16 + 4 * q4) = acc;
-          }
-          bar_chunk();
-          if (ctid < 128) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int mm = 0; mm < 16; ++mm) {
-              const float l = Tf[swz64(rb + rr, rb + mm)];
-              const float4 xv = *reinterpret_cast<const float4 *>(Xf + (blk * 16 + mm) * 16 + 4 * q4);
-              acc.x += l * xv.x; acc.y += l * xv.y; acc.z += l * xv.z; acc.w += l * xv.w;
-            }
-            *reinterpret_cast<float4 *>(Tf + swz64(rb + rr, cb + 4 * q4)) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-          }
-          bar_chunk();
-        }
-        {
-          // level 2: the 32x32 block below the diagonal, 256 tasks
-          const int rr = ctid >> 3, q4 = ctid & 7;  // output row 32 + rr, columns 4 q4 .. 4 q4 + 3
+          for (int c4 = 0; c4 < 4; ++c4) l[c4] = lds128(Lf + swz64(rb + rr, cb + 4 * c4));  // row of L_(rb, cb)
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int mm = 0; mm < 32; ++mm) {  // X = L_[23][01] T_[01][01]
-            const float l = Lf[swz64(32 + rr, mm)];
-            const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(mm, 4 * q4));
-            acc.x += l * t.x; acc.y += l * t.y; acc.z += l * t.z; acc.w += l * t.w;
+          for (int k0 = 0; k0 < 16; k0 += 8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t[i] = lds128(Lf + swz64(cb + k0 + i, cb + 4 * q4));
+            fma8(acc, l, k0, t);
           }
-          *reinterpret_cast<float4 *>(Xf + rr * 32 + 4 * q4) = acc;
-          bar_chunk();
+          *reinterpret_cast<float4 *>(X1 + rr * 16 + 4 * q4) = acc;
+          bar_sync_n(3, 128);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) l[c4] = lds128(Lf + swz64(rb + rr, rb + 4 * c4));  // row of T_(rb, rb)
           acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int mm = 0; mm < 32; ++mm) {  // -T_[23][23] X
-            const float l = Tf[swz64(32 + rr, 32 + mm)];
-            const float4 xv = *reinterpret_cast<const float4 *>(Xf + mm * 32 + 4 * q4);
-            acc.x += l * xv.x; acc.y += l * xv.y; acc.z += l * xv.z; acc.w += l * xv.w;
+          for (int k0 = 0; k0 < 16; k0 += 8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t[i] = lds128(X1 + (k0 + i) * 16 + 4 * q4);
+            fma8(acc, l, k0, t);
           }
-          *reinterpret_cast<float4 *>(Tf + swz64(32 + rr, 4 * q4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-          bar_chunk();
-        }
-        {
-          const int rr = ctid >> 2, s0 = (ctid & 3) * 16;
-          const bool upper = (ctid & 3) > (rr >> 4);  // block above the diagonal: T is zero there
+          acc = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+          *reinterpret_cast<float4 *>(Lf + swz64(rb + rr, cb + 4 * q4)) = acc;
+          st_row4_bf16(zt, rb + rr, cb + 4 * q4, mul4(acc, bs4[cb / 4 + q4]));
+        } else if (ctid < 192) {
+          // T_b of the diagonal blocks: row rr of block db, its 16 columns
+          const int e = ctid - 128, db = e >> 4, rr = e & 15;
+          const int row = 16 * db + rr, c0 = 16 * db;
           float v[16];
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 t = *reinterpret_cast<const float4 *>(Tf + swz64(rr, s0 + 4 * c4));
-            v[4 * c4] = upper ? 0.f : t.x * ctl->bs[s0 + 4 * c4];
-            v[4 * c4 + 1] = upper ? 0.f : t.y * ctl->bs[s0 + 4 * c4 + 1];
-            v[4 * c4 + 2] = upper ? 0.f : t.z * ctl->bs[s0 + 4 * c4 + 2];
-            v[4 * c4 + 3] = upper ? 0.f : t.w * ctl->bs[s0 + 4 * c4 + 3];
+            const float4 tv = mul4(lds128(Lf + swz64(row, c0 + 4 * c4)), bs4[c0 / 4 + c4]);
+            v[4 * c4] = tv.x; v[4 * c4 + 1] = tv.y; v[4 * c4 + 2] = tv.z; v[4 * c4 + 3] = tv.w;
           }
-          st_row16_bf16(sm + OFF_ZT, rr, s0, v);
+          st_row16_bf16(zt, row, c0, v);
+        }
+        bar_chunk();
+        {
+          // level 2: thread = output rows 32 + 4 rg .. + 3, columns 4 q4 .. + 3,
+          // k in [8 kq, 8 kq + 8).  Partial sums of kq = 1..3 meet in Pf
+          // ([kq - 1][i][rg, q4] float4, conflict-free); kq = 0 completes.
+          const int q4 = ctid & 7, rg = (ctid >> 3) & 7, kq = ctid >> 6, k0 = 8 * kq;
+          float4 *Pf = reinterpret_cast<float4 *>(Xf + 32 * 32);  // 12 KB after X
+          float4 acc[4], lv[4][2], t[8];
+          // X = L_[23][01] T_[01][01]
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) lv[i][h2] = lds128(Lf + swz64(32 + 4 * rg + i, k0 + 4 * h2));
+#pragma unroll
+          for (int j = 0; j < 8; ++j) t[j] = lds128(Lf + swz64(k0 + j, 4 * q4));
+          fma4x8(acc, lv, t);
+          if (kq > 0)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) Pf[((kq - 1) * 4 + i) * 64 + rg * 8 + q4] = acc[i];
+          bar_chunk();
+          if (kq == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float4 x = acc[i];
+#pragma unroll
+              for (int kk = 0; kk < 3; ++kk) x = add4(x, Pf[(kk * 4 + i) * 64 + rg * 8 + q4]);
+              *reinterpret_cast<float4 *>(Xf + (4 * rg + i) * 32 + 4 * q4) = x;
+            }
+          }
+          bar_chunk();
+          // -T_[23][23] X
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) lv[i][h2] = lds128(Lf + swz64(32 + 4 * rg + i, 32 + k0 + 4 * h2));
+#pragma unroll
+          for (int j = 0; j < 8; ++j) t[j] = lds128(Xf + (k0 + j) * 32 + 4 * q4);
+          fma4x8(acc, lv, t);
+          if (kq > 0)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) Pf[((kq - 1) * 4 + i) * 64 + rg * 8 + q4] = acc[i];
+          bar_chunk();
+          if (kq == 0) {
+            const float4 b = bs4[q4];
+            const float4 nb = make_float4(-b.x, -b.y, -b.z, -b.w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float4 x = acc[i];
+#pragma unroll
+              for (int kk = 0; kk < 3; ++kk) x = add4(x, Pf[(kk * 4 + i) * 64 + rg * 8 + q4]);
+              st_row4_bf16(zt, 32 + 4 * rg + i, 4 * q4, mul4(x, nb));
+            }
+          }
         }
       }
       group_publish<true>();
 
-      // ---------------- U^T and W^T; then hand the chunk to the state group
+      // ---------------- U^T and W^T; their completion hands the chunk to the
+      // state group.  A failed wait here sets the abort flag, which the next
+      // group wait turns into a verdict for the whole group.
       if (ctid == 0) {
-        if (m + 1 < nchunks) ld.qk(t0 + kC);  // L and T are dead: their space takes the next q, k
         bool ok = true;
         if (!zero_v) {
           ok = solo_wait(ctl, B_VFULL, ph_v, A.err);
           ph_v ^= 1u;
-          if (ok) ld.landed[2] = ld.issued[2];
+          if (ok) ld.landed[1] = ld.issued[1];
         }
         if (ok && m >= 1) ok = solo_wait(ctl, B_WFREE, (m - 1) & 1, A.err);
         if (ok) {
           issue_m23(tbase, sm_base + OFF_V, smem_u32(qg), sm_base + OFF_ZT, TM_U + par * 64);
           mma_commit(smem_u32(&ctl->bar[B_M23]));
-          ok = solo_wait(ctl, B_M23, ph_m23, A.err);
-          ph_m23 ^= 1u;
+          mma_commit(smem_u32(&ctl->bar[B_READY0 + par]));
+          mbar_arrive(smem_u32(&ctl->bar[B_READY0 + par]));  // releases the chunk's shared-memory state
         }
-        if (ok && !zero_v && m + 1 < nchunks) ld.v(t0 + kC);  // the v buffer is free again
-        if (ok) mbar_arrive(smem_u32(&ctl->bar[B_READY0 + par]));
-        ctl->go_c[seq & 1] = ok && !ctl->abort;
       }
-      bar_chunk();
-      alive = ctl->go_c[seq & 1] != 0;
-      ++seq;
     }
     if (ctid == 0) {
       ld.drain(A.err);
@@ -727,7 +871,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     }
   } else {
     // =========================================================== state group
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
     const int stid = tid - kChunkThreads;  // = TMEM lane j of every state-group product
     const int qw = warp & 3;                // lane quarter, = stid >> 5
     const int j = stid;
@@ -906,9 +1050,7 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   TcMaps maps;
-  if (encode_tok_head(encode, &maps.q, a.q, a.T_total, a.H, false) != CUDA_SUCCESS ||
-      encode_tok_head(encode, &maps.k, a.k, a.T_total, a.H, false) != CUDA_SUCCESS ||
-      encode_tok_head(encode, &maps.v, a.v, a.T_total, a.H, false) != CUDA_SUCCESS ||
+  if (encode_tok_head(encode, &maps.v, a.v, a.T_total, a.H, false) != CUDA_SUCCESS ||
       encode_tok_head(encode, &maps.g, a.g, a.T_total, a.H, true) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
