@@ -1,6 +1,6 @@
 // Chunked KDA prefill on the 5th-generation tensor cores (tcgen05 MMA with
-// TMEM accumulators, operands in 128-byte-swizzled shared memory; log-decay
-// and v brought in by TMA, q and k prefetched into registers a chunk ahead).  bf16 q/k/v/out, fp32 log-decay and beta, fp32 state,
+// TMEM accumulators, operands in 128-byte-swizzled shared memory, inputs
+// brought in by TMA).  bf16 q/k/v/out, fp32 log-decay and beta, fp32 state,
 // dk = dv = 128, chunk C = 64.
 //
 // Cited page: "Kimi K3：从 3T 稀疏预训练到百万 Token Agent 的端到端扩展"
@@ -23,10 +23,11 @@
 // M4 reads its A operand, the bf16 copy of S^T, straight from TMEM.
 //
 // Two warp groups overlap consecutive chunks.  The chunk group (warps 0-7)
-// runs one chunk ahead: decay prologue, M1, the UT solve, M2/M3, the TMA
-// loads of log-decay and v and the register prefetch of the next q and k.
-// M2/M3 complete asynchronously: their completion is what hands the chunk to
-// the state group.  The state group (warps 8-11) runs the
+// runs one chunk ahead: decay prologue, M1, the UT solve, M2/M3, and the TMA
+// loads of q, k, log-decay and v.  q and k land in the buffers that become
+// the chunk's Q o Gamma and K o gamma_C / Gamma operands, which are then
+// scaled in place.  M2/M3 complete asynchronously: their completion is what
+// hands the chunk to the state group.  The state group (warps 8-11) runs the
 // serial state chain: -W staging, M4, V~ staging, the gamma scaling, M5/M6,
 // the bf16 state copy and the output.  Operands the state group still reads
 // while the chunk group prepares the next chunk are double-buffered by chunk
@@ -90,7 +91,7 @@ constexpr uint32_t TM_STB = 320;  // bf16 S^T, two values per column (A operand 
 constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
-  B_M1 = 0, B_M23, B_VFULL, B_GFULL, B_READY0, B_READY1, B_FREE0, B_FREE1, B_WFREE, B_M4,
+  B_M1 = 0, B_M23, B_VFULL, B_GFULL, B_QKFULL, B_READY0, B_READY1, B_FREE0, B_FREE1, B_WFREE, B_M4,
   B_M56, B_TD_C, B_TD_S, B_COUNT
 };
 
@@ -111,7 +112,7 @@ struct TcArgs {
 };
 
 struct TcMaps {
-  CUtensorMap v, g;
+  CUtensorMap q, k, v, g;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -171,19 +172,7 @@ __device__ __forceinline__ void st_row4_bf16(uint8_t *tile, uint32_t row, uint32
   *reinterpret_cast<uint2 *>(tile + sw128_offset(row, c0)) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
 }
 
-__device__ __forceinline__ void unpack8_bf16(const uint4 &u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = unpack_bf16(w[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
-}
-
-__device__ __forceinline__ void st_shared_8bf16(uint8_t *p, const float (&f)[8]) {
-  st_shared_v4(p, pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-}
+__device__ __forceinline__ void sts32(uint8_t *p, uint32_t v) { *reinterpret_cast<uint32_t *>(p) = v; }
 
 // Packs 32 fp32 values into 16 bf16 pairs (even element in the low half), the
 // TMEM layout of an MMA A operand, and stores them at TMEM address taddr.
@@ -292,8 +281,19 @@ struct Loader {
   Ctl *ctl;
   uint32_t sm_base;
   int h;
-  int issued[2];  // g, v
-  int landed[2];
+  int issued[3];  // g, v, q/k
+  int landed[3];
+
+  // q and k of the chunk at t0 into the Q o Gamma and K-hat buffers of parity par
+  __device__ void qk(int t0, int par) {
+    const uint32_t full = smem_u32(&ctl->bar[B_QKFULL]);
+    mbar_arrive_expect_tx(full, 4 * 8192);
+    tma_load_3d(sm_base + OFF_QG + par * 16384, &maps->q, full, 0, h, t0);
+    tma_load_3d(sm_base + OFF_QG + KHALF + par * 16384, &maps->q, full, 64, h, t0);
+    tma_load_3d(sm_base + OFF_KH + par * 16384, &maps->k, full, 0, h, t0);
+    tma_load_3d(sm_base + OFF_KH + par * 16384 + 8192, &maps->k, full, 64, h, t0);
+    ++issued[2];
+  }
 
   __device__ void g(int t0) {
     const uint32_t full = smem_u32(&ctl->bar[B_GFULL]);
@@ -310,41 +310,13 @@ struct Loader {
   }
   // copies still in flight after an abort must land before the CTA retires
   __device__ void drain(unsigned int *err) {
-    const int bars[2] = {B_GFULL, B_VFULL};
+    const int bars[3] = {B_GFULL, B_VFULL, B_QKFULL};
     volatile int no_abort = 0;
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < 3; ++i)
       if (issued[i] > landed[i])
         mbar_wait(smem_u32(&ctl->bar[bars[i]]), landed[i] & 1, &no_abort, err, 1u << (20 + i));
   }
 };
-
-// 16-byte read-only global load that does not allocate in L1 (q and k are
-// read once).
-__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-// q and k rows of the chunk starting at token t0, in the operand pass's
-// layout: rows 4 rg .. 4 rg + 3, channels 8 o .. 8 o + 7; rows at or past eos
-// read as 0.
-__device__ __forceinline__ void load_qk_rows(const PrefillArgs &a, int t0, int eos, int h, int rg, int o,
-                                             uint4 (&qn)[4], uint4 (&kn)[4]) {
-  const uint4 *q = reinterpret_cast<const uint4 *>(a.q), *k = reinterpret_cast<const uint4 *>(a.k);
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int t = t0 + 4 * rg + r;
-    qn[r] = kn[r] = make_uint4(0u, 0u, 0u, 0u);
-    if (t < eos) {
-      const size_t idx = ((size_t)t * a.H + h) * (kD / 8) + o;
-      qn[r] = ld_stream16(q + idx);
-      kn[r] = ld_stream16(k + idx);
-    }
-  }
-}
 
 // ------------------------------------------------------------- MMA batches
 
@@ -456,20 +428,21 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
     const int ctid = tid;
     const int qw = warp & 3, ch = warp >> 2;
-    // prologue layout: channel octet o (channels [8o, 8o+8)), row group rg
-    // (rows [4rg, 4rg+4)), 16-token tile of those rows
-    const int o = ctid & 15, rg = ctid >> 4, tile = rg >> 2;
+    // prologue layout: channel pair p (channels 2p, 2p + 1) of the 16-token
+    // tile t4 (rows [16 t4, 16 t4 + 16)); a warp covers one 64-column K-half
+    const int p = ctid & 63, t4 = ctid >> 6;
     int seq = 0;
-    uint32_t ph_m1 = 0, ph_m23 = 0, ph_v = 0, ph_g = 0;
-    Loader ld{&maps, ctl, sm_base, h, {0, 0}, {0, 0}};
+    uint32_t ph_m1 = 0, ph_m23 = 0, ph_v = 0, ph_g = 0, ph_qk = 0;
+    Loader ld{&maps, ctl, sm_base, h, {0, 0, 0}, {0, 0, 0}};
     if (ctid == 0 && nchunks > 0) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.g);
       ld.g(bos);
+      ld.qk(bos, 0);
       if (!zero_v) ld.v(bos);
     }
-    uint4 qn[4], kn[4];  // q and k rows of the next chunk, in flight during the current one
-    if (nchunks > 0) load_qk_rows(a, bos, eos, h, rg, o, qn, kn);
     if (zero_v)  // the v tile stays zero for the whole item
       for (int e = ctid; e < 16384 / 16; e += kChunkThreads)
         reinterpret_cast<uint4 *>(sm + OFF_V)[e] = make_uint4(0u, 0u, 0u, 0u);
@@ -477,12 +450,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       reinterpret_cast<uint4 *>(sm + OFF_ZT)[e] = make_uint4(0u, 0u, 0u, 0u);
     float beta_next = 0.f;
     if (ctid < kC && ctid < eos - bos) beta_next = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(bos + ctid) * H + h);
-    // prologue scratch in the T_b buffer: per-tile sums, tile references, chunk totals
-    float *tot = reinterpret_cast<float *>(sm + OFF_PRO);  // [4][128]
-    float *refs = tot + 4 * 128;                          // [4][128]
-    float *gct = refs + 4 * 128;                          // [128]
-    float *gs_w = reinterpret_cast<float *>(sm + OFF_GS);
-    const float *gs = gs_w;
+    float *tot = reinterpret_cast<float *>(sm + OFF_PRO);  // [4][128] per-tile decay sums
+    const float *gs = reinterpret_cast<const float *>(sm + OFF_GS);
     uint8_t *qg = sm + OFF_QG;
     bool alive = true;
     for (int m = 0; m < nchunks && alive; ++m) {
@@ -490,19 +459,16 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       const int t0 = bos + m * kC;
       const int len = min(kC, eos - t0);
       uint8_t *kh = sm + OFF_KH + par * 16384;
-      if (m >= 2 && !(alive = group_wait<true>(ctl, B_FREE0 + par, ((m >> 1) - 1) & 1, ctid, seq, A.err))) break;
 
       // ---------------- decay prologue: cumulative log2-decay and scaled operands
-      // Cumulative sums run channel-pair-major (thread = channel pair p,
-      // 16-row tile t4) and are written back over the log-decay tile, so the
-      // operand pass below can read them in its own layout.
+      // Each thread keeps its channel pair's cumulative decay for its 16 rows
+      // in registers; the tiles' totals meet in shared memory to give every
+      // tile its reference (the cumulative decay before its first row).
       if (!(alive = group_wait<true>(ctl, B_GFULL, ph_g, ctid, seq, A.err))) break;
       ph_g ^= 1u;
       if (ctid == 0) ld.landed[0] = ld.issued[0];
-      bool vote;  // a channel's chunk total is below the single-reference bound
+      float2 Gl[16];  // cumulative log2-decay within the tile, then from the chunk start
       {
-        const int p = ctid & 63, t4 = ctid >> 6;
-        float2 Gl[16];
         float2 run = make_float2(0.f, 0.f);
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -515,31 +481,38 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
         *reinterpret_cast<float2 *>(tot + t4 * 128 + 2 * p) = run;
         if (ctid < kC) ctl->bs[ctid] = beta_next;
-        bar_chunk();
-        float2 off = make_float2(0.f, 0.f), tc = make_float2(0.f, 0.f);
+      }
+      bar_chunk();
+      if (ctid == 0 && m + 1 < nchunks) ld.g(t0 + kC);  // the log-decay tile has been consumed
+      float2 ref[4], tc = make_float2(0.f, 0.f);  // tile references; chunk total G_C
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const float2 tb = *reinterpret_cast<const float2 *>(tot + b * 128 + 2 * p);
-          if (b < t4) { off.x += tb.x; off.y += tb.y; }
-          tc.x += tb.x;
-          tc.y += tb.y;
-        }
-        *reinterpret_cast<float2 *>(refs + t4 * 128 + 2 * p) = off;  // reference of 16-token tile t4
+      for (int b = 0; b < 4; ++b) {
+        const float2 tb = *reinterpret_cast<const float2 *>(tot + b * 128 + 2 * p);
+        ref[b] = tc;
+        tc.x += tb.x;
+        tc.y += tb.y;
+      }
+      {
+        float2 off = ref[0];
+#pragma unroll
+        for (int b = 1; b < 4; ++b)
+          if (t4 == b) off = ref[b];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-          const int row = 16 * t4 + r;
-          *reinterpret_cast<float2 *>(gs_w + row * kD + 2 * p) = make_float2(Gl[r].x + off.x, Gl[r].y + off.y);
+          Gl[r].x += off.x;
+          Gl[r].y += off.y;
         }
-        if (t4 == 0) *reinterpret_cast<float2 *>(&ctl->gam[par][2 * p]) = make_float2(ex2(tc.x), ex2(tc.y));
-        if (t4 == 0) *reinterpret_cast<float2 *>(gct + 2 * p) = tc;
-        vote = tc.x < kSingleRefBound2 || tc.y < kSingleRefBound2;
       }
+      const float2 gam = make_float2(ex2(tc.x), ex2(tc.y));
+      if (t4 == 0) *reinterpret_cast<float2 *>(&ctl->gam[par][2 * p]) = gam;
+      const bool vote = tc.x < kSingleRefBound2 || tc.y < kSingleRefBound2;
       if (ctid < kC)  // beta of the next chunk's rows, 0 past the end
         beta_next = ctid < eos - (t0 + kC)
                         ? __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + kC + ctid) * H + h)
                         : 0.f;
       // The previous chunk's M2/M3 must be done with Gamma o K, T_b and the v
       // tile before this chunk overwrites them; then this chunk's v tile.
+      // This chunk's q and k have landed.
       if (ctid == 0) {
         bool ok = true;
         if (m >= 1) {
@@ -547,58 +520,44 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           ph_m23 ^= 1u;
           if (ok && !zero_v) ld.v(t0);
         }
+        if (ok) {
+          ok = solo_wait(ctl, B_QKFULL, ph_qk, A.err);
+          ph_qk ^= 1u;
+          if (ok) ld.landed[2] = ld.issued[2];
+        }
         ctl->go_c[seq & 1] = ok && !ctl->abort;
       }
-      // the barrier publishes the cumulative sums and closes the vote
+      // the barrier also publishes gamma_C and closes the range-guard vote
       const bool slow = bar_chunk_or(vote);
       alive = ctl->go_c[seq & 1] != 0;
       ++seq;
       if (!alive) break;
-      const uint32_t half = (uint32_t)(o >> 3), col = (uint32_t)(8 * (o & 7));
-      float G[4][8], gc[8], GC[8];
+      // operand tiles: channel pair p sits in K-half p / 32 at column 2p mod 64
+      const uint32_t half = (uint32_t)(p >> 5), col = (uint32_t)(2 * p) & 63u;
+      uint8_t *qb_h = qg + half * KHALF + par * 16384;  // q -> Q o Gamma (in place)
+      uint8_t *gk_h = qg + half * KHALF + 8192;         // Gamma o K
+      uint8_t *kb_h = sm + OFF_KB + half * 8192;        // K / Gamma
+      uint8_t *kh_h = kh + half * 8192;                 // k -> K o gamma_C / Gamma (in place)
+      uint32_t qr[16], kr[16];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float4 a0 = *reinterpret_cast<const float4 *>(gs + (4 * rg + r) * kD + 8 * o);
-        const float4 a1 = *reinterpret_cast<const float4 *>(gs + (4 * rg + r) * kD + 8 * o + 4);
-        G[r][0] = a0.x; G[r][1] = a0.y; G[r][2] = a0.z; G[r][3] = a0.w;
-        G[r][4] = a1.x; G[r][5] = a1.y; G[r][6] = a1.z; G[r][7] = a1.w;
+      for (int r = 0; r < 16; ++r) {
+        const uint32_t off = sw128_offset(16 * t4 + r, col);
+        const bool in = 16 * t4 + r < len;  // rows past the end are zero
+        qr[r] = in ? *reinterpret_cast<const uint32_t *>(qb_h + off) : 0u;
+        kr[r] = in ? *reinterpret_cast<const uint32_t *>(kh_h + off) : 0u;
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        gc[c] = ctl->gam[par][8 * o + c];
-        GC[c] = gct[8 * o + c];
-      }
-      uint4 qr[4], kr[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        qr[r] = qn[r];
-        kr[r] = kn[r];
-      }
-      uint8_t *qb_h = qg + half * KHALF + par * 16384;   // Q o Gamma of this parity
-      uint8_t *gk_h = qg + half * KHALF + 8192;          // Gamma o K
-      uint8_t *kb_h = sm + OFF_KB + half * 8192;
-      uint8_t *kh_h = kh + half * 8192;
       if (!slow) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const uint32_t row = 4 * rg + r;
-          float qv[8], kv[8], fq[8], fk[8], fb[8], fh[8];
-          unpack8_bf16(qr[r], qv);
-          unpack8_bf16(kr[r], kv);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float e = ex2(G[r][c]), i = ex2(-G[r][c]);
-            fq[c] = qv[c] * e;
-            fk[c] = kv[c] * e;
-            fb[c] = kv[c] * i;
-            fh[c] = fb[c] * gc[c];
-          }
-          st_shared_8bf16(qb_h + sw128_offset(row, col), fq);
-          st_shared_8bf16(gk_h + sw128_offset(row, col), fk);
-          st_shared_8bf16(kb_h + sw128_offset(row, col), fb);
-          st_shared_8bf16(kh_h + sw128_offset(row, col), fh);
+        for (int r = 0; r < 16; ++r) {
+          const uint32_t off = sw128_offset(16 * t4 + r, col);
+          const float2 qv = unpack_bf16(qr[r]), kv = unpack_bf16(kr[r]);
+          const float ex = ex2(Gl[r].x), ey = ex2(Gl[r].y);
+          const float ix = ex2(-Gl[r].x), iy = ex2(-Gl[r].y);
+          sts32(qb_h + off, pack_bf16(qv.x * ex, qv.y * ey));
+          sts32(gk_h + off, pack_bf16(kv.x * ex, kv.y * ey));
+          sts32(kb_h + off, pack_bf16(kv.x * ix, kv.y * iy));
+          sts32(kh_h + off, pack_bf16(kv.x * ix * gam.x, kv.y * iy * gam.y));
         }
-        if (m + 1 < nchunks) load_qk_rows(a, t0 + kC, eos, h, rg, o, qn, kn);
         group_publish<true>();
         if (ctid == 0) {
           issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, par, false);
@@ -607,32 +566,30 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
         ph_m1 ^= 1u;
       } else {
+        // M1 in four accumulating rounds, one per 16-token key tile b, with
+        // the cumulative decay before tile b as the reference: query rows of
+        // tiles >= b, key rows of tile b only (a thread's rows are all in tile t4)
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
           if (!alive) break;
-          // reference of key tile b: the cumulative decay before its first row
-          float ref[8];
+          const float2 rb = b == 0 ? ref[0] : b == 1 ? ref[1] : b == 2 ? ref[2] : ref[3];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) ref[c] = refs[b * 128 + 8 * o + c];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const uint32_t row = 4 * rg + r;
-            float qv[8], kv[8], fq[8], fk[8], fb[8];
-            unpack8_bf16(qr[r], qv);
-            unpack8_bf16(kr[r], kv);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              fq[c] = fk[c] = fb[c] = 0.f;
-              if (tile >= b) {
-                const float e = ex2(G[r][c] - ref[c]);
-                fq[c] = qv[c] * e;
-                fk[c] = kv[c] * e;
-              }
-              if (tile == b) fb[c] = kv[c] * ex2(ref[c] - G[r][c]);
+          for (int r = 0; r < 16; ++r) {
+            const uint32_t off = sw128_offset(16 * t4 + r, col);
+            const float2 qv = unpack_bf16(qr[r]), kv = unpack_bf16(kr[r]);
+            float fqx = 0.f, fqy = 0.f, fkx = 0.f, fky = 0.f, fbx = 0.f, fby = 0.f;
+            if (t4 >= b) {
+              const float ex = ex2(Gl[r].x - rb.x), ey = ex2(Gl[r].y - rb.y);
+              fqx = qv.x * ex; fqy = qv.y * ey;
+              fkx = kv.x * ex; fky = kv.y * ey;
             }
-            st_shared_8bf16(qb_h + sw128_offset(row, col), fq);
-            st_shared_8bf16(gk_h + sw128_offset(row, col), fk);
-            st_shared_8bf16(kb_h + sw128_offset(row, col), fb);
+            if (t4 == b) {
+              fbx = kv.x * ex2(rb.x - Gl[r].x);
+              fby = kv.y * ex2(rb.y - Gl[r].y);
+            }
+            sts32(qb_h + off, pack_bf16(fqx, fqy));
+            sts32(gk_h + off, pack_bf16(fkx, fky));
+            sts32(kb_h + off, pack_bf16(fbx, fby));
           }
           group_publish<true>();
           if (ctid == 0) {
@@ -645,26 +602,16 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         if (!alive) break;
         // operands with the chunk start as reference (may underflow to 0: fine)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const uint32_t row = 4 * rg + r;
-          float qv[8], kv[8], fq[8], fk[8], fh[8];
-          unpack8_bf16(qr[r], qv);
-          unpack8_bf16(kr[r], kv);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float e = ex2(G[r][c]);
-            fq[c] = qv[c] * e;
-            fk[c] = kv[c] * e;
-            fh[c] = kv[c] * ex2(GC[c] - G[r][c]);
-          }
-          st_shared_8bf16(qb_h + sw128_offset(row, col), fq);
-          st_shared_8bf16(gk_h + sw128_offset(row, col), fk);
-          st_shared_8bf16(kh_h + sw128_offset(row, col), fh);
+        for (int r = 0; r < 16; ++r) {
+          const uint32_t off = sw128_offset(16 * t4 + r, col);
+          const float2 qv = unpack_bf16(qr[r]), kv = unpack_bf16(kr[r]);
+          const float ex = ex2(Gl[r].x), ey = ex2(Gl[r].y);
+          sts32(qb_h + off, pack_bf16(qv.x * ex, qv.y * ey));
+          sts32(gk_h + off, pack_bf16(kv.x * ex, kv.y * ey));
+          sts32(kh_h + off, pack_bf16(kv.x * ex2(tc.x - Gl[r].x), kv.y * ex2(tc.y - Gl[r].y)));
         }
-        if (m + 1 < nchunks) load_qk_rows(a, t0 + kC, eos, h, rg, o, qn, kn);
       }
       if (!alive) break;
-      if (ctid == 0 && m + 1 < nchunks) ld.g(t0 + kC);  // the cumulative sums have been consumed
 
       // ---------------- masks, L, and T_b = (I + L)^{-1} diag(beta)
       // L is stored with zeros on and above its diagonal and T is computed in
@@ -861,6 +808,12 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           mma_commit(smem_u32(&ctl->bar[B_READY0 + par]));
           mbar_arrive(smem_u32(&ctl->bar[B_READY0 + par]));  // releases the chunk's shared-memory state
         }
+        // the next chunk's q and k go to its Q o Gamma and K-hat buffers, free
+        // once the state group has finished the chunk before it
+        if (ok && m + 1 < nchunks) {
+          if (m + 1 >= 2) ok = solo_wait(ctl, B_FREE0 + (par ^ 1), (((m + 1) >> 1) - 1) & 1, A.err);
+          if (ok) ld.qk(t0 + kC, par ^ 1);
+        }
       }
     }
     if (ctid == 0) {
@@ -1050,7 +1003,9 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   TcMaps maps;
-  if (encode_tok_head(encode, &maps.v, a.v, a.T_total, a.H, false) != CUDA_SUCCESS ||
+  if (encode_tok_head(encode, &maps.q, a.q, a.T_total, a.H, false) != CUDA_SUCCESS ||
+      encode_tok_head(encode, &maps.k, a.k, a.T_total, a.H, false) != CUDA_SUCCESS ||
+      encode_tok_head(encode, &maps.v, a.v, a.T_total, a.H, false) != CUDA_SUCCESS ||
       encode_tok_head(encode, &maps.g, a.g, a.T_total, a.H, true) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
