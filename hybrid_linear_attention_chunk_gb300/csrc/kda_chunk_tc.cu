@@ -91,7 +91,7 @@ constexpr uint32_t TM_STB = 320;  // bf16 S^T, two values per column (A operand 
 constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
-  B_M1 = 0, B_M23, B_VFULL, B_GFULL, B_QKFULL, B_READY0, B_READY1, B_FREE0, B_FREE1, B_WFREE, B_M4,
+  B_M1 = 0, B_M23, B_VFULL, B_GFULL, B_QK0, B_QK1, B_TB, B_M4,
   B_M56, B_TD_C, B_TD_S, B_COUNT
 };
 
@@ -103,6 +103,8 @@ struct Ctl {
   int abort;             // any thread gave up
   int go_c[2];           // chunk-group wait verdicts (double-buffered)
   int go_s[2];           // state-group wait verdicts
+  int qk_iss[2], qk_lnd[2];  // q/k copies issued and waited for, by chunk parity
+  int v_iss, v_lnd;          // v copies issued (chunk group) and waited for (state group)
 };
 static_assert(sizeof(Ctl) <= 4096, "control block");
 
@@ -172,7 +174,16 @@ __device__ __forceinline__ void st_row4_bf16(uint8_t *tile, uint32_t row, uint32
   *reinterpret_cast<uint2 *>(tile + sw128_offset(row, c0)) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
 }
 
-__device__ __forceinline__ void sts32(uint8_t *p, uint32_t v) { *reinterpret_cast<uint32_t *>(p) = v; }
+__device__ __forceinline__ void sts64(uint8_t *p, uint2 v) { *reinterpret_cast<uint2 *>(p) = v; }
+
+__device__ __forceinline__ float4 unpack4_bf16(uint2 u) {
+  const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ uint2 pack4_bf16(const float4 &v) {
+  return make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+}
 
 // Packs 32 fp32 values into 16 bf16 pairs (even element in the low half), the
 // TMEM layout of an MMA A operand, and stores them at TMEM address taddr.
@@ -204,6 +215,11 @@ __device__ __forceinline__ float4 mul4(const float4 &a, const float4 &b) {
 __device__ __forceinline__ float4 add4(const float4 &a, const float4 &b) {
   return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
+__device__ __forceinline__ float4 sub4(const float4 &a, const float4 &b) {
+  return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
+}
+__device__ __forceinline__ float4 neg4(const float4 &a) { return make_float4(-a.x, -a.y, -a.z, -a.w); }
+__device__ __forceinline__ float4 ex2_4(const float4 &a) { return make_float4(ex2(a.x), ex2(a.y), ex2(a.z), ex2(a.w)); }
 
 // acc[i] = sum_j l[i][j] t[j] over eight k (l[i][h] holds k = 4h .. 4h + 3):
 // a 4x4 block of a product
@@ -281,42 +297,39 @@ struct Loader {
   Ctl *ctl;
   uint32_t sm_base;
   int h;
-  int issued[3];  // g, v, q/k
-  int landed[3];
-
-  // q and k of the chunk at t0 into the Q o Gamma and K-hat buffers of parity par
-  __device__ void qk(int t0, int par) {
-    const uint32_t full = smem_u32(&ctl->bar[B_QKFULL]);
-    mbar_arrive_expect_tx(full, 4 * 8192);
-    tma_load_3d(sm_base + OFF_QG + par * 16384, &maps->q, full, 0, h, t0);
-    tma_load_3d(sm_base + OFF_QG + KHALF + par * 16384, &maps->q, full, 64, h, t0);
-    tma_load_3d(sm_base + OFF_KH + par * 16384, &maps->k, full, 0, h, t0);
-    tma_load_3d(sm_base + OFF_KH + par * 16384 + 8192, &maps->k, full, 64, h, t0);
-    ++issued[2];
-  }
+  int issued, landed;  // g copies
 
   __device__ void g(int t0) {
     const uint32_t full = smem_u32(&ctl->bar[B_GFULL]);
     mbar_arrive_expect_tx(full, kC * kD * 4);
     tma_load_3d(sm_base + OFF_GS, &maps->g, full, 0, h, t0);
-    ++issued[0];
+    ++issued;
   }
   __device__ void v(int t0) {
     const uint32_t full = smem_u32(&ctl->bar[B_VFULL]);
     mbar_arrive_expect_tx(full, 2 * 8192);
     tma_load_3d(sm_base + OFF_V, &maps->v, full, 0, h, t0);
     tma_load_3d(sm_base + OFF_V + 8192, &maps->v, full, 64, h, t0);
-    ++issued[1];
+    ++ctl->v_iss;
   }
-  // copies still in flight after an abort must land before the CTA retires
+  // a g copy still in flight after an abort must land before the CTA retires
   __device__ void drain(unsigned int *err) {
-    const int bars[3] = {B_GFULL, B_VFULL, B_QKFULL};
     volatile int no_abort = 0;
-    for (int i = 0; i < 3; ++i)
-      if (issued[i] > landed[i])
-        mbar_wait(smem_u32(&ctl->bar[bars[i]]), landed[i] & 1, &no_abort, err, 1u << (20 + i));
+    if (issued > landed) mbar_wait(smem_u32(&ctl->bar[B_GFULL]), landed & 1, &no_abort, err, 1u << 20);
   }
 };
+
+// q and k of the chunk at t0 into the Q o Gamma and K-hat buffers of chunk
+// parity par (issued by one thread of either group).
+__device__ __forceinline__ void issue_qk(const TcMaps *maps, Ctl *ctl, uint32_t sm_base, int h, int t0, int par) {
+  const uint32_t full = smem_u32(&ctl->bar[B_QK0 + par]);
+  ++ctl->qk_iss[par];
+  mbar_arrive_expect_tx(full, 4 * 8192);
+  tma_load_3d(sm_base + OFF_QG + par * 16384, &maps->q, full, 0, h, t0);
+  tma_load_3d(sm_base + OFF_QG + KHALF + par * 16384, &maps->q, full, 64, h, t0);
+  tma_load_3d(sm_base + OFF_KH + par * 16384, &maps->k, full, 0, h, t0);
+  tma_load_3d(sm_base + OFF_KH + par * 16384 + 8192, &maps->k, full, 64, h, t0);
+}
 
 // ------------------------------------------------------------- MMA batches
 
@@ -409,10 +422,10 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     tmem_relinquish();
   }
   if (tid == 32) {
-    // READY: M2/M3 completion (tcgen05.commit) and the chunk group's thread 0
-    for (int b = 0; b < B_COUNT; ++b)
-      mbar_init(smem_u32(&ctl->bar[b]), (b == B_READY0 || b == B_READY1) ? 2 : 1);
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(smem_u32(&ctl->bar[b]), 1);
     ctl->abort = 0;
+    ctl->qk_iss[0] = ctl->qk_iss[1] = ctl->qk_lnd[0] = ctl->qk_lnd[1] = 0;
+    ctl->v_iss = ctl->v_lnd = 0;
     ctl->go_c[0] = ctl->go_c[1] = ctl->go_s[0] = ctl->go_s[1] = 0;
     fence_mbar_init();
   }
@@ -428,19 +441,23 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
     const int ctid = tid;
     const int qw = warp & 3, ch = warp >> 2;
-    // prologue layout: channel pair p (channels 2p, 2p + 1) of the 16-token
-    // tile t4 (rows [16 t4, 16 t4 + 16)); a warp covers one 64-column K-half
-    const int p = ctid & 63, t4 = ctid >> 6;
+    // prologue layout: channel quad p4 (channels 4 p4 .. 4 p4 + 3) of the
+    // 8-row group t8 = warp (rows [8 t8, 8 t8 + 8)); a half-warp covers one
+    // 64-column K-half, and a thread's rows lie in one 16-token tile, t8 / 2
+    const int p4 = ctid & 31, t8 = ctid >> 5;
     int seq = 0;
-    uint32_t ph_m1 = 0, ph_m23 = 0, ph_v = 0, ph_g = 0, ph_qk = 0;
-    Loader ld{&maps, ctl, sm_base, h, {0, 0, 0}, {0, 0, 0}};
+    uint32_t ph_m1 = 0, ph_m23 = 0, ph_g = 0;
+    Loader ld{&maps, ctl, sm_base, h, 0, 0};
     if (ctid == 0 && nchunks > 0) {
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.g);
       ld.g(bos);
-      ld.qk(bos, 0);
+      // q and k of the first two chunks; later ones are issued by the state
+      // group as it frees each parity's buffers
+      issue_qk(&maps, ctl, sm_base, h, bos, 0);
+      if (nchunks > 1) issue_qk(&maps, ctl, sm_base, h, bos + kC, 1);
       if (!zero_v) ld.v(bos);
     }
     if (zero_v)  // the v tile stays zero for the whole item
@@ -461,51 +478,48 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       uint8_t *kh = sm + OFF_KH + par * 16384;
 
       // ---------------- decay prologue: cumulative log2-decay and scaled operands
-      // Each thread keeps its channel pair's cumulative decay for its 16 rows
-      // in registers; the tiles' totals meet in shared memory to give every
-      // tile its reference (the cumulative decay before its first row).
+      // Each thread keeps its channel quad's cumulative decay for its 8 rows in
+      // registers; the row groups' totals meet in shared memory to give every
+      // row group its offset and every 16-token tile its reference (the
+      // cumulative decay before its first row).
       if (!(alive = group_wait<true>(ctl, B_GFULL, ph_g, ctid, seq, A.err))) break;
       ph_g ^= 1u;
-      if (ctid == 0) ld.landed[0] = ld.issued[0];
-      float2 Gl[16];  // cumulative log2-decay within the tile, then from the chunk start
+      if (ctid == 0) ld.landed = ld.issued;
+      float4 Gl[8];  // cumulative log2-decay within the row group, then from the chunk start
       {
-        float2 run = make_float2(0.f, 0.f);
+        float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const int row = 16 * t4 + r;
-          float2 gv = *reinterpret_cast<const float2 *>(gs + row * kD + 2 * p);
-          if (row >= len) gv = make_float2(0.f, 0.f);  // past the end: identity step
+        for (int r = 0; r < 8; ++r) {
+          const int row = 8 * t8 + r;
+          float4 gv = *reinterpret_cast<const float4 *>(gs + row * kD + 4 * p4);
+          if (row >= len) gv = make_float4(0.f, 0.f, 0.f, 0.f);  // past the end: identity step
           run.x += gv.x * kLog2e;
           run.y += gv.y * kLog2e;
+          run.z += gv.z * kLog2e;
+          run.w += gv.w * kLog2e;
           Gl[r] = run;
         }
-        *reinterpret_cast<float2 *>(tot + t4 * 128 + 2 * p) = run;
+        *reinterpret_cast<float4 *>(tot + t8 * 128 + 4 * p4) = run;
         if (ctid < kC) ctl->bs[ctid] = beta_next;
       }
       bar_chunk();
       if (ctid == 0 && m + 1 < nchunks) ld.g(t0 + kC);  // the log-decay tile has been consumed
-      float2 ref[4], tc = make_float2(0.f, 0.f);  // tile references; chunk total G_C
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const float2 tb = *reinterpret_cast<const float2 *>(tot + b * 128 + 2 * p);
-        ref[b] = tc;
-        tc.x += tb.x;
-        tc.y += tb.y;
-      }
+      float4 ref[4], tc = make_float4(0.f, 0.f, 0.f, 0.f);  // tile references; chunk total G_C
       {
-        float2 off = ref[0];
+        float4 off = tc;
 #pragma unroll
-        for (int b = 1; b < 4; ++b)
-          if (t4 == b) off = ref[b];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          Gl[r].x += off.x;
-          Gl[r].y += off.y;
+        for (int g8 = 0; g8 < 8; ++g8) {
+          const float4 tg = *reinterpret_cast<const float4 *>(tot + g8 * 128 + 4 * p4);
+          if ((g8 & 1) == 0) ref[g8 >> 1] = tc;
+          if (g8 == t8) off = tc;
+          tc = add4(tc, tg);
         }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) Gl[r] = add4(Gl[r], off);
       }
-      const float2 gam = make_float2(ex2(tc.x), ex2(tc.y));
-      if (t4 == 0) *reinterpret_cast<float2 *>(&ctl->gam[par][2 * p]) = gam;
-      const bool vote = tc.x < kSingleRefBound2 || tc.y < kSingleRefBound2;
+      const float4 gam = make_float4(ex2(tc.x), ex2(tc.y), ex2(tc.z), ex2(tc.w));
+      if (t8 == 0) *reinterpret_cast<float4 *>(&ctl->gam[par][4 * p4]) = gam;
+      const bool vote = fminf(fminf(tc.x, tc.y), fminf(tc.z, tc.w)) < kSingleRefBound2;
       if (ctid < kC)  // beta of the next chunk's rows, 0 past the end
         beta_next = ctid < eos - (t0 + kC)
                         ? __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + kC + ctid) * H + h)
@@ -521,9 +535,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           if (ok && !zero_v) ld.v(t0);
         }
         if (ok) {
-          ok = solo_wait(ctl, B_QKFULL, ph_qk, A.err);
-          ph_qk ^= 1u;
-          if (ok) ld.landed[2] = ld.issued[2];
+          ok = solo_wait(ctl, B_QK0 + par, (m >> 1) & 1, A.err);
+          if (ok) ++ctl->qk_lnd[par];
         }
         ctl->go_c[seq & 1] = ok && !ctl->abort;
       }
@@ -532,31 +545,30 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       alive = ctl->go_c[seq & 1] != 0;
       ++seq;
       if (!alive) break;
-      // operand tiles: channel pair p sits in K-half p / 32 at column 2p mod 64
-      const uint32_t half = (uint32_t)(p >> 5), col = (uint32_t)(2 * p) & 63u;
+      // operand tiles: channel quad p4 sits in K-half p4 / 16 at column 4 p4 mod 64
+      const uint32_t half = (uint32_t)(p4 >> 4), col = (uint32_t)(4 * p4) & 63u;
       uint8_t *qb_h = qg + half * KHALF + par * 16384;  // q -> Q o Gamma (in place)
       uint8_t *gk_h = qg + half * KHALF + 8192;         // Gamma o K
       uint8_t *kb_h = sm + OFF_KB + half * 8192;        // K / Gamma
       uint8_t *kh_h = kh + half * 8192;                 // k -> K o gamma_C / Gamma (in place)
-      uint32_t qr[16], kr[16];
+      float4 qv[8], kv[8];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const uint32_t off = sw128_offset(16 * t4 + r, col);
-        const bool in = 16 * t4 + r < len;  // rows past the end are zero
-        qr[r] = in ? *reinterpret_cast<const uint32_t *>(qb_h + off) : 0u;
-        kr[r] = in ? *reinterpret_cast<const uint32_t *>(kh_h + off) : 0u;
+      for (int r = 0; r < 8; ++r) {
+        const uint32_t off = sw128_offset(8 * t8 + r, col);
+        const bool in = 8 * t8 + r < len;  // rows past the end are zero
+        qv[r] = unpack4_bf16(in ? *reinterpret_cast<const uint2 *>(qb_h + off) : make_uint2(0u, 0u));
+        kv[r] = unpack4_bf16(in ? *reinterpret_cast<const uint2 *>(kh_h + off) : make_uint2(0u, 0u));
       }
       if (!slow) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const uint32_t off = sw128_offset(16 * t4 + r, col);
-          const float2 qv = unpack_bf16(qr[r]), kv = unpack_bf16(kr[r]);
-          const float ex = ex2(Gl[r].x), ey = ex2(Gl[r].y);
-          const float ix = ex2(-Gl[r].x), iy = ex2(-Gl[r].y);
-          sts32(qb_h + off, pack_bf16(qv.x * ex, qv.y * ey));
-          sts32(gk_h + off, pack_bf16(kv.x * ex, kv.y * ey));
-          sts32(kb_h + off, pack_bf16(kv.x * ix, kv.y * iy));
-          sts32(kh_h + off, pack_bf16(kv.x * ix * gam.x, kv.y * iy * gam.y));
+        for (int r = 0; r < 8; ++r) {
+          const uint32_t off = sw128_offset(8 * t8 + r, col);
+          const float4 e = ex2_4(Gl[r]), i = ex2_4(neg4(Gl[r]));
+          const float4 kb = mul4(kv[r], i);
+          sts64(qb_h + off, pack4_bf16(mul4(qv[r], e)));
+          sts64(gk_h + off, pack4_bf16(mul4(kv[r], e)));
+          sts64(kb_h + off, pack4_bf16(kb));
+          sts64(kh_h + off, pack4_bf16(mul4(kb, gam)));
         }
         group_publish<true>();
         if (ctid == 0) {
@@ -568,28 +580,25 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       } else {
         // M1 in four accumulating rounds, one per 16-token key tile b, with
         // the cumulative decay before tile b as the reference: query rows of
-        // tiles >= b, key rows of tile b only (a thread's rows are all in tile t4)
+        // tiles >= b, key rows of tile b only (a thread's rows are all in tile t8 / 2)
+        const int tile = t8 >> 1;
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
           if (!alive) break;
-          const float2 rb = b == 0 ? ref[0] : b == 1 ? ref[1] : b == 2 ? ref[2] : ref[3];
+          const float4 rb = b == 0 ? ref[0] : b == 1 ? ref[1] : b == 2 ? ref[2] : ref[3];
 #pragma unroll
-          for (int r = 0; r < 16; ++r) {
-            const uint32_t off = sw128_offset(16 * t4 + r, col);
-            const float2 qv = unpack_bf16(qr[r]), kv = unpack_bf16(kr[r]);
-            float fqx = 0.f, fqy = 0.f, fkx = 0.f, fky = 0.f, fbx = 0.f, fby = 0.f;
-            if (t4 >= b) {
-              const float ex = ex2(Gl[r].x - rb.x), ey = ex2(Gl[r].y - rb.y);
-              fqx = qv.x * ex; fqy = qv.y * ey;
-              fkx = kv.x * ex; fky = kv.y * ey;
+          for (int r = 0; r < 8; ++r) {
+            const uint32_t off = sw128_offset(8 * t8 + r, col);
+            float4 fq = make_float4(0.f, 0.f, 0.f, 0.f), fk = fq, fb = fq;
+            if (tile >= b) {
+              const float4 e = ex2_4(sub4(Gl[r], rb));
+              fq = mul4(qv[r], e);
+              fk = mul4(kv[r], e);
             }
-            if (t4 == b) {
-              fbx = kv.x * ex2(rb.x - Gl[r].x);
-              fby = kv.y * ex2(rb.y - Gl[r].y);
-            }
-            sts32(qb_h + off, pack_bf16(fqx, fqy));
-            sts32(gk_h + off, pack_bf16(fkx, fky));
-            sts32(kb_h + off, pack_bf16(fbx, fby));
+            if (tile == b) fb = mul4(kv[r], ex2_4(sub4(rb, Gl[r])));
+            sts64(qb_h + off, pack4_bf16(fq));
+            sts64(gk_h + off, pack4_bf16(fk));
+            sts64(kb_h + off, pack4_bf16(fb));
           }
           group_publish<true>();
           if (ctid == 0) {
@@ -602,13 +611,12 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         if (!alive) break;
         // operands with the chunk start as reference (may underflow to 0: fine)
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const uint32_t off = sw128_offset(16 * t4 + r, col);
-          const float2 qv = unpack_bf16(qr[r]), kv = unpack_bf16(kr[r]);
-          const float ex = ex2(Gl[r].x), ey = ex2(Gl[r].y);
-          sts32(qb_h + off, pack_bf16(qv.x * ex, qv.y * ey));
-          sts32(gk_h + off, pack_bf16(kv.x * ex, kv.y * ey));
-          sts32(kh_h + off, pack_bf16(kv.x * ex2(tc.x - Gl[r].x), kv.y * ex2(tc.y - Gl[r].y)));
+        for (int r = 0; r < 8; ++r) {
+          const uint32_t off = sw128_offset(8 * t8 + r, col);
+          const float4 e = ex2_4(Gl[r]);
+          sts64(qb_h + off, pack4_bf16(mul4(qv[r], e)));
+          sts64(gk_h + off, pack4_bf16(mul4(kv[r], e)));
+          sts64(kh_h + off, pack4_bf16(mul4(kv[r], ex2_4(sub4(tc, Gl[r])))));
         }
       }
       if (!alive) break;
@@ -790,31 +798,9 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
       }
       group_publish<true>();
-
-      // ---------------- U^T and W^T; their completion hands the chunk to the
-      // state group.  A failed wait here sets the abort flag, which the next
-      // group wait turns into a verdict for the whole group.
-      if (ctid == 0) {
-        bool ok = true;
-        if (!zero_v) {
-          ok = solo_wait(ctl, B_VFULL, ph_v, A.err);
-          ph_v ^= 1u;
-          if (ok) ld.landed[1] = ld.issued[1];
-        }
-        if (ok && m >= 1) ok = solo_wait(ctl, B_WFREE, (m - 1) & 1, A.err);
-        if (ok) {
-          issue_m23(tbase, sm_base + OFF_V, smem_u32(qg), sm_base + OFF_ZT, TM_U + par * 64);
-          mma_commit(smem_u32(&ctl->bar[B_M23]));
-          mma_commit(smem_u32(&ctl->bar[B_READY0 + par]));
-          mbar_arrive(smem_u32(&ctl->bar[B_READY0 + par]));  // releases the chunk's shared-memory state
-        }
-        // the next chunk's q and k go to its Q o Gamma and K-hat buffers, free
-        // once the state group has finished the chunk before it
-        if (ok && m + 1 < nchunks) {
-          if (m + 1 >= 2) ok = solo_wait(ctl, B_FREE0 + (par ^ 1), (((m + 1) >> 1) - 1) & 1, A.err);
-          if (ok) ld.qk(t0 + kC, par ^ 1);
-        }
-      }
+      // ---------------- hand the chunk to the state group, which issues M2/M3
+      // (the arrive releases the chunk's shared-memory state to it)
+      if (ctid == 0) mbar_arrive(smem_u32(&ctl->bar[B_TB]));
     }
     if (ctid == 0) {
       ld.drain(A.err);
@@ -851,7 +837,20 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       const int t0 = bos + c * kC;
       const int len = min(kC, eos - t0);
       const uint32_t tm_u = TM_U + par * 64;
-      if (!(alive = group_wait<false>(ctl, B_READY0 + par, (c >> 1) & 1, stid, seq, A.err))) break;
+      // ---------------- M2/M3: U^T and W^T, once the chunk group has T_b
+      if (!(alive = group_wait<false>(ctl, B_TB, c & 1, stid, seq, A.err))) break;
+      if (stid == 0) {
+        bool ok = true;
+        if (!zero_v) {
+          ok = solo_wait(ctl, B_VFULL, c & 1, A.err);
+          if (ok) ++ctl->v_lnd;
+        }
+        if (ok) {
+          issue_m23(tbase, sm_base + OFF_V, sm_base + OFF_QG, sm_base + OFF_ZT, tm_u);
+          mma_commit(smem_u32(&ctl->bar[B_M23]));
+        }
+      }
+      if (!(alive = group_wait<false>(ctl, B_M23, c & 1, stid, seq, A.err))) break;
 
       // ---------------- -W^T (TMEM) -> MN-major operand in the V~ buffer
       {
@@ -866,7 +865,6 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       }
       group_publish<false>();
       if (stid == 0) {
-        mbar_arrive(smem_u32(&ctl->bar[B_WFREE]));
         issue_m4(tbase, sm_base + OFF_VT, sm_base + OFF_QG, par, tm_u);
         mma_commit(smem_u32(&ctl->bar[B_M4]));
       }
@@ -903,6 +901,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       }
       if (!(alive = group_wait<false>(ctl, B_M56, ph_m56, stid, seq, A.err))) break;
       ph_m56 ^= 1u;
+      // This parity's operand buffers are free (M4-M6 have completed and
+      // gamma_C was read before M5/M6 were issued): q and k of the chunk two
+      // ahead land in them; its A tile, gamma_C and TMEM U^T are written only
+      // after that copy has been waited for.
+      if (stid == 0 && c + 2 < nchunks) issue_qk(&maps, ctl, sm_base, h, t0 + 2 * kC, par);
 
       // ---------------- bf16 copy of the new state; the output rows
 #pragma unroll 1
@@ -933,8 +936,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           if (row < len) o[((size_t)(t0 + row) * H + h) * (kD / 8) + c16] = src[idx];
         }
       }
-      group_publish<false>();
-      if (stid == 0) mbar_arrive(smem_u32(&ctl->bar[B_FREE0 + par]));
+      // (the next chunk's first group wait orders these reads of the staging
+      // tile before it is written again)
     }
     if (alive && s_out) {
 #pragma unroll 1
@@ -956,6 +959,14 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) {  // q/k and v copies still in flight after an abort land before the CTA retires
+    volatile int no_abort = 0;
+    for (int i = 0; i < 2; ++i)
+      for (int n = ctl->qk_lnd[i]; n < ctl->qk_iss[i]; ++n)
+        mbar_wait(smem_u32(&ctl->bar[B_QK0 + i]), n & 1, &no_abort, A.err, 1u << 25);
+    for (int n = ctl->v_lnd; n < ctl->v_iss; ++n)
+      mbar_wait(smem_u32(&ctl->bar[B_VFULL]), n & 1, &no_abort, A.err, 1u << 26);
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
