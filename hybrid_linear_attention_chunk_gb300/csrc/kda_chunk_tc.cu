@@ -305,19 +305,21 @@ struct Loader {
     tma_load_3d(sm_base + OFF_GS, &maps->g, full, 0, h, t0);
     ++issued;
   }
-  __device__ void v(int t0) {
-    const uint32_t full = smem_u32(&ctl->bar[B_VFULL]);
-    mbar_arrive_expect_tx(full, 2 * 8192);
-    tma_load_3d(sm_base + OFF_V, &maps->v, full, 0, h, t0);
-    tma_load_3d(sm_base + OFF_V + 8192, &maps->v, full, 64, h, t0);
-    ++ctl->v_iss;
-  }
   // a g copy still in flight after an abort must land before the CTA retires
   __device__ void drain(unsigned int *err) {
     volatile int no_abort = 0;
     if (issued > landed) mbar_wait(smem_u32(&ctl->bar[B_GFULL]), landed & 1, &no_abort, err, 1u << 20);
   }
 };
+
+// v of the chunk at t0 (issued by one thread of either group).
+__device__ __forceinline__ void issue_v(const TcMaps *maps, Ctl *ctl, uint32_t sm_base, int h, int t0) {
+  const uint32_t full = smem_u32(&ctl->bar[B_VFULL]);
+  ++ctl->v_iss;
+  mbar_arrive_expect_tx(full, 2 * 8192);
+  tma_load_3d(sm_base + OFF_V, &maps->v, full, 0, h, t0);
+  tma_load_3d(sm_base + OFF_V + 8192, &maps->v, full, 64, h, t0);
+}
 
 // q and k of the chunk at t0 into the Q o Gamma and K-hat buffers of chunk
 // parity par (issued by one thread of either group).
@@ -458,7 +460,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // group as it frees each parity's buffers
       issue_qk(&maps, ctl, sm_base, h, bos, 0);
       if (nchunks > 1) issue_qk(&maps, ctl, sm_base, h, bos + kC, 1);
-      if (!zero_v) ld.v(bos);
+      if (!zero_v) issue_v(&maps, ctl, sm_base, h, bos);
     }
     if (zero_v)  // the v tile stays zero for the whole item
       for (int e = ctid; e < 16384 / 16; e += kChunkThreads)
@@ -524,15 +526,13 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         beta_next = ctid < eos - (t0 + kC)
                         ? __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + kC + ctid) * H + h)
                         : 0.f;
-      // The previous chunk's M2/M3 must be done with Gamma o K, T_b and the v
-      // tile before this chunk overwrites them; then this chunk's v tile.
-      // This chunk's q and k have landed.
+      // The previous chunk's M2/M3 must be done with Gamma o K and T_b before
+      // this chunk overwrites them; this chunk's q and k have landed.
       if (ctid == 0) {
         bool ok = true;
         if (m >= 1) {
           ok = solo_wait(ctl, B_M23, ph_m23, A.err);
           ph_m23 ^= 1u;
-          if (ok && !zero_v) ld.v(t0);
         }
         if (ok) {
           ok = solo_wait(ctl, B_QK0 + par, (m >> 1) & 1, A.err);
@@ -851,6 +851,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
       }
       if (!(alive = group_wait<false>(ctl, B_M23, c & 1, stid, seq, A.err))) break;
+      if (stid == 0 && !zero_v && c + 1 < nchunks) issue_v(&maps, ctl, sm_base, h, t0 + kC);  // M2 is done with v
 
       // ---------------- -W^T (TMEM) -> MN-major operand in the V~ buffer
       {
