@@ -11,7 +11,7 @@
 // r), Gamma = exp(G) and gamma_C = exp(G_C) ([K3-notes §2.2, chunkwise form]):
 //   M1  [A ; L''] = [Q o Gamma ; Gamma o K] (K / Gamma)^T      (M=128 N=64 K=128)
 //   A  = Tril_incl(A), L = StrictTril(diag(beta) L'')
-//   T_b = (I + L)^{-1} diag(beta)   blocked forward substitution on CUDA cores
+//   T_b = (I + L)^{-1} diag(beta)   blocked substitution: CUDA cores (fp32), last level tf32 MMA
 //   M2  U^T = V^T T_b^T                                          (M=128 N=64 K=64)
 //   M3  W^T = (Gamma o K)^T T_b^T                                (M=128 N=64 K=64)
 //   M4  V~^T = U^T - S^T W^T ;  O^T = S^T (Q o Gamma)^T          (M=128 N=64 K=128, twice)
@@ -70,7 +70,8 @@ constexpr uint32_t OFF_QG = 0;        // 48 KB: per 64-column K-half (stride KHA
                                       //   [Q o Gamma, even chunks | Gamma o K | Q o Gamma, odd chunks]
 constexpr uint32_t KHALF = 24576;
 constexpr uint32_t OFF_KB = 49152;    // 16 KB: K / Gamma -> L, then T over it (fp32 64x64)
-constexpr uint32_t OFF_TF = 65536;    // 16 KB: scratch of the solve's block products
+constexpr uint32_t OFF_TF = 65536;    // 16 KB: solve scratch: T_[01][01]^T and X^T (tf32 B operands of
+                                      //   the level-2 products, 4 KB each), level-1 products (2 KB)
 constexpr uint32_t OFF_KH = 81920;    // x2 16 KB: K o gamma_C / Gamma (MN-major B of M6)
 constexpr uint32_t OFF_AM = 114688;   // x2 8 KB: A bf16, 64 rows x 64
 constexpr uint32_t OFF_ZT = 131072;   // 8 KB: T_b bf16 (read by M2/M3)
@@ -92,7 +93,7 @@ constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
   B_M1 = 0, B_M23, B_VFULL, B_GFULL, B_QK0, B_QK1, B_TB, B_M4,
-  B_M56, B_TD_C, B_TD_S, B_COUNT
+  B_M56, B_L2, B_TD_C, B_TD_S, B_COUNT
 };
 
 struct Ctl {
@@ -221,20 +222,6 @@ __device__ __forceinline__ float4 sub4(const float4 &a, const float4 &b) {
 __device__ __forceinline__ float4 neg4(const float4 &a) { return make_float4(-a.x, -a.y, -a.z, -a.w); }
 __device__ __forceinline__ float4 ex2_4(const float4 &a) { return make_float4(ex2(a.x), ex2(a.y), ex2(a.z), ex2(a.w)); }
 
-// acc[i] = sum_j l[i][j] t[j] over eight k (l[i][h] holds k = 4h .. 4h + 3):
-// a 4x4 block of a product
-__device__ __forceinline__ void fma4x8(float4 (&acc)[4], const float4 (&l)[4][2], const float4 (&t)[8]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float lv = f4c(l[i][j >> 2], j & 3);
-      acc[i].x += lv * t[j].x; acc[i].y += lv * t[j].y; acc[i].z += lv * t[j].z; acc[i].w += lv * t[j].w;
-    }
-  }
-}
-
 // acc += l[k0 + i] * t[i] for i < 8 (l: the left factor's row, four per float4)
 __device__ __forceinline__ void fma8(float4 &acc, const float4 *l, int k0, const float4 (&t)[8]) {
 #pragma unroll
@@ -251,10 +238,17 @@ __device__ __forceinline__ void bar_sync_n(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// fp32 64x64 matrices of the solve (L, T) are stored row-major with the
-// column index XORed with 4*(row & 7): columns keep 4-float groups intact,
-// and eight consecutive rows read at one column hit eight different banks.
-__device__ __forceinline__ int swz64(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
+// fp32 64x64 matrices of the solve (L, T) are stored as two 32-column halves
+// of 64 rows x 128 bytes whose 16-byte chunks are XORed with (row & 7): the
+// 128-byte-swizzled K-major layout of a tf32 MMA operand.  Columns keep
+// 4-float groups intact, and eight consecutive rows read at one column hit
+// eight different banks.
+__device__ __forceinline__ int lt_idx(int r, int c) {
+  return ((c >> 5) << 11) + (r << 5) + ((((c >> 2) & 7) ^ (r & 7)) << 2) + (c & 3);
+}
+
+// Element (n, k) of a 32x32 fp32 K-major tf32 operand tile in the same layout.
+__device__ __forceinline__ int tt_idx(int n, int k) { return (n << 5) + ((((k >> 2) & 7) ^ (n & 7)) << 2) + (k & 3); }
 
 // A group-wide view of an mbarrier wait: the group's thread 0 waits, the
 // group synchronises, and every thread gets the same verdict (so no thread
@@ -448,7 +442,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     // 64-column K-half, and a thread's rows lie in one 16-token tile, t8 / 2
     const int p4 = ctid & 31, t8 = ctid >> 5;
     int seq = 0;
-    uint32_t ph_m1 = 0, ph_m23 = 0, ph_g = 0;
+    uint32_t ph_m1 = 0, ph_m23 = 0, ph_g = 0, ph_l2 = 0;
     Loader ld{&maps, ctl, sm_base, h, 0, 0};
     if (ctid == 0 && nchunks > 0) {
       tma_prefetch_desc(&maps.q);
@@ -467,6 +461,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         reinterpret_cast<uint4 *>(sm + OFF_V)[e] = make_uint4(0u, 0u, 0u, 0u);
     for (int e = ctid; e < 8192 / 16; e += kChunkThreads)  // T_b above the diagonal: zero for good
       reinterpret_cast<uint4 *>(sm + OFF_ZT)[e] = make_uint4(0u, 0u, 0u, 0u);
+    if (ctid < 64) {  // T_01^T in the transposed copy of T_[01][01]: zero for good
+      const int n = 16 + (ctid >> 2), k0 = 4 * (ctid & 3);
+      *reinterpret_cast<float4 *>(reinterpret_cast<float *>(sm + OFF_TF) + tt_idx(n, k0)) =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float beta_next = 0.f;
     if (ctid < kC && ctid < eos - bos) beta_next = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(bos + ctid) * H + h);
     float *tot = reinterpret_cast<float *>(sm + OFF_PRO);  // [4][128] per-tile decay sums
@@ -627,36 +626,29 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // there are already T's.
       {
         float *Lf = reinterpret_cast<float *>(sm + OFF_KB);  // K / Gamma is dead once M1 is done
-        float *Xf = reinterpret_cast<float *>(sm + OFF_TF);  // scratch of the block products
+        float *TTf = reinterpret_cast<float *>(sm + OFF_TF);      // T_[01][01]^T, [32][32] K-major
+        float *XTf = TTf + 1024;                                  // X^T of level 2, [32][32] K-major
+        float *Xf = TTf + 2048;                                   // level-1 products
         // even chunks: TMEM lanes 0..63 hold A's rows, 64..127 L''; odd chunks the reverse
         const bool a_rows = (qw < 2) == (par == 0);
         const int r = 32 * (qw & 1) + lane;
+        float v[32];  // row r, columns [32 ch, 32 ch + 32) of the Gram product
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_D1 + 32 * ch), v);
+        tmem_wait_ld();
+        const int s0 = 32 * ch;
         if (a_rows) {
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float v[16];
-            const int s0 = 32 * ch + 16 * hh;
-            tmem_ld16(tmem_addr(tbase, 32 * qw, TM_D1 + s0), v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int cc = 0; cc < 16; ++cc) v[cc] = (s0 + cc <= r) ? v[cc] : 0.f;
-            st_row16_bf16(sm + OFF_AM + par * 8192, r, s0, v);
-          }
+          for (int cc = 0; cc < 32; ++cc) v[cc] = (s0 + cc <= r) ? v[cc] : 0.f;
+          st_row16_bf16(sm + OFF_AM + par * 8192, r, s0, v);
+          st_row16_bf16(sm + OFF_AM + par * 8192, r, s0 + 16, v + 16);
         } else {
           const float br = ctl->bs[r];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float v[16];
-            const int s0 = 32 * ch + 16 * hh;
-            tmem_ld16(tmem_addr(tbase, 32 * qw, TM_D1 + s0), v);
-            tmem_wait_ld();
+          for (int cc = 0; cc < 32; ++cc) v[cc] = (s0 + cc < r) ? br * v[cc] : 0.f;
 #pragma unroll
-            for (int cc = 0; cc < 16; ++cc) v[cc] = (s0 + cc < r) ? br * v[cc] : 0.f;
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-              *reinterpret_cast<float4 *>(Lf + swz64(r, s0 + 4 * c4)) =
-                  make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
-          }
+          for (int c4 = 0; c4 < 8; ++c4)
+            *reinterpret_cast<float4 *>(Lf + lt_idx(r, s0 + 4 * c4)) =
+                make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
         }
         bar_chunk();
         // Diagonal 16x16 blocks: one column of T per thread, rows in groups of
@@ -674,7 +666,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
             for (int i = 0; i < 4; ++i)
 #pragma unroll
               for (int q = 0; q <= R; ++q)
-                lr[i][q] = *reinterpret_cast<const float4 *>(Lf + swz64(base + 4 * R + i, base + 4 * q));
+                lr[i][q] = *reinterpret_cast<const float4 *>(Lf + lt_idx(base + 4 * R + i, base + 4 * q));
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int rr = 4 * R + i;
@@ -686,19 +678,23 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           }
           bar_sync_n(3, 64);  // the block's L is read in full before T overwrites it
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) Lf[swz64(base + rr, base + cc)] = x[rr];
+          for (int rr = 0; rr < 16; ++rr) Lf[lt_idx(base + rr, base + cc)] = x[rr];
+          if (base < 32)  // column cc of T_00 / T_11 is row cc of the transposed copy
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<float4 *>(TTf + tt_idx(base + cc, base + 4 * j)) =
+                  make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
         }
         bar_chunk();
         // Off-diagonal blocks in two levels of the 2x2 block inverse
         // [[P, 0], [R, Q]]^{-1} = [[P^-1, 0], [-Q^-1 R P^-1, Q^-1]]:
         //   level 1 (16-row blocks): T_10 and T_32;
         //   level 2 (32-row blocks): T_[23][01].
-        // Each output is X = R P^-1 into scratch, then -Q^-1 X.  Shared-memory
-        // bandwidth limits these products, so level 2 blocks 4x4 outputs per
-        // thread and splits k four ways across the warps.  Every block of
+        // Each output is X = R P^-1, then -Q^-1 X.  Level 1 runs on CUDA cores
+        // (fp32); level 2 on the tensor core (tf32, below).  Every block of
         // T_b = T diag(beta) is written as soon as its T block is final, the
-        // product outputs straight from registers; T_b's blocks above the
-        // diagonal stay zero from the start.
+        // product outputs straight from registers or TMEM; T_b's blocks above
+        // the diagonal stay zero from the start.
         const float4 *bs4 = reinterpret_cast<const float4 *>(ctl->bs);
         uint8_t *zt = sm + OFF_ZT;
         if (ctid < 128) {
@@ -708,18 +704,18 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           float *X1 = Xf + blk * 256;                              // [16][16]
           float4 l[4], t[8];
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) l[c4] = lds128(Lf + swz64(rb + rr, cb + 4 * c4));  // row of L_(rb, cb)
+          for (int c4 = 0; c4 < 4; ++c4) l[c4] = lds128(Lf + lt_idx(rb + rr, cb + 4 * c4));  // row of L_(rb, cb)
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int k0 = 0; k0 < 16; k0 += 8) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) t[i] = lds128(Lf + swz64(cb + k0 + i, cb + 4 * q4));
+            for (int i = 0; i < 8; ++i) t[i] = lds128(Lf + lt_idx(cb + k0 + i, cb + 4 * q4));
             fma8(acc, l, k0, t);
           }
           *reinterpret_cast<float4 *>(X1 + rr * 16 + 4 * q4) = acc;
           bar_sync_n(3, 128);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) l[c4] = lds128(Lf + swz64(rb + rr, rb + 4 * c4));  // row of T_(rb, rb)
+          for (int c4 = 0; c4 < 4; ++c4) l[c4] = lds128(Lf + lt_idx(rb + rr, rb + 4 * c4));  // row of T_(rb, rb)
           acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int k0 = 0; k0 < 16; k0 += 8) {
@@ -728,8 +724,14 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
             fma8(acc, l, k0, t);
           }
           acc = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-          *reinterpret_cast<float4 *>(Lf + swz64(rb + rr, cb + 4 * q4)) = acc;
+          *reinterpret_cast<float4 *>(Lf + lt_idx(rb + rr, cb + 4 * q4)) = acc;
           st_row4_bf16(zt, rb + rr, cb + 4 * q4, mul4(acc, bs4[cb / 4 + q4]));
+          if (blk == 0) {  // T_10 into the transposed copy
+            TTf[tt_idx(4 * q4, 16 + rr)] = acc.x;
+            TTf[tt_idx(4 * q4 + 1, 16 + rr)] = acc.y;
+            TTf[tt_idx(4 * q4 + 2, 16 + rr)] = acc.z;
+            TTf[tt_idx(4 * q4 + 3, 16 + rr)] = acc.w;
+          }
         } else if (ctid < 192) {
           // T_b of the diagonal blocks: row rr of block db, its 16 columns
           const int e = ctid - 128, db = e >> 4, rr = e & 15;
@@ -737,64 +739,54 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           float v[16];
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 tv = mul4(lds128(Lf + swz64(row, c0 + 4 * c4)), bs4[c0 / 4 + c4]);
+            const float4 tv = mul4(lds128(Lf + lt_idx(row, c0 + 4 * c4)), bs4[c0 / 4 + c4]);
             v[4 * c4] = tv.x; v[4 * c4 + 1] = tv.y; v[4 * c4 + 2] = tv.z; v[4 * c4 + 3] = tv.w;
           }
           st_row16_bf16(zt, row, c0, v);
         }
-        bar_chunk();
-        {
-          // level 2: thread = output rows 32 + 4 rg .. + 3, columns 4 q4 .. + 3,
-          // k in [8 kq, 8 kq + 8).  Partial sums of kq = 1..3 meet in Pf
-          // ([kq - 1][i][rg, q4] float4, conflict-free); kq = 0 completes.
-          const int q4 = ctid & 7, rg = (ctid >> 3) & 7, kq = ctid >> 6, k0 = 8 * kq;
-          float4 *Pf = reinterpret_cast<float4 *>(Xf + 32 * 32);  // 12 KB after X
-          float4 acc[4], lv[4][2], t[8];
-          // X = L_[23][01] T_[01][01]
+        // level 2 on the tensor core (tf32; the level-2 block of T is small
+        // beside the diagonal, and T_b is rounded to bf16 after it):
+        //   X = L_[23][01] T_[01][01], then T_[23][01] = -T_[23][23] X.
+        // M = 128 rows of the row-major operand (rows 0-31 and 64-127 of the
+        // product are not used), N = 32, K = 32; D in the M1 result's columns.
+        group_publish<true>();
+        if (ctid == 0) {
+          constexpr uint32_t id = idesc_tf32_f32(128, 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int kk = 0; kk < 4; ++kk)
+            mma_tf32_ss(tbase + TM_D1, smem_desc_sw128(sm_base + OFF_KB + kk * 32, 16, 1024),
+                        smem_desc_sw128(sm_base + OFF_TF + kk * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
+          mma_commit(smem_u32(&ctl->bar[B_L2]));
+        }
+        if (!(alive = group_wait<true>(ctl, B_L2, ph_l2, ctid, seq, A.err))) break;
+        ph_l2 ^= 1u;
+        if ((warp & 3) == 1) {  // rows 32-63 of the product: X (TMEM lanes 32-63) -> X^T
+          const int n0 = 16 * (warp >> 2);
+          float x[16];
+          tmem_ld16(tmem_addr(tbase, 32, TM_D1 + n0), x);
+          tmem_wait_ld();
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) lv[i][h2] = lds128(Lf + swz64(32 + 4 * rg + i, k0 + 4 * h2));
+          for (int i = 0; i < 16; ++i) XTf[tt_idx(n0 + i, lane)] = x[i];
+        }
+        group_publish<true>();
+        if (ctid == 0) {
+          constexpr uint32_t id = idesc_tf32_f32(128, 32);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) t[j] = lds128(Lf + swz64(k0 + j, 4 * q4));
-          fma4x8(acc, lv, t);
-          if (kq > 0)
+          for (int kk = 0; kk < 4; ++kk)
+            mma_tf32_ss(tbase + TM_D1 + 32, smem_desc_sw128(sm_base + OFF_KB + 8192 + kk * 32, 16, 1024),
+                        smem_desc_sw128(sm_base + OFF_TF + 4096 + kk * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
+          mma_commit(smem_u32(&ctl->bar[B_L2]));
+        }
+        if (!(alive = group_wait<true>(ctl, B_L2, ph_l2, ctid, seq, A.err))) break;
+        ph_l2 ^= 1u;
+        if ((warp & 3) == 1) {  // rows 32-63: T_[23][23] X = -T_[23][01]  ->  T_b
+          const int n0 = 16 * (warp >> 2);
+          float y[16];
+          tmem_ld16(tmem_addr(tbase, 32, TM_D1 + 32 + n0), y);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) Pf[((kq - 1) * 4 + i) * 64 + rg * 8 + q4] = acc[i];
-          bar_chunk();
-          if (kq == 0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float4 x = acc[i];
-#pragma unroll
-              for (int kk = 0; kk < 3; ++kk) x = add4(x, Pf[(kk * 4 + i) * 64 + rg * 8 + q4]);
-              *reinterpret_cast<float4 *>(Xf + (4 * rg + i) * 32 + 4 * q4) = x;
-            }
-          }
-          bar_chunk();
-          // -T_[23][23] X
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) lv[i][h2] = lds128(Lf + swz64(32 + 4 * rg + i, 32 + k0 + 4 * h2));
-#pragma unroll
-          for (int j = 0; j < 8; ++j) t[j] = lds128(Xf + (k0 + j) * 32 + 4 * q4);
-          fma4x8(acc, lv, t);
-          if (kq > 0)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) Pf[((kq - 1) * 4 + i) * 64 + rg * 8 + q4] = acc[i];
-          bar_chunk();
-          if (kq == 0) {
-            const float4 b = bs4[q4];
-            const float4 nb = make_float4(-b.x, -b.y, -b.z, -b.w);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float4 x = acc[i];
-#pragma unroll
-              for (int kk = 0; kk < 3; ++kk) x = add4(x, Pf[(kk * 4 + i) * 64 + rg * 8 + q4]);
-              st_row4_bf16(zt, 32 + 4 * rg + i, 4 * q4, mul4(x, nb));
-            }
-          }
+          for (int i = 0; i < 16; ++i) y[i] *= -ctl->bs[n0 + i];
+          st_row16_bf16(zt, 32 + lane, n0, y);
         }
       }
       group_publish<true>();
