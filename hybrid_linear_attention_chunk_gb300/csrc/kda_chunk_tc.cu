@@ -380,6 +380,25 @@ __device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t vt, uint32_t 
                 smem_desc_sw128(kh + kk * 2048, 8192, 1024), id6, 1u);
 }
 
+// The sequence of rank r when N packed sequences are ordered by length,
+// longest first (ties by index).  Every thread of the CTA calls it; s holds
+// N + 1 ints of shared scratch.
+constexpr int kLongestFirstMax = 512;
+__device__ int longest_first(const int32_t *cu, int N, int r, int *s, int tid) {
+  for (int i = tid; i < N; i += kThreads) s[i] = cu[i + 1] - cu[i];
+  __syncthreads();
+  for (int j = tid; j < N; j += kThreads) {
+    const int lj = s[j];
+    int rank = 0;
+    for (int i = 0; i < N; ++i) rank += (s[i] > lj) || (s[i] == lj && i < j);
+    if (rank == r) s[N] = j;
+  }
+  __syncthreads();
+  const int n = s[N];
+  __syncthreads();  // the scratch is reused later
+  return n;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   extern __shared__ uint8_t smem_raw[];
@@ -396,7 +415,12 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   item /= a.kinds;
   const int h = item % H;
   item /= H;
-  const int seg = item % a.nseg, n = item / a.nseg;
+  const int seg = item % a.nseg;
+  int n = item / a.nseg;
+  // Packed sequences run longest first: work items are handed to SMs in
+  // index order, so a long sequence that came late would finish last.
+  if (a.cu && a.N > 1 && a.N <= kLongestFirstMax)
+    n = longest_first(a.cu, a.N, n, reinterpret_cast<int *>(sm + OFF_TF), tid);
   int bos, eos;
   seq_range(a, n, bos, eos);
   if (a.seg_tokens > 0) {
