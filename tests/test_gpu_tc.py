@@ -141,3 +141,22 @@ def test_tc_deterministic_and_resume(kda):
     oa, sa = run(kda, {**pa, "initial_state": x["initial_state"], "cu_seqlens": None})
     ob, sb = run(kda, {**pb, "initial_state": sa, "cu_seqlens": None})
     assert torch.equal(torch.cat([oa, ob]), o1) and torch.equal(sb, s1)
+
+
+@pytest.mark.parametrize("nseq", [512, 600])
+def test_tc_many_packed_sequences(kda, nseq):
+    """Packed batches of many short sequences, ragged and empty ones among them:
+    up to 512 sequences each work item ranks the lengths and runs the sequences
+    longest first; beyond that it keeps index order.  Either way every
+    (sequence, head) chain must match the oracle and land in its own rows and
+    final-state slot."""
+    rng = np.random.default_rng(nseq)
+    lens = rng.integers(0, 140, size=nseq)
+    lens[::37] = 0
+    lens[5] = 257  # one long sequence that is not first in index order
+    w = inputs.scaled(inputs.VARLEN_64, H=2)
+    x = inputs.make_prefill(w, device=DEV, lengths=lens)
+    o, s = run(kda, x)
+    o_ref, s_ref = oracle_prefill(x)
+    assert_close(to_np(o), o_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="o")
+    assert_close(to_np(s), s_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="S")
