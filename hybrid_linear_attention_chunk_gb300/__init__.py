@@ -7,7 +7,9 @@ synthetic input generator.  Importing the package does not load the library;
 the first call does, and raises if it is missing.
 """
 from ._lib import (KdaChunkDesc, KdaDecodeDesc, KdaError, chunk_desc, kda_chunk_fwd,  # noqa: F401
-                   kda_chunk_fwd_noalloc, kda_chunk_fwd_workspace_size, kda_decode_step, load, LIB_PATH)
+                   kda_chunk_fwd_ckpt, kda_chunk_fwd_noalloc, kda_chunk_fwd_workspace_size, kda_decode_step,
+                   load, LIB_PATH)
 
-__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_decode_step", "kda_chunk_fwd_workspace_size", "load", "KdaError",
-           "KdaChunkDesc", "KdaDecodeDesc", "chunk_desc", "LIB_PATH"]
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_ckpt", "kda_chunk_fwd_noalloc", "kda_decode_step",
+           "kda_chunk_fwd_workspace_size", "load", "KdaError", "KdaChunkDesc", "KdaDecodeDesc", "chunk_desc",
+           "LIB_PATH"]

@@ -73,6 +73,9 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
         lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(KdaChunkDesc), P, P, P, P, P, P, P, P, P, P]
         lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.kda_chunk_fwd_ckpt.argtypes = [ctypes.POINTER(KdaChunkDesc), P, P, P, P, P, P, P, P, P,
+                                           ctypes.c_int, P, P, P, ctypes.c_size_t, P]
+        lib.kda_chunk_fwd_ckpt.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [ctypes.POINTER(KdaDecodeDesc), P, P, P, P, P, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -191,6 +194,39 @@ def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, initial_state=None, cu_seqle
                                    _stream_handle(stream, dev))
     _check(st, "kda_chunk_fwd_noalloc")
     return out, final_state
+
+
+def kda_chunk_fwd_ckpt(q, k, v, log_alpha, beta, every, initial_state=None, cu_seqlens=None,
+                       cu_ckpt=None, out=None, final_state=None, ckpt=None, *, chunk=64, kernel="auto",
+                       segments=0, validate=False, out_dtype=None, want_final_state=True, B=None,
+                       stream=None, workspace=None):
+    """kda_chunk_fwd that also stores the fp32 state after every `every`
+    tokens of each sequence (prefix-cache checkpoints).
+
+    cu_ckpt: int32 [N+1] on the device with cu_ckpt[n+1] - cu_ckpt[n] =
+    len_n // every (required with cu_seqlens).  When `ckpt` is None it is
+    allocated here with cu_ckpt[-1] slots (a device-to-host read) or, for a
+    B x T batch, B * (T // every) slots.  Returns (out, final_state, ckpt).
+    """
+    lib = load()
+    dev = q.device
+    d = chunk_desc(q, v, chunk=chunk, cu_seqlens=cu_seqlens, out_dtype=out_dtype or q.dtype,
+                   gate_dtype=_dt(log_alpha), validate=validate, kernel=kernel, segments=segments, B=B)
+    Nseq = d.num_seqs if cu_seqlens is not None else d.B
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (d.dv,), dtype=out_dtype or q.dtype, device=dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(Nseq, d.H, d.dk, d.dv, dtype=torch.float32, device=dev)
+    if ckpt is None:
+        slots = int(cu_ckpt[-1].item()) if cu_seqlens is not None else d.B * (d.T // every if every > 0 else 0)
+        ckpt = torch.empty(max(slots, 1), d.H, d.dk, d.dv, dtype=torch.float32, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_chunk_fwd_ckpt(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                int(every), _ptr(cu_ckpt), _ptr(ckpt), _ptr(workspace), ws_bytes,
+                                _stream_handle(stream, dev))
+    _check(st, "kda_chunk_fwd_ckpt")
+    return out, final_state, ckpt
 
 
 def kda_chunk_fwd_workspace_size(desc: KdaChunkDesc) -> int:

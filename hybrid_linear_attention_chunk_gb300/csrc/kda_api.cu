@@ -61,6 +61,16 @@ __global__ void validate_prefill_kernel(PrefillArgs a, int *flag) {
       if (n > 0 && c < a.cu[n - 1]) bad |= 4;
     }
   }
+  if (a.ck && a.ck_cu && blockIdx.x == 1) {  // checkpoint slots: floor(len / every) per sequence
+    for (int n = threadIdx.x; n <= a.N; n += blockDim.x) {
+      const int c = a.ck_cu[n];
+      if (n == 0 && c != 0) bad |= 8;
+      if (n > 0) {
+        const int len = a.cu ? a.cu[n] - a.cu[n - 1] : a.T_seq;
+        if (len >= 0 && c - a.ck_cu[n - 1] != len / a.ck_every) bad |= 8;
+      }
+    }
+  }
   if (bad) atomicOr(flag, bad);
 }
 
@@ -261,6 +271,43 @@ kda_status kda_chunk_fwd_ex(const kda_chunk_desc *desc, const void *q, const voi
                                 final_state, &a);
   if (st != KDA_OK) return st;
   return run_prefill(desc, a, reinterpret_cast<cudaStream_t>(stream), 1, workspace, workspace_bytes);
+}
+
+kda_status kda_chunk_fwd_ckpt(const kda_chunk_desc *desc, const void *q, const void *k,
+                              const void *v, const void *log_alpha, const void *beta,
+                              const float *initial_state, const int32_t *cu_seqlens, void *out,
+                              float *final_state, int every, const int32_t *cu_ckpt, float *ckpt,
+                              void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+  PrefillArgs a;
+  kda_status st = check_prefill(desc, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out,
+                                final_state, &a);
+  if (st != KDA_OK) return st;
+  if (!ckpt || (cu_seqlens && !cu_ckpt)) return KDA_ERR_NULL;
+  if (every <= 0 || every % desc->chunk != 0) return KDA_ERR_SHAPE;
+  if (!aligned_to(ckpt, 4) || (cu_ckpt && !aligned_to(cu_ckpt, 4))) return KDA_ERR_ALIGN;
+  // the checkpoints may alias nothing the call reads or writes (their count is
+  // known on the host only for a B x T batch)
+  const size_t state = (size_t)desc->H * desc->dk * desc->dv * 4;
+  const size_t slots = cu_seqlens ? 1 : (size_t)a.N * (size_t)(desc->T / every);
+  const size_t th = (size_t)a.T_total * desc->H;
+  Range r_ck = span(ckpt, slots * state);
+  Range others[] = {span(q, th * desc->dk * esize(desc->qkv_dtype)),
+                    span(k, th * desc->dk * esize(desc->qkv_dtype)),
+                    span(v, th * desc->dv * esize(desc->qkv_dtype)),
+                    span(log_alpha, th * desc->dk * esize(desc->gate_dtype)),
+                    span(beta, th * esize(desc->gate_dtype)),
+                    span(out, th * desc->dv * esize(desc->out_dtype)),
+                    span(initial_state, initial_state ? (size_t)a.N * state : 0),
+                    span(final_state, final_state ? (size_t)a.N * state : 0),
+                    span(cu_seqlens, cu_seqlens ? (size_t)(a.N + 1) * 4 : 0),
+                    span(cu_ckpt, cu_ckpt ? (size_t)(a.N + 1) * 4 : 0)};
+  for (const Range &r : others)
+    if (overlap(r_ck, r)) return KDA_ERR_ALIAS;
+  a.ck_every = every;
+  a.ck_cu = cu_ckpt;
+  a.ck = ckpt;
+  return run_prefill(desc, a, reinterpret_cast<cudaStream_t>(stream), workspace ? 1 : 0, workspace,
+                     workspace_bytes);
 }
 
 kda_status kda_decode_step(const kda_decode_desc *d, const void *q, const void *k, const void *v,

@@ -218,6 +218,13 @@ chunk_simt_kernel(PrefillArgs a, int dvt) {
       for (int r = 0; r < C; ++r) acc += m.K[r * ld + i] * m.Vt[r * dvt + j];
       m.S[e] = acc;
     }
+    if (float *cp = ckpt_ptr(a, n, h, t0 + len - bos)) {  // a checkpoint ends this chunk
+      __syncthreads();
+      for (int e = tid; e < dk * dvt; e += kSimtThreads) {
+        int i = e / dvt, j = e % dvt;
+        cp[(size_t)i * dv + j0 + j] = m.S[e];
+      }
+    }
   }
   __syncthreads();
   if (a.sT) {

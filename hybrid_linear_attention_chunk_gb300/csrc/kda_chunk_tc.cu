@@ -423,6 +423,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     n = longest_first(a.cu, a.N, n, reinterpret_cast<int *>(sm + OFF_TF), tid);
   int bos, eos;
   seq_range(a, n, bos, eos);
+  const int seq_bos = bos;  // checkpoints count tokens from the sequence start
   if (a.seg_tokens > 0) {
     const int sb = min(eos, bos + seg * a.seg_tokens);
     eos = min(eos, sb + a.seg_tokens);
@@ -924,13 +925,18 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // after that copy has been waited for.
       if (stid == 0 && c + 2 < nchunks) issue_qk(&maps, ctl, sm_base, h, t0 + 2 * kC, par);
 
-      // ---------------- bf16 copy of the new state; the output rows
+      // ---------------- bf16 copy of the new state (and a checkpoint of the
+      // fp32 state when one ends this chunk); the output rows
+      float *cp = ckpt_ptr(a, n, h, t0 + len - seq_bos);
 #pragma unroll 1
       for (int i0 = 0; i0 < kD; i0 += 32) {
         float s[32];
         tmem_ld32(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
         tmem_wait_ld();
         tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_STB + i0 / 2), s);
+        if (cp)
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) cp[(size_t)(i0 + cc) * kD + j] = s[cc];
       }
       {
         __nv_bfloat16 *ostage = reinterpret_cast<__nv_bfloat16 *>(vt);

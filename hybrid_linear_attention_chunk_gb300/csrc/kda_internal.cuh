@@ -43,7 +43,22 @@ struct PrefillArgs {
   int seg_tokens = 0;        // 0: the whole sequence is one segment
   int nseg = 1;
   int kinds = 1;
+  // State checkpoints (nullable ck): the state after every ck_every tokens of
+  // a sequence (a multiple of the chunk) goes to slot first + j - 1 of ck
+  // [slots][H][dk][dv], first = ck_cu[n] when ck_cu is given, else
+  // n * (T_seq / ck_every).
+  int ck_every = 0;
+  const int32_t *ck_cu = nullptr;
+  float *ck = nullptr;
 };
+
+// Where the state of (sequence n, head h) goes once `done` tokens of the
+// sequence have been processed, or nullptr when no checkpoint falls there.
+__device__ __forceinline__ float *ckpt_ptr(const PrefillArgs &a, int n, int h, int done) {
+  if (!a.ck || done <= 0 || done % a.ck_every != 0) return nullptr;
+  const long long first = a.ck_cu ? (long long)a.ck_cu[n] : (long long)n * (a.T_seq / a.ck_every);
+  return a.ck + ((size_t)(first + done / a.ck_every - 1) * a.H + h) * a.dk * a.dv;
+}
 
 struct DecodeArgs {
   int N, H, dk, dv;

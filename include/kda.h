@@ -126,6 +126,36 @@ kda_status kda_chunk_fwd_ex(const kda_chunk_desc *desc, const void *q, const voi
                             float *final_state, void *workspace, size_t workspace_bytes,
                             kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_ckpt - kda_chunk_fwd that also stores the state at fixed
+ * intervals along each sequence, for prefix-cache reuse ([K3-notes §2.5,
+ * Fig. 12]: a request that shares a cached prefix resumes from the state at
+ * the prefix's end; a cache that keeps a state every `every` tokens can
+ * resume at any multiple of it).
+ *
+ *   every     checkpoint interval in tokens, a positive multiple of
+ *             desc->chunk (KDA_ERR_SHAPE otherwise)
+ *   cu_ckpt   [N+1] int32 device, required with cu_seqlens: sequence n's
+ *             checkpoints go to slots cu_ckpt[n] .. cu_ckpt[n+1]-1, and
+ *             cu_ckpt[n+1] - cu_ckpt[n] must be floor(len_n / every)
+ *             (checked in validate mode); NULL for a B x T batch, whose
+ *             sequence n uses slots n*floor(T/every) .. (n+1)*floor(T/every)-1
+ *   ckpt      [slots, H, dk, dv] fp32 device, written: the j-th slot of a
+ *             sequence (j = 1, 2, ...) holds its state after its first
+ *             j*every tokens, exactly what kda_chunk_fwd on that prefix
+ *             alone would return as final_state (up to rounding)
+ *   workspace as in kda_chunk_fwd_ex; NULL makes a split plan allocate its
+ *             workspace stream-ordered, as kda_chunk_fwd does
+ * Other arguments and conventions as kda_chunk_fwd.  ckpt may alias no other
+ * argument (KDA_ERR_ALIAS; for packed sequences only its first slot's extent
+ * is known on the host and checked).
+ */
+kda_status kda_chunk_fwd_ckpt(const kda_chunk_desc *desc, const void *q, const void *k,
+                              const void *v, const void *log_alpha, const void *beta,
+                              const float *initial_state, const int32_t *cu_seqlens, void *out,
+                              float *final_state, int every, const int32_t *cu_ckpt, float *ckpt,
+                              void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
 typedef struct {
   int N;          /* independent sequences, one token each                    */
   int H;          /* heads                                                    */

@@ -77,6 +77,8 @@ def _load():
     lib.oracle_kda_decode_step.restype = I
     lib.oracle_kda_affine_pair.argtypes = [I, I, I, I, L, L, P, P, P, P, P, P]
     lib.oracle_kda_affine_pair.restype = I
+    lib.oracle_kda_recurrent_ckpt.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, P, I]
+    lib.oracle_kda_recurrent_ckpt.restype = I
     _lib = lib
     return lib
 
@@ -144,6 +146,32 @@ def recurrent(q, k, v, g, beta, initial_state=None, cu_seqlens=None, chains=None
     if st != 0:
         raise RuntimeError(f"oracle_kda_recurrent failed with {st}")
     return o, sf
+
+
+def recurrent_ckpt(q, k, v, g, beta, every, initial_state=None, cu_seqlens=None, nthreads=None,
+                   want_o: bool = True):
+    """The fp64 token recurrence that also records each sequence's state after
+    every `every` tokens ([K3-notes §2.5, Fig. 12]: the state at a prefix's end
+    is what a request sharing that prefix resumes from).
+
+    Returns (o, S_final, ckpt [slots, H, dk, dv], cu_ckpt [N+1]) where sequence
+    n's j-th checkpoint (after its first j*every tokens) is slot cu_ckpt[n] + j - 1.
+    """
+    lib = _load()
+    T, H, dk, dv, N, cu, arrs = _prep(q, k, v, g, beta, cu_seqlens)
+    s0 = None if initial_state is None else _f64(initial_state)[0]
+    o = np.full((T, H, dv), np.nan) if want_o else None
+    sf = np.full((N, H, dk, dv), np.nan)
+    cu_ck = np.zeros(N + 1, dtype=np.int64)
+    cu_ck[1:] = np.cumsum(np.diff(cu) // int(every))
+    ck = np.full((max(int(cu_ck[-1]), 1), H, dk, dv), np.nan)
+    st = lib.oracle_kda_recurrent_ckpt(N, H, dk, dv, cu.ctypes.data_as(ctypes.c_void_p),
+                                       *[a[1] for a in arrs], _ptr(s0), _ptr(o), _ptr(sf), int(every),
+                                       cu_ck.ctypes.data_as(ctypes.c_void_p), _ptr(ck),
+                                       nthreads or default_threads())
+    if st != 0:
+        raise RuntimeError(f"oracle_kda_recurrent_ckpt failed with {st}")
+    return o, sf, ck[:int(cu_ck[-1])], cu_ck
 
 
 def chunked(q, k, v, g, beta, initial_state=None, cu_seqlens=None, chunk=64, subtile_ref=False,

@@ -25,6 +25,9 @@
  *        S' = Diag(gamma_C) S + (K o gamma_C / Gamma)^T V~.
  *  - [K3-notes §2.5, context-parallel affine pair]: a segment maps its entry
  *    state to S_out = S~_local + M_local S_in.
+ *  - [K3-notes §2.5, Fig. 12, prefix-cache resume]: the state after a prefix
+ *    is what a request sharing that prefix resumes from; the recurrence can
+ *    record it every `every` tokens (oracle_kda_recurrent_ckpt).
  *
  * Layouts (all row-major, token-major like the CUDA library's inputs):
  *   q, k, g : [T_total][H][dk] float32  (the exact values the GPU receives)
@@ -72,6 +75,9 @@ typedef struct {
   int mutation;
   int chunk;         /* chunk form only */
   int subtile_ref;   /* chunk form only */
+  int ckpt_every;    /* > 0: record the state every ckpt_every tokens */
+  const int64_t *cu_ckpt;
+  double *ckpt;
   int next;          /* work counter */
   int status;
 } job_t;
@@ -169,6 +175,11 @@ static void *recurrent_worker(void *arg) {
       kda_token(dk, dv, S, J->q + th * dk, J->k + th * dk, J->v + th * dv, J->g + th * dk,
                 (double)J->beta[th], obuf, work, J->mutation);
       if (J->o) memcpy(J->o + th * dv, obuf, sizeof(double) * (size_t)dv);
+      const int64_t done = t - J->cu[n] + 1;
+      if (J->ckpt && done % J->ckpt_every == 0) {
+        const int64_t slot = J->cu_ckpt[n] + done / J->ckpt_every - 1;
+        memcpy(J->ckpt + ((size_t)slot * H + h) * (size_t)dk * dv, S, sizeof(double) * (size_t)dk * dv);
+      }
     }
     if (J->s_final) memcpy(J->s_final + sidx, S, sizeof(double) * (size_t)dk * dv);
   }
@@ -224,6 +235,29 @@ int oracle_kda_recurrent(int N, int H, int dk, int dv, const int64_t *cu, const 
   J.s0 = s0; J.o = o; J.s_final = s_final;
   J.chains = chains; J.nchains = chains ? nchains : N * H;
   J.mutation = mutation;
+  return run_threads(&J, nthreads, recurrent_worker);
+}
+
+/* oracle_kda_recurrent over all chains that also records each sequence's
+ * state after every `every` tokens: after its first j*every tokens (j >= 1)
+ * into slot cu_ckpt[n] + j - 1 of ckpt [slots][H][dk][dv]; cu_ckpt[n+1] -
+ * cu_ckpt[n] must be floor(len_n / every). */
+int oracle_kda_recurrent_ckpt(int N, int H, int dk, int dv, const int64_t *cu, const float *q,
+                              const float *k, const float *v, const float *g, const float *beta,
+                              const double *s0, double *o, double *s_final, int every,
+                              const int64_t *cu_ckpt, double *ckpt, int nthreads) {
+  int st = check_common(N, H, dk, dv, cu);
+  if (st) return st;
+  if (every <= 0 || !cu_ckpt || !ckpt) return ORACLE_EINVAL;
+  for (int n = 0; n < N; ++n)
+    if (cu_ckpt[n + 1] - cu_ckpt[n] != (cu[n + 1] - cu[n]) / every) return ORACLE_EINVAL;
+  job_t J;
+  memset(&J, 0, sizeof(J));
+  J.N = N; J.H = H; J.dk = dk; J.dv = dv; J.cu = cu;
+  J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta;
+  J.s0 = s0; J.o = o; J.s_final = s_final;
+  J.nchains = N * H;
+  J.ckpt_every = every; J.cu_ckpt = cu_ckpt; J.ckpt = ckpt;
   return run_threads(&J, nthreads, recurrent_worker);
 }
 

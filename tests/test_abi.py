@@ -126,3 +126,19 @@ def test_segment_planner_sizes(lib):
     assert n.value == (3 * 4 - 2) * 2 * 128 * 128 * 4
     varlen_split = _desc(B=1, T=4096, H=2, dk=128, dv=128, num_seqs=2, segments=4)
     assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(varlen_split), ctypes.byref(n)) == -7
+
+
+def test_checkpoint_argument_errors(lib):
+    P = ctypes.c_void_p
+
+    def call(d, every, ckpt=FAKE * 7, cu=None, cu_ck=None):
+        return lib.kda_chunk_fwd_ckpt(ctypes.byref(d), P(FAKE), P(FAKE * 2), P(FAKE * 3), P(FAKE * 4),
+                                      P(FAKE * 5), None, P(cu) if cu else None, P(FAKE * 6), None, every,
+                                      P(cu_ck) if cu_ck else None, P(ckpt) if ckpt else None, None, 0, None)
+
+    assert call(_desc(), 64, ckpt=None) == -1                   # no checkpoint buffer
+    assert call(_desc(), 96) == -2                              # not a multiple of the chunk
+    assert call(_desc(), 0) == -2
+    assert call(_desc(num_seqs=2), 64, cu=FAKE * 9) == -1       # packed sequences need cu_ckpt
+    assert call(_desc(), 64, ckpt=FAKE * 6) == -8               # checkpoints alias out
+    assert call(_desc(), 64, ckpt=FAKE * 7 + 2) == -4           # misaligned

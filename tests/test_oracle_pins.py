@@ -393,3 +393,48 @@ def test_affine_pair_maps_any_entry_state():
     kk = k[5, h].astype(np.float64)
     want = (np.eye(dk) - float(beta[5, h]) * np.outer(kk, kk)) @ np.diag(np.exp(g[5, h].astype(np.float64)))
     assert np.max(np.abs(M0 - want)) <= 1e-14
+
+
+def test_checkpoints_are_prefix_final_states():
+    """[K3-notes §2.5, Fig. 12]: the state a request resumes from is the state
+    after the shared prefix.  Every recorded checkpoint must equal the final
+    state of the recurrence run on that prefix alone (an independent call of
+    the pinned token recurrence), and sequences shorter than the interval
+    record nothing."""
+    rng = np.random.default_rng(11)
+    lens = [130, 0, 64, 200, 63]
+    every, H, d = 64, 2, 16
+    T = sum(lens)
+    q = rng.standard_normal((T, H, d)).astype(np.float32)
+    k = (q / np.linalg.norm(q, axis=-1, keepdims=True)).astype(np.float32)
+    v = rng.standard_normal((T, H, d)).astype(np.float32)
+    g = rng.uniform(-0.7, -1e-3, (T, H, d)).astype(np.float32)
+    beta = rng.uniform(0, 1, (T, H)).astype(np.float32)
+    s0 = rng.standard_normal((len(lens), H, d, d)) * 0.1
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    _, _, ck, cuc = oracle.recurrent_ckpt(q, k, v, g, beta, every, initial_state=s0, cu_seqlens=cu)
+    assert list(np.diff(cuc)) == [n // every for n in lens]
+    for n, L in enumerate(lens):
+        for j in range(1, L // every + 1):
+            rows = slice(cu[n], cu[n] + j * every)
+            _, s_pre = oracle.recurrent(q[rows], k[rows], v[rows], g[rows], beta[rows],
+                                        initial_state=s0[n:n + 1])
+            np.testing.assert_allclose(ck[cuc[n] + j - 1], s_pre[0], rtol=0, atol=1e-12)
+
+
+def test_resume_from_checkpoint_matches_full_run():
+    """Resuming the recurrence from a checkpoint on the rest of the sequence
+    gives the full run's outputs and final state (prefix-cache reuse)."""
+    rng = np.random.default_rng(12)
+    T, H, d, every = 320, 2, 16, 64
+    q = rng.standard_normal((T, H, d)).astype(np.float32)
+    k = (q / np.linalg.norm(q, axis=-1, keepdims=True)).astype(np.float32)
+    v = rng.standard_normal((T, H, d)).astype(np.float32)
+    g = rng.uniform(-0.7, -1e-3, (T, H, d)).astype(np.float32)
+    beta = rng.uniform(0, 1, (T, H)).astype(np.float32)
+    o, sf, ck, _ = oracle.recurrent_ckpt(q, k, v, g, beta, every)
+    for j in (1, 3):
+        cut = j * every
+        o2, s2 = oracle.recurrent(q[cut:], k[cut:], v[cut:], g[cut:], beta[cut:], initial_state=ck[j - 1:j])
+        np.testing.assert_allclose(o2, o[cut:], rtol=0, atol=1e-10)
+        np.testing.assert_allclose(s2, sf, rtol=0, atol=1e-10)
