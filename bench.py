@@ -345,6 +345,9 @@ def run_gpu(args):
         if nsteps > 0:
             extra[key] = time_prefill_workload(kda, inputs, wl, nsteps, dev, stream, world, rank, hbm_peak)
 
+    if args.ckpt_steps > 0:
+        extra["checkpoints"] = time_checkpoints(kda, x, w, args.ckpt_steps, 512, ms_step, dev, stream, world)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -410,6 +413,38 @@ def time_prefill_workload(kda, inputs, w, steps, dev, stream, world, rank, hbm_p
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                         "frac": round(gbs / hbm_peak, 4), "algorithmic_bytes_per_step": int(alg)}}
     del x, out, sT
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_checkpoints(kda, x, w, steps, every, ms_headline, dev, stream, world):
+    """The headline batch through kda_chunk_fwd_ckpt, keeping the state every
+    `every` tokens (the prefix cache's 512-token hash block)."""
+    import torch
+    slots = w.B * (w.T // every)
+    ck = torch.empty(slots, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+    out = torch.empty(w.B * w.T, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    sT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+
+    def step():
+        kda.kda_chunk_fwd_ckpt(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], every, out=out,
+                               final_state=sT, ckpt=ck, B=w.B, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = reduce_max(ev0.elapsed_time(ev1) / steps, world, dev)
+    res = {"workload": w.name, "every": every, "slots": slots, "steps": steps, "ms_per_step": round(ms, 4),
+           "checkpoint_bytes_per_step": int(ck.numel() * 4),
+           "time_vs_headline": round(ms / ms_headline, 4)}
+    del ck, out, sT
     torch.cuda.empty_cache()
     return res
 
@@ -509,6 +544,8 @@ def main(argv=None):
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--long-steps", type=int, default=3, help="steps of the 2^20-token workload (0: skip)")
     ap.add_argument("--varlen-steps", type=int, default=5, help="steps of the 64-sequence varlen workload")
+    ap.add_argument("--ckpt-steps", type=int, default=100,
+                    help="steps of the headline batch with 512-token state checkpoints (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
