@@ -16,6 +16,10 @@ the GPU receives, so a bf16 input is passed as its exact float32 upcast):
                       formulas that the page leaves out (derivation in the C file).
 * ``decode_step``   - one token of the recurrence per sequence, state in place.
 * ``affine_pair``   - [K3-notes §2.5, context-parallel affine pair] (M, S~).
+* ``layer``, ``layer_decode_step`` - the recurrence inside the KDA layer's gates
+                      ([K3-notes §2.2, Eq. 5 and the KDA output equation]): the
+                      log-decay g_min Sigmoid(exp(A_h) z) from decay logits z, and
+                      the output Sigmoid(gate) o RMSNorm(o~) per token and head.
 
 Pins that tie these functions to the pages and to mathematics other than
 themselves live in ``tests/test_oracle_pins.py``; every function here is pinned.
@@ -44,6 +48,17 @@ MUTATIONS = {
     "beta_only_on_write": 6,
     "decay_by_column": 7,
     "beta_squared": 8,
+}
+
+# Planted mistakes in the layer gates (``layer`` only).
+GATE_MUTATIONS = {
+    "gate_neg_logit": 9,
+    "gate_no_exp": 10,
+    "gate_head0": 11,
+    "norm_sum": 12,
+    "norm_eps_outside": 13,
+    "ogate_neg": 14,
+    "norm_w_reversed": 15,
 }
 
 
@@ -77,6 +92,11 @@ def _load():
     lib.oracle_kda_decode_step.restype = I
     lib.oracle_kda_affine_pair.argtypes = [I, I, I, I, L, L, P, P, P, P, P, P]
     lib.oracle_kda_affine_pair.restype = I
+    D = ctypes.c_double
+    lib.oracle_kda_layer.argtypes = [I, I, I, I, P, P, P, P, P, P, D, P, P, P, D, P, P, P, I, I]
+    lib.oracle_kda_layer.restype = I
+    lib.oracle_kda_layer_decode_step.argtypes = [I, I, I, I, P, P, P, P, P, D, P, P, P, D, P, P, I]
+    lib.oracle_kda_layer_decode_step.restype = I
     lib.oracle_kda_recurrent_ckpt.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, P, I]
     lib.oracle_kda_recurrent_ckpt.restype = I
     _lib = lib
@@ -225,3 +245,57 @@ def affine_pair(k, v, g, beta, h, t0, t1):
     if st != 0:
         raise RuntimeError(f"oracle_kda_affine_pair failed with {st}")
     return M, St
+
+
+def layer(q, k, v, z, beta, A_log, g_min=-5.0, out_gate=None, norm_weight=None, norm_eps=1e-6,
+          initial_state=None, cu_seqlens=None, nthreads=None, mutation: int = 0):
+    """The KDA recurrence inside the layer's gates, in fp64.
+
+    z: [T_total, H, dk] decay logits, A_log: [H]; the log-decay is
+    g_min * Sigmoid(exp(A_log[h]) * z) ([K3-notes §2.2, Eq. 5]).  out_gate:
+    [T_total, H, dv] output gate logits (W_g x) or None; when given, each output
+    row becomes Sigmoid(out_gate) * o / sqrt(mean(o^2) + norm_eps) * norm_weight
+    ([K3-notes §2.2, KDA output]); norm_weight [dv] or None (ones).  Other
+    arguments and the returns (o, S_final) as ``recurrent``.
+    """
+    lib = _load()
+    T, H, dk, dv, N, cu, arrs = _prep(q, k, v, z, beta, cu_seqlens)
+    A, pA = _f32(np.asarray(A_log).reshape(-1))
+    if A.shape[0] != H:
+        raise ValueError("A_log must have H entries")
+    og = None if out_gate is None else _f32(out_gate)
+    w = None if norm_weight is None else _f32(np.asarray(norm_weight).reshape(-1))
+    s0 = None if initial_state is None else _f64(initial_state)[0]
+    o = np.full((T, H, dv), np.nan)
+    sf = np.full((N, H, dk, dv), np.nan)
+    st = lib.oracle_kda_layer(N, H, dk, dv, cu.ctypes.data_as(ctypes.c_void_p), arrs[0][1], arrs[1][1],
+                              arrs[2][1], arrs[3][1], pA, float(g_min), arrs[4][1],
+                              None if og is None else og[1], None if w is None else w[1], float(norm_eps),
+                              _ptr(s0), _ptr(o), _ptr(sf), nthreads or default_threads(), int(mutation))
+    if st != 0:
+        raise RuntimeError(f"oracle_kda_layer failed with {st}")
+    return o, sf
+
+
+def layer_decode_step(q, k, v, z, beta, state, A_log, g_min=-5.0, out_gate=None, norm_weight=None,
+                      norm_eps=1e-6, nthreads=None):
+    """One decode step of ``layer``: q, k, z [N,H,dk], v [N,H,dv], beta [N,H],
+    out_gate [N,H,dv] or None, state [N,H,dk,dv].  Returns (o, new_state); the
+    input state is not modified."""
+    lib = _load()
+    q, k, v, z = (np.asarray(x) for x in (q, k, v, z))
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    arrs = [_f32(x) for x in (q, k, v, z, beta)]
+    A, pA = _f32(np.asarray(A_log).reshape(-1))
+    og = None if out_gate is None else _f32(out_gate)
+    w = None if norm_weight is None else _f32(np.asarray(norm_weight).reshape(-1))
+    S = np.array(state, dtype=np.float64, copy=True, order="C")
+    o = np.full((N, H, dv), np.nan)
+    st = lib.oracle_kda_layer_decode_step(N, H, dk, dv, arrs[0][1], arrs[1][1], arrs[2][1], arrs[3][1], pA,
+                                          float(g_min), arrs[4][1], None if og is None else og[1],
+                                          None if w is None else w[1], float(norm_eps), _ptr(S), _ptr(o),
+                                          nthreads or default_threads())
+    if st != 0:
+        raise RuntimeError(f"oracle_kda_layer_decode_step failed with {st}")
+    return o, S

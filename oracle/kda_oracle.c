@@ -28,6 +28,15 @@
  *  - [K3-notes §2.5, Fig. 12, prefix-cache resume]: the state after a prefix
  *    is what a request sharing that prefix resumes from; the recurrence can
  *    record it every `every` tokens (oracle_kda_recurrent_ckpt).
+ *  - [K3-notes §2.2, Eq. 5 and the KDA output equation], the layer's gates
+ *    around the recurrence (oracle_kda_layer, oracle_kda_layer_decode_step):
+ *        g_t = g_min Sigmoid(exp(A_h) z_t)          (per channel; z the decay logits)
+ *        y_t = Sigmoid(gate_t) o RMSNorm(o~_t)      (per token and head, over dv)
+ *    with RMSNorm(x) = x / sqrt(mean_j x_j^2 + eps) o w.  The page gives no eps
+ *    or weight; the plainest reading is the usual RMSNorm with a learned
+ *    per-channel weight w [dv] (shared by the heads) and a small eps, both
+ *    passed in.  y_t is what W_o then projects; W_o and W_g x_t are plain
+ *    projections outside the recurrence (gate_t = W_g x_t is an input here).
  *
  * Layouts (all row-major, token-major like the CUDA library's inputs):
  *   q, k, g : [T_total][H][dk] float32  (the exact values the GPU receives)
@@ -60,7 +69,15 @@ enum {
   MUT_BETA_ONLY_ON_WRITE = 6,/* erase term without beta: u = beta v - x           */
   MUT_DECAY_BY_COLUMN = 7,   /* Diag(alpha) applied to dv index (needs dk == dv)  */
   MUT_BETA_SQUARED = 8,      /* u = beta^2 (v - x)                                */
-  MUT_COUNT = 9
+  /* layer gates (oracle_kda_layer only) */
+  MUT_GATE_NEG_LOGIT = 9,    /* g = g_min Sigmoid(-exp(A) z)                      */
+  MUT_GATE_NO_EXP = 10,      /* g = g_min Sigmoid(A z)                            */
+  MUT_GATE_HEAD0 = 11,       /* every head uses A_0                               */
+  MUT_NORM_SUM = 12,         /* RMS over the sum of squares, not the mean         */
+  MUT_NORM_EPS_OUTSIDE = 13, /* 1 / (sqrt(mean x^2) + eps)                        */
+  MUT_OGATE_NEG = 14,        /* Sigmoid(-gate)                                    */
+  MUT_NORM_W_REVERSED = 15,  /* weight indexed dv-1-j                             */
+  MUT_COUNT = 16
 };
 
 typedef struct {
@@ -78,6 +95,13 @@ typedef struct {
   int ckpt_every;    /* > 0: record the state every ckpt_every tokens */
   const int64_t *cu_ckpt;
   double *ckpt;
+  /* layer gates (nullable z / ogate): see the header */
+  const float *z;      /* [T][H][dk] decay logits; g is then ignored */
+  const float *A_log;  /* [H] */
+  double g_min;
+  const float *ogate;  /* [T][H][dv] output gate logits */
+  const float *norm_w; /* [dv], NULL: ones */
+  double norm_eps;
   int next;          /* work counter */
   int status;
 } job_t;
@@ -93,7 +117,7 @@ typedef struct {
  * The middle three lines expand (I - beta k k^T) Diag(alpha) S + beta k v^T.
  * work: dk + dv doubles of scratch. */
 static void kda_token(int dk, int dv, double *S, const float *q, const float *k,
-                      const float *v, const float *g, double beta, double *o,
+                      const float *v, const double *g, double beta, double *o,
                       double *work, int mutation) {
   double *x = work;       /* dv */
   double *u = work + dv;  /* dv */
@@ -108,7 +132,7 @@ static void kda_token(int dk, int dv, double *S, const float *q, const float *k,
   if (mutation != MUT_NO_DECAY) {
     for (int i = 0; i < dk; ++i) {
       for (int j = 0; j < dv; ++j) {
-        double a = exp((double)g[mutation == MUT_DECAY_BY_COLUMN ? j : i]);
+        double a = exp(g[mutation == MUT_DECAY_BY_COLUMN ? j : i]);
         S[(size_t)i * dv + j] *= a;
       }
     }
@@ -149,6 +173,30 @@ static void kda_token(int dk, int dv, double *S, const float *q, const float *k,
   }
 }
 
+/* [K3-notes §2.2, Eq. 5]: the log-decay of one token's dk channels from its
+ * decay logits, g_i = g_min Sigmoid(exp(A_h) z_i), Sigmoid(x) = 1 / (1 + e^-x). */
+static void decay_from_logits(int dk, const float *z, double A_log, double g_min, double *g,
+                              int mutation) {
+  const double scale = mutation == MUT_GATE_NO_EXP ? A_log : exp(A_log);
+  const double sgn = mutation == MUT_GATE_NEG_LOGIT ? -1.0 : 1.0;
+  for (int i = 0; i < dk; ++i) g[i] = g_min / (1.0 + exp(-sgn * scale * (double)z[i]));
+}
+
+/* [K3-notes §2.2, KDA output]: o <- Sigmoid(gate) o RMSNorm(o) over the dv
+ * channels of one token and head, RMSNorm(x)_j = x_j w_j / sqrt(mean x^2 + eps). */
+static void output_norm_gate(int dv, double *o, const float *gate, const float *w, double eps,
+                             int mutation) {
+  double ms = 0.0;
+  for (int j = 0; j < dv; ++j) ms += o[j] * o[j];
+  if (mutation != MUT_NORM_SUM) ms /= (double)dv;
+  const double r = mutation == MUT_NORM_EPS_OUTSIDE ? 1.0 / (sqrt(ms) + eps) : 1.0 / sqrt(ms + eps);
+  const double sgn = mutation == MUT_OGATE_NEG ? -1.0 : 1.0;
+  for (int j = 0; j < dv; ++j) {
+    const double wj = w ? (double)w[mutation == MUT_NORM_W_REVERSED ? dv - 1 - j : j] : 1.0;
+    o[j] = o[j] * r * wj / (1.0 + exp(-sgn * (double)gate[j]));
+  }
+}
+
 static int next_chain(job_t *J) { return __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED); }
 
 static void *recurrent_worker(void *arg) {
@@ -157,9 +205,10 @@ static void *recurrent_worker(void *arg) {
   double *S = (double *)malloc(sizeof(double) * (size_t)dk * dv);
   double *work = (double *)malloc(sizeof(double) * (size_t)(2 * dv));
   double *obuf = (double *)malloc(sizeof(double) * (size_t)dv);
-  if (!S || !work || !obuf) {
+  double *grow = (double *)malloc(sizeof(double) * (size_t)dk);
+  if (!S || !work || !obuf || !grow) {
     J->status = ORACLE_ENOMEM;
-    free(S); free(work); free(obuf);
+    free(S); free(work); free(obuf); free(grow);
     return NULL;
   }
   for (;;) {
@@ -172,8 +221,15 @@ static void *recurrent_worker(void *arg) {
     else memset(S, 0, sizeof(double) * (size_t)dk * dv);
     for (int64_t t = J->cu[n]; t < J->cu[n + 1]; ++t) {
       size_t th = (size_t)t * H + h;
-      kda_token(dk, dv, S, J->q + th * dk, J->k + th * dk, J->v + th * dv, J->g + th * dk,
+      if (J->z) {
+        decay_from_logits(dk, J->z + th * dk, (double)J->A_log[J->mutation == MUT_GATE_HEAD0 ? 0 : h],
+                          J->g_min, grow, J->mutation);
+      } else {
+        for (int i = 0; i < dk; ++i) grow[i] = (double)J->g[th * dk + i];
+      }
+      kda_token(dk, dv, S, J->q + th * dk, J->k + th * dk, J->v + th * dv, grow,
                 (double)J->beta[th], obuf, work, J->mutation);
+      if (J->ogate) output_norm_gate(dv, obuf, J->ogate + th * dv, J->norm_w, J->norm_eps, J->mutation);
       if (J->o) memcpy(J->o + th * dv, obuf, sizeof(double) * (size_t)dv);
       const int64_t done = t - J->cu[n] + 1;
       if (J->ckpt && done % J->ckpt_every == 0) {
@@ -183,7 +239,7 @@ static void *recurrent_worker(void *arg) {
     }
     if (J->s_final) memcpy(J->s_final + sidx, S, sizeof(double) * (size_t)dk * dv);
   }
-  free(S); free(work); free(obuf);
+  free(S); free(work); free(obuf); free(grow);
   return NULL;
 }
 
@@ -227,7 +283,7 @@ int oracle_kda_recurrent(int N, int H, int dk, int dv, const int64_t *cu, const 
   if (st) return st;
   if ((mutation == MUT_READ_TRANSPOSED || mutation == MUT_DECAY_BY_COLUMN) && dk != dv)
     return ORACLE_EINVAL;
-  if (mutation < 0 || mutation >= MUT_COUNT) return ORACLE_EINVAL;
+  if (mutation < 0 || mutation >= MUT_GATE_NEG_LOGIT) return ORACLE_EINVAL;
   job_t J;
   memset(&J, 0, sizeof(J));
   J.N = N; J.H = H; J.dk = dk; J.dv = dv; J.cu = cu;
@@ -259,6 +315,47 @@ int oracle_kda_recurrent_ckpt(int N, int H, int dk, int dv, const int64_t *cu, c
   J.nchains = N * H;
   J.ckpt_every = every; J.cu_ckpt = cu_ckpt; J.ckpt = ckpt;
   return run_threads(&J, nthreads, recurrent_worker);
+}
+
+/* The KDA layer around the recurrence ([K3-notes §2.2]): the log-decay comes
+ * from the decay logits z (Eq. 5) and, when ogate is given, each output row
+ * goes through the per-head RMSNorm and the sigmoid output gate.  All chains;
+ * arguments otherwise as oracle_kda_recurrent. */
+int oracle_kda_layer(int N, int H, int dk, int dv, const int64_t *cu, const float *q, const float *k,
+                     const float *v, const float *z, const float *A_log, double g_min, const float *beta,
+                     const float *ogate, const float *norm_w, double norm_eps, const double *s0,
+                     double *o, double *s_final, int nthreads, int mutation) {
+  int st = check_common(N, H, dk, dv, cu);
+  if (st) return st;
+  if (!z || !A_log || (ogate && !(norm_eps >= 0.0))) return ORACLE_EINVAL;
+  if (mutation != MUT_NONE && mutation < MUT_GATE_NEG_LOGIT) return ORACLE_EINVAL;
+  if (mutation < 0 || mutation >= MUT_COUNT) return ORACLE_EINVAL;
+  job_t J;
+  memset(&J, 0, sizeof(J));
+  J.N = N; J.H = H; J.dk = dk; J.dv = dv; J.cu = cu;
+  J.q = q; J.k = k; J.v = v; J.g = NULL; J.beta = beta;
+  J.z = z; J.A_log = A_log; J.g_min = g_min;
+  J.ogate = ogate; J.norm_w = norm_w; J.norm_eps = norm_eps;
+  J.s0 = s0; J.o = o; J.s_final = s_final;
+  J.nchains = N * H;
+  J.mutation = mutation;
+  return run_threads(&J, nthreads, recurrent_worker);
+}
+
+/* One decode step of the layer (oracle_kda_layer with every sequence one
+ * token long); state [N][H][dk][dv] updated in place. */
+int oracle_kda_layer_decode_step(int N, int H, int dk, int dv, const float *q, const float *k,
+                                 const float *v, const float *z, const float *A_log, double g_min,
+                                 const float *beta, const float *ogate, const float *norm_w,
+                                 double norm_eps, double *state, double *o, int nthreads) {
+  if (N <= 0) return ORACLE_EINVAL;
+  int64_t *cu = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N + 1));
+  if (!cu) return ORACLE_ENOMEM;
+  for (int n = 0; n <= N; ++n) cu[n] = n;
+  int st = oracle_kda_layer(N, H, dk, dv, cu, q, k, v, z, A_log, g_min, beta, ogate, norm_w, norm_eps,
+                            state, o, state, nthreads, MUT_NONE);
+  free(cu);
+  return st;
 }
 
 /* One decode step for N independent sequences: each (n, h) consumes one token
