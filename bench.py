@@ -347,6 +347,9 @@ def run_gpu(args):
 
     if args.ckpt_steps > 0:
         extra["checkpoints"] = time_checkpoints(kda, x, w, args.ckpt_steps, 512, ms_step, dev, stream, world)
+    if args.layer_steps > 0:
+        extra["layer_form"] = time_layer(kda, inputs, x, w, args.layer_steps, ms_step, dev, stream, world, rank,
+                                         hbm_peak)
 
     if rank == 0:
         line = {
@@ -449,6 +452,62 @@ def time_checkpoints(kda, x, w, steps, every, ms_headline, dev, stream, world):
     return res
 
 
+def time_layer(kda, inputs, x, w, steps, ms_headline, dev, stream, world, rank, hbm_peak):
+    """The headline batch in the layer form (kda_layer_fwd): log-decay from
+    bf16 decay logits inside the kernel, output RMSNorm and sigmoid gate in its
+    epilogue.  Beside it, the same layer unfused: torch forms the fp32
+    log-decay, kda_chunk_fwd runs, torch applies the norm and the gate."""
+    import torch
+    gt = inputs.make_layer_gates(w.B * w.T, w.H, w.dk, w.dv, w.qkv_dtype, device=dev,
+                                 seed=inputs.SEED_BASE + 100 + 1000 * rank)
+    out = torch.empty(w.B * w.T, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    sT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+
+    def fused():
+        kda.kda_layer_fwd(x["q"], x["k"], x["v"], gt["z"], x["beta"], gt["A_log"], -5.0, out_gate=gt["out_gate"],
+                          norm_weight=gt["norm_weight"], norm_eps=1e-6, out=out, final_state=sT, B=w.B,
+                          stream=stream)
+
+    def unfused():
+        g = -5.0 * torch.sigmoid(torch.exp(gt["A_log"])[None, :, None] * gt["z"].float())
+        o, _ = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], g, x["beta"], None, None, out, sT, B=w.B, stream=stream)
+        of = o.float()
+        y = of * torch.rsqrt(of.pow(2).mean(-1, keepdim=True) + 1e-6) * gt["norm_weight"]
+        return (y * torch.sigmoid(gt["out_gate"].float())).to(torch.bfloat16)
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(n):
+                fn()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return reduce_max(ev0.elapsed_time(ev1) / n, world, dev)
+
+    ms = timed(fused, steps)
+    ms_unfused = timed(unfused, max(steps // 5, 3))
+    tok = w.B * w.T
+    # per (token, head): q, k, v, z, out_gate and out in bf16, beta fp32
+    alg = tok * w.H * ((2 * w.dk + w.dv) * 2 + w.dk * 2 + 4 + w.dv * 2 + w.dv * 2) + w.B * w.H * w.dk * w.dv * 4
+    gbs = alg / (ms * 1e-3) / 1e9
+    res = {"workload": w.name, "api": "kda_layer_fwd (decay logits bf16, out_gate bf16, RMSNorm weight fp32)",
+           "steps": steps, "ms_per_step": round(ms, 4), "tokens_per_s": round(world * tok / (ms * 1e-3), 1),
+           "time_vs_headline": round(ms / ms_headline, 4),
+           "unfused_ms_per_step": round(ms_unfused, 4),
+           "unfused": "torch log-decay + kda_chunk_fwd + torch RMSNorm/gate",
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                        "frac": round(gbs / hbm_peak, 4), "algorithmic_bytes_per_step": int(alg)}}
+    del gt, out, sT
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------- oracle on the host
 
 def cpu_baseline(w, x, seconds=12.0):
@@ -544,6 +603,8 @@ def main(argv=None):
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--long-steps", type=int, default=3, help="steps of the 2^20-token workload (0: skip)")
     ap.add_argument("--varlen-steps", type=int, default=5, help="steps of the 64-sequence varlen workload")
+    ap.add_argument("--layer-steps", type=int, default=100,
+                    help="steps of the headline batch in the layer form (0: skip)")
     ap.add_argument("--ckpt-steps", type=int, default=100,
                     help="steps of the headline batch with 512-token state checkpoints (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

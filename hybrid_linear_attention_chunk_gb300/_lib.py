@@ -39,6 +39,11 @@ class KdaDecodeDesc(ctypes.Structure):
                 ("gate_dtype", ctypes.c_int), ("validate", ctypes.c_int)]
 
 
+class KdaLayerGates(ctypes.Structure):
+    _fields_ = [("A_log", ctypes.c_void_p), ("g_min", ctypes.c_float), ("out_gate", ctypes.c_void_p),
+                ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float)]
+
+
 class KdaError(RuntimeError):
     def __init__(self, status: int, fn: str, detail: str = ""):
         self.status = status
@@ -78,6 +83,12 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_fwd_ckpt.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [ctypes.POINTER(KdaDecodeDesc), P, P, P, P, P, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_layer_fwd.argtypes = [ctypes.POINTER(KdaChunkDesc), ctypes.POINTER(KdaLayerGates), P, P, P, P, P,
+                                      P, P, P, P, P, ctypes.c_size_t, P]
+        lib.kda_layer_fwd.restype = ctypes.c_int
+        lib.kda_layer_decode_step.argtypes = [ctypes.POINTER(KdaDecodeDesc), ctypes.POINTER(KdaLayerGates), P, P,
+                                              P, P, P, P, P, P]
+        lib.kda_layer_decode_step.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_last_cuda_error.argtypes = []
@@ -256,4 +267,70 @@ def kda_decode_step(q, k, v, log_alpha, beta, state_inout, out=None, *, validate
     st = lib.kda_decode_step(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                              _ptr(state_inout), _ptr(out), _stream_handle(stream, q.device))
     _check(st, "kda_decode_step")
+    return out
+
+
+def layer_gates(A_log, g_min=-5.0, out_gate=None, norm_weight=None, norm_eps=1e-6) -> KdaLayerGates:
+    """The kda_layer_gates struct for the given device tensors."""
+    lg = KdaLayerGates()
+    lg.A_log = None if A_log is None else A_log.data_ptr()
+    lg.g_min = float(g_min)
+    lg.out_gate = None if out_gate is None else _ptr(out_gate).value
+    lg.norm_weight = None if norm_weight is None else _ptr(norm_weight).value
+    lg.norm_eps = float(norm_eps)
+    return lg
+
+
+def kda_layer_fwd(q, k, v, z, beta, A_log, g_min=-5.0, out_gate=None, norm_weight=None, norm_eps=1e-6,
+                  initial_state=None, cu_seqlens=None, out=None, final_state=None, *, chunk=64, kernel="auto",
+                  segments=0, validate=False, out_dtype=None, want_final_state=True, B=None, stream=None,
+                  workspace=None):
+    """KDA prefill inside the layer's gates through the C ABI: the log-decay is
+    g_min * sigmoid(exp(A_log[h]) * z) (z: [.., H, dk] decay logits in q's
+    dtype; A_log: [H] fp32) and, with out_gate ([.., H, dv], q's dtype), the
+    output is sigmoid(out_gate) * RMSNorm(o) with norm_weight [dv] fp32 (None:
+    ones) and norm_eps.  beta: fp32 or bf16.  Returns (out, final_state)."""
+    lib = load()
+    dev = q.device
+    if z.dtype != q.dtype:
+        raise TypeError("z must have q's dtype")
+    if out_gate is not None and out_gate.dtype != q.dtype:
+        raise TypeError("out_gate must have q's dtype")
+    d = chunk_desc(q, v, chunk=chunk, cu_seqlens=cu_seqlens, out_dtype=out_dtype or q.dtype,
+                   gate_dtype=_dt(beta), validate=validate, kernel=kernel, segments=segments, B=B)
+    Nseq = d.num_seqs if cu_seqlens is not None else d.B
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (d.dv,), dtype=out_dtype or q.dtype, device=dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(Nseq, d.H, d.dk, d.dv, dtype=torch.float32, device=dev)
+    lg = layer_gates(A_log, g_min, out_gate, norm_weight, norm_eps)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_layer_fwd(ctypes.byref(d), ctypes.byref(lg), _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta),
+                           _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                           _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+    _check(st, "kda_layer_fwd")
+    return out, final_state
+
+
+def kda_layer_decode_step(q, k, v, z, beta, state_inout, A_log, g_min=-5.0, out_gate=None, norm_weight=None,
+                          norm_eps=1e-6, out=None, *, validate=False, out_dtype=None, stream=None):
+    """One decode step inside the layer's gates (see kda_layer_fwd): q, k, z
+    [N,H,dk], v and out_gate [N,H,dv], beta [N,H], state_inout [N,H,dk,dv] fp32
+    updated in place.  Returns out."""
+    lib = load()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    d = KdaDecodeDesc()
+    d.N, d.H, d.dk, d.dv = N, H, dk, dv
+    d.qkv_dtype = _dt(q)
+    od = out_dtype or q.dtype
+    d.out_dtype = _dt(torch.empty(0, dtype=od))
+    d.gate_dtype = _dt(beta)
+    d.validate = int(bool(validate))
+    if out is None:
+        out = torch.empty(N, H, dv, dtype=od, device=q.device)
+    lg = layer_gates(A_log, g_min, out_gate, norm_weight, norm_eps)
+    st = lib.kda_layer_decode_step(ctypes.byref(d), ctypes.byref(lg), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
+                                   _ptr(beta), _ptr(state_inout), _ptr(out), _stream_handle(stream, q.device))
+    _check(st, "kda_layer_decode_step")
     return out

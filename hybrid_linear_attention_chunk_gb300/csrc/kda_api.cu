@@ -40,15 +40,27 @@ bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.l
 
 // --------------------------------------------------------------- validation
 
+// The log-decay must lie in [g_min = -5, 0]; decay logits (layer form) may be
+// any number but NaN, and A_h must be finite.
+template <class Args>
+__device__ int check_decay(const Args &a, size_t nk, size_t stride) {
+  int bad = 0;
+  const kda_dtype gdt = a.gdt();
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nk; i += stride) {
+    const float g = ld_elem(a.g, i, gdt);
+    if (a.A_log ? isnan(g) : !(g >= kLogDecayFloor && g <= 0.f)) bad |= 1;
+  }
+  if (a.A_log && blockIdx.x == 2)
+    for (int h = threadIdx.x; h < a.H; h += blockDim.x)
+      if (!isfinite(a.A_log[h])) bad |= 16;
+  return bad;
+}
+
 __global__ void validate_prefill_kernel(PrefillArgs a, int *flag) {
   const size_t nk = (size_t)a.T_total * a.H * a.dk;
   const size_t nb = (size_t)a.T_total * a.H;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  int bad = 0;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nk; i += stride) {
-    float g = ld_elem(a.g, i, a.gate);
-    if (!(g >= kLogDecayFloor && g <= 0.f)) bad |= 1;
-  }
+  int bad = check_decay(a, nk, stride);
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nb; i += stride) {
     float b = ld_elem(a.beta, i, a.gate);
     if (!(b >= 0.f && b <= 1.f)) bad |= 2;
@@ -78,11 +90,7 @@ __global__ void validate_decode_kernel(DecodeArgs a, int *flag) {
   const size_t nk = (size_t)a.N * a.H * a.dk;
   const size_t nb = (size_t)a.N * a.H;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  int bad = 0;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nk; i += stride) {
-    float g = ld_elem(a.g, i, a.gate);
-    if (!(g >= kLogDecayFloor && g <= 0.f)) bad |= 1;
-  }
+  int bad = check_decay(a, nk, stride);
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nb; i += stride) {
     float b = ld_elem(a.beta, i, a.gate);
     if (!(b >= 0.f && b <= 1.f)) bad |= 2;
@@ -107,9 +115,27 @@ kda_status run_validation(cudaStream_t s, Launch launch) {
   return h_flag ? KDA_ERR_RANGE : KDA_OK;
 }
 
+// Host checks of the layer gates shared by the prefill and decode entries.
+kda_status check_gates(const kda_layer_gates *lg) {
+  if (!lg || !lg->A_log) return KDA_ERR_NULL;
+  if (!(lg->g_min >= kLogDecayFloor && lg->g_min < 0.f)) return KDA_ERR_RANGE;
+  if (lg->out_gate && !(lg->norm_eps >= 0.f)) return KDA_ERR_RANGE;
+  if (lg->out_gate && !aligned16(lg->out_gate)) return KDA_ERR_ALIGN;
+  if (!aligned_to(lg->A_log, 4) || (lg->norm_weight && !aligned_to(lg->norm_weight, 4))) return KDA_ERR_ALIGN;
+  return KDA_OK;
+}
+
+// Spans of the gate tensors: out_gate [rows, H, dv] in qkv dtype, A_log [H],
+// norm_weight [dv].
+void gate_spans(const kda_layer_gates *lg, size_t rows, int H, int dv, kda_dtype qkv, Range r[3]) {
+  r[0] = span(lg->out_gate, lg->out_gate ? rows * H * dv * esize(qkv) : 0);
+  r[1] = span(lg->A_log, (size_t)H * 4);
+  r[2] = span(lg->norm_weight, lg->norm_weight ? (size_t)dv * 4 : 0);
+}
+
 kda_status check_prefill(const kda_chunk_desc *d, const void *q, const void *k, const void *v,
                          const void *g, const void *beta, const float *s0, const int32_t *cu,
-                         void *out, float *sT, PrefillArgs *a) {
+                         void *out, float *sT, PrefillArgs *a, const kda_layer_gates *lg = nullptr) {
   if (!d || !q || !k || !v || !g || !beta || !out) return KDA_ERR_NULL;
   if (!dtype_ok(d->qkv_dtype) || !dtype_ok(d->out_dtype) || !dtype_ok(d->gate_dtype))
     return KDA_ERR_DTYPE;
@@ -133,9 +159,19 @@ kda_status check_prefill(const kda_chunk_desc *d, const void *q, const void *k, 
     if (p && !aligned_to(p, 4)) return KDA_ERR_ALIGN;
   const int Nseq = cu ? d->num_seqs : d->B;
   const size_t th = (size_t)T_total * d->H;
+  const kda_dtype gdt = lg ? d->qkv_dtype : d->gate_dtype;  // decay logits or log-decay
   Range r_out = span(out, th * d->dv * esize(d->out_dtype));
+  if (lg) {
+    kda_status st = check_gates(lg);
+    if (st != KDA_OK) return st;
+    Range rg[3];
+    gate_spans(lg, (size_t)T_total, d->H, d->dv, d->qkv_dtype, rg);
+    const Range r_sT = span(sT, sT ? (size_t)Nseq * d->H * d->dk * d->dv * 4 : 0);
+    for (const Range &r : rg)
+      if (overlap(r_out, r) || overlap(r_sT, r)) return KDA_ERR_ALIAS;
+  }
   Range ins[] = {span(q, th * d->dk * esize(d->qkv_dtype)), span(k, th * d->dk * esize(d->qkv_dtype)),
-                 span(v, th * d->dv * esize(d->qkv_dtype)), span(g, th * d->dk * esize(d->gate_dtype)),
+                 span(v, th * d->dv * esize(d->qkv_dtype)), span(g, th * d->dk * esize(gdt)),
                  span(beta, th * esize(d->gate_dtype)),
                  span(s0, s0 ? (size_t)Nseq * d->H * d->dk * d->dv * 4 : 0),
                  span(cu, cu ? (size_t)(Nseq + 1) * 4 : 0),
@@ -160,6 +196,13 @@ kda_status check_prefill(const kda_chunk_desc *d, const void *q, const void *k, 
   a->gate = d->gate_dtype;
   a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta;
   a->s0 = s0; a->cu = cu; a->o = out; a->sT = sT;
+  if (lg) {
+    a->A_log = lg->A_log;
+    a->g_min = lg->g_min;
+    a->og = lg->out_gate;
+    a->nw = lg->norm_weight;
+    a->eps = lg->norm_eps;
+  }
   return KDA_OK;
 }
 
@@ -184,6 +227,8 @@ kda_status run_prefill(const kda_chunk_desc *d, const PrefillArgs &a, cudaStream
   cudaError_t e;
   if (pl.P <= 1) {
     e = use_tc ? launch_chunk_tc(a, s) : launch_chunk_simt(a, s);
+    // the CUDA-core kernel leaves the output norm and gate to a row pass
+    if (e == cudaSuccess && !use_tc && a.og) e = launch_norm_gate(a, s);
   } else if (ws_mode == 1) {
     e = launch_chunk_tc_segmented(a, pl, ws, s);
   } else {
@@ -215,6 +260,61 @@ kda_status args_from_desc(const kda_chunk_desc *d, PrefillArgs *a) {
   a->s0 = nullptr; a->o = nullptr; a->sT = nullptr;
   static const int32_t dummy = 0;
   a->cu = varlen ? &dummy : nullptr;  // only its presence matters to the planner
+  return KDA_OK;
+}
+
+kda_status run_decode(const kda_decode_desc *d, const kda_layer_gates *lg, const void *q, const void *k,
+                      const void *v, const void *log_alpha, const void *beta, float *state_inout, void *out,
+                      kda_stream_t stream) {
+  if (!d || !q || !k || !v || !log_alpha || !beta || !state_inout || !out) return KDA_ERR_NULL;
+  if (!dtype_ok(d->qkv_dtype) || !dtype_ok(d->out_dtype) || !dtype_ok(d->gate_dtype))
+    return KDA_ERR_DTYPE;
+  if (d->N <= 0 || d->H <= 0 || !dim_ok(d->dk) || !dim_ok(d->dv)) return KDA_ERR_SHAPE;
+  if ((long long)d->N * d->H >= (1LL << 31)) return KDA_ERR_SHAPE;
+  // the state is streamed as 16-byte vectors; the rest needs element alignment
+  if (!aligned16(state_inout)) return KDA_ERR_ALIGN;
+  if (!aligned_to(q, esize(d->qkv_dtype)) || !aligned_to(k, esize(d->qkv_dtype)) ||
+      !aligned_to(v, esize(d->qkv_dtype)) || !aligned_to(out, esize(d->out_dtype)) ||
+      !aligned_to(log_alpha, esize(lg ? d->qkv_dtype : d->gate_dtype)) || !aligned_to(beta, esize(d->gate_dtype)))
+    return KDA_ERR_ALIGN;
+  const size_t nh = (size_t)d->N * d->H;
+  Range r_s = span(state_inout, nh * d->dk * d->dv * 4);
+  Range r_o = span(out, nh * d->dv * esize(d->out_dtype));
+  Range ins[] = {span(q, nh * d->dk * esize(d->qkv_dtype)), span(k, nh * d->dk * esize(d->qkv_dtype)),
+                 span(v, nh * d->dv * esize(d->qkv_dtype)),
+                 span(log_alpha, nh * d->dk * esize(lg ? d->qkv_dtype : d->gate_dtype)),
+                 span(beta, nh * esize(d->gate_dtype))};
+  if (overlap(r_s, r_o)) return KDA_ERR_ALIAS;
+  for (const Range &r : ins)
+    if (overlap(r_s, r) || overlap(r_o, r)) return KDA_ERR_ALIAS;
+  if (lg) {
+    kda_status st = check_gates(lg);
+    if (st != KDA_OK) return st;
+    if (lg->out_gate && !aligned_to(lg->out_gate, esize(d->qkv_dtype))) return KDA_ERR_ALIGN;
+    Range rg[3];
+    gate_spans(lg, (size_t)d->N, d->H, d->dv, d->qkv_dtype, rg);
+    for (const Range &r : rg)
+      if (overlap(r_s, r) || overlap(r_o, r)) return KDA_ERR_ALIAS;
+  }
+  DecodeArgs a;
+  a.N = d->N; a.H = d->H; a.dk = d->dk; a.dv = d->dv;
+  a.qkv = d->qkv_dtype; a.out = d->out_dtype; a.gate = d->gate_dtype;
+  a.q = q; a.k = k; a.v = v; a.g = log_alpha; a.beta = beta;
+  a.state = state_inout; a.o = out;
+  if (lg) {
+    a.A_log = lg->A_log;
+    a.g_min = lg->g_min;
+    a.og = lg->out_gate;
+    a.nw = lg->norm_weight;
+    a.eps = lg->norm_eps;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d->validate) {
+    kda_status st = run_validation(s, [&](int *flag) { return launch_validate_decode(a, flag, s); });
+    if (st != KDA_OK) return st;
+  }
+  cudaError_t e = launch_decode(a, s);
+  if (e != cudaSuccess) return cuda_fail(e);
   return KDA_OK;
 }
 
@@ -310,43 +410,32 @@ kda_status kda_chunk_fwd_ckpt(const kda_chunk_desc *desc, const void *q, const v
                      workspace_bytes);
 }
 
+
 kda_status kda_decode_step(const kda_decode_desc *d, const void *q, const void *k, const void *v,
                            const void *log_alpha, const void *beta, float *state_inout, void *out,
                            kda_stream_t stream) {
-  if (!d || !q || !k || !v || !log_alpha || !beta || !state_inout || !out) return KDA_ERR_NULL;
-  if (!dtype_ok(d->qkv_dtype) || !dtype_ok(d->out_dtype) || !dtype_ok(d->gate_dtype))
-    return KDA_ERR_DTYPE;
-  if (d->N <= 0 || d->H <= 0 || !dim_ok(d->dk) || !dim_ok(d->dv)) return KDA_ERR_SHAPE;
-  if ((long long)d->N * d->H >= (1LL << 31)) return KDA_ERR_SHAPE;
-  // the state is streamed as 16-byte vectors; the rest needs element alignment
-  if (!aligned16(state_inout)) return KDA_ERR_ALIGN;
-  if (!aligned_to(q, esize(d->qkv_dtype)) || !aligned_to(k, esize(d->qkv_dtype)) ||
-      !aligned_to(v, esize(d->qkv_dtype)) || !aligned_to(out, esize(d->out_dtype)) ||
-      !aligned_to(log_alpha, esize(d->gate_dtype)) || !aligned_to(beta, esize(d->gate_dtype)))
-    return KDA_ERR_ALIGN;
-  const size_t nh = (size_t)d->N * d->H;
-  Range r_s = span(state_inout, nh * d->dk * d->dv * 4);
-  Range r_o = span(out, nh * d->dv * esize(d->out_dtype));
-  Range ins[] = {span(q, nh * d->dk * esize(d->qkv_dtype)), span(k, nh * d->dk * esize(d->qkv_dtype)),
-                 span(v, nh * d->dv * esize(d->qkv_dtype)),
-                 span(log_alpha, nh * d->dk * esize(d->gate_dtype)),
-                 span(beta, nh * esize(d->gate_dtype))};
-  if (overlap(r_s, r_o)) return KDA_ERR_ALIAS;
-  for (const Range &r : ins)
-    if (overlap(r_s, r) || overlap(r_o, r)) return KDA_ERR_ALIAS;
-  DecodeArgs a;
-  a.N = d->N; a.H = d->H; a.dk = d->dk; a.dv = d->dv;
-  a.qkv = d->qkv_dtype; a.out = d->out_dtype; a.gate = d->gate_dtype;
-  a.q = q; a.k = k; a.v = v; a.g = log_alpha; a.beta = beta;
-  a.state = state_inout; a.o = out;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (d->validate) {
-    kda_status st = run_validation(s, [&](int *flag) { return launch_validate_decode(a, flag, s); });
-    if (st != KDA_OK) return st;
-  }
-  cudaError_t e = launch_decode(a, s);
-  if (e != cudaSuccess) return cuda_fail(e);
-  return KDA_OK;
+  return run_decode(d, nullptr, q, k, v, log_alpha, beta, state_inout, out, stream);
+}
+
+kda_status kda_layer_decode_step(const kda_decode_desc *desc, const kda_layer_gates *gates,
+                                 const void *q, const void *k, const void *v, const void *z,
+                                 const void *beta, float *state_inout, void *out,
+                                 kda_stream_t stream) {
+  if (!gates) return KDA_ERR_NULL;
+  return run_decode(desc, gates, q, k, v, z, beta, state_inout, out, stream);
+}
+
+kda_status kda_layer_fwd(const kda_chunk_desc *desc, const kda_layer_gates *gates, const void *q,
+                         const void *k, const void *v, const void *z, const void *beta,
+                         const float *initial_state, const int32_t *cu_seqlens, void *out,
+                         float *final_state, void *workspace, size_t workspace_bytes,
+                         kda_stream_t stream) {
+  if (!gates) return KDA_ERR_NULL;
+  PrefillArgs a;
+  kda_status st = check_prefill(desc, q, k, v, z, beta, initial_state, cu_seqlens, out, final_state, &a, gates);
+  if (st != KDA_OK) return st;
+  return run_prefill(desc, a, reinterpret_cast<cudaStream_t>(stream), workspace ? 1 : 0, workspace,
+                     workspace_bytes);
 }
 
 const char *kda_status_string(kda_status s) {

@@ -14,6 +14,10 @@
 //   V~  = T_b (V - (Gamma o K) S)                     (= U - W S with U = T_b V, W = T_b (Gamma o K))
 //   O   = (Gamma o Q) S + A V~
 //   S  <- Diag(gamma_C) S + (K o gamma_C / Gamma)^T V~
+// In the layer form the log-decay is formed on load from the decay logits z,
+// g = g_min Sigmoid(exp(A_h) z) ([K3-notes §2.2, Eq. 5]); the output norm and
+// gate run afterwards over whole rows (launch_norm_gate), since a CTA here
+// holds only a dv tile.
 // Range guard ([K3-notes §2.2, Eq. 5 and Fig. 3]): when every channel's
 // G_C >= -80 the Gram products use the chunk start as the one decay reference
 // (all factors within e^{+-80}); otherwise each entry uses exp(G_r - G_s) <= 1
@@ -67,6 +71,8 @@ chunk_simt_kernel(PrefillArgs a, int dvt) {
 
   int bos, eos;
   seq_range(a, n, bos, eos);
+  const kda_dtype gdt = a.gdt();
+  const float zscale = a.A_log ? expf(a.A_log[h]) : 0.f;
 
   // initial state tile S[i][j0 + j]
   const size_t sbase = (size_t)nh * dk * dv;
@@ -86,7 +92,8 @@ chunk_simt_kernel(PrefillArgs a, int dvt) {
         size_t idx = ((size_t)(t0 + r) * H + h) * dk + i;
         qv = ld_elem(a.q, idx, a.qkv);
         kv = ld_elem(a.k, idx, a.qkv);
-        gv = ld_elem(a.g, idx, a.gate);
+        gv = ld_elem(a.g, idx, gdt);
+        if (a.A_log) gv = decay_from_logit(gv, zscale, a.g_min);
       }
       m.Q[r * ld + i] = qv;
       m.K[r * ld + i] = kv;

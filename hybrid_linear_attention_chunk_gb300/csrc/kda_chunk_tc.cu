@@ -41,10 +41,19 @@
 // query-side factors are <= 1 (rows before the tile are zeroed) and key-side
 // factors are <= e^{80}.
 //
+// Layer gates ([K3-notes §2.2]), selected at compile time: with kZ the decay
+// tile is the bf16 decay logits z and the prologue forms the log-decay
+// g_min Sigmoid(exp(A_h) z) (Eq. 5) in registers; with kOG the output rows are
+// normalised (RMSNorm over dv, from the bf16-rounded output) and gated by
+// Sigmoid(out_gate), whose tile arrives by TMA during the chunk.
+//
 // Every wait on an mbarrier is bounded (2 s).  On a time-out both groups
 // leave their loops, drain their MMAs and copies, free TMEM and return with a
 // bit set in a device word the host can read (kda_device_watchdog).
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <stddef.h>
+#include <string.h>
 
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
@@ -81,7 +90,10 @@ constexpr uint32_t OFF_VT = 188416;   // 16 KB: -W^T (MN-major), then V~^T, then
 constexpr uint32_t OFF_PRO = 204800;  // 5 KB: decay prologue sums (written while M2/M3 may still run)
 constexpr uint32_t OFF_CTL = 209920;  // 4 KB control block
 constexpr uint32_t SMEM_USED = OFF_CTL + 4096;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
+constexpr uint32_t OFF_OG = SMEM_USED;  // 16 KB, output-gate variant only: out_gate tile (TMA), bf16 [64][128]
+// + 1024 bytes of alignment slack
+constexpr uint32_t smem_bytes(bool og) { return (og ? OFF_OG + 16384 : SMEM_USED) + 1024; }
+static_assert(smem_bytes(true) <= 232448, "shared memory per CTA");
 
 // TMEM columns (512 allocated).
 constexpr uint32_t TM_D1 = 0;     // M1 result (chunk group)
@@ -93,20 +105,23 @@ constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
   B_M1 = 0, B_M23, B_VFULL, B_GFULL, B_QK0, B_QK1, B_TB, B_M4,
-  B_M56, B_L2, B_TD_C, B_TD_S, B_COUNT
+  B_M56, B_L2, B_TD_C, B_TD_S, B_OG, B_COUNT
 };
 
 struct Ctl {
   uint64_t bar[16];
   float gam[2][128];     // gamma_C per channel, by chunk parity
   float bs[64];          // beta of the chunk's rows (0 past the end)
+  alignas(16) float nw[128];  // RMSNorm weight (output-gate variant), read as float4
   uint32_t tmem_slot;
   int abort;             // any thread gave up
   int go_c[2];           // chunk-group wait verdicts (double-buffered)
   int go_s[2];           // state-group wait verdicts
   int qk_iss[2], qk_lnd[2];  // q/k copies issued and waited for, by chunk parity
   int v_iss, v_lnd;          // v copies issued (chunk group) and waited for (state group)
+  int og_iss, og_lnd;        // out_gate copies issued and waited for (state group)
 };
+static_assert(offsetof(Ctl, nw) % 16 == 0 && offsetof(Ctl, gam) % 16 == 0, "vector reads of the control block");
 static_assert(sizeof(Ctl) <= 4096, "control block");
 
 struct TcArgs {
@@ -115,7 +130,7 @@ struct TcArgs {
 };
 
 struct TcMaps {
-  CUtensorMap q, k, v, g;
+  CUtensorMap q, k, v, g, og;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -222,6 +237,7 @@ __device__ __forceinline__ float4 sub4(const float4 &a, const float4 &b) {
 __device__ __forceinline__ float4 neg4(const float4 &a) { return make_float4(-a.x, -a.y, -a.z, -a.w); }
 __device__ __forceinline__ float4 ex2_4(const float4 &a) { return make_float4(ex2(a.x), ex2(a.y), ex2(a.z), ex2(a.w)); }
 
+
 // acc += l[k0 + i] * t[i] for i < 8 (l: the left factor's row, four per float4)
 __device__ __forceinline__ void fma8(float4 &acc, const float4 *l, int k0, const float4 (&t)[8]) {
 #pragma unroll
@@ -292,10 +308,11 @@ struct Loader {
   uint32_t sm_base;
   int h;
   int issued, landed;  // g copies
+  uint32_t bytes;      // of one decay tile: fp32 log-decay or bf16 logits
 
   __device__ void g(int t0) {
     const uint32_t full = smem_u32(&ctl->bar[B_GFULL]);
-    mbar_arrive_expect_tx(full, kC * kD * 4);
+    mbar_arrive_expect_tx(full, bytes);
     tma_load_3d(sm_base + OFF_GS, &maps->g, full, 0, h, t0);
     ++issued;
   }
@@ -313,6 +330,52 @@ __device__ __forceinline__ void issue_v(const TcMaps *maps, Ctl *ctl, uint32_t s
   mbar_arrive_expect_tx(full, 2 * 8192);
   tma_load_3d(sm_base + OFF_V, &maps->v, full, 0, h, t0);
   tma_load_3d(sm_base + OFF_V + 8192, &maps->v, full, 64, h, t0);
+}
+
+// out_gate tile of the chunk at t0 (state group).
+__device__ __forceinline__ void issue_og(const TcMaps *maps, Ctl *ctl, uint32_t sm_base, int h, int t0) {
+  const uint32_t full = smem_u32(&ctl->bar[B_OG]);
+  ++ctl->og_iss;
+  mbar_arrive_expect_tx(full, kC * kD * 2);
+  tma_load_3d(sm_base + OFF_OG, &maps->og, full, 0, h, t0);
+}
+
+
+// Sigmoid of two values as 1/2 + tanh(x/2)/2, the tanh by the hardware's
+// paired half-precision approximation (one special-function operation for
+// two values).  Absolute error of the sigmoid < 1e-3, below the bf16 rounding
+// of the gated output it scales.
+__device__ __forceinline__ float2 sigmoid2_tanh(float a, float b) {
+  __half2 h = __floats2half2_rn(0.5f * a, 0.5f * b);
+  uint32_t t;
+  asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<uint32_t *>(&h)));
+  const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&t));
+  return make_float2(fmaf(0.5f, f.x, 0.5f), fmaf(0.5f, f.y, 0.5f));
+}
+
+// Sum of squares of eight bf16 values.
+__device__ __forceinline__ float sumsq8_bf16(uint4 o8) {
+  const uint32_t ov[4] = {o8.x, o8.y, o8.z, o8.w};
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = unpack_bf16(ov[i]);
+    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+  }
+  return ss;
+}
+
+// Eight output channels (bf16 in o8) times r w Sigmoid(gate) (gate bf16 in g8).
+__device__ __forceinline__ uint4 scale_gate8(uint4 o8, uint4 g8, const float *w, float r) {
+  const uint32_t ov[4] = {o8.x, o8.y, o8.z, o8.w}, gv[4] = {g8.x, g8.y, g8.z, g8.w};
+  uint32_t y[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = unpack_bf16(ov[i]), g = unpack_bf16(gv[i]);
+    const float2 sg = sigmoid2_tanh(g.x, g.y);
+    y[i] = pack_bf16(x.x * r * w[2 * i] * sg.x, x.y * r * w[2 * i + 1] * sg.y);
+  }
+  return make_uint4(y[0], y[1], y[2], y[3]);
 }
 
 // q and k of the chunk at t0 into the Q o Gamma and K-hat buffers of chunk
@@ -399,6 +462,7 @@ __device__ int longest_first(const int32_t *cu, int N, int r, int *s, int tid) {
   return n;
 }
 
+template <bool kZ, bool kOG>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   extern __shared__ uint8_t smem_raw[];
@@ -447,9 +511,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     ctl->abort = 0;
     ctl->qk_iss[0] = ctl->qk_iss[1] = ctl->qk_lnd[0] = ctl->qk_lnd[1] = 0;
     ctl->v_iss = ctl->v_lnd = 0;
+    ctl->og_iss = ctl->og_lnd = 0;
     ctl->go_c[0] = ctl->go_c[1] = ctl->go_s[0] = ctl->go_s[1] = 0;
     fence_mbar_init();
   }
+  if (kOG && tid >= 64 && tid < 64 + kD) ctl->nw[tid - 64] = a.nw ? a.nw[tid - 64] : 1.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -468,7 +534,10 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     const int p4 = ctid & 31, t8 = ctid >> 5;
     int seq = 0;
     uint32_t ph_m1 = 0, ph_m23 = 0, ph_g = 0, ph_l2 = 0;
-    Loader ld{&maps, ctl, sm_base, h, 0, 0};
+    Loader ld{&maps, ctl, sm_base, h, 0, 0, (uint32_t)(kC * kD * (kZ ? 2 : 4))};
+    // decay gate (Eq. 5) in log2 units: g log2(e) = zg_min / (1 + 2^(zs z))
+    const float zs = kZ ? -expf(a.A_log[h]) * kLog2e : 0.f;
+    const float zg_min = kZ ? a.g_min * kLog2e : 0.f;
     if (ctid == 0 && nchunks > 0) {
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
@@ -517,12 +586,18 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           const int row = 8 * t8 + r;
-          float4 gv = *reinterpret_cast<const float4 *>(gs + row * kD + 4 * p4);
+          float4 gv;  // log2-decay
+          if constexpr (kZ) {
+            const float4 zv = unpack4_bf16(*reinterpret_cast<const uint2 *>(
+                reinterpret_cast<const __nv_bfloat16 *>(gs) + row * kD + 4 * p4));
+            gv = make_float4(__fdividef(zg_min, 1.f + ex2(zs * zv.x)), __fdividef(zg_min, 1.f + ex2(zs * zv.y)),
+                             __fdividef(zg_min, 1.f + ex2(zs * zv.z)), __fdividef(zg_min, 1.f + ex2(zs * zv.w)));
+          } else {
+            gv = mul4(*reinterpret_cast<const float4 *>(gs + row * kD + 4 * p4),
+                      make_float4(kLog2e, kLog2e, kLog2e, kLog2e));
+          }
           if (row >= len) gv = make_float4(0.f, 0.f, 0.f, 0.f);  // past the end: identity step
-          run.x += gv.x * kLog2e;
-          run.y += gv.y * kLog2e;
-          run.z += gv.z * kLog2e;
-          run.w += gv.w * kLog2e;
+          run = add4(run, gv);
           Gl[r] = run;
         }
         *reinterpret_cast<float4 *>(tot + t8 * 128 + 4 * p4) = run;
@@ -834,6 +909,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     int seq = 0;
     uint32_t ph_m4 = 0, ph_m56 = 0;
     uint8_t *vt = sm + OFF_VT;
+    if (kOG && stid == 0) tma_prefetch_desc(&maps.og);
     // entry state -> TMEM: fp32 master and the bf16 copy M4 reads (S^T row j;
     // the identity for a transition item, zero without an initial state)
 #pragma unroll 1
@@ -856,6 +932,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       const uint32_t tm_u = TM_U + par * 64;
       // ---------------- M2/M3: U^T and W^T, once the chunk group has T_b
       if (!(alive = group_wait<false>(ctl, B_TB, c & 1, stid, seq, A.err))) break;
+      // (every thread is past the previous chunk's reads of the out_gate tile)
+      if (kOG && stid == 0) issue_og(&maps, ctl, sm_base, h, t0);
       if (stid == 0) {
         bool ok = true;
         if (!zero_v) {
@@ -949,14 +1027,50 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       }
       tmem_wait_st();
       tc_fence_before();
-      bar_state();
+      if constexpr (kOG) {  // the barrier also waits for this chunk's out_gate tile
+        if (!(alive = group_wait<false>(ctl, B_OG, c & 1, stid, seq, A.err))) break;
+        if (stid == 0) ++ctl->og_lnd;
+      } else {
+        bar_state();
+      }
       if (a.o) {  // segment passes of the long-sequence plan write no output
         const uint4 *src = reinterpret_cast<const uint4 *>(vt);
         uint4 *o = reinterpret_cast<uint4 *>(a.o);
+        float w8[8];
+        if constexpr (kOG) {
+          const float4 wa = *reinterpret_cast<const float4 *>(&ctl->nw[8 * (stid & 15)]);
+          const float4 wb = *reinterpret_cast<const float4 *>(&ctl->nw[8 * (stid & 15) + 4]);
+          w8[0] = wa.x; w8[1] = wa.y; w8[2] = wa.z; w8[3] = wa.w;
+          w8[4] = wb.x; w8[5] = wb.y; w8[6] = wb.z; w8[7] = wb.w;
+        }
+        if constexpr (kOG) {
+          // RMSNorm and gate: a thread holds 8 channels of each of 8 rows, and
+          // the 16 lanes of a half-warp share a row.  Four rows' sums of
+          // squares at a time are reduced side by side so that their shuffles
+          // overlap.
+          const uint4 *ogt = reinterpret_cast<const uint4 *>(sm + OFF_OG);
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int idx = it * kStateThreads + stid, row = idx >> 4, c16 = idx & 15;
-          if (row < len) o[((size_t)(t0 + row) * H + h) * (kD / 8) + c16] = src[idx];
+          for (int i0 = 0; i0 < 8; i0 += 4) {
+            float ss[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ss[i] = sumsq8_bf16(src[(i0 + i) * kStateThreads + stid]);
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], off);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int idx = (i0 + i) * kStateThreads + stid, row = idx >> 4, c16 = idx & 15;
+              const uint4 val = scale_gate8(src[idx], ogt[idx], w8, rsqrtf(ss[i] * (1.f / kD) + a.eps));
+              if (row < len) o[((size_t)(t0 + row) * H + h) * (kD / 8) + c16] = val;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int idx = it * kStateThreads + stid, row = idx >> 4, c16 = idx & 15;
+            if (row < len) o[((size_t)(t0 + row) * H + h) * (kD / 8) + c16] = src[idx];
+          }
         }
       }
       // (the next chunk's first group wait orders these reads of the staging
@@ -989,6 +1103,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         mbar_wait(smem_u32(&ctl->bar[B_QK0 + i]), n & 1, &no_abort, A.err, 1u << 25);
     for (int n = ctl->v_lnd; n < ctl->v_iss; ++n)
       mbar_wait(smem_u32(&ctl->bar[B_VFULL]), n & 1, &no_abort, A.err, 1u << 26);
+    for (int n = ctl->og_lnd; n < ctl->og_iss; ++n)
+      mbar_wait(smem_u32(&ctl->bar[B_OG]), n & 1, &no_abort, A.err, 1u << 27);
   }
   if (warp == 0) {
     tc_fence_after();
@@ -1010,24 +1126,35 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // [T_total, H, 128] row-major tensor; boxes of 64 tokens of one head.
+// Operand layout: bf16, two 64-column boxes with the 128-byte swizzle the MMA
+// operands use.  Row layout: the whole row (fp32 or bf16), unswizzled.
 CUresult encode_tok_head(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const void *base, int T, int H,
-                         bool fp32) {
+                         bool fp32, bool operand) {
   const cuuint64_t esz = fp32 ? 4 : 2;
   const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
   const cuuint64_t strides[2] = {(cuuint64_t)kD * esz, (cuuint64_t)H * kD * esz};
-  // bf16: two 64-column boxes with the 128-byte swizzle the MMA operands use;
-  // fp32: the whole 512-byte row, unswizzled
-  const cuuint32_t box[3] = {fp32 ? (cuuint32_t)kD : 64u, 1, (cuuint32_t)kC};
+  const cuuint32_t box[3] = {operand ? 64u : (cuuint32_t)kD, 1, (cuuint32_t)kC};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             fp32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             operand ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <bool kZ, bool kOG>
+cudaError_t launch_variant(const TcMaps &maps, const TcArgs &args, int grid, cudaStream_t s) {
+  constexpr uint32_t bytes = smem_bytes(kOG);
+  cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<kZ, kOG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)bytes);
+  if (e != cudaSuccess) return e;
+  chunk_tc_kernel<kZ, kOG><<<grid, kThreads, bytes, s>>>(maps, args);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 bool chunk_tc_supports(const PrefillArgs &a) {
+  // (in the layer form the decay logits are bf16 like q; beta stays fp32)
   return a.qkv == KDA_BF16 && a.out == KDA_BF16 && a.gate == KDA_F32 && a.dk == kD && a.dv == kD &&
          a.chunk == kC;
 }
@@ -1036,21 +1163,22 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
   if (a.N * a.H == 0) return cudaSuccess;
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
+  const bool z = a.A_log != nullptr, og = a.og != nullptr && a.o != nullptr;
   TcMaps maps;
-  if (encode_tok_head(encode, &maps.q, a.q, a.T_total, a.H, false) != CUDA_SUCCESS ||
-      encode_tok_head(encode, &maps.k, a.k, a.T_total, a.H, false) != CUDA_SUCCESS ||
-      encode_tok_head(encode, &maps.v, a.v, a.T_total, a.H, false) != CUDA_SUCCESS ||
-      encode_tok_head(encode, &maps.g, a.g, a.T_total, a.H, true) != CUDA_SUCCESS)
+  memset(&maps, 0, sizeof(maps));
+  if (encode_tok_head(encode, &maps.q, a.q, a.T_total, a.H, false, true) != CUDA_SUCCESS ||
+      encode_tok_head(encode, &maps.k, a.k, a.T_total, a.H, false, true) != CUDA_SUCCESS ||
+      encode_tok_head(encode, &maps.v, a.v, a.T_total, a.H, false, true) != CUDA_SUCCESS ||
+      encode_tok_head(encode, &maps.g, a.g, a.T_total, a.H, !z, false) != CUDA_SUCCESS ||
+      (og && encode_tok_head(encode, &maps.og, a.og, a.T_total, a.H, false, false) != CUDA_SUCCESS))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
   void *wd = nullptr;
-  e = cudaGetSymbolAddress(&wd, g_tc_watchdog);
+  cudaError_t e = cudaGetSymbolAddress(&wd, g_tc_watchdog);
   if (e != cudaSuccess) return e;
   TcArgs args{a, reinterpret_cast<unsigned int *>(wd)};
-  chunk_tc_kernel<<<a.N * a.nseg * a.H * a.kinds, kThreads, SMEM_BYTES, s>>>(maps, args);
-  return cudaGetLastError();
+  const int grid = a.N * a.nseg * a.H * a.kinds;
+  if (z) return og ? launch_variant<true, true>(maps, args, grid, s) : launch_variant<true, false>(maps, args, grid, s);
+  return og ? launch_variant<false, true>(maps, args, grid, s) : launch_variant<false, false>(maps, args, grid, s);
 }
 
 cudaError_t read_tc_watchdog(unsigned int *flags, bool clear) {

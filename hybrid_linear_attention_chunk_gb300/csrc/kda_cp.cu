@@ -131,6 +131,7 @@ cudaError_t launch_chunk_tc_segmented(const PrefillArgs &a, const SegPlan &pl, v
   p1.nseg = pl.P - 1;
   p1.kinds = 2;
   p1.ck = nullptr;  // checkpoints come from the rerun
+  p1.og = nullptr;  // (no output in pass 1, so no output gate)
   cudaError_t e = launch_chunk_tc(p1, s);
   if (e != cudaSuccess) return e;
   const size_t smem = 2 * DD * sizeof(float);

@@ -10,6 +10,9 @@
 //     u = beta (v - x)
 //     S' = Diag(a) S + k u^T                (= (I - b k k^T) Diag(a) S + b k v^T)
 //     o  = S'^T q = y + u (k . q)
+// In the layer form ([K3-notes §2.2]) alpha comes from the decay logits z,
+// g = g_min Sigmoid(exp(A_h) z) (Eq. 5), and the output row is normalised over
+// dv and gated, Sigmoid(out_gate) o RMSNorm(o), before it is stored.
 // The step is bound by HBM: 2 x dk x dv x 4 bytes of state per head against
 // ~7 dk dv flops, so the kernel is a streaming read-modify-write with the
 // state held in registers between the read and the write, column sums over
@@ -31,6 +34,7 @@ decode_d128_kernel(DecodeArgs a) {
   __shared__ float4 s_x[8][32], s_y[8][32];
   __shared__ float s_u[D];
   __shared__ float s_kq;
+  __shared__ float s_ss[4];
 
   float4 *S = reinterpret_cast<float4 *>(a.state + (size_t)nh * D * D);
   float4 reg[16];
@@ -38,8 +42,10 @@ decode_d128_kernel(DecodeArgs a) {
   for (int r = 0; r < 16; ++r) reg[r] = __ldcs(S + (size_t)(16 * warp + r) * (D / 4) + lane);
 
   const size_t base = (size_t)nh * D;
+  const float ogv = (a.og && tid < D) ? ld_elem(a.og, base + tid, a.qkv) : 0.f;
   if (tid < D) {
-    float g = ld_elem(a.g, base + tid, a.gate);
+    float g = ld_elem(a.g, base + tid, a.gdt());
+    if (a.A_log) g = decay_from_logit(g, expf(a.A_log[nh % a.H]), a.g_min);
     float al = expf(g);
     float kk = ld_elem(a.k, base + tid, a.qkv);
     float qq = ld_elem(a.q, base + tid, a.qkv);
@@ -73,6 +79,7 @@ decode_d128_kernel(DecodeArgs a) {
   s_y[warp][lane] = y;
   __syncthreads();
 
+  float o_val = 0.f;
   if (tid < D) {
     const int l = tid >> 2, c = tid & 3;
     float X = 0.f, Y = 0.f;
@@ -84,9 +91,20 @@ decode_d128_kernel(DecodeArgs a) {
     const float b = ld_elem(a.beta, (size_t)nh, a.gate);
     const float u = b * (ld_elem(a.v, base + tid, a.qkv) - X);
     s_u[tid] = u;
-    st_elem(a.o, base + tid, Y + u * s_kq, a.out);
+    o_val = Y + u * s_kq;
+    if (!a.og) st_elem(a.o, base + tid, o_val, a.out);
+  }
+  if (a.og) {  // the row's sum of squares: warps 0-3 hold its 128 channels
+    float ss = o_val * o_val;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0 && warp < 4) s_ss[warp] = ss;
   }
   __syncthreads();
+  if (a.og && tid < D) {
+    const float r = rsqrtf((s_ss[0] + s_ss[1] + s_ss[2] + s_ss[3]) * (1.f / D) + a.eps);
+    st_elem(a.o, base + tid, o_val * r * (a.nw ? a.nw[tid] : 1.f) * sigmoid_f(ogv), a.out);
+  }
 
   const float4 u4 = reinterpret_cast<const float4 *>(s_u)[lane];
 #pragma unroll
@@ -109,11 +127,13 @@ decode_generic_kernel(DecodeArgs a) {
   const int nh = blockIdx.x;
   const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
   __shared__ float s_a[128], s_k[128], s_q[128];
-  __shared__ float s_part[4];
+  __shared__ float s_part[4], s_ss[4];
   const size_t bk = (size_t)nh * dk, bv = (size_t)nh * dv;
   float kq = 0.f;
   if (tid < dk) {
-    float al = expf(ld_elem(a.g, bk + tid, a.gate));
+    float g = ld_elem(a.g, bk + tid, a.gdt());
+    if (a.A_log) g = decay_from_logit(g, expf(a.A_log[nh % a.H]), a.g_min);
+    float al = expf(g);
     float kk = ld_elem(a.k, bk + tid, a.qkv), qq = ld_elem(a.q, bk + tid, a.qkv);
     s_a[tid] = al;
     s_k[tid] = kk;
@@ -125,16 +145,33 @@ decode_generic_kernel(DecodeArgs a) {
   if ((tid & 31) == 0) s_part[tid >> 5] = kq;
   __syncthreads();
   kq = s_part[0] + s_part[1] + s_part[2] + s_part[3];
-  if (tid >= dv) return;
+  const bool act = tid < dv;
   float *S = a.state + (size_t)nh * dk * dv;
-  float x = 0.f, y = 0.f;
-  for (int i = 0; i < dk; ++i) {
-    float s = S[(size_t)i * dv + tid];
-    x += s * s_a[i] * s_k[i];
-    y += s * s_a[i] * s_q[i];
+  float u = 0.f, o_val = 0.f;
+  if (act) {
+    float x = 0.f, y = 0.f;
+    for (int i = 0; i < dk; ++i) {
+      float s = S[(size_t)i * dv + tid];
+      x += s * s_a[i] * s_k[i];
+      y += s * s_a[i] * s_q[i];
+    }
+    u = ld_elem(a.beta, (size_t)nh, a.gate) * (ld_elem(a.v, bv + tid, a.qkv) - x);
+    o_val = y + u * kq;
+    if (!a.og) st_elem(a.o, bv + tid, o_val, a.out);
   }
-  const float u = ld_elem(a.beta, (size_t)nh, a.gate) * (ld_elem(a.v, bv + tid, a.qkv) - x);
-  st_elem(a.o, bv + tid, y + u * kq, a.out);
+  if (a.og) {  // RMSNorm over the dv outputs, then the gate
+    float ss = o_val * o_val;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((tid & 31) == 0) s_ss[tid >> 5] = ss;
+    __syncthreads();
+    if (act) {
+      const float r = rsqrtf((s_ss[0] + s_ss[1] + s_ss[2] + s_ss[3]) / (float)dv + a.eps);
+      st_elem(a.o, bv + tid, o_val * r * (a.nw ? a.nw[tid] : 1.f) * sigmoid_f(ld_elem(a.og, bv + tid, a.qkv)),
+              a.out);
+    }
+  }
+  if (!act) return;
   for (int i = 0; i < dk; ++i) {
     float *p = S + (size_t)i * dv + tid;
     *p = s_a[i] * *p + s_k[i] * u;

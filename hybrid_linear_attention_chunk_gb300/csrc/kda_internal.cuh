@@ -50,6 +50,17 @@ struct PrefillArgs {
   int ck_every = 0;
   const int32_t *ck_cu = nullptr;
   float *ck = nullptr;
+  // KDA layer gates ([K3-notes §2.2]).  With A_log set, g holds the decay
+  // logits z (dtype qkv) and the log-decay is g_min Sigmoid(exp(A_log[h]) z)
+  // (Eq. 5).  With og set, every output row is Sigmoid(og) o RMSNorm(o) over
+  // its dv channels, RMSNorm(x)_j = x_j nw_j / sqrt(mean x^2 + eps) (nw
+  // nullable: ones).
+  const float *A_log = nullptr;
+  float g_min = 0.f;
+  const void *og = nullptr;
+  const float *nw = nullptr;
+  float eps = 0.f;
+  __host__ __device__ kda_dtype gdt() const { return A_log ? qkv : gate; }  // dtype of the g array
 };
 
 // Where the state of (sequence n, head h) goes once `done` tokens of the
@@ -66,9 +77,26 @@ struct DecodeArgs {
   const void *q, *k, *v, *g, *beta;
   float *state;
   void *o;
+  // layer gates, as in PrefillArgs
+  const float *A_log = nullptr;
+  float g_min = 0.f;
+  const void *og = nullptr;
+  const float *nw = nullptr;
+  float eps = 0.f;
+  __host__ __device__ kda_dtype gdt() const { return A_log ? qkv : gate; }
 };
 
+// Eq. 5 of [K3-notes §2.2] for one element: the log-decay from its logit z,
+// with scale = exp(A_h) (fp32 library exponentials).
+__device__ __forceinline__ float decay_from_logit(float z, float scale, float g_min) {
+  return g_min / (1.f + expf(-scale * z));
+}
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+// In place on a.o: every (token, head) row -> Sigmoid(og) o RMSNorm(row).
+cudaError_t launch_norm_gate(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_chunk_simt(const PrefillArgs &a, cudaStream_t s);
 bool chunk_tc_supports(const PrefillArgs &a);
 cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s);

@@ -160,6 +160,26 @@ def make_decode(w: DecodeWorkload, steps: int, device="cpu", seed: Optional[int]
     return dict(q=q, k=k, v=v, log_alpha=g, beta=beta, state=s0)
 
 
+def make_layer_gates(rows: int, H: int, dk: int, dv: int, dtype: torch.dtype, device="cpu",
+                     seed: int = SEED_BASE + 100, z_mean: float = -3.0, z_std: float = 1.5) -> dict:
+    """Gate inputs of the KDA layer form for `rows` tokens (or decode rows).
+
+    z (decay logits) [rows,H,dk] ~ N(z_mean, z_std^2) and out_gate [rows,H,dv]
+    ~ N(0, 1), cast to `dtype`; A_log [H] ~ U[-0.5, 0.5] and norm_weight [dv]
+    ~ U[0.5, 1.5] in fp32.  With the default z the per-channel decays spread
+    from close to 1 to a few percent per token (most chunks keep one decay
+    reference); z_mean = 3 puts most channels near the Eq. 5 floor, where
+    every chunk takes the per-tile path.  Draw order: z, out_gate, A_log,
+    norm_weight.
+    """
+    gen = _gen(device, seed)
+    z = (torch.randn(rows, H, dk, generator=gen, device=device) * z_std + z_mean).to(dtype)
+    og = torch.randn(rows, H, dv, generator=gen, device=device).to(dtype)
+    A = torch.rand(H, generator=gen, device=device) - 0.5
+    w = torch.rand(dv, generator=gen, device=device) + 0.5
+    return dict(z=z.contiguous(), out_gate=og.contiguous(), A_log=A.contiguous(), norm_weight=w.contiguous())
+
+
 def host_f32(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
     """Exact float32 copy on the host (bf16 upcasts exactly)."""
     if t is None:

@@ -181,6 +181,66 @@ kda_status kda_decode_step(const kda_decode_desc *desc, const void *q, const voi
                            const void *v, const void *log_alpha, const void *beta,
                            float *state_inout, void *out, kda_stream_t stream);
 
+/*
+ * The KDA layer's gates around the recurrence ([K3-notes §2.2]):
+ *   decay gate (Eq. 5):  log_alpha = g_min * Sigmoid(exp(A_h) * z)
+ *       z the decay logits [tokens, H, dk] (from the layer's low-rank decay
+ *       projection), A_h a per-head log scale, Sigmoid(x) = 1 / (1 + e^-x);
+ *   output (the KDA output equation, before W_o):
+ *       y = Sigmoid(out_gate) * RMSNorm(o),   per token and head over dv,
+ *       RMSNorm(o)_j = o_j * norm_weight_j / sqrt(mean_j o_j^2 + norm_eps),
+ *       out_gate = W_g x [tokens, H, dv].
+ * The page names the RMSNorm without its weight or epsilon; here the weight
+ * is one learned value per channel, shared by the heads, and eps is given.
+ * The projections W_g x, W_o y and the one that makes z are plain GEMMs
+ * outside these calls.
+ */
+typedef struct {
+  const float *A_log;       /* [H] fp32 device, required                         */
+  float g_min;              /* log-decay floor, in [-5, 0) (-5 on the page: the
+                               kernels' range guard needs g_min >= -5)           */
+  const void *out_gate;     /* [tokens, H, dv] qkv_dtype device, or NULL: out is
+                               o itself (no norm, no gate)                       */
+  const float *norm_weight; /* [dv] fp32 device, or NULL for ones               */
+  float norm_eps;           /* >= 0 (used only with out_gate)                   */
+} kda_layer_gates;
+
+/*
+ * kda_layer_fwd - kda_chunk_fwd_ex with the layer's gates: the log-decay is
+ * computed in the kernels from z (so log_alpha is never materialised) and,
+ * when gates->out_gate is given, each output row is normalised and gated
+ * before it is stored.
+ *
+ *   z         [B*T, H, dk] qkv_dtype (takes log_alpha's place; desc->gate_dtype
+ *             now describes beta alone)
+ *   out       [B*T, H, dv] out_dtype: y, or o when out_gate is NULL
+ * Other arguments and conventions as kda_chunk_fwd_ex (workspace NULL: a
+ * split plan allocates its workspace stream-ordered).  z, out_gate and out are
+ * 16-byte aligned, A_log and norm_weight 4-byte aligned.  Validate mode checks
+ * that z has no NaN, A_log is finite and beta is in [0, 1]; g_min outside
+ * [-5, 0) or a negative (or NaN) norm_eps is KDA_ERR_RANGE without validate.
+ * On the tensor-core kernel the norm reads the bf16-rounded o, the value an
+ * unfused norm would read from out.
+ */
+kda_status kda_layer_fwd(const kda_chunk_desc *desc, const kda_layer_gates *gates, const void *q,
+                         const void *k, const void *v, const void *z, const void *beta,
+                         const float *initial_state, const int32_t *cu_seqlens, void *out,
+                         float *final_state, void *workspace, size_t workspace_bytes,
+                         kda_stream_t stream);
+
+/*
+ * kda_layer_decode_step - kda_decode_step with the layer's gates:
+ *   z        [N, H, dk] qkv_dtype (in log_alpha's place)
+ *   out      [N, H, dv] out_dtype: y, or o when gates->out_gate is NULL
+ *   gates->out_gate, when given, [N, H, dv] qkv_dtype
+ * Other arguments as kda_decode_step; alignment as kda_decode_step for z and
+ * out_gate, 4 bytes for A_log and norm_weight.
+ */
+kda_status kda_layer_decode_step(const kda_decode_desc *desc, const kda_layer_gates *gates,
+                                 const void *q, const void *k, const void *v, const void *z,
+                                 const void *beta, float *state_inout, void *out,
+                                 kda_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *kda_status_string(kda_status status);
 

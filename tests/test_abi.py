@@ -142,3 +142,42 @@ def test_checkpoint_argument_errors(lib):
     assert call(_desc(num_seqs=2), 64, cu=FAKE * 9) == -1       # packed sequences need cu_ckpt
     assert call(_desc(), 64, ckpt=FAKE * 6) == -8               # checkpoints alias out
     assert call(_desc(), 64, ckpt=FAKE * 7 + 2) == -4           # misaligned
+
+
+def test_layer_argument_errors(lib):
+    """kda_layer_fwd / kda_layer_decode_step check the gates before launching."""
+    from hybrid_linear_attention_chunk_gb300._lib import KdaDecodeDesc, KdaLayerGates
+    P = ctypes.c_void_p
+
+    def gates(A=FAKE * 10, g_min=-5.0, og=None, w=None, eps=1e-6):
+        lg = KdaLayerGates()
+        lg.A_log, lg.g_min, lg.out_gate, lg.norm_weight, lg.norm_eps = A, g_min, og, w, eps
+        return lg
+
+    def fwd(lg, out=FAKE * 6):
+        return lib.kda_layer_fwd(ctypes.byref(_desc()), None if lg is None else ctypes.byref(lg), P(FAKE),
+                                 P(FAKE * 2), P(FAKE * 3), P(FAKE * 4), P(FAKE * 5), None, None, P(out), None,
+                                 None, 0, None)
+
+    assert fwd(None) == -1                                   # no gates
+    assert fwd(gates(A=None)) == -1                          # A_h is required
+    assert fwd(gates(g_min=-6.0)) == -5                      # below the Eq. 5 floor the range guard fails
+    assert fwd(gates(g_min=0.0)) == -5
+    assert fwd(gates(og=FAKE * 11, eps=-1.0)) == -5
+    assert fwd(gates(og=FAKE * 11, eps=float("nan"))) == -5
+    assert fwd(gates(og=FAKE * 11 + 4)) == -4                # out_gate is tiled with 16-byte copies
+    assert fwd(gates(A=FAKE * 10 + 2)) == -4
+    assert fwd(gates(og=FAKE * 6)) == -8                     # out_gate aliases out
+    assert fwd(gates(w=FAKE * 6 + 64)) == -8                 # norm weight inside out
+
+    d = KdaDecodeDesc()
+    d.N, d.H, d.dk, d.dv, d.qkv_dtype, d.out_dtype, d.gate_dtype, d.validate = 4, 2, 64, 64, 1, 1, 0, 0
+
+    def dec(lg):
+        return lib.kda_layer_decode_step(ctypes.byref(d), None if lg is None else ctypes.byref(lg), P(FAKE),
+                                         P(FAKE * 2), P(FAKE * 3), P(FAKE * 4), P(FAKE * 5), P(FAKE * 7),
+                                         P(FAKE * 6), None)
+
+    assert dec(None) == -1
+    assert dec(gates(g_min=-5.5)) == -5
+    assert dec(gates(og=FAKE * 7)) == -8                     # out_gate aliases the state
