@@ -16,6 +16,9 @@ the GPU receives, so a bf16 input is passed as its exact float32 upcast):
                       formulas that the page leaves out (derivation in the C file).
 * ``decode_step``   - one token of the recurrence per sequence, state in place.
 * ``affine_pair``   - [K3-notes §2.5, context-parallel affine pair] (M, S~).
+* ``backward``      - gradients of <dO, o~> + <dS_T, S_T> with respect to every
+                      input, by reverse-mode differentiation of the token
+                      recurrence (the page names training but prints no backward).
 * ``layer``, ``layer_decode_step`` - the recurrence inside the KDA layer's gates
                       ([K3-notes §2.2, Eq. 5 and the KDA output equation]): the
                       log-decay g_min Sigmoid(exp(A_h) z) from decay logits z, and
@@ -48,6 +51,13 @@ MUTATIONS = {
     "beta_only_on_write": 6,
     "decay_by_column": 7,
     "beta_squared": 8,
+}
+
+# Planted mistakes in the backward (``backward`` only).
+BWD_MUTATIONS = {
+    "bwd_ds_undecayed": 16,
+    "bwd_dk_no_predict": 17,
+    "bwd_dg_from_ds": 18,
 }
 
 # Planted mistakes in the layer gates (``layer`` only).
@@ -97,6 +107,8 @@ def _load():
     lib.oracle_kda_layer.restype = I
     lib.oracle_kda_layer_decode_step.argtypes = [I, I, I, I, P, P, P, P, P, D, P, P, P, D, P, P, I]
     lib.oracle_kda_layer_decode_step.restype = I
+    lib.oracle_kda_backward.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I]
+    lib.oracle_kda_backward.restype = I
     lib.oracle_kda_recurrent_ckpt.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, P, I]
     lib.oracle_kda_recurrent_ckpt.restype = I
     _lib = lib
@@ -299,3 +311,28 @@ def layer_decode_step(q, k, v, z, beta, state, A_log, g_min=-5.0, out_gate=None,
     if st != 0:
         raise RuntimeError(f"oracle_kda_layer_decode_step failed with {st}")
     return o, S
+
+
+def backward(q, k, v, g, beta, d_out, initial_state=None, d_final_state=None, cu_seqlens=None,
+             nthreads=None, mutation: int = 0):
+    """fp64 gradients of L = sum_t <d_out_t, o~_t> + <d_final_state, S_T>.
+
+    Arguments as ``recurrent`` plus d_out [T_total, H, dv] and d_final_state
+    [N, H, dk, dv] (None: 0), both float32 like the other inputs.  Returns a
+    dict with dq, dk [T_total,H,dk], dv [T_total,H,dv], dg (log-decay)
+    [T_total,H,dk], dbeta [T_total,H] and ds0 [N,H,dk,dv].
+    """
+    lib = _load()
+    T, H, dk, dv, N, cu, arrs = _prep(q, k, v, g, beta, cu_seqlens)
+    s0 = None if initial_state is None else _f64(initial_state)[0]
+    dO = _f32(d_out)
+    dST = None if d_final_state is None else _f32(d_final_state)
+    out = dict(dq=np.zeros((T, H, dk)), dk=np.zeros((T, H, dk)), dv=np.zeros((T, H, dv)),
+               dg=np.zeros((T, H, dk)), dbeta=np.zeros((T, H)), ds0=np.zeros((N, H, dk, dv)))
+    st = lib.oracle_kda_backward(N, H, dk, dv, cu.ctypes.data_as(ctypes.c_void_p), *[a[1] for a in arrs],
+                                 _ptr(s0), dO[1], None if dST is None else dST[1], _ptr(out["dq"]),
+                                 _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
+                                 _ptr(out["ds0"]), nthreads or default_threads(), int(mutation))
+    if st != 0:
+        raise RuntimeError(f"oracle_kda_backward failed with {st}")
+    return out

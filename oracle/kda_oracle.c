@@ -28,6 +28,10 @@
  *  - [K3-notes §2.5, Fig. 12, prefix-cache resume]: the state after a prefix
  *    is what a request sharing that prefix resumes from; the recurrence can
  *    record it every `every` tokens (oracle_kda_recurrent_ckpt).
+ *  - Gradients (oracle_kda_backward): the page says the chunk form serves
+ *    training but prints no backward, so the oracle takes the plainest one,
+ *    reverse-mode differentiation of the token recurrence above for the loss
+ *    L = sum_t <dO_t, o~_t> + <dS_T, S_T>, written out in kda_token_bwd.
  *  - [K3-notes §2.2, Eq. 5 and the KDA output equation], the layer's gates
  *    around the recurrence (oracle_kda_layer, oracle_kda_layer_decode_step):
  *        g_t = g_min Sigmoid(exp(A_h) z_t)          (per channel; z the decay logits)
@@ -77,7 +81,11 @@ enum {
   MUT_NORM_EPS_OUTSIDE = 13, /* 1 / (sqrt(mean x^2) + eps)                        */
   MUT_OGATE_NEG = 14,        /* Sigmoid(-gate)                                    */
   MUT_NORM_W_REVERSED = 15,  /* weight indexed dv-1-j                             */
-  MUT_COUNT = 16
+  /* backward (oracle_kda_backward only) */
+  MUT_BWD_DS_UNDECAYED = 16, /* dS_{t-1} = dP instead of Diag(alpha) dP            */
+  MUT_BWD_DK_NO_PREDICT = 17,/* dk misses the prediction term P dx                 */
+  MUT_BWD_DG_FROM_DS = 18,   /* dg from dS instead of dP = dS + k dx^T             */
+  MUT_COUNT = 19
 };
 
 typedef struct {
@@ -198,6 +206,142 @@ static void output_norm_gate(int dv, double *o, const float *gate, const float *
 }
 
 static int next_chain(job_t *J) { return __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED); }
+
+/* ------------------------------------------------------------------ backward */
+
+/* Reverse of one kda_token step.  Sp = S_{t-1} and St = S_t (dk x dv), dS on
+ * entry = dL/dS_t from the later tokens; on return dS = dL/dS_{t-1}.  With
+ *   P = Diag(alpha) Sp,  x = P^T k,  u = beta (v - x),  S_t = P + k u^T,  o = S_t^T q:
+ *   dS += q do^T                  (o = S_t^T q)
+ *   dq  = S_t do
+ *   du  = dS^T k,   dk = dS u     (S_t = P + k u^T)
+ *   dbeta = du . (v - x),  dv = beta du,  dx = -beta du
+ *   dk += P dx,  dP = dS + k dx^T (x = P^T k)
+ *   dalpha_i = sum_j dP_ij Sp_ij,  dg = alpha o dalpha,  dS_{t-1} = Diag(alpha) dP.
+ * work: 3 dv + dk doubles. */
+static void kda_token_bwd(int dk, int dv, const double *Sp, const double *St, double *dS, const float *q,
+                          const float *k, const float *v, const double *g, double beta, const float *dO,
+                          double *dq, double *dkv, double *dvv, double *dg, double *dbeta, double *work,
+                          int mutation) {
+  double *x = work, *u = work + dv, *du = work + 2 * dv, *alpha = work + 3 * dv;
+  for (int i = 0; i < dk; ++i) alpha[i] = exp(g[i]);
+  for (int j = 0; j < dv; ++j) {
+    double acc = 0.0;
+    for (int i = 0; i < dk; ++i) acc += alpha[i] * Sp[(size_t)i * dv + j] * (double)k[i];
+    x[j] = acc;
+    u[j] = beta * ((double)v[j] - acc);
+  }
+  for (int i = 0; i < dk; ++i)
+    for (int j = 0; j < dv; ++j) dS[(size_t)i * dv + j] += (double)q[i] * (double)dO[j];
+  for (int i = 0; i < dk; ++i) {
+    double acc = 0.0;
+    for (int j = 0; j < dv; ++j) acc += St[(size_t)i * dv + j] * (double)dO[j];
+    dq[i] = acc;
+  }
+  double db = 0.0;
+  for (int j = 0; j < dv; ++j) {
+    double acc = 0.0;
+    for (int i = 0; i < dk; ++i) acc += dS[(size_t)i * dv + j] * (double)k[i];
+    du[j] = acc;
+    db += acc * ((double)v[j] - x[j]);
+    dvv[j] = beta * acc;
+  }
+  *dbeta = db;
+  for (int i = 0; i < dk; ++i) {
+    double acc = 0.0;
+    for (int j = 0; j < dv; ++j) {
+      acc += dS[(size_t)i * dv + j] * u[j];
+      if (mutation != MUT_BWD_DK_NO_PREDICT) acc += alpha[i] * Sp[(size_t)i * dv + j] * (-beta * du[j]);
+    }
+    dkv[i] = acc;
+  }
+  for (int i = 0; i < dk; ++i) {
+    double da = 0.0;
+    for (int j = 0; j < dv; ++j) {
+      const double dP = dS[(size_t)i * dv + j] + (double)k[i] * (-beta * du[j]);
+      da += (mutation == MUT_BWD_DG_FROM_DS ? dS[(size_t)i * dv + j] : dP) * Sp[(size_t)i * dv + j];
+      dS[(size_t)i * dv + j] = mutation == MUT_BWD_DS_UNDECAYED ? dP : alpha[i] * dP;
+    }
+    dg[i] = alpha[i] * da;
+  }
+}
+
+/* Work item of the backward: one chain, its states recomputed a block of
+ * kBwdBlock tokens at a time from states kept at block starts. */
+enum { kBwdBlock = 64 };
+
+typedef struct {
+  job_t base;
+  const float *dO;      /* [T][H][dv] */
+  const float *dST;     /* [N][H][dk][dv] or NULL */
+  double *dq, *dk, *dv, *dg, *dbeta, *ds0;
+} bwd_job_t;
+
+static void *backward_worker(void *arg) {
+  bwd_job_t *B = (bwd_job_t *)arg;
+  job_t *J = &B->base;
+  const int dk = J->dk, dv = J->dv, H = J->H;
+  const size_t SS = (size_t)dk * dv;
+  int64_t maxlen = 0;
+  for (int n = 0; n < J->N; ++n)
+    if (J->cu[n + 1] - J->cu[n] > maxlen) maxlen = J->cu[n + 1] - J->cu[n];
+  const int64_t nblk = (maxlen + kBwdBlock - 1) / kBwdBlock;
+  double *starts = (double *)malloc(sizeof(double) * SS * (size_t)(nblk > 0 ? nblk : 1));
+  double *states = (double *)malloc(sizeof(double) * SS * (kBwdBlock + 1));
+  double *dS = (double *)malloc(sizeof(double) * SS);
+  double *work = (double *)malloc(sizeof(double) * (size_t)(3 * dv + dk));
+  double *grow = (double *)malloc(sizeof(double) * (size_t)dk);
+  double *obuf = (double *)malloc(sizeof(double) * (size_t)dv);
+  if (!starts || !states || !dS || !work || !grow || !obuf) {
+    J->status = ORACLE_ENOMEM;
+    free(starts); free(states); free(dS); free(work); free(grow); free(obuf);
+    return NULL;
+  }
+  for (;;) {
+    int w = next_chain(J);
+    if (w >= J->nchains) break;
+    const int n = w / H, h = w % H;
+    const int64_t t0 = J->cu[n], t1 = J->cu[n + 1];
+    const size_t sidx = ((size_t)n * H + h) * SS;
+    /* forward: keep the state at every block start */
+    double *S = states;
+    if (J->s0) memcpy(S, J->s0 + sidx, sizeof(double) * SS);
+    else memset(S, 0, sizeof(double) * SS);
+    for (int64_t t = t0; t < t1; ++t) {
+      if ((t - t0) % kBwdBlock == 0) memcpy(starts + (size_t)((t - t0) / kBwdBlock) * SS, S, sizeof(double) * SS);
+      const size_t th = (size_t)t * H + h;
+      for (int i = 0; i < dk; ++i) grow[i] = (double)J->g[th * dk + i];
+      kda_token(dk, dv, S, J->q + th * dk, J->k + th * dk, J->v + th * dv, grow, (double)J->beta[th], obuf,
+                work, MUT_NONE);
+    }
+    /* backward, block by block from the end */
+    if (B->dST) for (size_t e = 0; e < SS; ++e) dS[e] = (double)B->dST[sidx + e];
+    else memset(dS, 0, sizeof(double) * SS);
+    for (int64_t b = (t1 - t0 + kBwdBlock - 1) / kBwdBlock - 1; b >= 0; --b) {
+      const int64_t bs = t0 + b * kBwdBlock, be = (bs + kBwdBlock < t1) ? bs + kBwdBlock : t1;
+      memcpy(states, starts + (size_t)b * SS, sizeof(double) * SS);
+      for (int64_t t = bs; t < be; ++t) {  /* states[t - bs] = S_{t-1}; states[t - bs + 1] = S_t */
+        double *Sn = states + (size_t)(t - bs + 1) * SS;
+        memcpy(Sn, states + (size_t)(t - bs) * SS, sizeof(double) * SS);
+        const size_t th = (size_t)t * H + h;
+        for (int i = 0; i < dk; ++i) grow[i] = (double)J->g[th * dk + i];
+        kda_token(dk, dv, Sn, J->q + th * dk, J->k + th * dk, J->v + th * dv, grow, (double)J->beta[th], obuf,
+                  work, MUT_NONE);
+      }
+      for (int64_t t = be - 1; t >= bs; --t) {
+        const size_t th = (size_t)t * H + h;
+        for (int i = 0; i < dk; ++i) grow[i] = (double)J->g[th * dk + i];
+        kda_token_bwd(dk, dv, states + (size_t)(t - bs) * SS, states + (size_t)(t - bs + 1) * SS, dS,
+                      J->q + th * dk, J->k + th * dk, J->v + th * dv, grow, (double)J->beta[th], B->dO + th * dv,
+                      B->dq + th * dk, B->dk + th * dk, B->dv + th * dv, B->dg + th * dk, B->dbeta + th, work,
+                      J->mutation);
+      }
+    }
+    if (B->ds0) memcpy(B->ds0 + sidx, dS, sizeof(double) * SS);
+  }
+  free(starts); free(states); free(dS); free(work); free(grow); free(obuf);
+  return NULL;
+}
 
 static void *recurrent_worker(void *arg) {
   job_t *J = (job_t *)arg;
@@ -356,6 +500,30 @@ int oracle_kda_layer_decode_step(int N, int H, int dk, int dv, const float *q, c
                             state, o, state, nthreads, MUT_NONE);
   free(cu);
   return st;
+}
+
+/* Gradients of L = sum_t <dO_t, o~_t> + <dST, S_T> (dST NULL: 0) with respect
+ * to q, k, v, g (log-decay), beta and the initial state, by reverse-mode
+ * differentiation of the token recurrence.  Layouts as the forward; ds0 is
+ * [N][H][dk][dv] (nullable).  All chains. */
+int oracle_kda_backward(int N, int H, int dk, int dv, const int64_t *cu, const float *q, const float *k,
+                        const float *v, const float *g, const float *beta, const double *s0, const float *dO,
+                        const float *dST, double *dq, double *dk_out, double *dv_out, double *dg, double *dbeta,
+                        double *ds0, int nthreads, int mutation) {
+  int st = check_common(N, H, dk, dv, cu);
+  if (st) return st;
+  if (!dO || !dq || !dk_out || !dv_out || !dg || !dbeta) return ORACLE_EINVAL;
+  if (mutation != MUT_NONE && (mutation < MUT_BWD_DS_UNDECAYED || mutation >= MUT_COUNT)) return ORACLE_EINVAL;
+  bwd_job_t B;
+  memset(&B, 0, sizeof(B));
+  job_t *J = &B.base;
+  J->N = N; J->H = H; J->dk = dk; J->dv = dv; J->cu = cu;
+  J->q = q; J->k = k; J->v = v; J->g = g; J->beta = beta; J->s0 = s0;
+  J->nchains = N * H;
+  J->mutation = mutation;
+  B.dO = dO; B.dST = dST;
+  B.dq = dq; B.dk = dk_out; B.dv = dv_out; B.dg = dg; B.dbeta = dbeta; B.ds0 = ds0;
+  return run_threads(J, nthreads, backward_worker);
 }
 
 /* One decode step for N independent sequences: each (n, h) consumes one token
