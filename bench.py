@@ -347,6 +347,8 @@ def run_gpu(args):
 
     if args.ckpt_steps > 0:
         extra["checkpoints"] = time_checkpoints(kda, x, w, args.ckpt_steps, 512, ms_step, dev, stream, world)
+    if args.bwd_steps > 0:
+        extra["backward"] = time_backward(kda, x, w, args.bwd_steps, ms_step, dev, stream, world)
     if args.layer_steps > 0:
         extra["layer_form"] = time_layer(kda, inputs, x, w, args.layer_steps, ms_step, dev, stream, world, rank,
                                          hbm_peak)
@@ -448,6 +450,46 @@ def time_checkpoints(kda, x, w, steps, every, ms_headline, dev, stream, world):
            "checkpoint_bytes_per_step": int(ck.numel() * 4),
            "time_vs_headline": round(ms / ms_headline, 4)}
     del ck, out, sT
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_backward(kda, x, w, steps, ms_headline, dev, stream, world):
+    """kda_chunk_bwd on the headline batch (the forward recomputed inside),
+    with a random d_out and a caller workspace."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(123)
+    dO = torch.randn(w.B * w.T, w.H, w.dv, generator=gen, device=dev).to(torch.bfloat16)
+    d = kda.chunk_desc(x["q"], x["v"], out_dtype=dO.dtype, gate_dtype=0, B=w.B)
+    ws_bytes = kda.kda_chunk_bwd_workspace_size(d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    f = dict(dtype=torch.float32, device=dev)
+    grads = dict(dq=torch.empty(x["q"].shape, **f), dk=torch.empty(x["k"].shape, **f),
+                 dv=torch.empty(x["v"].shape, **f), dlog_alpha=torch.empty(x["log_alpha"].shape, **f),
+                 dbeta=torch.empty(x["beta"].shape, **f), d_initial_state=None)
+
+    def step():
+        kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], dO, B=w.B, stream=stream,
+                          workspace=ws, grads=grads)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = reduce_max(ev0.elapsed_time(ev1) / steps, world, dev)
+    tok = w.B * w.T
+    res = {"workload": w.name, "api": "kda_chunk_bwd (fp32 CUDA-core kernels, 16-token chunks)", "steps": steps,
+           "ms_per_step": round(ms, 3), "tokens_per_s": round(world * tok / (ms * 1e-3), 1),
+           "time_vs_forward": round(ms / ms_headline, 3), "workspace_bytes": int(ws_bytes),
+           "launches_per_step": 4}
+    del dO, ws, grads
     torch.cuda.empty_cache()
     return res
 
@@ -603,6 +645,8 @@ def main(argv=None):
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--long-steps", type=int, default=3, help="steps of the 2^20-token workload (0: skip)")
     ap.add_argument("--varlen-steps", type=int, default=5, help="steps of the 64-sequence varlen workload")
+    ap.add_argument("--bwd-steps", type=int, default=10,
+                    help="steps of the backward on the headline batch (0: skip)")
     ap.add_argument("--layer-steps", type=int, default=100,
                     help="steps of the headline batch in the layer form (0: skip)")
     ap.add_argument("--ckpt-steps", type=int, default=100,

@@ -89,6 +89,11 @@ def load() -> ctypes.CDLL:
         lib.kda_layer_decode_step.argtypes = [ctypes.POINTER(KdaDecodeDesc), ctypes.POINTER(KdaLayerGates), P, P,
                                               P, P, P, P, P, P]
         lib.kda_layer_decode_step.restype = ctypes.c_int
+        lib.kda_chunk_bwd_workspace_size.argtypes = [ctypes.POINTER(KdaChunkDesc), ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_chunk_bwd_workspace_size.restype = ctypes.c_int
+        lib.kda_chunk_bwd.argtypes = [ctypes.POINTER(KdaChunkDesc), P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                      ctypes.c_size_t, P]
+        lib.kda_chunk_bwd.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_last_cuda_error.argtypes = []
@@ -334,3 +339,40 @@ def kda_layer_decode_step(q, k, v, z, beta, state_inout, A_log, g_min=-5.0, out_
                                    _ptr(beta), _ptr(state_inout), _ptr(out), _stream_handle(stream, q.device))
     _check(st, "kda_layer_decode_step")
     return out
+
+
+def kda_chunk_bwd_workspace_size(desc: KdaChunkDesc) -> int:
+    lib = load()
+    n = ctypes.c_size_t(0)
+    _check(lib.kda_chunk_bwd_workspace_size(ctypes.byref(desc), ctypes.byref(n)), "kda_chunk_bwd_workspace_size")
+    return n.value
+
+
+def kda_chunk_bwd(q, k, v, log_alpha, beta, d_out, initial_state=None, d_final_state=None, cu_seqlens=None,
+                  *, chunk=64, validate=False, want_d_initial_state=True, B=None, stream=None, workspace=None,
+                  grads=None):
+    """Gradients of kda_chunk_fwd through the C ABI for
+    L = sum <d_out, out> + <d_final_state, final_state>.
+
+    Arguments as kda_chunk_fwd plus d_out (out's shape and dtype) and
+    d_final_state ([N,H,dk,dv] fp32 or None).  Returns a dict of fp32 tensors
+    dq, dk, dv, dlog_alpha, dbeta and d_initial_state (None unless wanted).
+    `grads` may pass that dict preallocated."""
+    lib = load()
+    dev = q.device
+    d = chunk_desc(q, v, chunk=chunk, cu_seqlens=cu_seqlens, out_dtype=d_out.dtype, gate_dtype=_dt(log_alpha),
+                   validate=validate, B=B)
+    Nseq = d.num_seqs if cu_seqlens is not None else d.B
+    if grads is None:
+        f = dict(dtype=torch.float32, device=dev)
+        grads = dict(dq=torch.empty(q.shape, **f), dk=torch.empty(k.shape, **f), dv=torch.empty(v.shape, **f),
+                     dlog_alpha=torch.empty(log_alpha.shape, **f), dbeta=torch.empty(beta.shape, **f),
+                     d_initial_state=(torch.empty(Nseq, d.H, d.dk, d.dv, **f) if want_d_initial_state else None))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_chunk_bwd(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                           _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state),
+                           _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dlog_alpha"]),
+                           _ptr(grads["dbeta"]), _ptr(grads.get("d_initial_state")), _ptr(workspace), ws_bytes,
+                           _stream_handle(stream, dev))
+    _check(st, "kda_chunk_bwd")
+    return grads

@@ -438,6 +438,75 @@ kda_status kda_layer_fwd(const kda_chunk_desc *desc, const kda_layer_gates *gate
                      workspace_bytes);
 }
 
+kda_status kda_chunk_bwd_workspace_size(const kda_chunk_desc *desc, size_t *bytes) {
+  if (!desc || !bytes) return KDA_ERR_NULL;
+  *bytes = 0;
+  PrefillArgs a;
+  kda_status st = args_from_desc(desc, &a);
+  if (st != KDA_OK) return st;
+  *bytes = bwd_workspace_bytes(a);
+  return KDA_OK;
+}
+
+kda_status kda_chunk_bwd(const kda_chunk_desc *desc, const void *q, const void *k, const void *v,
+                         const void *log_alpha, const void *beta, const float *initial_state,
+                         const int32_t *cu_seqlens, const void *d_out, const float *d_final_state,
+                         float *dq, float *dk, float *dv, float *dlog_alpha, float *dbeta,
+                         float *d_initial_state, void *workspace, size_t workspace_bytes,
+                         kda_stream_t stream) {
+  PrefillArgs a;
+  // the forward's checks, with d_out in out's place (same shape and dtype)
+  kda_status st = check_prefill(desc, q, k, v, log_alpha, beta, initial_state, cu_seqlens,
+                                const_cast<void *>(d_out), nullptr, &a);
+  if (st != KDA_OK) return st;
+  if (desc->kernel == KDA_KERNEL_TC) return KDA_ERR_UNSUPPORTED;  // one CUDA-core implementation
+  if (!dq || !dk || !dv || !dlog_alpha || !dbeta) return KDA_ERR_NULL;
+  float *outs[] = {dq, dk, dv, dlog_alpha, dbeta, d_initial_state};
+  for (float *p : outs)
+    if (p && !aligned_to(p, 4)) return KDA_ERR_ALIGN;
+  if (d_final_state && !aligned_to(d_final_state, 4)) return KDA_ERR_ALIGN;
+  const size_t th = (size_t)a.T_total * a.H, state = (size_t)a.N * a.H * a.dk * a.dv * 4;
+  const Range r_out[] = {span(dq, th * a.dk * 4), span(dk, th * a.dk * 4), span(dv, th * a.dv * 4),
+                         span(dlog_alpha, th * a.dk * 4), span(dbeta, th * 4),
+                         span(d_initial_state, d_initial_state ? state : 0)};
+  const Range r_in[] = {span(q, th * a.dk * esize(a.qkv)), span(k, th * a.dk * esize(a.qkv)),
+                        span(v, th * a.dv * esize(a.qkv)), span(log_alpha, th * a.dk * esize(a.gate)),
+                        span(beta, th * esize(a.gate)), span(initial_state, initial_state ? state : 0),
+                        span(cu_seqlens, cu_seqlens ? (size_t)(a.N + 1) * 4 : 0),
+                        span(d_out, th * a.dv * esize(a.out)), span(d_final_state, d_final_state ? state : 0)};
+  for (int i = 0; i < 6; ++i) {
+    for (const Range &r : r_in)
+      if (overlap(r_out[i], r)) return KDA_ERR_ALIAS;
+    for (int j = i + 1; j < 6; ++j)
+      if (overlap(r_out[i], r_out[j])) return KDA_ERR_ALIAS;
+  }
+  const size_t need = bwd_workspace_bytes(a);
+  if (workspace) {
+    if (workspace_bytes < need) return KDA_ERR_SHAPE;
+    if (!aligned16(workspace)) return KDA_ERR_ALIGN;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (desc->validate) {
+    st = run_validation(s, [&](int *flag) { return launch_validate_prefill(a, flag, s); });
+    if (st != KDA_OK) return st;
+  }
+  BwdIo io{d_out, d_final_state, dq, dk, dv, dlog_alpha, dbeta, d_initial_state};
+  cudaError_t e;
+  if (workspace || need == 0) {
+    e = launch_chunk_bwd(a, io, workspace, s);
+  } else {
+    void *tmp = nullptr;
+    e = cudaMallocAsync(&tmp, need, s);
+    if (e == cudaSuccess) {
+      e = launch_chunk_bwd(a, io, tmp, s);
+      cudaError_t ef = cudaFreeAsync(tmp, s);
+      if (e == cudaSuccess) e = ef;
+    }
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KDA_OK;
+}
+
 const char *kda_status_string(kda_status s) {
   switch (s) {
     case KDA_OK: return "ok";

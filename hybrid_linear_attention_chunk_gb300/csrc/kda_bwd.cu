@@ -1,0 +1,569 @@
+// Backward of the chunked KDA prefill: gradients of
+//   L = sum_t <dO_t, o_t> + <dS_T, S_T>
+// with respect to q, k, v, the log-decay, beta and the initial state.
+//
+// Cited page: "Kimi K3：从 3T 稀疏预训练到百万 Token Agent 的端到端扩展"
+// (liuzhao09.github.io/papers/kimi-k3), [K3-notes] below.  [K3-notes §2.2]
+// gives the chunkwise form and says it serves training; it prints no
+// backward.  The one here differentiates the chunk form (per chunk of C
+// tokens, G the within-chunk cumulative log-decay, Gamma = exp(G), gamma =
+// exp(G_last)):
+//   Qb = Q o Gamma, Kb = K / Gamma, GK = Gamma o K, Kh = K o gamma / Gamma
+//   A = Tril_incl(Qb Kb^T),  M = GK Kb^T,  L = StrictTril(diag(beta) M),  T = (I + L)^-1
+//   T_b = T diag(beta),  P = V - GK S,  V~ = T_b P  (= U - W S, W = T_b GK)
+//   O = Qb S + A V~,  S' = diag(gamma) S + Kh^T V~
+// in reverse, given dO and dS' (the gradient after the chunk):
+//   dV~ = Kh dS' + A^T dO,  dV = T_b^T dV~,  dS = diag(gamma) dS' + Qb^T dO - W^T dV~
+//   dQb = dO S^T + dA Kb,  dA = Tril_incl(dO V~^T),  dKh = V~ dS'^T,  dgamma = rowsum(dS' o S)
+//   dT_b = dV~ P^T,  dbeta_s = sum_r dT_b[r,s] T[r,s] + sum_{s'<s} dL[s,s'] M[s,s']
+//   dL = StrictTril(-T^T (dT_b diag(beta)) T^T),  dM = diag(beta) dL
+//   dGK = -dV S^T + dM Kb,  dKb = dM^T GK + dA^T Qb
+//   dq = dQb o Gamma,  dk = dKb / Gamma + dGK o Gamma + dKh o gamma / Gamma
+//   dG = dQb o Qb - dKb o Kb + dGK o GK - dKh o Kh,  dG_last += colsum(dKh o Kh) + dgamma o gamma
+//   dg = reverse cumulative sum of dG over the chunk's rows.
+// The chunk is C = 16 tokens: by the decay floor of [K3-notes §2.2, Eq. 5]
+// a 16-token tile sums to >= -80, so the chunk start serves as the one decay
+// reference for every tile ([K3-notes §2.2, Fig. 3]) and all factors stay
+// within e^{+-80} in fp32.
+//
+// Four launches, fp32 on CUDA cores:
+//   bwd_prep   (every chunk in parallel)  Qb, Kh, W, A, T, gamma of each chunk
+//   bwd_scan<forward>  (per sequence, head, 32 dv columns)  the entry state of every chunk
+//   bwd_scan<reverse>  (same, last chunk first)  the state gradient after every chunk; dS_0
+//   bwd_grads  (every chunk in parallel)  dq, dk, dv, dg, dbeta of the chunk's rows
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kBC = 16;       // tokens per backward chunk
+constexpr int kBThreads = 256;
+constexpr int kScanDvt = 32;  // state columns per scan CTA
+constexpr int kGradDvt = 16;  // state columns per pass of the gradient kernel
+
+struct BwdArgs {
+  int N, T_total, T_seq, H, dk, dv;
+  kda_dtype qkv, out, gate;
+  const void *q, *k, *v, *g, *beta;
+  const float *s0;     // nullable
+  const int32_t *cu;   // nullable: B x T batch
+  const void *dO;      // out dtype
+  const float *dST;    // nullable
+  float *gq, *gk, *gv, *gg, *gbeta, *gs0;  // dq, dk, dv, dg, dbeta, dS_0 (gs0 nullable)
+  int nslots;          // chunk slots (see slot_base)
+  // workspace, per (slot, head)
+  float *Qb, *Kh, *W;  // [nslots * H][C][dk]
+  float *A, *T;        // [nslots * H][C][C]
+  float *gam;          // [nslots * H][dk]
+  float *Sent, *dSx;   // [nslots * H][dk][dv]: state before / state gradient after the chunk
+};
+
+__device__ __forceinline__ void bounds(const BwdArgs &a, int n, int &bos, int &eos) {
+  if (a.cu) {
+    bos = a.cu[n];
+    eos = a.cu[n + 1];
+  } else {
+    bos = n * a.T_seq;
+    eos = bos + a.T_seq;
+  }
+}
+
+// First chunk slot of sequence n: floor(cu[n] / C) + n for packed sequences
+// (strictly increasing, and sequence n's ceil(len / C) chunks fit before the
+// next base), n * ceil(T / C) for a batch.
+__device__ __forceinline__ int slot_base(const BwdArgs &a, int n) {
+  return a.cu ? a.cu[n] / kBC + n : n * ((a.T_seq + kBC - 1) / kBC);
+}
+
+// (sequence, chunk) held by a slot; false for a slot between sequences.
+__device__ bool locate(const BwdArgs &a, int slot, int &n, int &j) {
+  if (a.N <= 0) return false;
+  if (!a.cu) {
+    const int per = (a.T_seq + kBC - 1) / kBC;
+    if (per == 0) return false;
+    n = slot / per;
+    j = slot % per;
+    return n < a.N;
+  }
+  int lo = 0, hi = a.N - 1;  // the last n with slot_base(n) <= slot
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (slot_base(a, mid) <= slot) lo = mid;
+    else hi = mid - 1;
+  }
+  n = lo;
+  j = slot - slot_base(a, n);
+  const int len = a.cu[n + 1] - a.cu[n];
+  return j >= 0 && j < (len + kBC - 1) / kBC;
+}
+
+// ------------------------------------------------------------- chunk setup
+
+// Shared-memory arrays of one chunk (row stride ld = dk + 1 for [C][dk]).
+struct ChunkSm {
+  int ld;
+  float *G, *Qb, *Kb, *GK, *Kh;  // [C][ld]
+  float *A, *M, *T;              // [C][C]
+  float *beta, *gam;             // [C], [dk]
+};
+
+__device__ __forceinline__ float *carve_chunk(ChunkSm &c, float *p, int dk) {
+  c.ld = dk + 1;
+  c.G = p;  p += kBC * c.ld;
+  c.Qb = p; p += kBC * c.ld;
+  c.Kb = p; p += kBC * c.ld;
+  c.GK = p; p += kBC * c.ld;
+  c.Kh = p; p += kBC * c.ld;
+  c.A = p;  p += kBC * kBC;
+  c.M = p;  p += kBC * kBC;
+  c.T = p;  p += kBC * kBC;
+  c.beta = p; p += kBC;
+  c.gam = p;  p += 128;
+  return p;
+}
+
+// Loads the chunk's rows [t0, t0 + len) of head h (rows past len are the
+// identity step: q = k = 0, g = 0, beta = 0) and forms G, Qb, Kb, GK, Kh,
+// gamma, A, M and T = (I + L)^-1.  Ends with a barrier.
+__device__ void setup_chunk(const BwdArgs &a, const ChunkSm &c, int t0, int len, int h) {
+  const int dk = a.dk, H = a.H, ld = c.ld, tid = threadIdx.x;
+  for (int e = tid; e < kBC * dk; e += kBThreads) {
+    const int r = e / dk, i = e % dk;
+    float qv = 0.f, kv = 0.f, gv = 0.f;
+    if (r < len) {
+      const size_t idx = ((size_t)(t0 + r) * H + h) * dk + i;
+      qv = ld_elem(a.q, idx, a.qkv);
+      kv = ld_elem(a.k, idx, a.qkv);
+      gv = ld_elem(a.g, idx, a.gate);
+    }
+    c.Qb[r * ld + i] = qv;
+    c.Kb[r * ld + i] = kv;
+    c.G[r * ld + i] = gv;
+  }
+  if (tid < kBC) c.beta[tid] = tid < len ? ld_elem(a.beta, (size_t)(t0 + tid) * H + h, a.gate) : 0.f;
+  __syncthreads();
+  if (tid < dk) {  // within-chunk cumulative log-decay, per channel
+    float acc = 0.f;
+    for (int r = 0; r < kBC; ++r) {
+      acc += c.G[r * ld + tid];
+      c.G[r * ld + tid] = acc;
+    }
+    c.gam[tid] = expf(acc);
+  }
+  __syncthreads();
+  for (int e = tid; e < kBC * dk; e += kBThreads) {
+    const int r = e / dk, i = e % dk;
+    const float G = c.G[r * ld + i], Gl = c.G[(kBC - 1) * ld + i];
+    const float kv = c.Kb[r * ld + i];
+    const float eg = expf(G);
+    c.Qb[r * ld + i] *= eg;
+    c.GK[r * ld + i] = kv * eg;
+    c.Kb[r * ld + i] = kv * expf(-G);
+    c.Kh[r * ld + i] = kv * expf(Gl - G);
+  }
+  __syncthreads();
+  {  // one thread per (r, s): A and M
+    const int r = tid / kBC, s = tid % kBC;
+    float accA = 0.f, accM = 0.f;
+    if (s <= r) {
+      for (int i = 0; i < dk; ++i) {
+        const float kb = c.Kb[s * ld + i];
+        accA += c.Qb[r * ld + i] * kb;
+        accM += c.GK[r * ld + i] * kb;
+      }
+    }
+    c.A[tid] = accA;
+    c.M[tid] = s < r ? accM : 0.f;
+  }
+  __syncthreads();
+  if (tid < kBC) {  // T = (I + L)^-1, L = diag(beta) M: one column per thread
+    const int s = tid;
+    for (int r = 0; r < kBC; ++r) c.T[r * kBC + s] = r == s ? 1.f : 0.f;
+    for (int r = s + 1; r < kBC; ++r) {
+      float acc = 0.f;
+      for (int m = s; m < r; ++m) acc += c.beta[r] * c.M[r * kBC + m] * c.T[m * kBC + s];
+      c.T[r * kBC + s] = -acc;
+    }
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ kernels
+
+__global__ void __launch_bounds__(kBThreads) bwd_prep_kernel(BwdArgs a) {
+  extern __shared__ float smem[];
+  const int slot = blockIdx.x, h = blockIdx.y;
+  int n, j;
+  if (!locate(a, slot, n, j)) return;
+  int bos, eos;
+  bounds(a, n, bos, eos);
+  const int t0 = bos + j * kBC, len = min(kBC, eos - t0);
+  ChunkSm c;
+  carve_chunk(c, smem, a.dk);
+  setup_chunk(a, c, t0, len, h);
+  const int dk = a.dk, ld = c.ld;
+  const size_t sh = (size_t)slot * a.H + h;
+  float *Qb = a.Qb + sh * kBC * dk, *Kh = a.Kh + sh * kBC * dk, *W = a.W + sh * kBC * dk;
+  for (int e = threadIdx.x; e < kBC * dk; e += kBThreads) {
+    const int r = e / dk, i = e % dk;
+    float w = 0.f;  // W = T diag(beta) GK
+    for (int s = 0; s <= r; ++s) w += c.T[r * kBC + s] * c.beta[s] * c.GK[s * ld + i];
+    Qb[e] = c.Qb[r * ld + i];
+    Kh[e] = c.Kh[r * ld + i];
+    W[e] = w;
+  }
+  for (int e = threadIdx.x; e < kBC * kBC; e += kBThreads) {
+    a.A[sh * kBC * kBC + e] = c.A[e];
+    a.T[sh * kBC * kBC + e] = c.T[e];
+  }
+  for (int i = threadIdx.x; i < dk; i += kBThreads) a.gam[sh * dk + i] = c.gam[i];
+}
+
+// The state (kReverse false) or the state gradient (kReverse true) across the
+// chunks of one sequence, for kScanDvt state columns.  Forward: records the
+// entry state of each chunk, then S <- diag(gamma) S + Kh^T T_b (V - GK S)
+// (with W = T_b GK: V~ = T_b V - W S).  Reverse: records the gradient after
+// each chunk, then dS <- diag(gamma) dS + Qb^T dO - W^T (Kh dS + A^T dO).
+template <bool kReverse>
+__global__ void __launch_bounds__(kBThreads) bwd_scan_kernel(BwdArgs a) {
+  extern __shared__ float smem[];
+  const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H;
+  const int c0 = blockIdx.y * kScanDvt;
+  const int dk = a.dk, dv = a.dv, H = a.H, tid = threadIdx.x;
+  const int dvt = min(kScanDvt, dv - c0);
+  constexpr int lds = kScanDvt + 1;
+  float *S = smem;                    // [dk][lds]
+  float *X = S + 128 * lds;           // [C][lds]: V or dO rows
+  float *Y = X + kBC * lds;           // [C][lds]: V~ or dV~
+  float *Wm = Y + kBC * lds;          // [C][dk]
+  float *Km = Wm + kBC * 128;         // [C][dk]: Kh
+  float *Qm = Km + kBC * 128;         // [C][dk]: Qb (reverse)
+  float *Cm = Qm + kBC * 128;         // [C][C]: T (forward) or A (reverse)
+  float *bet = Cm + kBC * kBC;        // [C]
+  float *gm = bet + kBC;              // [dk]
+  int bos, eos;
+  bounds(a, n, bos, eos);
+  const int nch = (eos - bos + kBC - 1) / kBC;
+  const int base = slot_base(a, n);
+  const size_t soff = ((size_t)n * H + h) * dk * dv;
+  for (int e = tid; e < dk * dvt; e += kBThreads) {
+    const int i = e / dvt, cc = e % dvt;
+    const float *src = kReverse ? a.dST : a.s0;
+    S[i * lds + cc] = src ? src[soff + (size_t)i * dv + c0 + cc] : 0.f;
+  }
+  for (int jj = 0; jj < nch; ++jj) {
+    const int j = kReverse ? nch - 1 - jj : jj;
+    const int t0 = bos + j * kBC, len = min(kBC, eos - t0);
+    const size_t sh = (size_t)(base + j) * H + h;
+    __syncthreads();  // S final for this chunk; the previous chunk's operands are consumed
+    float *rec = (kReverse ? a.dSx : a.Sent) + sh * dk * dv;
+    for (int e = tid; e < dk * dvt; e += kBThreads) {
+      const int i = e / dvt, cc = e % dvt;
+      rec[(size_t)i * dv + c0 + cc] = S[i * lds + cc];
+    }
+    for (int e = tid; e < kBC * dvt; e += kBThreads) {
+      const int r = e / dvt, cc = e % dvt;
+      float x = 0.f;
+      if (r < len) {
+        const size_t idx = ((size_t)(t0 + r) * H + h) * dv + c0 + cc;
+        x = kReverse ? ld_elem(a.dO, idx, a.out) : ld_elem(a.v, idx, a.qkv);
+      }
+      X[r * lds + cc] = x;
+    }
+    for (int e = tid; e < kBC * dk; e += kBThreads) {
+      Wm[e] = a.W[sh * kBC * dk + e];
+      Km[e] = a.Kh[sh * kBC * dk + e];
+      if (kReverse) Qm[e] = a.Qb[sh * kBC * dk + e];
+    }
+    for (int e = tid; e < kBC * kBC; e += kBThreads) Cm[e] = kReverse ? a.A[sh * kBC * kBC + e] : a.T[sh * kBC * kBC + e];
+    if (!kReverse && tid < kBC) bet[tid] = tid < len ? ld_elem(a.beta, (size_t)(t0 + tid) * H + h, a.gate) : 0.f;
+    for (int i = tid; i < dk; i += kBThreads) gm[i] = a.gam[sh * dk + i];
+    __syncthreads();
+    for (int e = tid; e < kBC * dvt; e += kBThreads) {
+      const int r = e / dvt, cc = e % dvt;
+      float y = 0.f;
+      if (!kReverse) {  // V~ = T_b V - W S
+        for (int s = 0; s <= r; ++s) y += Cm[r * kBC + s] * bet[s] * X[s * lds + cc];
+        for (int i = 0; i < dk; ++i) y -= Wm[r * dk + i] * S[i * lds + cc];
+      } else {          // dV~ = A^T dO + Kh dS
+        for (int s = r; s < kBC; ++s) y += Cm[s * kBC + r] * X[s * lds + cc];
+        for (int i = 0; i < dk; ++i) y += Km[r * dk + i] * S[i * lds + cc];
+      }
+      Y[r * lds + cc] = y;
+    }
+    __syncthreads();
+    for (int e = tid; e < dk * dvt; e += kBThreads) {
+      const int i = e / dvt, cc = e % dvt;
+      float s = gm[i] * S[i * lds + cc];
+      if (!kReverse) {
+        for (int r = 0; r < kBC; ++r) s += Km[r * dk + i] * Y[r * lds + cc];
+      } else {
+        for (int r = 0; r < kBC; ++r) s += Qm[r * dk + i] * X[r * lds + cc] - Wm[r * dk + i] * Y[r * lds + cc];
+      }
+      S[i * lds + cc] = s;
+    }
+  }
+  if (kReverse && a.gs0) {
+    __syncthreads();
+    for (int e = tid; e < dk * dvt; e += kBThreads) {
+      const int i = e / dvt, cc = e % dvt;
+      a.gs0[soff + (size_t)i * dv + c0 + cc] = S[i * lds + cc];
+    }
+  }
+}
+
+size_t scan_smem_bytes() {
+  return sizeof(float) * ((size_t)128 * (kScanDvt + 1) + 2 * kBC * (kScanDvt + 1) + 3 * kBC * 128 + kBC * kBC + kBC + 128);
+}
+
+// Gradients of one chunk's rows, from its entry state and the state gradient
+// after it, streaming the state in kGradDvt-column passes.
+__global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
+  extern __shared__ float smem[];
+  const int slot = blockIdx.x, h = blockIdx.y;
+  int n, j;
+  if (!locate(a, slot, n, j)) return;
+  int bos, eos;
+  bounds(a, n, bos, eos);
+  const int t0 = bos + j * kBC, len = min(kBC, eos - t0);
+  const int dk = a.dk, dv = a.dv, H = a.H, tid = threadIdx.x;
+  ChunkSm c;
+  float *p = carve_chunk(c, smem, dk);
+  const int ld = c.ld;
+  constexpr int lt = kGradDvt + 1;
+  float *dQb = p; p += kBC * ld;
+  float *dKb = p; p += kBC * ld;
+  float *dGK = p; p += kBC * ld;
+  float *dKh = p; p += kBC * ld;
+  float *dA = p;  p += kBC * kBC;
+  float *dTb = p; p += kBC * kBC;
+  float *X = p;   p += kBC * kBC;
+  float *dgam = p; p += 128;
+  float *Ss = p;  p += 128 * lt;   // S columns of this pass
+  float *dSs = p; p += 128 * lt;   // dS' columns
+  float *Vs = p;  p += kBC * lt;   // V, then P = V - GK S
+  float *dOs = p; p += kBC * lt;
+  float *Vt = p;  p += kBC * lt;
+  float *dVt = p; p += kBC * lt;
+  float *dVs = p; p += kBC * lt;
+  setup_chunk(a, c, t0, len, h);
+  for (int e = tid; e < kBC * ld; e += kBThreads) dQb[e] = dKb[e] = dGK[e] = dKh[e] = 0.f;
+  for (int e = tid; e < kBC * kBC; e += kBThreads) dA[e] = dTb[e] = 0.f;
+  for (int i = tid; i < dk; i += kBThreads) dgam[i] = 0.f;
+  const size_t sh = (size_t)slot * H + h;
+  const float *Sg = a.Sent + sh * dk * dv, *dSg = a.dSx + sh * dk * dv;
+  for (int c0 = 0; c0 < dv; c0 += kGradDvt) {
+    const int w = min(kGradDvt, dv - c0);
+    __syncthreads();  // the previous pass is done with the column buffers
+    for (int e = tid; e < dk * w; e += kBThreads) {
+      const int i = e / w, cc = e % w;
+      Ss[i * lt + cc] = Sg[(size_t)i * dv + c0 + cc];
+      dSs[i * lt + cc] = dSg[(size_t)i * dv + c0 + cc];
+    }
+    for (int e = tid; e < kBC * w; e += kBThreads) {
+      const int r = e / w, cc = e % w;
+      float vv = 0.f, dd = 0.f;
+      if (r < len) {
+        const size_t idx = ((size_t)(t0 + r) * H + h) * dv + c0 + cc;
+        vv = ld_elem(a.v, idx, a.qkv);
+        dd = ld_elem(a.dO, idx, a.out);
+      }
+      Vs[r * lt + cc] = vv;
+      dOs[r * lt + cc] = dd;
+    }
+    __syncthreads();
+    for (int e = tid; e < kBC * w; e += kBThreads) {  // P = V - GK S;  dV~ = Kh dS' + A^T dO
+      const int r = e / w, cc = e % w;
+      float z = 0.f, y = 0.f;
+      for (int i = 0; i < dk; ++i) {
+        z += c.GK[r * ld + i] * Ss[i * lt + cc];
+        y += c.Kh[r * ld + i] * dSs[i * lt + cc];
+      }
+      for (int s = r; s < kBC; ++s) y += c.A[s * kBC + r] * dOs[s * lt + cc];
+      Vs[r * lt + cc] -= z;
+      dVt[r * lt + cc] = y;
+    }
+    __syncthreads();
+    for (int e = tid; e < kBC * w; e += kBThreads) {  // V~ = T_b P;  dV = T_b^T dV~
+      const int r = e / w, cc = e % w;
+      float y = 0.f, d = 0.f;
+      for (int s = 0; s <= r; ++s) y += c.T[r * kBC + s] * c.beta[s] * Vs[s * lt + cc];
+      for (int s = r; s < kBC; ++s) d += c.T[s * kBC + r] * dVt[s * lt + cc];
+      d *= c.beta[r];
+      Vt[r * lt + cc] = y;
+      dVs[r * lt + cc] = d;
+      if (r < len) a.gv[((size_t)(t0 + r) * H + h) * dv + c0 + cc] = d;
+    }
+    __syncthreads();
+    for (int e = tid; e < kBC * dk; e += kBThreads) {  // the C x dk sums over this pass's columns
+      const int r = e / dk, i = e % dk;
+      float q = 0.f, kh = 0.f, gk = 0.f;
+      for (int cc = 0; cc < w; ++cc) {
+        const float s = Ss[i * lt + cc];
+        q += dOs[r * lt + cc] * s;
+        kh += Vt[r * lt + cc] * dSs[i * lt + cc];
+        gk += dVs[r * lt + cc] * s;
+      }
+      dQb[r * ld + i] += q;
+      dKh[r * ld + i] += kh;
+      dGK[r * ld + i] -= gk;
+    }
+    {  // the C x C sums: dT_b += dV~ P^T, dA += dO V~^T
+      const int r = tid / kBC, s = tid % kBC;
+      float tb = 0.f, da = 0.f;
+      for (int cc = 0; cc < w; ++cc) {
+        tb += dVt[r * lt + cc] * Vs[s * lt + cc];
+        da += dOs[r * lt + cc] * Vt[s * lt + cc];
+      }
+      dTb[tid] += tb;
+      dA[tid] += da;
+    }
+    for (int i = tid; i < dk; i += kBThreads) {
+      float gsum = 0.f;
+      for (int cc = 0; cc < w; ++cc) gsum += dSs[i * lt + cc] * Ss[i * lt + cc];
+      dgam[i] += gsum;
+    }
+  }
+  __syncthreads();
+  // through T_b = T diag(beta) and T = (I + L)^-1:  X = T^T (dT_b diag(beta))
+  {
+    const int r = tid / kBC, s = tid % kBC;
+    float x = 0.f;
+    for (int m = 0; m < kBC; ++m) x += c.T[m * kBC + r] * dTb[m * kBC + s] * c.beta[s];
+    X[tid] = x;
+  }
+  __syncthreads();
+  {
+    // dL[r][s] = -(X T^T)[r][s] below the diagonal, then in X's place
+    const int r = tid / kBC, s = tid % kBC;
+    float dl = 0.f;
+    if (s < r)
+      for (int m = 0; m < kBC; ++m) dl -= X[r * kBC + m] * c.T[s * kBC + m];
+    __syncthreads();
+    X[tid] = dl;
+  }
+  __syncthreads();
+  if (tid < kBC) {  // dbeta_r = sum_s dT_b[s][r] T[s][r] + sum_{s<r} dL[r][s] M[r][s]
+    const int r = tid;
+    float acc = 0.f;
+    for (int s = 0; s < kBC; ++s) acc += dTb[s * kBC + r] * c.T[s * kBC + r];
+    for (int s = 0; s < r; ++s) acc += X[r * kBC + s] * c.M[r * kBC + s];
+    if (r < len) a.gbeta[(size_t)(t0 + r) * H + h] = acc;
+  }
+  __syncthreads();
+  {
+    const int r = tid / kBC, s = tid % kBC;
+    X[tid] *= c.beta[r];                   // dM = diag(beta) dL
+    if (s > r) dA[tid] = 0.f;              // Tril_incl
+  }
+  __syncthreads();
+  for (int e = tid; e < kBC * dk; e += kBThreads) {
+    const int r = e / dk, i = e % dk;
+    float gk = 0.f, kb = 0.f, qb = 0.f;
+    for (int s = 0; s < kBC; ++s) {
+      gk += X[r * kBC + s] * c.Kb[s * ld + i];      // dM Kb
+      kb += X[s * kBC + r] * c.GK[s * ld + i]       // dM^T GK
+            + dA[s * kBC + r] * c.Qb[s * ld + i];   // dA^T Qb
+      qb += dA[r * kBC + s] * c.Kb[s * ld + i];     // dA Kb
+    }
+    dGK[r * ld + i] += gk;
+    dKb[r * ld + i] = kb;
+    dQb[r * ld + i] += qb;
+  }
+  __syncthreads();
+  // elementwise to q, k and the cumulative log-decay G (dG in G's place)
+  for (int e = tid; e < kBC * dk; e += kBThreads) {
+    const int r = e / dk, i = e % dk;
+    const float G = c.G[r * ld + i], Gl = c.G[(kBC - 1) * ld + i];
+    const float eg = expf(G), ei = expf(-G), eh = expf(Gl - G);
+    const float q = dQb[r * ld + i], kb = dKb[r * ld + i], gk = dGK[r * ld + i], kh = dKh[r * ld + i];
+    if (r < len) {
+      const size_t idx = ((size_t)(t0 + r) * H + h) * dk + i;
+      a.gq[idx] = q * eg;
+      a.gk[idx] = kb * ei + gk * eg + kh * eh;
+    }
+    dKb[r * ld + i] = q * c.Qb[r * ld + i] - kb * c.Kb[r * ld + i] + gk * c.GK[r * ld + i] - kh * c.Kh[r * ld + i];
+  }
+  __syncthreads();
+  if (tid < dk) {  // G_last terms, then the reverse cumulative sum over rows
+    const int i = tid;
+    float last = dgam[i] * c.gam[i];
+    for (int r = 0; r < kBC; ++r) last += dKh[r * ld + i] * c.Kh[r * ld + i];
+    float acc = last;
+    for (int r = kBC - 1; r >= 0; --r) {
+      acc += dKb[r * ld + i];
+      if (r < len) a.gg[((size_t)(t0 + r) * H + h) * dk + i] = acc;
+    }
+  }
+}
+
+size_t grads_smem_bytes(int dk) {
+  const size_t ld = (size_t)dk + 1;
+  return sizeof(float) * (9 * kBC * ld + 6 * kBC * kBC + kBC + 2 * 128 + 2 * 128 * (kGradDvt + 1) +
+                          5 * kBC * (kGradDvt + 1));
+}
+
+size_t prep_smem_bytes(int dk) {
+  const size_t ld = (size_t)dk + 1;
+  return sizeof(float) * (5 * kBC * ld + 3 * kBC * kBC + kBC + 128);
+}
+
+}  // namespace
+
+int bwd_slots(const PrefillArgs &p) {
+  return p.cu ? p.T_total / kBC + p.N : p.N * ((p.T_seq + kBC - 1) / kBC);
+}
+
+size_t bwd_workspace_bytes(const PrefillArgs &p) {
+  const size_t per = (size_t)3 * kBC * p.dk + 2 * kBC * kBC + p.dk + 2 * (size_t)p.dk * p.dv;
+  return sizeof(float) * per * (size_t)bwd_slots(p) * p.H;
+}
+
+cudaError_t launch_chunk_bwd(const PrefillArgs &p, const BwdIo &io, void *ws, cudaStream_t s) {
+  BwdArgs a;
+  a.N = p.N; a.T_total = p.T_total; a.T_seq = p.T_seq; a.H = p.H; a.dk = p.dk; a.dv = p.dv;
+  a.qkv = p.qkv; a.out = p.out; a.gate = p.gate;
+  a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta; a.s0 = p.s0; a.cu = p.cu;
+  a.dO = io.dO; a.dST = io.dST;
+  a.gq = io.dq; a.gk = io.dk; a.gv = io.dv; a.gg = io.dg; a.gbeta = io.dbeta; a.gs0 = io.ds0;
+  a.nslots = bwd_slots(p);
+  const size_t sl = (size_t)a.nslots * p.H;
+  float *w = reinterpret_cast<float *>(ws);
+  a.Qb = w;  w += sl * kBC * p.dk;
+  a.Kh = w;  w += sl * kBC * p.dk;
+  a.W = w;   w += sl * kBC * p.dk;
+  a.A = w;   w += sl * kBC * kBC;
+  a.T = w;   w += sl * kBC * kBC;
+  a.gam = w; w += sl * p.dk;
+  a.Sent = w; w += sl * (size_t)p.dk * p.dv;
+  a.dSx = w;
+  if (a.N * a.H == 0) return cudaSuccess;
+  cudaError_t e;
+  if (a.nslots > 0) {
+    const size_t sp = prep_smem_bytes(p.dk);
+    e = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
+    if (e != cudaSuccess) return e;
+    bwd_prep_kernel<<<dim3(a.nslots, p.H), kBThreads, sp, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const size_t ss = scan_smem_bytes();
+  const dim3 sgrid(p.N * p.H, (p.dv + kScanDvt - 1) / kScanDvt);
+  e = cudaFuncSetAttribute(bwd_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+  if (e != cudaSuccess) return e;
+  bwd_scan_kernel<false><<<sgrid, kBThreads, ss, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_scan_kernel<true><<<sgrid, kBThreads, ss, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.nslots > 0) {
+    const size_t sg = grads_smem_bytes(p.dk);
+    e = cudaFuncSetAttribute(bwd_grads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg);
+    if (e != cudaSuccess) return e;
+    bwd_grads_kernel<<<dim3(a.nslots, p.H), kBThreads, sg, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace kda

@@ -102,6 +102,17 @@ bool chunk_tc_supports(const PrefillArgs &a);
 cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s);
 cudaError_t read_tc_watchdog(unsigned int *flags, bool clear);
 
+// Backward of the chunked prefill (kda_bwd.cu).  dO in the forward's out
+// dtype; dST and ds0 nullable; every gradient fp32.
+struct BwdIo {
+  const void *dO;
+  const float *dST;
+  float *dq, *dk, *dv, *dg, *dbeta, *ds0;
+};
+int bwd_slots(const PrefillArgs &p);
+size_t bwd_workspace_bytes(const PrefillArgs &p);
+cudaError_t launch_chunk_bwd(const PrefillArgs &p, const BwdIo &io, void *ws, cudaStream_t s);
+
 // Segment plan for long sequences (kda_cp.cu).
 struct SegPlan {
   int P;              // segments per sequence (1: no split)

@@ -241,6 +241,47 @@ kda_status kda_layer_decode_step(const kda_decode_desc *desc, const kda_layer_ga
                                  const void *beta, float *state_inout, void *out,
                                  kda_stream_t stream);
 
+/*
+ * kda_chunk_bwd - gradients of kda_chunk_fwd, for training (the chunkwise form
+ * of [K3-notes §2.2] is the training form; the page prints no backward, and
+ * this one is the exact derivative of the forward's mathematics).  For the
+ * scalar L = sum_t <d_out_t, o_t> + sum_n <d_final_state_n, S_T(n)> it writes
+ *
+ *   dq, dk       [B*T, H, dk] fp32    dL/dq, dL/dk
+ *   dv           [B*T, H, dv] fp32    dL/dv
+ *   dlog_alpha   [B*T, H, dk] fp32    dL/dlog_alpha
+ *   dbeta        [B*T, H]     fp32    dL/dbeta
+ *   d_initial_state [Nseq, H, dk, dv] fp32, or NULL   dL/dinitial_state
+ *
+ * from the forward's inputs (same arguments and conventions as kda_chunk_fwd;
+ * initial_state NULL = zeros) and
+ *   d_out          [B*T, H, dv] out_dtype   (gradient of out)
+ *   d_final_state  [Nseq, H, dk, dv] fp32, or NULL for zero.
+ * The forward is recomputed inside; nothing of it needs to be kept.  The
+ * gradients do not depend on desc->chunk (the backward works on 16-token
+ * chunks, the tile within which the decay floor keeps every factor in fp32
+ * range); desc->segments is ignored and desc->kernel = KDA_KERNEL_TC returns
+ * KDA_ERR_UNSUPPORTED (the backward runs on CUDA cores, in fp32).
+ *
+ *   workspace  device buffer of kda_chunk_bwd_workspace_size bytes, 16-byte
+ *              aligned, or NULL: then the call allocates it stream-ordered
+ *              (cudaMallocAsync / cudaFreeAsync on `stream`).  It holds, per
+ *              16-token chunk and head, the state before the chunk and the
+ *              state gradient after it (2 dk dv floats) and 3 C dk + 2 C^2 + dk
+ *              floats of chunk matrices: about 130 KB per 16 tokens per head at
+ *              dk = dv = 128.
+ * Gradients may alias no input and no other gradient (KDA_ERR_ALIAS); all
+ * pointers 4-byte aligned except q, k, v, log_alpha, d_out (16 bytes, as the
+ * forward's q/k/v/log_alpha/out).
+ */
+kda_status kda_chunk_bwd_workspace_size(const kda_chunk_desc *desc, size_t *bytes);
+kda_status kda_chunk_bwd(const kda_chunk_desc *desc, const void *q, const void *k, const void *v,
+                         const void *log_alpha, const void *beta, const float *initial_state,
+                         const int32_t *cu_seqlens, const void *d_out, const float *d_final_state,
+                         float *dq, float *dk, float *dv, float *dlog_alpha, float *dbeta,
+                         float *d_initial_state, void *workspace, size_t workspace_bytes,
+                         kda_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *kda_status_string(kda_status status);
 

@@ -181,3 +181,24 @@ def test_layer_argument_errors(lib):
     assert dec(None) == -1
     assert dec(gates(g_min=-5.5)) == -5
     assert dec(gates(og=FAKE * 7)) == -8                     # out_gate aliases the state
+
+
+def test_backward_argument_errors(lib):
+    P = ctypes.c_void_p
+
+    def bwd(d=None, dq=FAKE * 20, dk=FAKE * 21, dv=FAKE * 22, dg=FAKE * 23, db=FAKE * 24, ws=None, ws_bytes=0):
+        d = d or _desc()
+        return lib.kda_chunk_bwd(ctypes.byref(d), P(FAKE), P(FAKE * 2), P(FAKE * 3), P(FAKE * 4), P(FAKE * 5),
+                                 None, None, P(FAKE * 6), None, P(dq) if dq else None, P(dk), P(dv), P(dg), P(db),
+                                 None, P(ws) if ws else None, ws_bytes, None)
+
+    assert bwd(d=_desc(kernel=2)) == -7          # no tensor-core backward
+    assert bwd(dq=None) == -1
+    assert bwd(dq=FAKE) == -8                    # dq aliases q
+    assert bwd(dk=FAKE * 20) == -8               # two gradients overlap
+    assert bwd(db=FAKE * 24 + 2) == -4
+    n = ctypes.c_size_t(0)
+    assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(_desc()), ctypes.byref(n)) == 0
+    # 8 chunks of 16 tokens x 2 heads x (3*16*64 + 2*256 + 64 + 2*64*64) floats
+    assert n.value == 8 * 2 * (3 * 16 * 64 + 2 * 256 + 64 + 2 * 64 * 64) * 4
+    assert bwd(ws=FAKE * 40, ws_bytes=n.value - 4) == -2
