@@ -221,26 +221,36 @@ __global__ void __launch_bounds__(kBThreads) bwd_prep_kernel(BwdArgs a) {
 
 // The state (kReverse false) or the state gradient (kReverse true) across the
 // chunks of one sequence, for kScanDvt state columns.  Forward: records the
-// entry state of each chunk, then S <- diag(gamma) S + Kh^T T_b (V - GK S)
-// (with W = T_b GK: V~ = T_b V - W S).  Reverse: records the gradient after
-// each chunk, then dS <- diag(gamma) dS + Qb^T dO - W^T (Kh dS + A^T dO).
+// entry state of each chunk, then S <- diag(gamma) S + Kh^T (T_b V - W S).
+// Reverse: records the gradient after each chunk, then
+// dS <- diag(gamma) dS + Qb^T dO - W^T (Kh dS + A^T dO).
+// Products are register-tiled: the C x dvt product Y = (W or Kh) S is split
+// over dk between thread groups (2 x 4 outputs per thread, partial sums
+// meeting in shared memory), the dk x dvt update takes 4 x 4 outputs per
+// thread from 128-bit shared loads.
+constexpr int kSP = kScanDvt + 4;  // row stride of the [.][dvt] arrays (16-byte rows)
+
 template <bool kReverse>
 __global__ void __launch_bounds__(kBThreads) bwd_scan_kernel(BwdArgs a) {
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) float smem[];
   const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H;
-  const int c0 = blockIdx.y * kScanDvt;
+  const int c0g = blockIdx.y * kScanDvt;
   const int dk = a.dk, dv = a.dv, H = a.H, tid = threadIdx.x;
-  const int dvt = min(kScanDvt, dv - c0);
-  constexpr int lds = kScanDvt + 1;
-  float *S = smem;                    // [dk][lds]
-  float *X = S + 128 * lds;           // [C][lds]: V or dO rows
-  float *Y = X + kBC * lds;           // [C][lds]: V~ or dV~
-  float *Wm = Y + kBC * lds;          // [C][dk]
-  float *Km = Wm + kBC * 128;         // [C][dk]: Kh
-  float *Qm = Km + kBC * 128;         // [C][dk]: Qb (reverse)
-  float *Cm = Qm + kBC * 128;         // [C][C]: T (forward) or A (reverse)
-  float *bet = Cm + kBC * kBC;        // [C]
-  float *gm = bet + kBC;              // [dk]
+  const int dvt = min(kScanDvt, dv - c0g);   // 16 or 32
+  const int ncb = dvt / 4;                   // 4-column blocks
+  const int nblk = 8 * ncb;                  // (row pair, column block) tasks of the C x dvt product
+  const int nsplit = kBThreads / nblk;       // dk split of that product
+  const int ilen = dk / nsplit;
+  float *S = smem;                     // [128][kSP]
+  float *X = S + 128 * kSP;            // [C][kSP]: V or dO rows
+  float *Y = X + kBC * kSP;            // [C][kSP]: V~ or dV~
+  float *red = Y + kBC * kSP;          // [8][C][kSP]: partial sums
+  float *Wm = red + 8 * kBC * kSP;     // [C][dk]
+  float *Km = Wm + kBC * 128;          // [C][dk]: Kh
+  float *Qm = Km + kBC * 128;          // [C][dk]: Qb (reverse)
+  float *Cm = Qm + kBC * 128;          // [C][C]: T (forward) or A (reverse)
+  float *bet = Cm + kBC * kBC;         // [C]
+  float *gm = bet + kBC;               // [dk]
   int bos, eos;
   bounds(a, n, bos, eos);
   const int nch = (eos - bos + kBC - 1) / kBC;
@@ -249,71 +259,124 @@ __global__ void __launch_bounds__(kBThreads) bwd_scan_kernel(BwdArgs a) {
   for (int e = tid; e < dk * dvt; e += kBThreads) {
     const int i = e / dvt, cc = e % dvt;
     const float *src = kReverse ? a.dST : a.s0;
-    S[i * lds + cc] = src ? src[soff + (size_t)i * dv + c0 + cc] : 0.f;
+    S[i * kSP + cc] = src ? src[soff + (size_t)i * dv + c0g + cc] : 0.f;
   }
+  // tasks: the C x dvt product (row pair rp, column block cb, dk split sp) and
+  // the dk x dvt update (rows i0..i0+3, columns c0..c0+3)
+  const int blk = tid % nblk, sp = tid / nblk;
+  const int r0 = 2 * (blk / ncb), cy = 4 * (blk % ncb);
+  const int ib = tid / ncb, i0 = 4 * ib, cu0 = 4 * (tid % ncb);
+  const bool upd = i0 < dk;
   for (int jj = 0; jj < nch; ++jj) {
     const int j = kReverse ? nch - 1 - jj : jj;
     const int t0 = bos + j * kBC, len = min(kBC, eos - t0);
     const size_t sh = (size_t)(base + j) * H + h;
     __syncthreads();  // S final for this chunk; the previous chunk's operands are consumed
     float *rec = (kReverse ? a.dSx : a.Sent) + sh * dk * dv;
-    for (int e = tid; e < dk * dvt; e += kBThreads) {
-      const int i = e / dvt, cc = e % dvt;
-      rec[(size_t)i * dv + c0 + cc] = S[i * lds + cc];
-    }
+    if (upd)
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        *reinterpret_cast<float4 *>(rec + (size_t)(i0 + r) * dv + c0g + cu0) =
+            *reinterpret_cast<const float4 *>(S + (i0 + r) * kSP + cu0);
     for (int e = tid; e < kBC * dvt; e += kBThreads) {
       const int r = e / dvt, cc = e % dvt;
       float x = 0.f;
       if (r < len) {
-        const size_t idx = ((size_t)(t0 + r) * H + h) * dv + c0 + cc;
+        const size_t idx = ((size_t)(t0 + r) * H + h) * dv + c0g + cc;
         x = kReverse ? ld_elem(a.dO, idx, a.out) : ld_elem(a.v, idx, a.qkv);
       }
-      X[r * lds + cc] = x;
+      X[r * kSP + cc] = x;
     }
-    for (int e = tid; e < kBC * dk; e += kBThreads) {
-      Wm[e] = a.W[sh * kBC * dk + e];
-      Km[e] = a.Kh[sh * kBC * dk + e];
-      if (kReverse) Qm[e] = a.Qb[sh * kBC * dk + e];
+    {
+      const float4 *w4 = reinterpret_cast<const float4 *>(a.W + sh * kBC * dk);
+      const float4 *k4 = reinterpret_cast<const float4 *>(a.Kh + sh * kBC * dk);
+      const float4 *q4 = reinterpret_cast<const float4 *>(a.Qb + sh * kBC * dk);
+      for (int e = tid; e < kBC * dk / 4; e += kBThreads) {
+        reinterpret_cast<float4 *>(Wm)[e] = w4[e];
+        reinterpret_cast<float4 *>(Km)[e] = k4[e];
+        if (kReverse) reinterpret_cast<float4 *>(Qm)[e] = q4[e];
+      }
     }
-    for (int e = tid; e < kBC * kBC; e += kBThreads) Cm[e] = kReverse ? a.A[sh * kBC * kBC + e] : a.T[sh * kBC * kBC + e];
+    Cm[tid] = kReverse ? a.A[sh * kBC * kBC + tid] : a.T[sh * kBC * kBC + tid];  // kBThreads == C * C
     if (!kReverse && tid < kBC) bet[tid] = tid < len ? ld_elem(a.beta, (size_t)(t0 + tid) * H + h, a.gate) : 0.f;
     for (int i = tid; i < dk; i += kBThreads) gm[i] = a.gam[sh * dk + i];
     __syncthreads();
-    for (int e = tid; e < kBC * dvt; e += kBThreads) {
-      const int r = e / dvt, cc = e % dvt;
-      float y = 0.f;
-      if (!kReverse) {  // V~ = T_b V - W S
-        for (int s = 0; s <= r; ++s) y += Cm[r * kBC + s] * bet[s] * X[s * lds + cc];
-        for (int i = 0; i < dk; ++i) y -= Wm[r * dk + i] * S[i * lds + cc];
-      } else {          // dV~ = A^T dO + Kh dS
-        for (int s = r; s < kBC; ++s) y += Cm[s * kBC + r] * X[s * lds + cc];
-        for (int i = 0; i < dk; ++i) y += Km[r * dk + i] * S[i * lds + cc];
+    {  // partial (W S) or (Kh S) over this thread's slice of dk
+      const float *Mm = kReverse ? Km : Wm;
+      float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+      const int ia = sp * ilen;
+#pragma unroll 4
+      for (int i = ia; i < ia + ilen; ++i) {
+        const float4 s4 = *reinterpret_cast<const float4 *>(S + i * kSP + cy);
+        const float m0 = Mm[r0 * dk + i], m1 = Mm[(r0 + 1) * dk + i];
+        acc0.x += m0 * s4.x; acc0.y += m0 * s4.y; acc0.z += m0 * s4.z; acc0.w += m0 * s4.w;
+        acc1.x += m1 * s4.x; acc1.y += m1 * s4.y; acc1.z += m1 * s4.z; acc1.w += m1 * s4.w;
       }
-      Y[r * lds + cc] = y;
+      *reinterpret_cast<float4 *>(red + (sp * kBC + r0) * kSP + cy) = acc0;
+      *reinterpret_cast<float4 *>(red + (sp * kBC + r0 + 1) * kSP + cy) = acc1;
     }
     __syncthreads();
-    for (int e = tid; e < dk * dvt; e += kBThreads) {
-      const int i = e / dvt, cc = e % dvt;
-      float s = gm[i] * S[i * lds + cc];
-      if (!kReverse) {
-        for (int r = 0; r < kBC; ++r) s += Km[r * dk + i] * Y[r * lds + cc];
-      } else {
-        for (int r = 0; r < kBC; ++r) s += Qm[r * dk + i] * X[r * lds + cc] - Wm[r * dk + i] * Y[r * lds + cc];
+    for (int e = tid; e < kBC * dvt; e += kBThreads) {
+      const int r = e / dvt, cc = e % dvt;
+      float part = 0.f;
+      for (int q = 0; q < nsplit; ++q) part += red[(q * kBC + r) * kSP + cc];
+      float y = 0.f;
+      if (!kReverse) {  // V~ = T_b V - W S
+        for (int s = 0; s <= r; ++s) y += Cm[r * kBC + s] * bet[s] * X[s * kSP + cc];
+        y -= part;
+      } else {          // dV~ = A^T dO + Kh dS
+        for (int s = r; s < kBC; ++s) y += Cm[s * kBC + r] * X[s * kSP + cc];
+        y += part;
       }
-      S[i * lds + cc] = s;
+      Y[r * kSP + cc] = y;
+    }
+    __syncthreads();
+    if (upd) {  // rows i0..i0+3, columns cu0..cu0+3 of the new S
+      float4 sv[4];
+      float g4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        sv[q] = *reinterpret_cast<const float4 *>(S + (i0 + q) * kSP + cu0);
+        g4[q] = gm[i0 + q];
+        sv[q].x *= g4[q]; sv[q].y *= g4[q]; sv[q].z *= g4[q]; sv[q].w *= g4[q];
+      }
+#pragma unroll 4
+      for (int r = 0; r < kBC; ++r) {
+        const float4 y4 = *reinterpret_cast<const float4 *>(Y + r * kSP + cu0);
+        if (!kReverse) {
+          const float4 k4 = *reinterpret_cast<const float4 *>(Km + r * dk + i0);
+          const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            sv[q].x += kk[q] * y4.x; sv[q].y += kk[q] * y4.y; sv[q].z += kk[q] * y4.z; sv[q].w += kk[q] * y4.w;
+          }
+        } else {
+          const float4 o4 = *reinterpret_cast<const float4 *>(X + r * kSP + cu0);
+          const float4 q4 = *reinterpret_cast<const float4 *>(Qm + r * dk + i0);
+          const float4 w4 = *reinterpret_cast<const float4 *>(Wm + r * dk + i0);
+          const float qq[4] = {q4.x, q4.y, q4.z, q4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            sv[q].x += qq[q] * o4.x - ww[q] * y4.x; sv[q].y += qq[q] * o4.y - ww[q] * y4.y;
+            sv[q].z += qq[q] * o4.z - ww[q] * y4.z; sv[q].w += qq[q] * o4.w - ww[q] * y4.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<float4 *>(S + (i0 + q) * kSP + cu0) = sv[q];
     }
   }
   if (kReverse && a.gs0) {
     __syncthreads();
     for (int e = tid; e < dk * dvt; e += kBThreads) {
       const int i = e / dvt, cc = e % dvt;
-      a.gs0[soff + (size_t)i * dv + c0 + cc] = S[i * lds + cc];
+      a.gs0[soff + (size_t)i * dv + c0g + cc] = S[i * kSP + cc];
     }
   }
 }
 
 size_t scan_smem_bytes() {
-  return sizeof(float) * ((size_t)128 * (kScanDvt + 1) + 2 * kBC * (kScanDvt + 1) + 3 * kBC * 128 + kBC * kBC + kBC + 128);
+  return sizeof(float) * ((size_t)128 * kSP + 2 * kBC * kSP + 8 * kBC * kSP + 3 * kBC * 128 + kBC * kBC + kBC + 128);
 }
 
 // Gradients of one chunk's rows, from its entry state and the state gradient
