@@ -40,6 +40,7 @@ constexpr int kBC = 16;       // tokens per backward chunk
 constexpr int kBThreads = 256;
 constexpr int kScanDvt = 32;  // state columns per scan CTA
 constexpr int kGradDvt = 16;  // state columns per pass of the gradient kernel
+static_assert(kBThreads == kBC * kBC && kBThreads == kBC * kGradDvt, "one thread per C x C and C x pass element");
 
 struct BwdArgs {
   int N, T_total, T_seq, H, dk, dv;
@@ -99,7 +100,7 @@ __device__ bool locate(const BwdArgs &a, int slot, int &n, int &j) {
 
 // ------------------------------------------------------------- chunk setup
 
-// Shared-memory arrays of one chunk (row stride ld = dk + 1 for [C][dk]).
+// Shared-memory arrays of one chunk (row stride ld = dk + 4 for [C][dk]).
 struct ChunkSm {
   int ld;
   float *G, *Qb, *Kb, *GK, *Kh;  // [C][ld]
@@ -108,7 +109,7 @@ struct ChunkSm {
 };
 
 __device__ __forceinline__ float *carve_chunk(ChunkSm &c, float *p, int dk) {
-  c.ld = dk + 1;
+  c.ld = dk + 4;  // 16-byte rows
   c.G = p;  p += kBC * c.ld;
   c.Qb = p; p += kBC * c.ld;
   c.Kb = p; p += kBC * c.ld;
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(kBThreads) bwd_prep_kernel(BwdArgs a) {
 constexpr int kSP = kScanDvt + 4;  // row stride of the [.][dvt] arrays (16-byte rows)
 
 template <bool kReverse>
-__global__ void __launch_bounds__(kBThreads) bwd_scan_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
   extern __shared__ __align__(16) float smem[];
   const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H;
   const int c0g = blockIdx.y * kScanDvt;
@@ -241,14 +242,14 @@ __global__ void __launch_bounds__(kBThreads) bwd_scan_kernel(BwdArgs a) {
   const int nblk = 8 * ncb;                  // (row pair, column block) tasks of the C x dvt product
   const int nsplit = kBThreads / nblk;       // dk split of that product
   const int ilen = dk / nsplit;
-  float *S = smem;                     // [128][kSP]
-  float *X = S + 128 * kSP;            // [C][kSP]: V or dO rows
-  float *Y = X + kBC * kSP;            // [C][kSP]: V~ or dV~
-  float *red = Y + kBC * kSP;          // [8][C][kSP]: partial sums
-  float *Wm = red + 8 * kBC * kSP;     // [C][dk]
-  float *Km = Wm + kBC * 128;          // [C][dk]: Kh
-  float *Qm = Km + kBC * 128;          // [C][dk]: Qb (reverse)
-  float *Cm = Qm + kBC * 128;          // [C][C]: T (forward) or A (reverse)
+  float *S = smem;                     // [dk][kSP]
+  float *X = S + dk * kSP;             // [C][kSP]: V or dO rows
+  float *red = X + kBC * kSP;          // [nsplit][C][kSP]: partial sums
+  float *Y = red;                      // [C][kSP]: V~ or dV~, over the first partial sums
+  float *Wm = red + nsplit * kBC * kSP;  // [C][dk]
+  float *Km = Wm + kBC * dk;           // [C][dk]: Kh
+  float *Qm = Km + kBC * dk;           // [C][dk]: Qb (reverse only)
+  float *Cm = Qm + (kReverse ? kBC * dk : 0);  // [C][C]: T (forward) or A (reverse)
   float *bet = Cm + kBC * kBC;         // [C]
   float *gm = bet + kBC;               // [dk]
   int bos, eos;
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kBThreads) bwd_scan_kernel(BwdArgs a) {
       *reinterpret_cast<float4 *>(red + (sp * kBC + r0 + 1) * kSP + cy) = acc1;
     }
     __syncthreads();
-    for (int e = tid; e < kBC * dvt; e += kBThreads) {
+    for (int e = tid; e < kBC * dvt; e += kBThreads) {  // (each (r, cc) is read and then written by one thread)
       const int r = e / dvt, cc = e % dvt;
       float part = 0.f;
       for (int q = 0; q < nsplit; ++q) part += red[(q * kBC + r) * kSP + cc];
@@ -375,14 +376,19 @@ __global__ void __launch_bounds__(kBThreads) bwd_scan_kernel(BwdArgs a) {
   }
 }
 
-size_t scan_smem_bytes() {
-  return sizeof(float) * ((size_t)128 * kSP + 2 * kBC * kSP + 8 * kBC * kSP + 3 * kBC * 128 + kBC * kBC + kBC + 128);
+size_t scan_smem_bytes(bool reverse, int dk, int dv) {
+  const int ncb = (dv < kScanDvt ? dv : kScanDvt) / 4, nsplit = kBThreads / (8 * ncb);
+  return sizeof(float) * ((size_t)dk * kSP + kBC * kSP + (size_t)nsplit * kBC * kSP +
+                          (reverse ? 3 : 2) * kBC * dk + kBC * kBC + kBC + dk);
 }
 
 // Gradients of one chunk's rows, from its entry state and the state gradient
-// after it, streaming the state in kGradDvt-column passes.
+// after it, streaming the state in kGradDvt-column passes.  Each pass keeps
+// its state columns transposed ([column][dk], 16-byte rows) so that every
+// product reads 128-bit operands; the C x dk gradient sums live in registers
+// across the passes (4 rows x 2 channels of dQb, dKh and dGK per thread).
 __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) float smem[];
   const int slot = blockIdx.x, h = blockIdx.y;
   int n, j;
   if (!locate(a, slot, n, j)) return;
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
   ChunkSm c;
   float *p = carve_chunk(c, smem, dk);
   const int ld = c.ld;
-  constexpr int lt = kGradDvt + 1;
+  constexpr int lw = kBC + 4;      // row stride of the [column][C] arrays
   float *dQb = p; p += kBC * ld;
   float *dKb = p; p += kBC * ld;
   float *dGK = p; p += kBC * ld;
@@ -402,91 +408,125 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
   float *dTb = p; p += kBC * kBC;
   float *X = p;   p += kBC * kBC;
   float *dgam = p; p += 128;
-  float *Ss = p;  p += 128 * lt;   // S columns of this pass
-  float *dSs = p; p += 128 * lt;   // dS' columns
-  float *Vs = p;  p += kBC * lt;   // V, then P = V - GK S
-  float *dOs = p; p += kBC * lt;
-  float *Vt = p;  p += kBC * lt;
-  float *dVt = p; p += kBC * lt;
-  float *dVs = p; p += kBC * lt;
+  float *St = p;  p += kGradDvt * ld;   // S^T of this pass: [column][dk]
+  float *dSt = p; p += kGradDvt * ld;   // dS'^T
+  float *Pt = p;  p += kGradDvt * lw;   // V, then P = V - GK S: [column][row]
+  float *dOt = p; p += kGradDvt * lw;
+  float *Vtt = p; p += kGradDvt * lw;   // V~
+  float *dVtt = p; p += kGradDvt * lw;  // dV~
+  float *dVv = p; p += kGradDvt * lw;   // dV
+  float *red = p; p += 4 * kBC * kBC;   // [product][dk half][row][column]
   setup_chunk(a, c, t0, len, h);
-  for (int e = tid; e < kBC * ld; e += kBThreads) dQb[e] = dKb[e] = dGK[e] = dKh[e] = 0.f;
-  for (int e = tid; e < kBC * kBC; e += kBThreads) dA[e] = dTb[e] = 0.f;
-  for (int i = tid; i < dk; i += kBThreads) dgam[i] = 0.f;
+  // register accumulators
+  const int rb = 4 * (tid & 3), ip = 2 * (tid >> 2);  // rows rb..rb+3, channels ip, ip+1
+  const bool own = ip < dk;
+  float aQ[4][2] = {}, aH[4][2] = {}, aG[4][2] = {};
+  const int rr = tid / kBC, ss = tid % kBC;  // (row, column) of the C x C sums
+  float accTb = 0.f, accA = 0.f, accGam = 0.f;
+  // tasks of the two C x w products over dk: Z = GK S, Y = Kh dS'
+  const int zp = tid >> 7, zq = (tid >> 6) & 1, zb = tid & 63;
+  const int zr = 2 * (zb >> 3), zc = 2 * (zb & 7);
   const size_t sh = (size_t)slot * H + h;
   const float *Sg = a.Sent + sh * dk * dv, *dSg = a.dSx + sh * dk * dv;
   for (int c0 = 0; c0 < dv; c0 += kGradDvt) {
-    const int w = min(kGradDvt, dv - c0);
     __syncthreads();  // the previous pass is done with the column buffers
-    for (int e = tid; e < dk * w; e += kBThreads) {
-      const int i = e / w, cc = e % w;
-      Ss[i * lt + cc] = Sg[(size_t)i * dv + c0 + cc];
-      dSs[i * lt + cc] = dSg[(size_t)i * dv + c0 + cc];
+    for (int e = tid; e < dk * (kGradDvt / 4); e += kBThreads) {  // S, dS' columns, transposed
+      const int i = e / (kGradDvt / 4), cq = 4 * (e % (kGradDvt / 4));
+      const float4 sv = *reinterpret_cast<const float4 *>(Sg + (size_t)i * dv + c0 + cq);
+      const float4 dv4 = *reinterpret_cast<const float4 *>(dSg + (size_t)i * dv + c0 + cq);
+      St[(cq + 0) * ld + i] = sv.x; St[(cq + 1) * ld + i] = sv.y;
+      St[(cq + 2) * ld + i] = sv.z; St[(cq + 3) * ld + i] = sv.w;
+      dSt[(cq + 0) * ld + i] = dv4.x; dSt[(cq + 1) * ld + i] = dv4.y;
+      dSt[(cq + 2) * ld + i] = dv4.z; dSt[(cq + 3) * ld + i] = dv4.w;
     }
-    for (int e = tid; e < kBC * w; e += kBThreads) {
-      const int r = e / w, cc = e % w;
+    {  // V and dO rows (one element per thread: kBThreads == C * kGradDvt)
+      const int r = tid / kGradDvt, cc = tid % kGradDvt;
       float vv = 0.f, dd = 0.f;
       if (r < len) {
         const size_t idx = ((size_t)(t0 + r) * H + h) * dv + c0 + cc;
         vv = ld_elem(a.v, idx, a.qkv);
         dd = ld_elem(a.dO, idx, a.out);
       }
-      Vs[r * lt + cc] = vv;
-      dOs[r * lt + cc] = dd;
+      Pt[cc * lw + r] = vv;
+      dOt[cc * lw + r] = dd;
     }
     __syncthreads();
-    for (int e = tid; e < kBC * w; e += kBThreads) {  // P = V - GK S;  dV~ = Kh dS' + A^T dO
-      const int r = e / w, cc = e % w;
-      float z = 0.f, y = 0.f;
-      for (int i = 0; i < dk; ++i) {
-        z += c.GK[r * ld + i] * Ss[i * lt + cc];
-        y += c.Kh[r * ld + i] * dSs[i * lt + cc];
+    {  // partial Z = GK S (zp = 0) or Y = Kh dS' (zp = 1) over half of dk, 2 x 2 outputs
+      const float *Mm = zp ? c.Kh : c.GK;
+      const float *Vm = zp ? dSt : St;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+      const int half = dk / 2, ia = zq * half;
+#pragma unroll 2
+      for (int i = ia; i < ia + half; i += 4) {
+        const float4 m0 = *reinterpret_cast<const float4 *>(Mm + zr * ld + i);
+        const float4 m1 = *reinterpret_cast<const float4 *>(Mm + (zr + 1) * ld + i);
+        const float4 v0 = *reinterpret_cast<const float4 *>(Vm + zc * ld + i);
+        const float4 v1 = *reinterpret_cast<const float4 *>(Vm + (zc + 1) * ld + i);
+        a00 += m0.x * v0.x + m0.y * v0.y + m0.z * v0.z + m0.w * v0.w;
+        a01 += m0.x * v1.x + m0.y * v1.y + m0.z * v1.z + m0.w * v1.w;
+        a10 += m1.x * v0.x + m1.y * v0.y + m1.z * v0.z + m1.w * v0.w;
+        a11 += m1.x * v1.x + m1.y * v1.y + m1.z * v1.z + m1.w * v1.w;
       }
-      for (int s = r; s < kBC; ++s) y += c.A[s * kBC + r] * dOs[s * lt + cc];
-      Vs[r * lt + cc] -= z;
-      dVt[r * lt + cc] = y;
+      float *rd = red + (zp * 2 + zq) * kBC * kBC;
+      rd[zr * kBC + zc] = a00;
+      rd[zr * kBC + zc + 1] = a01;
+      rd[(zr + 1) * kBC + zc] = a10;
+      rd[(zr + 1) * kBC + zc + 1] = a11;
     }
     __syncthreads();
-    for (int e = tid; e < kBC * w; e += kBThreads) {  // V~ = T_b P;  dV = T_b^T dV~
-      const int r = e / w, cc = e % w;
+    {  // P = V - Z;  dV~ = Y + A^T dO   (thread = (row rr, column ss))
+      const float z = red[rr * kBC + ss] + red[kBC * kBC + rr * kBC + ss];
+      float y = red[2 * kBC * kBC + rr * kBC + ss] + red[3 * kBC * kBC + rr * kBC + ss];
+      for (int s2 = rr; s2 < kBC; ++s2) y += c.A[s2 * kBC + rr] * dOt[ss * lw + s2];
+      Pt[ss * lw + rr] -= z;
+      dVtt[ss * lw + rr] = y;
+    }
+    __syncthreads();
+    {  // V~ = T_b P;  dV = T_b^T dV~
       float y = 0.f, d = 0.f;
-      for (int s = 0; s <= r; ++s) y += c.T[r * kBC + s] * c.beta[s] * Vs[s * lt + cc];
-      for (int s = r; s < kBC; ++s) d += c.T[s * kBC + r] * dVt[s * lt + cc];
-      d *= c.beta[r];
-      Vt[r * lt + cc] = y;
-      dVs[r * lt + cc] = d;
-      if (r < len) a.gv[((size_t)(t0 + r) * H + h) * dv + c0 + cc] = d;
+      for (int s2 = 0; s2 <= rr; ++s2) y += c.T[rr * kBC + s2] * c.beta[s2] * Pt[ss * lw + s2];
+      for (int s2 = rr; s2 < kBC; ++s2) d += c.T[s2 * kBC + rr] * dVtt[ss * lw + s2];
+      d *= c.beta[rr];
+      Vtt[ss * lw + rr] = y;
+      dVv[ss * lw + rr] = d;
+      if (rr < len) a.gv[((size_t)(t0 + rr) * H + h) * dv + c0 + ss] = d;
     }
     __syncthreads();
-    for (int e = tid; e < kBC * dk; e += kBThreads) {  // the C x dk sums over this pass's columns
-      const int r = e / dk, i = e % dk;
-      float q = 0.f, kh = 0.f, gk = 0.f;
-      for (int cc = 0; cc < w; ++cc) {
-        const float s = Ss[i * lt + cc];
-        q += dOs[r * lt + cc] * s;
-        kh += Vt[r * lt + cc] * dSs[i * lt + cc];
-        gk += dVs[r * lt + cc] * s;
+    if (own) {  // dQb += dO S^T, dKh += V~ dS'^T, dGK -= dV S^T on this thread's 4 x 2 block
+#pragma unroll 4
+      for (int cc = 0; cc < kGradDvt; ++cc) {
+        const float4 o4 = *reinterpret_cast<const float4 *>(dOt + cc * lw + rb);
+        const float4 v4 = *reinterpret_cast<const float4 *>(Vtt + cc * lw + rb);
+        const float4 d4 = *reinterpret_cast<const float4 *>(dVv + cc * lw + rb);
+        const float2 s2 = *reinterpret_cast<const float2 *>(St + cc * ld + ip);
+        const float2 ds2 = *reinterpret_cast<const float2 *>(dSt + cc * ld + ip);
+        const float oo[4] = {o4.x, o4.y, o4.z, o4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w},
+                    dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          aQ[q][0] += oo[q] * s2.x; aQ[q][1] += oo[q] * s2.y;
+          aH[q][0] += vv[q] * ds2.x; aH[q][1] += vv[q] * ds2.y;
+          aG[q][0] -= dd[q] * s2.x; aG[q][1] -= dd[q] * s2.y;
+        }
       }
-      dQb[r * ld + i] += q;
-      dKh[r * ld + i] += kh;
-      dGK[r * ld + i] -= gk;
     }
-    {  // the C x C sums: dT_b += dV~ P^T, dA += dO V~^T
-      const int r = tid / kBC, s = tid % kBC;
-      float tb = 0.f, da = 0.f;
-      for (int cc = 0; cc < w; ++cc) {
-        tb += dVt[r * lt + cc] * Vs[s * lt + cc];
-        da += dOs[r * lt + cc] * Vt[s * lt + cc];
-      }
-      dTb[tid] += tb;
-      dA[tid] += da;
+    for (int cc = 0; cc < kGradDvt; ++cc) {  // dT_b += dV~ P^T, dA += dO V~^T
+      accTb += dVtt[cc * lw + rr] * Pt[cc * lw + ss];
+      accA += dOt[cc * lw + rr] * Vtt[cc * lw + ss];
     }
-    for (int i = tid; i < dk; i += kBThreads) {
-      float gsum = 0.f;
-      for (int cc = 0; cc < w; ++cc) gsum += dSs[i * lt + cc] * Ss[i * lt + cc];
-      dgam[i] += gsum;
-    }
+    if (tid < dk)
+      for (int cc = 0; cc < kGradDvt; ++cc) accGam += dSt[cc * ld + tid] * St[cc * ld + tid];
   }
+  if (own)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      dQb[(rb + q) * ld + ip] = aQ[q][0]; dQb[(rb + q) * ld + ip + 1] = aQ[q][1];
+      dKh[(rb + q) * ld + ip] = aH[q][0]; dKh[(rb + q) * ld + ip + 1] = aH[q][1];
+      dGK[(rb + q) * ld + ip] = aG[q][0]; dGK[(rb + q) * ld + ip + 1] = aG[q][1];
+    }
+  dTb[tid] = accTb;
+  dA[tid] = accA;
+  if (tid < dk) dgam[tid] = accGam;
   __syncthreads();
   // through T_b = T diag(beta) and T = (I + L)^-1:  X = T^T (dT_b diag(beta))
   {
@@ -534,7 +574,7 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
     dQb[r * ld + i] += qb;
   }
   __syncthreads();
-  // elementwise to q, k and the cumulative log-decay G (dG in G's place)
+  // elementwise to q, k and the cumulative log-decay G (dG in dKb's place)
   for (int e = tid; e < kBC * dk; e += kBThreads) {
     const int r = e / dk, i = e % dk;
     const float G = c.G[r * ld + i], Gl = c.G[(kBC - 1) * ld + i];
@@ -561,13 +601,13 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
 }
 
 size_t grads_smem_bytes(int dk) {
-  const size_t ld = (size_t)dk + 1;
-  return sizeof(float) * (9 * kBC * ld + 6 * kBC * kBC + kBC + 2 * 128 + 2 * 128 * (kGradDvt + 1) +
-                          5 * kBC * (kGradDvt + 1));
+  const size_t ld = (size_t)dk + 4, lw = kBC + 4;
+  return sizeof(float) * (9 * kBC * ld + 6 * kBC * kBC + kBC + 2 * 128 + 2 * kGradDvt * ld + 5 * kGradDvt * lw +
+                          4 * kBC * kBC);
 }
 
 size_t prep_smem_bytes(int dk) {
-  const size_t ld = (size_t)dk + 1;
+  const size_t ld = (size_t)dk + 4;
   return sizeof(float) * (5 * kBC * ld + 3 * kBC * kBC + kBC + 128);
 }
 
@@ -609,15 +649,15 @@ cudaError_t launch_chunk_bwd(const PrefillArgs &p, const BwdIo &io, void *ws, cu
     bwd_prep_kernel<<<dim3(a.nslots, p.H), kBThreads, sp, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  const size_t ss = scan_smem_bytes();
+  const size_t ssf = scan_smem_bytes(false, p.dk, p.dv), ssr = scan_smem_bytes(true, p.dk, p.dv);
   const dim3 sgrid(p.N * p.H, (p.dv + kScanDvt - 1) / kScanDvt);
-  e = cudaFuncSetAttribute(bwd_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+  e = cudaFuncSetAttribute(bwd_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssf);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(bwd_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+    e = cudaFuncSetAttribute(bwd_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssr);
   if (e != cudaSuccess) return e;
-  bwd_scan_kernel<false><<<sgrid, kBThreads, ss, s>>>(a);
+  bwd_scan_kernel<false><<<sgrid, kBThreads, ssf, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_scan_kernel<true><<<sgrid, kBThreads, ss, s>>>(a);
+  bwd_scan_kernel<true><<<sgrid, kBThreads, ssr, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.nslots > 0) {
     const size_t sg = grads_smem_bytes(p.dk);
