@@ -94,6 +94,11 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_bwd.argtypes = [ctypes.POINTER(KdaChunkDesc), P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
                                       ctypes.c_size_t, P]
         lib.kda_chunk_bwd.restype = ctypes.c_int
+        lib.kda_chunk_affine_pair.argtypes = [ctypes.POINTER(KdaChunkDesc), P, P, P, P, P, P, P, P]
+        lib.kda_chunk_affine_pair.restype = ctypes.c_int
+        lib.kda_affine_compose.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           P, P, P, P]
+        lib.kda_affine_compose.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_last_cuda_error.argtypes = []
@@ -376,3 +381,32 @@ def kda_chunk_bwd(q, k, v, log_alpha, beta, d_out, initial_state=None, d_final_s
                            _stream_handle(stream, dev))
     _check(st, "kda_chunk_bwd")
     return grads
+
+
+def kda_chunk_affine_pair(q, k, v, log_alpha, beta, cu_seqlens=None, pairs=None, *, B=None, validate=False,
+                          stream=None):
+    """The affine pair (S~, M) of each sequence of the call: returns pairs
+    [2, N, H, dk, dv] fp32 with pairs[0] = S~ and pairs[1] = M."""
+    lib = load()
+    d = chunk_desc(q, v, cu_seqlens=cu_seqlens, gate_dtype=_dt(log_alpha), validate=validate, B=B)
+    Nseq = d.num_seqs if cu_seqlens is not None else d.B
+    if pairs is None:
+        pairs = torch.empty(2, Nseq, d.H, d.dk, d.dv, dtype=torch.float32, device=q.device)
+    st = lib.kda_chunk_affine_pair(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                   _ptr(cu_seqlens), _ptr(pairs), _stream_handle(stream, q.device))
+    _check(st, "kda_chunk_affine_pair")
+    return pairs
+
+
+def kda_affine_compose(pairs, initial_state=None, entry_states=None, *, stream=None):
+    """Entry states [N, P, H, dk, dv] of P consecutive segments from the pairs
+    [2, N, P-1, H, dk, dv] of the first P-1 and the first entry state."""
+    lib = load()
+    _, N, Pm1, H, dk, dv = pairs.shape
+    P = Pm1 + 1
+    if entry_states is None:
+        entry_states = torch.empty(N, P, H, dk, dv, dtype=torch.float32, device=pairs.device)
+    st = lib.kda_affine_compose(N, H, dk, dv, P, _ptr(initial_state), _ptr(pairs) if Pm1 > 0 else None,
+                                _ptr(entry_states), _stream_handle(stream, pairs.device))
+    _check(st, "kda_affine_compose")
+    return entry_states

@@ -133,10 +133,12 @@ void gate_spans(const kda_layer_gates *lg, size_t rows, int H, int dv, kda_dtype
   r[2] = span(lg->norm_weight, lg->norm_weight ? (size_t)dv * 4 : 0);
 }
 
+// out may be NULL only with has_out = false (calls that write no output).
 kda_status check_prefill(const kda_chunk_desc *d, const void *q, const void *k, const void *v,
                          const void *g, const void *beta, const float *s0, const int32_t *cu,
-                         void *out, float *sT, PrefillArgs *a, const kda_layer_gates *lg = nullptr) {
-  if (!d || !q || !k || !v || !g || !beta || !out) return KDA_ERR_NULL;
+                         void *out, float *sT, PrefillArgs *a, const kda_layer_gates *lg = nullptr,
+                         bool has_out = true) {
+  if (!d || !q || !k || !v || !g || !beta || (has_out && !out)) return KDA_ERR_NULL;
   if (!dtype_ok(d->qkv_dtype) || !dtype_ok(d->out_dtype) || !dtype_ok(d->gate_dtype))
     return KDA_ERR_DTYPE;
   if (d->H <= 0 || !dim_ok(d->dk) || !dim_ok(d->dv) || d->T < 0 || d->B <= 0) return KDA_ERR_SHAPE;
@@ -153,14 +155,14 @@ kda_status check_prefill(const kda_chunk_desc *d, const void *q, const void *k, 
   // beta, the states and cu_seqlens only need their element alignment.
   const void *ptrs16[] = {q, k, v, g, out};
   for (const void *p : ptrs16)
-    if (!aligned16(p)) return KDA_ERR_ALIGN;
+    if (p && !aligned16(p)) return KDA_ERR_ALIGN;
   const void *ptrs4[] = {beta, s0, cu, sT};
   for (const void *p : ptrs4)
     if (p && !aligned_to(p, 4)) return KDA_ERR_ALIGN;
   const int Nseq = cu ? d->num_seqs : d->B;
   const size_t th = (size_t)T_total * d->H;
   const kda_dtype gdt = lg ? d->qkv_dtype : d->gate_dtype;  // decay logits or log-decay
-  Range r_out = span(out, th * d->dv * esize(d->out_dtype));
+  Range r_out = span(out, has_out ? th * d->dv * esize(d->out_dtype) : 0);
   if (lg) {
     kda_status st = check_gates(lg);
     if (st != KDA_OK) return st;
@@ -436,6 +438,52 @@ kda_status kda_layer_fwd(const kda_chunk_desc *desc, const kda_layer_gates *gate
   if (st != KDA_OK) return st;
   return run_prefill(desc, a, reinterpret_cast<cudaStream_t>(stream), workspace ? 1 : 0, workspace,
                      workspace_bytes);
+}
+
+kda_status kda_chunk_affine_pair(const kda_chunk_desc *desc, const void *q, const void *k, const void *v,
+                                 const void *log_alpha, const void *beta, const int32_t *cu_seqlens,
+                                 float *pairs, kda_stream_t stream) {
+  PrefillArgs a;
+  if (!pairs) return KDA_ERR_NULL;
+  kda_status st = check_prefill(desc, q, k, v, log_alpha, beta, nullptr, cu_seqlens, nullptr, nullptr, &a,
+                                nullptr, false);
+  if (st != KDA_OK) return st;
+  if (!chunk_tc_supports(a) || desc->kernel == KDA_KERNEL_SIMT) return KDA_ERR_UNSUPPORTED;
+  const size_t bytes = (size_t)2 * a.N * a.H * a.dk * a.dv * 4;
+  const Range r_p = span(pairs, bytes);
+  const Range ins[] = {span(q, (size_t)a.T_total * a.H * a.dk * 2), span(k, (size_t)a.T_total * a.H * a.dk * 2),
+                       span(v, (size_t)a.T_total * a.H * a.dv * 2), span(log_alpha, (size_t)a.T_total * a.H * a.dk * 4),
+                       span(beta, (size_t)a.T_total * a.H * 4),
+                       span(cu_seqlens, cu_seqlens ? (size_t)(a.N + 1) * 4 : 0)};
+  for (const Range &r : ins)
+    if (overlap(r_p, r)) return KDA_ERR_ALIAS;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (desc->validate) {
+    st = run_validation(s, [&](int *flag) { return launch_validate_prefill(a, flag, s); });
+    if (st != KDA_OK) return st;
+  }
+  if (!aligned16(pairs)) return KDA_ERR_ALIGN;
+  cudaError_t e = launch_affine_pair(a, pairs, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KDA_OK;
+}
+
+kda_status kda_affine_compose(int N, int H, int dk, int dv, int P, const float *initial_state, const float *pairs,
+                              float *entry_states, kda_stream_t stream) {
+  if (!entry_states || (P > 1 && !pairs)) return KDA_ERR_NULL;
+  if (N < 0 || H <= 0 || P <= 0 || dk != 128 || dv != 128) return KDA_ERR_SHAPE;
+  const void *ptrs[] = {initial_state, pairs, entry_states};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+  const size_t DD = (size_t)dk * dv * 4;
+  const Range r_e = span(entry_states, (size_t)N * P * H * DD);
+  if (overlap(r_e, span(pairs, pairs ? (size_t)2 * N * (P - 1) * H * DD : 0)) ||
+      overlap(r_e, span(initial_state, initial_state ? (size_t)N * H * DD : 0)))
+    return KDA_ERR_ALIAS;
+  cudaError_t e = launch_affine_compose(N, H, P, initial_state, pairs, entry_states,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KDA_OK;
 }
 
 kda_status kda_chunk_bwd_workspace_size(const kda_chunk_desc *desc, size_t *bytes) {

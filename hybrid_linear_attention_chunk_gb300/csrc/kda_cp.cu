@@ -119,6 +119,35 @@ SegPlan plan_segments(const PrefillArgs &a, int requested) {
   return pl;
 }
 
+// The affine pair of each whole sequence of the call: kind 0 (from S = 0
+// with the real v) into pairs[0][n][h], kind 1 (from S = I, v = 0) into
+// pairs[1][n][h].
+cudaError_t launch_affine_pair(const PrefillArgs &a, float *pairs, cudaStream_t s) {
+  PrefillArgs p1 = a;
+  p1.o = nullptr;
+  p1.s0 = nullptr;
+  p1.sT = pairs;
+  p1.seg_tokens = 0;
+  p1.nseg = 1;
+  p1.kinds = 2;
+  p1.ck = nullptr;
+  p1.og = nullptr;
+  return launch_chunk_tc(p1, s);
+}
+
+// Entry states E [N][P][H][D][D] of P consecutive segments from the pairs of
+// the first P - 1 ([2][N][P-1][H][D][D]) and the first segment's entry s0
+// (nullable: zero).
+cudaError_t launch_affine_compose(int N, int H, int P, const float *s0, const float *pairs, float *E,
+                                  cudaStream_t s) {
+  if (N * H == 0 || P <= 0) return cudaSuccess;
+  const size_t smem = 2 * (size_t)kD * kD * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(cp_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cp_scan_kernel<<<N * H, kScanThreads, smem, s>>>(N, H, P, s0, pairs, E);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_chunk_tc_segmented(const PrefillArgs &a, const SegPlan &pl, void *ws, cudaStream_t s) {
   const size_t DD = (size_t)kD * kD;
   float *pairs = static_cast<float *>(ws);                                    // [2][N][P-1][H][D][D]

@@ -121,6 +121,9 @@ struct SegPlan {
 };
 SegPlan plan_segments(const PrefillArgs &a, int requested);
 cudaError_t launch_chunk_tc_segmented(const PrefillArgs &a, const SegPlan &pl, void *ws, cudaStream_t s);
+cudaError_t launch_affine_pair(const PrefillArgs &a, float *pairs, cudaStream_t s);
+cudaError_t launch_affine_compose(int N, int H, int P, const float *s0, const float *pairs, float *E,
+                                  cudaStream_t s);
 cudaError_t launch_validate_prefill(const PrefillArgs &a, int *d_flag, cudaStream_t s);
 cudaError_t launch_validate_decode(const DecodeArgs &a, int *d_flag, cudaStream_t s);
 

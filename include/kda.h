@@ -242,6 +242,38 @@ kda_status kda_layer_decode_step(const kda_decode_desc *desc, const kda_layer_ga
                                  kda_stream_t stream);
 
 /*
+ * Context parallelism across GPUs ([K3-notes §2.5, context-parallel affine
+ * pair]): a segment of a sequence maps any entry state to
+ *     S_out = S~ + M S_in,
+ * S~ its final state from S_in = 0 and M (dk x dk) the product of its
+ * per-token transitions (I - beta k k^T) Diag(alpha); the pairs compose.  A
+ * sequence split over R GPUs runs on each rank r: kda_chunk_affine_pair on
+ * its segment, an all-gather of the R pairs (fixed size, independent of the
+ * segment length), kda_affine_compose for the entry states, and
+ * kda_chunk_fwd on its segment from entry state r.
+ *
+ * kda_chunk_affine_pair - the pair of each sequence of the call (each whole
+ * sequence is one segment).  Arguments as kda_chunk_fwd (no states, no out);
+ *   pairs  [2][Nseq][H][dk][dv] fp32 device, written: [0] = S~, [1] = M.
+ * Tensor-core arguments only (bf16 q/k/v, fp32 gates, dk = dv = 128, chunk
+ * 64); KDA_ERR_UNSUPPORTED otherwise or with desc->kernel = KDA_KERNEL_SIMT.
+ */
+kda_status kda_chunk_affine_pair(const kda_chunk_desc *desc, const void *q, const void *k, const void *v,
+                                 const void *log_alpha, const void *beta, const int32_t *cu_seqlens,
+                                 float *pairs, kda_stream_t stream);
+
+/*
+ * kda_affine_compose - entry states of P consecutive segments:
+ *   E_0 = initial_state (NULL: zero),  E_{p+1} = S~_p + M_p E_p   (fp32)
+ *   pairs         [2][N][P-1][H][dk][dv] fp32 device (S~ block, then M block;
+ *                 may be NULL when P = 1)
+ *   entry_states  [N][P][H][dk][dv] fp32 device, written
+ * dk = dv = 128; pointers 16-byte aligned; entry_states may alias nothing.
+ */
+kda_status kda_affine_compose(int N, int H, int dk, int dv, int P, const float *initial_state, const float *pairs,
+                              float *entry_states, kda_stream_t stream);
+
+/*
  * kda_chunk_bwd - gradients of kda_chunk_fwd, for training (the chunkwise form
  * of [K3-notes §2.2] is the training form; the page prints no backward, and
  * this one is the exact derivative of the forward's mathematics).  For the

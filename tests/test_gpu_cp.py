@@ -94,3 +94,93 @@ def test_long_context_full_size(kda):
     o_ref, _ = oracle_prefill(sub, chains=[0, 11])
     for h in (0, 11):
         assert_close(to_np(o_cp[:L, h]), o_ref[:, h], TOL_BF16_FRO, TOL_BF16_MAXN, what=f"o head {h}")
+
+
+# ----------------------------------------------- context parallelism across ranks
+
+def _shard(t, B, T, rank, world):
+    L = T // world
+    return torch.cat([t[n * T + rank * L: n * T + (rank + 1) * L] for n in range(B)], 0).contiguous()
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_cp_ranks_emulated_in_sequence(kda, world):
+    """The multi-GPU schedule (kda_chunk_fwd_cp) with the library on this GPU,
+    its ranks run one after another; the all-gather hands every rank the
+    stack of what all ranks send (each rank's own send is checked against
+    it).  Outputs and the last rank's final state match the oracle."""
+    from hybrid_linear_attention_chunk_gb300.cp import LibraryBackend, kda_chunk_fwd_cp
+    w = inputs.scaled(inputs.LONG_T1M, B=2, T=4096, H=2)
+    x = inputs.make_prefill(w, device=DEV)
+    B, T = w.B, w.T
+    names = ("q", "k", "v", "log_alpha", "beta")
+    shards = [[_shard(x[nm], B, T, r, world) for nm in names] for r in range(world)]
+    backend = LibraryBackend(kda)
+    sends = []
+    for r in range(world):
+        pair = (backend.affine_pair(*shards[r], B) if r < world - 1
+                else torch.zeros(2, B, w.H, w.dk, w.dv, device=DEV))
+        s0 = x["initial_state"] if r == 0 else torch.zeros_like(pair[0])
+        sends.append(torch.cat([pair, s0[None]], 0))
+    stacked = torch.stack(sends)
+
+    def gather_for(r):
+        def gather(t):
+            assert torch.equal(t, stacked[r]), f"rank {r} sent something else"
+            return stacked
+        return gather
+
+    outs, state = [], None
+    for r in range(world):
+        o, s = kda_chunk_fwd_cp(*shards[r], x["initial_state"] if r == 0 else None, rank=r, world=world, B=B,
+                                all_gather=gather_for(r), backend=backend)
+        outs.append(o)
+        state = s
+    torch.cuda.synchronize()
+    L = T // world
+    o_full = torch.empty(B * T, w.H, w.dv, dtype=outs[0].dtype, device=DEV)
+    for r in range(world):
+        for n in range(B):
+            o_full[n * T + r * L: n * T + (r + 1) * L] = outs[r][n * L:(n + 1) * L]
+    o_ref, s_ref = oracle_prefill(x)
+    assert_close(to_np(o_full), o_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="o")
+    assert_close(to_np(state), s_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="final state")
+
+
+def test_affine_pair_and_compose_match_the_segmented_plan(kda):
+    """The two CP entry points on one GPU: the pair of the first half and the
+    composed entry state of the second half give the same final state as the
+    unsplit call, within bf16 tolerance."""
+    w = inputs.scaled(inputs.LONG_T1M, B=1, T=2048, H=3)
+    x = inputs.make_prefill(w, device=DEV)
+    first = {nm: x[nm][:1024].contiguous() for nm in ("q", "k", "v", "log_alpha", "beta")}
+    second = {nm: x[nm][1024:].contiguous() for nm in ("q", "k", "v", "log_alpha", "beta")}
+    pairs = kda.kda_chunk_affine_pair(first["q"], first["k"], first["v"], first["log_alpha"], first["beta"], B=1)
+    E = kda.kda_affine_compose(pairs[:, :, None].contiguous(), x["initial_state"])
+    o2, s2 = kda.kda_chunk_fwd(second["q"], second["k"], second["v"], second["log_alpha"], second["beta"],
+                               E[:, 1].contiguous(), None, B=1)
+    o, s = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["initial_state"], None, B=1,
+                             segments=1)
+    torch.cuda.synchronize()
+    assert torch.equal(E[:, 0], x["initial_state"])
+    assert_close(to_np(s2), to_np(s), TOL_BF16_FRO, TOL_BF16_MAXN, what="final state")
+    assert_close(to_np(o2), to_np(o[1024:]), TOL_BF16_FRO, TOL_BF16_MAXN, what="second half o")
+
+
+def test_nccl_all_gather_single_rank(kda):
+    """The schedule's all-gather through NCCL on a one-rank group."""
+    import socket
+
+    import torch.distributed as dist
+    from hybrid_linear_attention_chunk_gb300.cp import torch_all_gather
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        t = torch.arange(24, dtype=torch.float32, device=DEV).reshape(2, 3, 4)
+        got = torch_all_gather()(t)
+        torch.cuda.synchronize()
+        assert got.shape == (1, 2, 3, 4) and torch.equal(got[0], t)
+    finally:
+        dist.destroy_process_group()

@@ -11,6 +11,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+
 from _helpers import (TOL_BF16_FRO, TOL_BF16_MAXN, assert_close, oracle_prefill, rel_fro, to_np)
 from hybrid_linear_attention_chunk_gb300 import inputs
 
@@ -126,6 +128,31 @@ def test_tc_full_size_batch_workload_sampled(kda):
         n = c // w.H
         assert_close(to_np(o[sl, h]), o_ref[sl, h], TOL_BF16_FRO, TOL_BF16_MAXN, what=f"o chain {c}")
         assert_close(to_np(s[n, h]), s_ref[n, h], TOL_BF16_FRO, TOL_BF16_MAXN, what=f"S chain {c}")
+
+
+def test_tc_full_size_varlen_workload_sampled(kda):
+    """The packed varlen workload at full size (64 sequences of 512..32768
+    tokens, H=32, random initial states), run as the benchmark runs it; the
+    oracle checks the chains of the shortest and the longest sequence and of
+    four others."""
+    w = inputs.VARLEN_64
+    x = inputs.make_prefill(w, device=DEV)
+    o, s = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["initial_state"],
+                             x["cu_seqlens"])
+    torch.cuda.synchronize()
+    lens = np.asarray(x["lengths"])
+    seqs = [int(np.argmin(lens)), int(np.argmax(lens)), 1, 17, 40, 63]
+    heads = [0, 31, 5, 12, 20, 27]
+    cu = x["cu_seqlens"].cpu().numpy()
+    for n, h in zip(seqs, heads):
+        # the chain alone (one sequence, one head) keeps the host copies small
+        sl = slice(int(cu[n]), int(cu[n + 1]))
+        hs = slice(h, h + 1)
+        sub = {name: inputs.host_f32(x[name][sl, hs].contiguous()) for name in ("q", "k", "v", "log_alpha", "beta")}
+        s0 = inputs.host_f32(x["initial_state"][n:n + 1, hs].contiguous())
+        o_ref, s_ref = oracle.recurrent(sub["q"], sub["k"], sub["v"], sub["log_alpha"], sub["beta"], s0)
+        assert_close(to_np(o[sl, hs]), o_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what=f"o seq {n} head {h}")
+        assert_close(to_np(s[n:n + 1, hs]), s_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what=f"S seq {n} head {h}")
 
 
 def test_tc_deterministic_and_resume(kda):
