@@ -114,3 +114,17 @@ def test_bwd_matches_forward_differences(kda):
     fd = (L(x["log_alpha"] + eps * u) - L(x["log_alpha"] - eps * u)) / (2 * eps)
     an = float((gr["dlog_alpha"].double() * u.double()).sum())
     assert abs(fd - an) <= 2e-3 * max(abs(an), 1.0), (fd, an)
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 16), (16, 64), (128, 32), (64, 128)])
+def test_bwd_shapes_fp32(kda, dk, dv):
+    """Other head sizes (the scans' 16-column tiling at dv = 16, a dk split of
+    two channels per thread group at dk = 16), packed ragged sequences."""
+    lens = np.array([50, 17, 33])
+    w = inputs.scaled(inputs.TINY_FP32, H=3, dk=dk, dv=dv, varlen_seqs=len(lens), random_initial_state=True)
+    x = inputs.make_prefill(w, device=DEV, lengths=lens)
+    dO, dST = upstream(x, w, torch.float32, seed=dk + dv)
+    gr = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], dO, x["initial_state"], dST,
+                           x["cu_seqlens"])
+    torch.cuda.synchronize()
+    check(gr, oracle_grads(x, dO, dST), f"dk={dk} dv={dv}")
