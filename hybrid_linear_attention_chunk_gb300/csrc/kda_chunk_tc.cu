@@ -16,8 +16,12 @@
 //   M3  W^T = (Gamma o K)^T T_b^T                                (M=128 N=64 K=64)
 //   M4  V~^T = U^T - S^T W^T ;  O^T = S^T (Q o Gamma)^T          (M=128 N=64 K=128, twice)
 //   M5  O^T += V~^T A^T                                          (M=128 N=64 K=64)
-//   S^T <- S^T Diag(gamma_C)           (fp32 master state in TMEM, scaled in place)
-//   M6  S^T += V~^T (K o gamma_C / Gamma)                        (M=128 N=128 K=64)
+//   M6  S^T <- (S^T + V~^T (K / Gamma)) Diag(gamma_C)            (M=128 N=128 K=64)
+// (fp32 master state in TMEM; the Diag(gamma_C) scaling is applied to the
+// accumulated state in the same TMEM pass that refreshes its bf16 copy, and
+// K / Gamma doubles as M1's key operand.  When the chunk took the per-tile
+// range path, K / Gamma may not be formed: the state is scaled first and M6
+// takes K o gamma_C / Gamma, as S^T <- S^T Diag(gamma_C) + V~^T (K o gamma_C / Gamma).)
 // Every product is computed transposed so that M = 128 (dv or dk) and the
 // tensor core runs at full width; TMEM lane j holds row j of the result.
 // M4 reads its A operand, the bf16 copy of S^T, straight from TMEM.
@@ -28,7 +32,7 @@
 // the chunk's Q o Gamma and K o gamma_C / Gamma operands, which are then
 // scaled in place.  M2/M3 complete asynchronously: their completion is what
 // hands the chunk to the state group.  The state group (warps 8-11) runs the
-// serial state chain: -W staging, M4, V~ staging, the gamma scaling, M5/M6,
+// serial state chain: -W staging, M4, V~ staging, M5/M6, the gamma scaling,
 // the bf16 state copy and the output.  Operands the state group still reads
 // while the chunk group prepares the next chunk are double-buffered by chunk
 // parity.  Thread 0 of each group issues that group's MMAs.
@@ -81,7 +85,8 @@ constexpr uint32_t KHALF = 24576;
 constexpr uint32_t OFF_KB = 49152;    // 16 KB: K / Gamma -> L, then T over it (fp32 64x64)
 constexpr uint32_t OFF_TF = 65536;    // 16 KB: solve scratch: T_[01][01]^T and X^T (tf32 B operands of
                                       //   the level-2 products, 4 KB each), level-1 products (2 KB)
-constexpr uint32_t OFF_KH = 81920;    // x2 16 KB: K o gamma_C / Gamma (MN-major B of M6)
+constexpr uint32_t OFF_KH = 81920;    // x2 16 KB: K / Gamma (B of M1, MN-major B of M6), or
+                                      //   K o gamma_C / Gamma after the per-tile range path
 constexpr uint32_t OFF_AM = 114688;   // x2 8 KB: A bf16, 64 rows x 64
 constexpr uint32_t OFF_ZT = 131072;   // 8 KB: T_b bf16 (read by M2/M3)
 constexpr uint32_t OFF_V = 139264;    // 16 KB: v tile (TMA), two 64-column boxes
@@ -120,6 +125,7 @@ struct Ctl {
   int qk_iss[2], qk_lnd[2];  // q/k copies issued and waited for, by chunk parity
   int v_iss, v_lnd;          // v copies issued (chunk group) and waited for (state group)
   int og_iss, og_lnd;        // out_gate copies issued and waited for (state group)
+  int slow[2];               // the chunk took the per-tile range path (by chunk parity)
 };
 static_assert(offsetof(Ctl, nw) % 16 == 0 && offsetof(Ctl, gam) % 16 == 0, "vector reads of the control block");
 static_assert(sizeof(Ctl) <= 4096, "control block");
@@ -619,7 +625,6 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         for (int r = 0; r < 8; ++r) Gl[r] = add4(Gl[r], off);
       }
       const float4 gam = make_float4(ex2(tc.x), ex2(tc.y), ex2(tc.z), ex2(tc.w));
-      if (t8 == 0) *reinterpret_cast<float4 *>(&ctl->gam[par][4 * p4]) = gam;
       const bool vote = fminf(fminf(tc.x, tc.y), fminf(tc.z, tc.w)) < kSingleRefBound2;
       if (ctid < kC)  // beta of the next chunk's rows, 0 past the end
         beta_next = ctid < eos - (t0 + kC)
@@ -639,11 +644,15 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
         ctl->go_c[seq & 1] = ok && !ctl->abort;
       }
-      // the barrier also publishes gamma_C and closes the range-guard vote
+      // the barrier also closes the range-guard vote
       const bool slow = bar_chunk_or(vote);
       alive = ctl->go_c[seq & 1] != 0;
       ++seq;
       if (!alive) break;
+      // gamma_C of this parity is free only now: the q/k copy just waited for
+      // was issued after the state group's last read of it (two chunks back);
+      // the state group reads it after the hand-off below
+      if (t8 == 0) *reinterpret_cast<float4 *>(&ctl->gam[par][4 * p4]) = gam;
       // operand tiles: channel quad p4 sits in K-half p4 / 16 at column 4 p4 mod 64
       const uint32_t half = (uint32_t)(p4 >> 4), col = (uint32_t)(4 * p4) & 63u;
       uint8_t *qb_h = qg + half * KHALF + par * 16384;  // q -> Q o Gamma (in place)
@@ -660,18 +669,16 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       }
       if (!slow) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int r = 0; r < 8; ++r) {  // K / Gamma in place of k: M1's keys and M6's operand
           const uint32_t off = sw128_offset(8 * t8 + r, col);
           const float4 e = ex2_4(Gl[r]), i = ex2_4(neg4(Gl[r]));
-          const float4 kb = mul4(kv[r], i);
           sts64(qb_h + off, pack4_bf16(mul4(qv[r], e)));
           sts64(gk_h + off, pack4_bf16(mul4(kv[r], e)));
-          sts64(kb_h + off, pack4_bf16(kb));
-          sts64(kh_h + off, pack4_bf16(mul4(kb, gam)));
+          sts64(kh_h + off, pack4_bf16(mul4(kv[r], i)));
         }
         group_publish<true>();
         if (ctid == 0) {
-          issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, par, false);
+          issue_m1(tbase, smem_u32(qg), sm_base + OFF_KH + par * 16384, par, false);
           mma_commit(smem_u32(&ctl->bar[B_M1]));
         }
         alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
@@ -889,6 +896,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           st_row16_bf16(zt, 32 + lane, n0, y);
         }
       }
+      if (ctid == 0) ctl->slow[par] = slow;
       group_publish<true>();
       // ---------------- hand the chunk to the state group, which issues M2/M3
       // (the arrive releases the chunk's shared-memory state to it)
@@ -967,7 +975,9 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       if (!(alive = group_wait<false>(ctl, B_M4, ph_m4, stid, seq, A.err))) break;
       ph_m4 ^= 1u;
 
-      // ---------------- V~^T -> bf16 operand; S^T <- S^T Diag(gamma_C)
+      // ---------------- V~^T -> bf16 operand; after the per-tile range path,
+      // S^T <- S^T Diag(gamma_C) before M6 (else the scaling follows M6)
+      const bool slow = ctl->slow[par] != 0;
       {
         float v[64];
         tmem_ld32(tmem_addr(tbase, 32 * qw, tm_u), *reinterpret_cast<float(*)[32]>(v));
@@ -976,7 +986,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
 #pragma unroll
         for (int r0 = 0; r0 < 64; r0 += 16) st_row16_bf16(vt, j, r0, v + r0);
       }
-      {
+      if (slow) {
         const float *gam = ctl->gam[par];
 #pragma unroll 1
         for (int i0 = 0; i0 < kD; i0 += 32) {
@@ -997,24 +1007,29 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       }
       if (!(alive = group_wait<false>(ctl, B_M56, ph_m56, stid, seq, A.err))) break;
       ph_m56 ^= 1u;
-      // This parity's operand buffers are free (M4-M6 have completed and
-      // gamma_C was read before M5/M6 were issued): q and k of the chunk two
-      // ahead land in them; its A tile, gamma_C and TMEM U^T are written only
-      // after that copy has been waited for.
-      if (stid == 0 && c + 2 < nchunks) issue_qk(&maps, ctl, sm_base, h, t0 + 2 * kC, par);
 
-      // ---------------- bf16 copy of the new state (and a checkpoint of the
-      // fp32 state when one ends this chunk); the output rows
+      // ---------------- S^T <- S^T Diag(gamma_C) (unless done before M6), the
+      // bf16 copy of the new state (and a checkpoint of the fp32 state when
+      // one ends this chunk); the output rows
       float *cp = ckpt_ptr(a, n, h, t0 + len - seq_bos);
+      {
+        const float *gam = ctl->gam[par];
 #pragma unroll 1
-      for (int i0 = 0; i0 < kD; i0 += 32) {
-        float s[32];
-        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
-        tmem_wait_ld();
-        tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_STB + i0 / 2), s);
-        if (cp)
+        for (int i0 = 0; i0 < kD; i0 += 32) {
+          float s[32];
+          tmem_ld32(tmem_addr(tbase, 32 * qw, TM_S + i0), s);
+          tmem_wait_ld();
+          if (!slow) {
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) cp[(size_t)(i0 + cc) * kD + j] = s[cc];
+            for (int cc = 0; cc < 32; ++cc) s[cc] *= gam[i0 + cc];
+            tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), *reinterpret_cast<float(*)[16]>(s));
+            tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0 + 16), *reinterpret_cast<float(*)[16]>(s + 16));
+          }
+          tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_STB + i0 / 2), s);
+          if (cp)
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) cp[(size_t)(i0 + cc) * kD + j] = s[cc];
+        }
       }
       {
         __nv_bfloat16 *ostage = reinterpret_cast<__nv_bfloat16 *>(vt);
@@ -1033,6 +1048,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       } else {
         bar_state();
       }
+      // This parity's operand buffers are free (M4-M6 have completed and every
+      // state thread has read gamma_C): q and k of the chunk two ahead land in
+      // them; its A tile, gamma_C and TMEM U^T are written only after that
+      // copy has been waited for.
+      if (stid == 0 && c + 2 < nchunks) issue_qk(&maps, ctl, sm_base, h, t0 + 2 * kC, par);
       if (a.o) {  // segment passes of the long-sequence plan write no output
         const uint4 *src = reinterpret_cast<const uint4 *>(vt);
         uint4 *o = reinterpret_cast<uint4 *>(a.o);
