@@ -333,7 +333,7 @@ def run_gpu(args):
                "state_gbs": round(world * db_ / (per * 1e-3) / 1e9, 1),
                "seq_steps_per_s": round(world * dw.N / (per * 1e-3), 1),
                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                            "frac": round(gbs / hbm_peak, 4), "kernel": "decode_d128_kernel",
+                            "frac": round(gbs / hbm_peak, 4), "kernel": "decode_d128_half_kernel",
                             "algorithmic_bytes_per_launch": db_},
                "launches": dsteps}
         del dx, views

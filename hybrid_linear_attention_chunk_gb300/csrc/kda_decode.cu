@@ -120,6 +120,88 @@ decode_d128_kernel(DecodeArgs a) {
   }
 }
 
+// dk = dv = 128, no output gate: one CTA per (sequence, head, half of the
+// state's columns).  The columns are independent in this update (x, y, u, o
+// and the new column depend only on their own column and on k, q, alpha,
+// beta), so a head splits into two CTAs of 128 threads that each stream
+// 32 KB of state; four of them share an SM and overlap one another's load and
+// store phases.  Warp w owns rows [32w, 32w+32), lane l columns
+// [64 half + 2l, 64 half + 2l + 2).
+constexpr int kHalfThreads = 128;
+
+__global__ void __launch_bounds__(kHalfThreads, 4)
+decode_d128_half_kernel(DecodeArgs a) {
+  constexpr int D = 128;
+  const int nh = blockIdx.x >> 1, c0 = 64 * (blockIdx.x & 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ float s_ak[D], s_aq[D], s_k[D], s_a[D];
+  __shared__ float2 s_x[4][32], s_y[4][32];
+  __shared__ __align__(16) float s_u[64];
+  __shared__ float s_kq[4];
+
+  float2 *S = reinterpret_cast<float2 *>(a.state + (size_t)nh * D * D + c0);
+  float2 reg[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) reg[r] = __ldcs(S + (size_t)(32 * warp + r) * (D / 2) + lane);
+
+  const size_t base = (size_t)nh * D;
+  float kk = 0.f, qq = 0.f;
+  {  // thread t handles channel t
+    float g = ld_elem(a.g, base + tid, a.gdt());
+    if (a.A_log) g = decay_from_logit(g, expf(a.A_log[nh % a.H]), a.g_min);
+    const float al = expf(g);
+    kk = ld_elem(a.k, base + tid, a.qkv);
+    qq = ld_elem(a.q, base + tid, a.qkv);
+    s_a[tid] = al;
+    s_k[tid] = kk;
+    s_ak[tid] = al * kk;
+    s_aq[tid] = al * qq;
+  }
+  float kq = kk * qq;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+  if (lane == 0) s_kq[warp] = kq;
+  __syncthreads();
+
+  float2 x = make_float2(0.f, 0.f), y = x;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const int i = 32 * warp + r;
+    const float ak = s_ak[i], aq = s_aq[i];
+    x.x += reg[r].x * ak; x.y += reg[r].y * ak;
+    y.x += reg[r].x * aq; y.y += reg[r].y * aq;
+  }
+  s_x[warp][lane] = x;
+  s_y[warp][lane] = y;
+  __syncthreads();
+
+  if (tid < 64) {  // column c0 + tid
+    const int l = tid >> 1, c = tid & 1;
+    float X = 0.f, Y = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      X += c ? s_x[w][l].y : s_x[w][l].x;
+      Y += c ? s_y[w][l].y : s_y[w][l].x;
+    }
+    const float b = ld_elem(a.beta, (size_t)nh, a.gate);
+    const float u = b * (ld_elem(a.v, base + c0 + tid, a.qkv) - X);
+    s_u[tid] = u;
+    st_elem(a.o, base + c0 + tid, Y + u * (s_kq[0] + s_kq[1] + s_kq[2] + s_kq[3]), a.out);
+  }
+  __syncthreads();
+
+  const float2 u2 = reinterpret_cast<const float2 *>(s_u)[lane];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const int i = 32 * warp + r;
+    const float al = s_a[i], kv = s_k[i];
+    float2 sv = reg[r];
+    sv.x = al * sv.x + kv * u2.x;
+    sv.y = al * sv.y + kv * u2.y;
+    __stcs(S + (size_t)i * (D / 2) + lane, sv);
+  }
+}
+
 // Any supported dk, dv (<= 128): thread j owns state column j and walks the
 // rows twice (the second read mostly hits L1/L2).
 __global__ void __launch_bounds__(128)
@@ -183,7 +265,9 @@ decode_generic_kernel(DecodeArgs a) {
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
   const int blocks = a.N * a.H;
   if (blocks == 0) return cudaSuccess;
-  if (a.dk == 128 && a.dv == 128) {
+  if (a.dk == 128 && a.dv == 128 && !a.og) {
+    decode_d128_half_kernel<<<2 * blocks, kHalfThreads, 0, s>>>(a);
+  } else if (a.dk == 128 && a.dv == 128) {
     decode_d128_kernel<<<blocks, kDecThreads, 0, s>>>(a);
   } else {
     decode_generic_kernel<<<blocks, 128, 0, s>>>(a);
