@@ -248,40 +248,53 @@ def run_gpu(args):
         hq, hk, hv, hg, hb = (t.cpu().pin_memory() for t in (q, k, v, g, beta))
         ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         hs = torch.empty(sT.shape, dtype=sT.dtype).pin_memory()
-        dq, dk_, dv_, dg, db = (torch.empty_like(t) for t in (q, k, v, g, beta))
         e2e_steps = max(3, min(20, args.steps // 20))
 
-        # One sequence at a time, so that the host-to-device copy of sequence
-        # b + 1 and the device-to-host copy of sequence b - 1 overlap the call
-        # for sequence b (three streams; events keep a buffer from being
+        # The batch goes through in P token ranges of every sequence: range p
+        # of all B sequences is one kda_chunk_fwd call that resumes from the
+        # states range p - 1 left (initial_state = final_state, in place), so
+        # every call keeps all B x H chains busy.  The host-to-device copy of
+        # range p + 1 and the device-to-host copy of range p - 1 overlap the
+        # call for range p (three streams; events keep a buffer from being
         # refilled or read back while a call still uses it).
+        P = 8 if w.T % (8 * w.chunk) == 0 else 1
+        Tp = w.T // P
+        pieces = [tuple(torch.empty((w.B * Tp,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev)
+                        for t in (q, k, v, g, beta, out)) for _ in range(P)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        nb = w.B
-        ev_in = [torch.cuda.Event() for _ in range(nb)]
-        ev_done = [torch.cuda.Event() for _ in range(nb)]
-        ev_back = [torch.cuda.Event() for _ in range(nb)]
+        ev_in = [torch.cuda.Event() for _ in range(P)]
+        ev_done = [torch.cuda.Event() for _ in range(P)]
+        ev_back = [torch.cuda.Event() for _ in range(P)]
+
+        def rows(b, p):  # host rows of sequence b, range p; device rows of sequence b in a piece
+            return slice(b * w.T + p * Tp, b * w.T + (p + 1) * Tp), slice(b * Tp, (b + 1) * Tp)
 
         def e2e_step(first):
             s_in.wait_stream(stream)
-            for b in range(nb):
-                rows = slice(b * w.T, (b + 1) * w.T)
+            for p in range(P):
+                dq, dk_, dv_, dg, db, do_ = pieces[p]
                 if not first:
-                    s_in.wait_event(ev_done[b])  # the previous step's call has read these rows
+                    s_in.wait_event(ev_done[p])  # the previous step's call has read this piece
                 with torch.cuda.stream(s_in):
-                    for d_, h_ in ((dq, hq), (dk_, hk), (dv_, hv), (dg, hg), (db, hb)):
-                        d_[rows].copy_(h_[rows], non_blocking=True)
-                    ev_in[b].record(s_in)
-                stream.wait_event(ev_in[b])
+                    for b in range(w.B):
+                        hr, dr = rows(b, p)
+                        for d_, h_ in ((dq, hq), (dk_, hk), (dv_, hv), (dg, hg), (db, hb)):
+                            d_[dr].copy_(h_[hr], non_blocking=True)
+                    ev_in[p].record(s_in)
+                stream.wait_event(ev_in[p])
                 if not first:
-                    stream.wait_event(ev_back[b])  # the previous step's output rows are back on the host
-                kda.kda_chunk_fwd(dq[rows], dk_[rows], dv_[rows], dg[rows], db[rows], None, None, out[rows],
-                                  sT[b:b + 1], B=1, stream=stream)
-                ev_done[b].record(stream)
-                s_out.wait_event(ev_done[b])
+                    stream.wait_event(ev_back[p])  # the previous step's output piece is back on the host
+                kda.kda_chunk_fwd(dq, dk_, dv_, dg, db, sT if p > 0 else None, None, do_, sT, B=w.B,
+                                  stream=stream)
+                ev_done[p].record(stream)
+                s_out.wait_event(ev_done[p])
                 with torch.cuda.stream(s_out):
-                    ho[rows].copy_(out[rows], non_blocking=True)
-                    hs[b].copy_(sT[b], non_blocking=True)
-                    ev_back[b].record(s_out)
+                    for b in range(w.B):
+                        hr, dr = rows(b, p)
+                        ho[hr].copy_(do_[dr], non_blocking=True)
+                    if p == P - 1:
+                        hs.copy_(sT, non_blocking=True)
+                    ev_back[p].record(s_out)
             stream.wait_stream(s_out)
 
         e2e_step(True)
@@ -299,8 +312,9 @@ def run_gpu(args):
         e2e = {"value": round(world * tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": e2e_steps,
-               "api": "kda_chunk_fwd via ctypes per sequence, pinned host buffers, copies overlapped on two streams"}
-        del hq, hk, hv, hg, hb, dq, dk_, dv_, dg, db
+               "api": "kda_chunk_fwd via ctypes on 8 token ranges of the batch (each resuming from the previous "
+                      "range's states), pinned host buffers, copies overlapped on two streams"}
+        del hq, hk, hv, hg, hb, pieces
 
     # decode: 1000 consecutive steps of the N=256 workload
     dw = inputs.DECODE_N256
