@@ -96,10 +96,12 @@ SegPlan plan_segments(const PrefillArgs &a, int requested) {
     // time in chunk-steps of one CTA: the segment passes plus a scan step
     // (about one chunk) per segment boundary
     double best = (double)waves(chains) * nc;
-    for (int cand = 2; cand <= 64 && cand <= nc; ++cand) {
+    // (at most 16 segments: the model's gains beyond that are within its error
+    // and the workspace grows with P)
+    for (int cand = 2; cand <= 16 && cand <= nc; ++cand) {
       const long long len = (nc + cand - 1) / cand;
       const double t = (double)(waves(2 * (cand - 1) * chains) + waves(cand * chains)) * len + (cand - 1);
-      if (t < 0.8 * best) {
+      if (t < 0.97 * best) {  // (a small margin keeps ties at fewer segments)
         best = t;
         P = cand;
       }
