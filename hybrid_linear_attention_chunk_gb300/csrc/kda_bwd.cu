@@ -27,7 +27,7 @@
 // within e^{+-80} in fp32.
 //
 // Four launches, fp32 on CUDA cores:
-//   bwd_prep   (every chunk in parallel)  Qb, Kh, W, A, T, gamma of each chunk
+//   bwd_prep   (every chunk in parallel)  Qb, Kh, W, A, T_b, gamma of each chunk
 //   bwd_scan<forward>  (per sequence, head, 32 dv columns)  the entry state of every chunk
 //   bwd_scan<reverse>  (same, last chunk first)  the state gradient after every chunk; dS_0
 //   bwd_grads  (every chunk in parallel)  dq, dk, dv, dg, dbeta of the chunk's rows
@@ -41,6 +41,7 @@ constexpr int kBThreads = 256;
 constexpr int kScanDvt = 32;  // state columns per scan CTA
 constexpr int kGradDvt = 16;  // state columns per pass of the gradient kernel
 static_assert(kBThreads == kBC * kBC && kBThreads == kBC * kGradDvt, "one thread per C x C and C x pass element");
+static_assert(kBThreads == 2 * 128 && kBC == 16, "gradient tail: one channel and eight rows per thread");
 
 struct BwdArgs {
   int N, T_total, T_seq, H, dk, dv;
@@ -54,7 +55,7 @@ struct BwdArgs {
   int nslots;          // chunk slots (see slot_base)
   // workspace, per (slot, head)
   float *Qb, *Kh, *W;  // [nslots * H][C][dk]
-  float *A, *T;        // [nslots * H][C][C]
+  float *A, *Tb;       // [nslots * H][C][C]: A and T_b = T diag(beta)
   float *gam;          // [nslots * H][dk]
   float *Sent, *dSx;   // [nslots * H][dk][dv]: state before / state gradient after the chunk
 };
@@ -163,28 +164,36 @@ __device__ void setup_chunk(const BwdArgs &a, const ChunkSm &c, int t0, int len,
     c.Kh[r * ld + i] = kv * expf(Gl - G);
   }
   __syncthreads();
-  {  // one thread per (r, s): A and M
+  {  // one thread per (r, s): A and M, four channels per 128-bit load
     const int r = tid / kBC, s = tid % kBC;
     float accA = 0.f, accM = 0.f;
     if (s <= r) {
-      for (int i = 0; i < dk; ++i) {
-        const float kb = c.Kb[s * ld + i];
-        accA += c.Qb[r * ld + i] * kb;
-        accM += c.GK[r * ld + i] * kb;
+      const float *qr = c.Qb + r * ld, *gr = c.GK + r * ld, *ks = c.Kb + s * ld;
+      for (int i = 0; i < dk; i += 4) {
+        const float4 kb = *reinterpret_cast<const float4 *>(ks + i);
+        const float4 qb = *reinterpret_cast<const float4 *>(qr + i);
+        const float4 gk = *reinterpret_cast<const float4 *>(gr + i);
+        accA += qb.x * kb.x + qb.y * kb.y + qb.z * kb.z + qb.w * kb.w;
+        accM += gk.x * kb.x + gk.y * kb.y + gk.z * kb.z + gk.w * kb.w;
       }
     }
     c.A[tid] = accA;
     c.M[tid] = s < r ? accM : 0.f;
   }
   __syncthreads();
-  if (tid < kBC) {  // T = (I + L)^-1, L = diag(beta) M: one column per thread
+  if (tid < kBC) {  // T = (I + L)^-1, L = diag(beta) M: one column per thread, held in registers
+    // (I + L) T = I row by row: T[r][s] = [r == s] - beta_r sum_{m<r} M[r][m] T[m][s]
     const int s = tid;
-    for (int r = 0; r < kBC; ++r) c.T[r * kBC + s] = r == s ? 1.f : 0.f;
-    for (int r = s + 1; r < kBC; ++r) {
+    float t[kBC];
+#pragma unroll
+    for (int r = 0; r < kBC; ++r) {
       float acc = 0.f;
-      for (int m = s; m < r; ++m) acc += c.beta[r] * c.M[r * kBC + m] * c.T[m * kBC + s];
-      c.T[r * kBC + s] = -acc;
+#pragma unroll
+      for (int m = 0; m < r; ++m) acc += c.M[r * kBC + m] * t[m];
+      t[r] = r == s ? 1.f : (r > s ? -c.beta[r] * acc : 0.f);
     }
+#pragma unroll
+    for (int r = 0; r < kBC; ++r) c.T[r * kBC + s] = t[r];
   }
   __syncthreads();
 }
@@ -215,7 +224,7 @@ __global__ void __launch_bounds__(kBThreads) bwd_prep_kernel(BwdArgs a) {
   }
   for (int e = threadIdx.x; e < kBC * kBC; e += kBThreads) {
     a.A[sh * kBC * kBC + e] = c.A[e];
-    a.T[sh * kBC * kBC + e] = c.T[e];
+    a.Tb[sh * kBC * kBC + e] = c.T[e] * c.beta[e % kBC];
   }
   for (int i = threadIdx.x; i < dk; i += kBThreads) a.gam[sh * dk + i] = c.gam[i];
 }
@@ -226,9 +235,11 @@ __global__ void __launch_bounds__(kBThreads) bwd_prep_kernel(BwdArgs a) {
 // Reverse: records the gradient after each chunk, then
 // dS <- diag(gamma) dS + Qb^T dO - W^T (Kh dS + A^T dO).
 // Products are register-tiled: the C x dvt product Y = (W or Kh) S is split
-// over dk between thread groups (2 x 4 outputs per thread, partial sums
-// meeting in shared memory), the dk x dvt update takes 4 x 4 outputs per
-// thread from 128-bit shared loads.
+// over dk between thread groups (2 x 4 outputs per thread from 128-bit loads
+// of four channels, partial sums meeting in shared memory), the dk x dvt
+// update takes 4 x 4 outputs per thread from 128-bit shared loads.  The
+// [C][dk] operands keep 16-byte-padded rows so that the row pairs a warp
+// reads fall in distinct banks.
 constexpr int kSP = kScanDvt + 4;  // row stride of the [.][dvt] arrays (16-byte rows)
 
 template <bool kReverse>
@@ -246,12 +257,12 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
   float *X = S + dk * kSP;             // [C][kSP]: V or dO rows
   float *red = X + kBC * kSP;          // [nsplit][C][kSP]: partial sums
   float *Y = red;                      // [C][kSP]: V~ or dV~, over the first partial sums
-  float *Wm = red + nsplit * kBC * kSP;  // [C][dk]
-  float *Km = Wm + kBC * dk;           // [C][dk]: Kh
-  float *Qm = Km + kBC * dk;           // [C][dk]: Qb (reverse only)
-  float *Cm = Qm + (kReverse ? kBC * dk : 0);  // [C][C]: T (forward) or A (reverse)
-  float *bet = Cm + kBC * kBC;         // [C]
-  float *gm = bet + kBC;               // [dk]
+  const int ldm = dk + 4;              // row stride of the [C][dk] operands
+  float *Wm = red + nsplit * kBC * kSP;  // [C][ldm]
+  float *Km = Wm + kBC * ldm;          // [C][ldm]: Kh
+  float *Qm = Km + kBC * ldm;          // [C][ldm]: Qb (reverse only)
+  float *Cm = Qm + (kReverse ? kBC * ldm : 0);  // [C][C]: T_b (forward) or A (reverse)
+  float *gm = Cm + kBC * kBC;          // [dk]
   int bos, eos;
   bounds(a, n, bos, eos);
   const int nch = (eos - bos + kBC - 1) / kBC;
@@ -292,24 +303,37 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
       const float4 *w4 = reinterpret_cast<const float4 *>(a.W + sh * kBC * dk);
       const float4 *k4 = reinterpret_cast<const float4 *>(a.Kh + sh * kBC * dk);
       const float4 *q4 = reinterpret_cast<const float4 *>(a.Qb + sh * kBC * dk);
-      for (int e = tid; e < kBC * dk / 4; e += kBThreads) {
-        reinterpret_cast<float4 *>(Wm)[e] = w4[e];
-        reinterpret_cast<float4 *>(Km)[e] = k4[e];
-        if (kReverse) reinterpret_cast<float4 *>(Qm)[e] = q4[e];
+      const int q4r = dk / 4;
+      for (int e = tid; e < kBC * q4r; e += kBThreads) {
+        const int o = (e / q4r) * ldm + 4 * (e % q4r);
+        *reinterpret_cast<float4 *>(Wm + o) = w4[e];
+        *reinterpret_cast<float4 *>(Km + o) = k4[e];
+        if (kReverse) *reinterpret_cast<float4 *>(Qm + o) = q4[e];
       }
     }
-    Cm[tid] = kReverse ? a.A[sh * kBC * kBC + tid] : a.T[sh * kBC * kBC + tid];  // kBThreads == C * C
-    if (!kReverse && tid < kBC) bet[tid] = tid < len ? ld_elem(a.beta, (size_t)(t0 + tid) * H + h, a.gate) : 0.f;
+    Cm[tid] = kReverse ? a.A[sh * kBC * kBC + tid] : a.Tb[sh * kBC * kBC + tid];  // kBThreads == C * C
     for (int i = tid; i < dk; i += kBThreads) gm[i] = a.gam[sh * dk + i];
     __syncthreads();
     {  // partial (W S) or (Kh S) over this thread's slice of dk
-      const float *Mm = kReverse ? Km : Wm;
+      const float *m0p = (kReverse ? Km : Wm) + r0 * ldm, *m1p = m0p + ldm;
       float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-      const int ia = sp * ilen;
-#pragma unroll 4
-      for (int i = ia; i < ia + ilen; ++i) {
+      const int ia = sp * ilen, ie = ia + ilen;
+      int i = ia;
+#pragma unroll 2
+      for (; i + 4 <= ie; i += 4) {  // (ilen is a multiple of 4 whenever this runs: ia is aligned)
+        const float4 a4 = *reinterpret_cast<const float4 *>(m0p + i);
+        const float4 b4 = *reinterpret_cast<const float4 *>(m1p + i);
+        const float ma[4] = {a4.x, a4.y, a4.z, a4.w}, mb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 s4 = *reinterpret_cast<const float4 *>(S + (i + q) * kSP + cy);
+          acc0.x += ma[q] * s4.x; acc0.y += ma[q] * s4.y; acc0.z += ma[q] * s4.z; acc0.w += ma[q] * s4.w;
+          acc1.x += mb[q] * s4.x; acc1.y += mb[q] * s4.y; acc1.z += mb[q] * s4.z; acc1.w += mb[q] * s4.w;
+        }
+      }
+      for (; i < ie; ++i) {  // slices of fewer than four channels (dk = 16 with 16 state columns)
         const float4 s4 = *reinterpret_cast<const float4 *>(S + i * kSP + cy);
-        const float m0 = Mm[r0 * dk + i], m1 = Mm[(r0 + 1) * dk + i];
+        const float m0 = m0p[i], m1 = m1p[i];
         acc0.x += m0 * s4.x; acc0.y += m0 * s4.y; acc0.z += m0 * s4.z; acc0.w += m0 * s4.w;
         acc1.x += m1 * s4.x; acc1.y += m1 * s4.y; acc1.z += m1 * s4.z; acc1.w += m1 * s4.w;
       }
@@ -323,7 +347,7 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
       for (int q = 0; q < nsplit; ++q) part += red[(q * kBC + r) * kSP + cc];
       float y = 0.f;
       if (!kReverse) {  // V~ = T_b V - W S
-        for (int s = 0; s <= r; ++s) y += Cm[r * kBC + s] * bet[s] * X[s * kSP + cc];
+        for (int s = 0; s <= r; ++s) y += Cm[r * kBC + s] * X[s * kSP + cc];
         y -= part;
       } else {          // dV~ = A^T dO + Kh dS
         for (int s = r; s < kBC; ++s) y += Cm[s * kBC + r] * X[s * kSP + cc];
@@ -345,7 +369,7 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
       for (int r = 0; r < kBC; ++r) {
         const float4 y4 = *reinterpret_cast<const float4 *>(Y + r * kSP + cu0);
         if (!kReverse) {
-          const float4 k4 = *reinterpret_cast<const float4 *>(Km + r * dk + i0);
+          const float4 k4 = *reinterpret_cast<const float4 *>(Km + r * ldm + i0);
           const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -353,8 +377,8 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
           }
         } else {
           const float4 o4 = *reinterpret_cast<const float4 *>(X + r * kSP + cu0);
-          const float4 q4 = *reinterpret_cast<const float4 *>(Qm + r * dk + i0);
-          const float4 w4 = *reinterpret_cast<const float4 *>(Wm + r * dk + i0);
+          const float4 q4 = *reinterpret_cast<const float4 *>(Qm + r * ldm + i0);
+          const float4 w4 = *reinterpret_cast<const float4 *>(Wm + r * ldm + i0);
           const float qq[4] = {q4.x, q4.y, q4.z, q4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -379,7 +403,7 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
 size_t scan_smem_bytes(bool reverse, int dk, int dv) {
   const int ncb = (dv < kScanDvt ? dv : kScanDvt) / 4, nsplit = kBThreads / (8 * ncb);
   return sizeof(float) * ((size_t)dk * kSP + kBC * kSP + (size_t)nsplit * kBC * kSP +
-                          (reverse ? 3 : 2) * kBC * dk + kBC * kBC + kBC + dk);
+                          (reverse ? 3 : 2) * kBC * ((size_t)dk + 4) + kBC * kBC + dk);
 }
 
 // Gradients of one chunk's rows, from its entry state and the state gradient
@@ -428,28 +452,47 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
   const int zr = 2 * (zb >> 3), zc = 2 * (zb & 7);
   const size_t sh = (size_t)slot * H + h;
   const float *Sg = a.Sent + sh * dk * dv, *dSg = a.dSx + sh * dk * dv;
+  // A pass's inputs are fetched into registers one pass ahead, so that their
+  // global-memory latency overlaps the previous pass: S and dS' columns (two
+  // 4-column pieces per thread, dk <= 128) and one element each of V and dO
+  // (kBThreads == C * kGradDvt).
+  float4 pS[2], pD[2];
+  float pv = 0.f, pd = 0.f;
+  const int vr = tid / kGradDvt, vc = tid % kGradDvt;
+  auto fetch = [&](int c0) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = tid + u * kBThreads;
+      if (e < dk * (kGradDvt / 4)) {
+        const size_t o = (size_t)(e / (kGradDvt / 4)) * dv + c0 + 4 * (e % (kGradDvt / 4));
+        pS[u] = *reinterpret_cast<const float4 *>(Sg + o);
+        pD[u] = *reinterpret_cast<const float4 *>(dSg + o);
+      }
+    }
+    pv = pd = 0.f;
+    if (vr < len) {
+      const size_t idx = ((size_t)(t0 + vr) * H + h) * dv + c0 + vc;
+      pv = ld_elem(a.v, idx, a.qkv);
+      pd = ld_elem(a.dO, idx, a.out);
+    }
+  };
+  fetch(0);
   for (int c0 = 0; c0 < dv; c0 += kGradDvt) {
     __syncthreads();  // the previous pass is done with the column buffers
-    for (int e = tid; e < dk * (kGradDvt / 4); e += kBThreads) {  // S, dS' columns, transposed
-      const int i = e / (kGradDvt / 4), cq = 4 * (e % (kGradDvt / 4));
-      const float4 sv = *reinterpret_cast<const float4 *>(Sg + (size_t)i * dv + c0 + cq);
-      const float4 dv4 = *reinterpret_cast<const float4 *>(dSg + (size_t)i * dv + c0 + cq);
-      St[(cq + 0) * ld + i] = sv.x; St[(cq + 1) * ld + i] = sv.y;
-      St[(cq + 2) * ld + i] = sv.z; St[(cq + 3) * ld + i] = sv.w;
-      dSt[(cq + 0) * ld + i] = dv4.x; dSt[(cq + 1) * ld + i] = dv4.y;
-      dSt[(cq + 2) * ld + i] = dv4.z; dSt[(cq + 3) * ld + i] = dv4.w;
-    }
-    {  // V and dO rows (one element per thread: kBThreads == C * kGradDvt)
-      const int r = tid / kGradDvt, cc = tid % kGradDvt;
-      float vv = 0.f, dd = 0.f;
-      if (r < len) {
-        const size_t idx = ((size_t)(t0 + r) * H + h) * dv + c0 + cc;
-        vv = ld_elem(a.v, idx, a.qkv);
-        dd = ld_elem(a.dO, idx, a.out);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {  // S, dS' columns, transposed
+      const int e = tid + u * kBThreads;
+      if (e < dk * (kGradDvt / 4)) {
+        const int i = e / (kGradDvt / 4), cq = 4 * (e % (kGradDvt / 4));
+        St[(cq + 0) * ld + i] = pS[u].x; St[(cq + 1) * ld + i] = pS[u].y;
+        St[(cq + 2) * ld + i] = pS[u].z; St[(cq + 3) * ld + i] = pS[u].w;
+        dSt[(cq + 0) * ld + i] = pD[u].x; dSt[(cq + 1) * ld + i] = pD[u].y;
+        dSt[(cq + 2) * ld + i] = pD[u].z; dSt[(cq + 3) * ld + i] = pD[u].w;
       }
-      Pt[cc * lw + r] = vv;
-      dOt[cc * lw + r] = dd;
     }
+    Pt[vc * lw + vr] = pv;  // V rows (P = V - GK S after the next step)
+    dOt[vc * lw + vr] = pd;
+    if (c0 + kGradDvt < dv) fetch(c0 + kGradDvt);
     __syncthreads();
     {  // partial Z = GK S (zp = 0) or Y = Kh dS' (zp = 1) over half of dk, 2 x 2 outputs
       const float *Mm = zp ? c.Kh : c.GK;
@@ -560,18 +603,45 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
     if (s > r) dA[tid] = 0.f;              // Tril_incl
   }
   __syncthreads();
-  for (int e = tid; e < kBC * dk; e += kBThreads) {
-    const int r = e / dk, i = e % dk;
-    float gk = 0.f, kb = 0.f, qb = 0.f;
-    for (int s = 0; s < kBC; ++s) {
-      gk += X[r * kBC + s] * c.Kb[s * ld + i];      // dM Kb
-      kb += X[s * kBC + r] * c.GK[s * ld + i]       // dM^T GK
-            + dA[s * kBC + r] * c.Qb[s * ld + i];   // dA^T Qb
-      qb += dA[r * kBC + s] * c.Kb[s * ld + i];     // dA Kb
+  {  // dGK += dM Kb, dKb = dM^T GK + dA^T Qb, dQb += dA Kb: channel i, rows r0..r0+7 per thread
+    const int i = tid & 127, r0 = 8 * (tid >> 7);
+    if (i < dk) {
+      float gk[8] = {}, kb[8] = {}, qb[8] = {};
+#pragma unroll 1
+      for (int s0 = 0; s0 < kBC; s0 += 4) {
+        float kbs[4], gks[4], qbs[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          kbs[u] = c.Kb[(s0 + u) * ld + i];
+          gks[u] = c.GK[(s0 + u) * ld + i];
+          qbs[u] = c.Qb[(s0 + u) * ld + i];
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {  // row r0 + q of dM and dA, columns s0..s0+3
+          const float4 x4 = *reinterpret_cast<const float4 *>(X + (r0 + q) * kBC + s0);
+          const float4 a4 = *reinterpret_cast<const float4 *>(dA + (r0 + q) * kBC + s0);
+          gk[q] += x4.x * kbs[0] + x4.y * kbs[1] + x4.z * kbs[2] + x4.w * kbs[3];
+          qb[q] += a4.x * kbs[0] + a4.y * kbs[1] + a4.z * kbs[2] + a4.w * kbs[3];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {  // row s0 + u of dM and dA, columns r0..r0+7
+          const float4 xa = *reinterpret_cast<const float4 *>(X + (s0 + u) * kBC + r0);
+          const float4 xb = *reinterpret_cast<const float4 *>(X + (s0 + u) * kBC + r0 + 4);
+          const float4 da = *reinterpret_cast<const float4 *>(dA + (s0 + u) * kBC + r0);
+          const float4 db = *reinterpret_cast<const float4 *>(dA + (s0 + u) * kBC + r0 + 4);
+          const float xm[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+          const float dm[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) kb[q] += xm[q] * gks[u] + dm[q] * qbs[u];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        dGK[(r0 + q) * ld + i] += gk[q];
+        dKb[(r0 + q) * ld + i] = kb[q];
+        dQb[(r0 + q) * ld + i] += qb[q];
+      }
     }
-    dGK[r * ld + i] += gk;
-    dKb[r * ld + i] = kb;
-    dQb[r * ld + i] += qb;
   }
   __syncthreads();
   // elementwise to q, k and the cumulative log-decay G (dG in dKb's place)
@@ -636,7 +706,7 @@ cudaError_t launch_chunk_bwd(const PrefillArgs &p, const BwdIo &io, void *ws, cu
   a.Kh = w;  w += sl * kBC * p.dk;
   a.W = w;   w += sl * kBC * p.dk;
   a.A = w;   w += sl * kBC * kBC;
-  a.T = w;   w += sl * kBC * kBC;
+  a.Tb = w;  w += sl * kBC * kBC;
   a.gam = w; w += sl * p.dk;
   a.Sent = w; w += sl * (size_t)p.dk * p.dv;
   a.dSx = w;
