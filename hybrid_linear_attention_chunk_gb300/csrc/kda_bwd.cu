@@ -42,6 +42,7 @@ constexpr int kScanDvt = 32;  // state columns per scan CTA
 constexpr int kGradDvt = 16;  // state columns per pass of the gradient kernel
 static_assert(kBThreads == kBC * kBC && kBThreads == kBC * kGradDvt, "one thread per C x C and C x pass element");
 static_assert(kBThreads == 2 * 128 && kBC == 16, "gradient tail: one channel and eight rows per thread");
+static_assert(kBC * 128 / 4 <= 2 * kBThreads, "chunk loads: at most two 4-channel pieces per thread");
 
 struct BwdArgs {
   int N, T_total, T_seq, H, dk, dv;
@@ -99,6 +100,15 @@ __device__ bool locate(const BwdArgs &a, int slot, int &n, int &j) {
   return j >= 0 && j < (len + kBC - 1) / kBC;
 }
 
+// 16-byte asynchronous global -> shared copies (zero-filled past src_bytes).
+// Unlike a load into registers, a copy in flight does not hold up a barrier.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 // ------------------------------------------------------------- chunk setup
 
 // Shared-memory arrays of one chunk (row stride ld = dk + 4 for [C][dk]).
@@ -129,18 +139,30 @@ __device__ __forceinline__ float *carve_chunk(ChunkSm &c, float *p, int dk) {
 // gamma, A, M and T = (I + L)^-1.  Ends with a barrier.
 __device__ void setup_chunk(const BwdArgs &a, const ChunkSm &c, int t0, int len, int h) {
   const int dk = a.dk, H = a.H, ld = c.ld, tid = threadIdx.x;
-  for (int e = tid; e < kBC * dk; e += kBThreads) {
-    const int r = e / dk, i = e % dk;
-    float qv = 0.f, kv = 0.f, gv = 0.f;
-    if (r < len) {
-      const size_t idx = ((size_t)(t0 + r) * H + h) * dk + i;
-      qv = ld_elem(a.q, idx, a.qkv);
-      kv = ld_elem(a.k, idx, a.qkv);
-      gv = ld_elem(a.g, idx, a.gate);
+  {  // q, k and the log-decay in 4-channel pieces (at most two per thread), all loads issued first
+    const int q4 = dk / 4;
+    float4 qv[2], kv[2], gv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = tid + u * kBThreads, r = e / q4;
+      qv[u] = kv[u] = gv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < kBC * q4 && r < len) {
+        const size_t idx = ((size_t)(t0 + r) * H + h) * dk + 4 * (e % q4);
+        qv[u] = ld4_elem(a.q, idx, a.qkv);
+        kv[u] = ld4_elem(a.k, idx, a.qkv);
+        gv[u] = ld4_elem(a.g, idx, a.gate);
+      }
     }
-    c.Qb[r * ld + i] = qv;
-    c.Kb[r * ld + i] = kv;
-    c.G[r * ld + i] = gv;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = tid + u * kBThreads;
+      if (e < kBC * q4) {
+        const int o = (e / q4) * ld + 4 * (e % q4);
+        *reinterpret_cast<float4 *>(c.Qb + o) = qv[u];
+        *reinterpret_cast<float4 *>(c.Kb + o) = kv[u];
+        *reinterpret_cast<float4 *>(c.G + o) = gv[u];
+      }
+    }
   }
   if (tid < kBC) c.beta[tid] = tid < len ? ld_elem(a.beta, (size_t)(t0 + tid) * H + h, a.gate) : 0.f;
   __syncthreads();
@@ -173,8 +195,8 @@ __device__ void setup_chunk(const BwdArgs &a, const ChunkSm &c, int t0, int len,
         const float4 kb = *reinterpret_cast<const float4 *>(ks + i);
         const float4 qb = *reinterpret_cast<const float4 *>(qr + i);
         const float4 gk = *reinterpret_cast<const float4 *>(gr + i);
-        accA += qb.x * kb.x + qb.y * kb.y + qb.z * kb.z + qb.w * kb.w;
-        accM += gk.x * kb.x + gk.y * kb.y + gk.z * kb.z + gk.w * kb.w;
+        accA = fmaf(qb.x, kb.x, fmaf(qb.y, kb.y, fmaf(qb.z, kb.z, fmaf(qb.w, kb.w, accA))));
+        accM = fmaf(gk.x, kb.x, fmaf(gk.y, kb.y, fmaf(gk.z, kb.z, fmaf(gk.w, kb.w, accM))));
       }
     }
     c.A[tid] = accA;
@@ -411,7 +433,7 @@ size_t scan_smem_bytes(bool reverse, int dk, int dv) {
 // its state columns transposed ([column][dk], 16-byte rows) so that every
 // product reads 128-bit operands; the C x dk gradient sums live in registers
 // across the passes (4 rows x 2 channels of dQb, dKh and dGK per thread).
-__global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(kBThreads, 2) bwd_grads_kernel(BwdArgs a) {
   extern __shared__ __align__(16) float smem[];
   const int slot = blockIdx.x, h = blockIdx.y;
   int n, j;
@@ -424,14 +446,12 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
   float *p = carve_chunk(c, smem, dk);
   const int ld = c.ld;
   constexpr int lw = kBC + 4;      // row stride of the [column][C] arrays
-  float *dQb = p; p += kBC * ld;
-  float *dKb = p; p += kBC * ld;
-  float *dGK = p; p += kBC * ld;
-  float *dKh = p; p += kBC * ld;
   float *dA = p;  p += kBC * kBC;
   float *dTb = p; p += kBC * kBC;
   float *X = p;   p += kBC * kBC;
   float *dgam = p; p += 128;
+  // The rest is used twice: by the column passes, then by the tail's [C][dk] gradients.
+  float *dQb = p, *dKb = p + kBC * ld, *dGK = p + 2 * kBC * ld, *dKh = p + 3 * kBC * ld;
   float *St = p;  p += kGradDvt * ld;   // S^T of this pass: [column][dk]
   float *dSt = p; p += kGradDvt * ld;   // dS'^T
   float *Pt = p;  p += kGradDvt * lw;   // V, then P = V - GK S: [column][row]
@@ -440,6 +460,10 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
   float *dVtt = p; p += kGradDvt * lw;  // dV~
   float *dVv = p; p += kGradDvt * lw;   // dV
   float *red = p; p += 4 * kBC * kBC;   // [product][dk half][row][column]
+  float *Sst = p; p += dk * kGradDvt;   // staging of the next pass: S columns [dk][kGradDvt]
+  float *dSst = p; p += dk * kGradDvt;  // dS' columns
+  float *Vst = p; p += kBC * kGradDvt;  // V rows [C][kGradDvt], qkv dtype
+  float *dOst = p;                      // dO rows, out dtype
   setup_chunk(a, c, t0, len, h);
   // register accumulators
   const int rb = 4 * (tid & 3), ip = 2 * (tid >> 2);  // rows rb..rb+3, channels ip, ip+1
@@ -452,48 +476,57 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
   const int zr = 2 * (zb >> 3), zc = 2 * (zb & 7);
   const size_t sh = (size_t)slot * H + h;
   const float *Sg = a.Sent + sh * dk * dv, *dSg = a.dSx + sh * dk * dv;
-  // A pass's inputs are fetched into registers one pass ahead, so that their
-  // global-memory latency overlaps the previous pass: S and dS' columns (two
-  // 4-column pieces per thread, dk <= 128) and one element each of V and dO
-  // (kBThreads == C * kGradDvt).
-  float4 pS[2], pD[2];
-  float pv = 0.f, pd = 0.f;
-  const int vr = tid / kGradDvt, vc = tid % kGradDvt;
+  // A pass's inputs are copied into the staging area one pass ahead, so that
+  // their global-memory latency overlaps the previous pass: S and dS' columns
+  // (64 bytes of each of dk rows) and the C rows of V and dO (kGradDvt
+  // elements each, rows past the chunk's end zero-filled).
+  static_assert(kGradDvt == 16, "a pass row is four 16-byte pieces of fp32, two or four of its V / dO row");
+  const int vsz = a.qkv == KDA_BF16 ? 2 : 4, osz = a.out == KDA_BF16 ? 2 : 4;
+  // This thread's V / dO piece: rows of 16 elements are 2 (bf16) or 4 (fp32) pieces.
+  const int vsh = vsz == 2 ? 1 : 2, osh = osz == 2 ? 1 : 2;
+  const bool vpiece = tid < (kBC << vsh), opiece = tid >= 128 && tid - 128 < (kBC << osh);
+  const int vrow = vpiece ? tid >> vsh : opiece ? (tid - 128) >> osh : 0;
+  const int vpc = vpiece ? tid & ((1 << vsh) - 1) : opiece ? (tid - 128) & ((1 << osh) - 1) : 0;
+  const size_t vrow_off = ((size_t)(t0 + (vrow < len ? vrow : 0)) * H + h) * dv;  // (in range when zero-filled)
   auto fetch = [&](int c0) {
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int e = tid + u * kBThreads;
-      if (e < dk * (kGradDvt / 4)) {
-        const size_t o = (size_t)(e / (kGradDvt / 4)) * dv + c0 + 4 * (e % (kGradDvt / 4));
-        pS[u] = *reinterpret_cast<const float4 *>(Sg + o);
-        pD[u] = *reinterpret_cast<const float4 *>(dSg + o);
-      }
+    for (int e = tid; e < dk * 4; e += kBThreads) {  // row e / 4, columns 4 (e % 4) .. + 3
+      const size_t go = (size_t)(e >> 2) * dv + c0 + 4 * (e & 3);
+      cp_async16(Sst + 4 * e, Sg + go, 16);
+      cp_async16(dSst + 4 * e, dSg + go, 16);
     }
-    pv = pd = 0.f;
-    if (vr < len) {
-      const size_t idx = ((size_t)(t0 + vr) * H + h) * dv + c0 + vc;
-      pv = ld_elem(a.v, idx, a.qkv);
-      pd = ld_elem(a.dO, idx, a.out);
-    }
+    if (vpiece)
+      cp_async16(reinterpret_cast<char *>(Vst) + 16 * tid,
+                 reinterpret_cast<const char *>(a.v) + (vrow_off + c0) * vsz + 16 * vpc, vrow < len ? 16 : 0);
+    if (opiece)
+      cp_async16(reinterpret_cast<char *>(dOst) + 16 * (tid - 128),
+                 reinterpret_cast<const char *>(a.dO) + (vrow_off + c0) * osz + 16 * vpc, vrow < len ? 16 : 0);
+    cp_async_commit();
   };
+  const int vr = tid / kGradDvt, vc = tid % kGradDvt;  // kBThreads == C * kGradDvt
   fetch(0);
   for (int c0 = 0; c0 < dv; c0 += kGradDvt) {
-    __syncthreads();  // the previous pass is done with the column buffers
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {  // S, dS' columns, transposed
-      const int e = tid + u * kBThreads;
-      if (e < dk * (kGradDvt / 4)) {
-        const int i = e / (kGradDvt / 4), cq = 4 * (e % (kGradDvt / 4));
-        St[(cq + 0) * ld + i] = pS[u].x; St[(cq + 1) * ld + i] = pS[u].y;
-        St[(cq + 2) * ld + i] = pS[u].z; St[(cq + 3) * ld + i] = pS[u].w;
-        dSt[(cq + 0) * ld + i] = pD[u].x; dSt[(cq + 1) * ld + i] = pD[u].y;
-        dSt[(cq + 2) * ld + i] = pD[u].z; dSt[(cq + 3) * ld + i] = pD[u].w;
-      }
+    cp_async_wait_all();
+    __syncthreads();  // this pass's staging has landed; the previous pass is done with the column buffers
+    for (int e = tid; e < 2 * dk; e += kBThreads) {  // S, dS' columns, transposed in 4 x 4 blocks
+      const int w = e >= dk, b = w ? e - dk : e;  // array, then block b < dk: rows 4 (b / 4).., columns 4 (b % 4)..
+      const int i0 = 4 * (b >> 2), cq = 4 * (b & 3);
+      const float *src = (w ? dSst : Sst) + i0 * kGradDvt + cq;
+      float *dst = (w ? dSt : St) + cq * ld + i0;
+      const float4 r0 = *reinterpret_cast<const float4 *>(src), r1 = *reinterpret_cast<const float4 *>(src + kGradDvt),
+                   r2 = *reinterpret_cast<const float4 *>(src + 2 * kGradDvt),
+                   r3 = *reinterpret_cast<const float4 *>(src + 3 * kGradDvt);
+      *reinterpret_cast<float4 *>(dst) = make_float4(r0.x, r1.x, r2.x, r3.x);
+      *reinterpret_cast<float4 *>(dst + ld) = make_float4(r0.y, r1.y, r2.y, r3.y);
+      *reinterpret_cast<float4 *>(dst + 2 * ld) = make_float4(r0.z, r1.z, r2.z, r3.z);
+      *reinterpret_cast<float4 *>(dst + 3 * ld) = make_float4(r0.w, r1.w, r2.w, r3.w);
     }
-    Pt[vc * lw + vr] = pv;  // V rows (P = V - GK S after the next step)
-    dOt[vc * lw + vr] = pd;
+    {  // V rows (P = V - GK S after the next step) and dO rows, widened to fp32
+      const int o = vr * kGradDvt + vc;
+      Pt[vc * lw + vr] = vsz == 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(Vst)[o]) : Vst[o];
+      dOt[vc * lw + vr] = osz == 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dOst)[o]) : dOst[o];
+    }
+    __syncthreads();  // the staging area is free for the next pass
     if (c0 + kGradDvt < dv) fetch(c0 + kGradDvt);
-    __syncthreads();
     {  // partial Z = GK S (zp = 0) or Y = Kh dS' (zp = 1) over half of dk, 2 x 2 outputs
       const float *Mm = zp ? c.Kh : c.GK;
       const float *Vm = zp ? dSt : St;
@@ -505,10 +538,10 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
         const float4 m1 = *reinterpret_cast<const float4 *>(Mm + (zr + 1) * ld + i);
         const float4 v0 = *reinterpret_cast<const float4 *>(Vm + zc * ld + i);
         const float4 v1 = *reinterpret_cast<const float4 *>(Vm + (zc + 1) * ld + i);
-        a00 += m0.x * v0.x + m0.y * v0.y + m0.z * v0.z + m0.w * v0.w;
-        a01 += m0.x * v1.x + m0.y * v1.y + m0.z * v1.z + m0.w * v1.w;
-        a10 += m1.x * v0.x + m1.y * v0.y + m1.z * v0.z + m1.w * v0.w;
-        a11 += m1.x * v1.x + m1.y * v1.y + m1.z * v1.z + m1.w * v1.w;
+        a00 = fmaf(m0.x, v0.x, fmaf(m0.y, v0.y, fmaf(m0.z, v0.z, fmaf(m0.w, v0.w, a00))));
+        a01 = fmaf(m0.x, v1.x, fmaf(m0.y, v1.y, fmaf(m0.z, v1.z, fmaf(m0.w, v1.w, a01))));
+        a10 = fmaf(m1.x, v0.x, fmaf(m1.y, v0.y, fmaf(m1.z, v0.z, fmaf(m1.w, v0.w, a10))));
+        a11 = fmaf(m1.x, v1.x, fmaf(m1.y, v1.y, fmaf(m1.z, v1.z, fmaf(m1.w, v1.w, a11))));
       }
       float *rd = red + (zp * 2 + zq) * kBC * kBC;
       rd[zr * kBC + zc] = a00;
@@ -560,6 +593,7 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
     if (tid < dk)
       for (int cc = 0; cc < kGradDvt; ++cc) accGam += dSt[cc * ld + tid] * St[cc * ld + tid];
   }
+  __syncthreads();  // the pass buffers become dQb, dKb, dGK, dKh
   if (own)
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -672,8 +706,10 @@ __global__ void __launch_bounds__(kBThreads) bwd_grads_kernel(BwdArgs a) {
 
 size_t grads_smem_bytes(int dk) {
   const size_t ld = (size_t)dk + 4, lw = kBC + 4;
-  return sizeof(float) * (9 * kBC * ld + 6 * kBC * kBC + kBC + 2 * 128 + 2 * kGradDvt * ld + 5 * kGradDvt * lw +
-                          4 * kBC * kBC);
+  const size_t pass = 2 * kGradDvt * ld + 5 * kGradDvt * lw + 4 * kBC * kBC + 2 * (size_t)dk * kGradDvt +
+                      2 * kBC * kGradDvt;
+  const size_t tail = 4 * kBC * ld;
+  return sizeof(float) * (5 * kBC * ld + 6 * kBC * kBC + kBC + 2 * 128 + (pass > tail ? pass : tail));
 }
 
 size_t prep_smem_bytes(int dk) {

@@ -134,6 +134,17 @@ __device__ __forceinline__ float ld_elem(const void *p, size_t i, kda_dtype t) {
   return reinterpret_cast<const float *>(p)[i];
 }
 
+// Four consecutive elements from index i (a multiple of 4; base 16-byte aligned).
+__device__ __forceinline__ float4 ld4_elem(const void *p, size_t i, kda_dtype t) {
+  if (t == KDA_BF16) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p) + i);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+  }
+  return *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p) + i);
+}
+
 __device__ __forceinline__ void st_elem(void *p, size_t i, float x, kda_dtype t) {
   if (t == KDA_BF16) reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
   else reinterpret_cast<float *>(p)[i] = x;
