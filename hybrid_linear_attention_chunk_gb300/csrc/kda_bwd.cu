@@ -109,6 +109,52 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_b
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
+// fp32 products on the tensor cores: mma.sync m16n8k8 with tf32 operands,
+// each operand x split as hi = tf32(x), lo = tf32(x - hi) and the product
+// taken as lo_a hi_b + hi_a lo_b + hi_a hi_b (the dropped lo_a lo_b term is
+// below fp32 rounding).  Fragments per the PTX ISA for this shape, with
+// g = lane / 4 and t = lane % 4: A (16 x 8, row) holds (g, t), (g + 8, t),
+// (g, t + 4), (g + 8, t + 4); B (8 x 8, col) holds (t, g), (t + 4, g);
+// D (16 x 8) holds (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void split_frag(uint32_t (&hi)[4], uint32_t (&lo)[4], float x0, float x1, float x2,
+                                           float x3) {
+  const float x[4] = {x0, x1, x2, x3};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    hi[i] = to_tf32(x[i]);
+    lo[i] = to_tf32(x[i] - __uint_as_float(hi[i]));
+  }
+}
+__device__ __forceinline__ void split_frag(uint32_t (&hi)[2], uint32_t (&lo)[2], float x0, float x1) {
+  hi[0] = to_tf32(x0);
+  lo[0] = to_tf32(x0 - __uint_as_float(hi[0]));
+  hi[1] = to_tf32(x1);
+  lo[1] = to_tf32(x1 - __uint_as_float(hi[1]));
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                           const uint32_t (&bh)[2], const uint32_t (&bl)[2]) {
+  mma_tf32(d, al, bh);
+  mma_tf32(d, ah, bl);
+  mma_tf32(d, ah, bh);
+}
+__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+  split_frag(ah, al, a[0], a[1], a[2], a[3]);
+  split_frag(bh, bl, b[0], b[1]);
+  mma_3xtf32(d, ah, al, bh, bl);
+}
+
 // ------------------------------------------------------------- chunk setup
 
 // Shared-memory arrays of one chunk (row stride ld = dk + 4 for [C][dk]).
@@ -445,38 +491,30 @@ __global__ void __launch_bounds__(kBThreads, 2) bwd_grads_kernel(BwdArgs a) {
   ChunkSm c;
   float *p = carve_chunk(c, smem, dk);
   const int ld = c.ld;
-  constexpr int lw = kBC + 4;      // row stride of the [column][C] arrays
+  constexpr int lr = kGradDvt + 4;  // row stride of the [row][column] pass arrays and of the staged rows
   float *dA = p;  p += kBC * kBC;
   float *dTb = p; p += kBC * kBC;
   float *X = p;   p += kBC * kBC;
   float *dgam = p; p += 128;
   // The rest is used twice: by the column passes, then by the tail's [C][dk] gradients.
   float *dQb = p, *dKb = p + kBC * ld, *dGK = p + 2 * kBC * ld, *dKh = p + 3 * kBC * ld;
-  float *St = p;  p += kGradDvt * ld;   // S^T of this pass: [column][dk]
-  float *dSt = p; p += kGradDvt * ld;   // dS'^T
-  float *Pt = p;  p += kGradDvt * lw;   // V, then P = V - GK S: [column][row]
-  float *dOt = p; p += kGradDvt * lw;
-  float *Vtt = p; p += kGradDvt * lw;   // V~
-  float *dVtt = p; p += kGradDvt * lw;  // dV~
-  float *dVv = p; p += kGradDvt * lw;   // dV
-  float *red = p; p += 4 * kBC * kBC;   // [product][dk half][row][column]
-  float *Sst = p; p += dk * kGradDvt;   // staging of the next pass: S columns [dk][kGradDvt]
-  float *dSst = p; p += dk * kGradDvt;  // dS' columns
-  float *Vst = p; p += kBC * kGradDvt;  // V rows [C][kGradDvt], qkv dtype
-  float *dOst = p;                      // dO rows, out dtype
+  float *Pr = p;   p += kBC * lr;   // V, then P = V - GK S: [row][column]
+  float *dOr = p;  p += kBC * lr;   // dO
+  float *Vtr = p;  p += kBC * lr;   // V~
+  float *dVtr = p; p += kBC * lr;   // dV~
+  float *dVr = p;  p += kBC * lr;   // dV
+  float *red = p;  p += 4 * kBC * kBC;  // [product][dk half][row][column]
+  float *Sb = p;   p += 4 * dk * lr;    // two staging buffers, each the pass's S rows then dS' rows: [dk][lr]
+  float *Vb = p;                        // two staging buffers of 2 KB: V rows, then dO rows at +1 KB, in their dtypes
   setup_chunk(a, c, t0, len, h);
-  // register accumulators
-  const int rb = 4 * (tid & 3), ip = 2 * (tid >> 2);  // rows rb..rb+3, channels ip, ip+1
-  const bool own = ip < dk;
-  float aQ[4][2] = {}, aH[4][2] = {}, aG[4][2] = {};
-  const int rr = tid / kBC, ss = tid % kBC;  // (row, column) of the C x C sums
-  float accTb = 0.f, accA = 0.f, accGam = 0.f;
-  // tasks of the two C x w products over dk: Z = GK S, Y = Kh dS'
-  const int zp = tid >> 7, zq = (tid >> 6) & 1, zb = tid & 63;
-  const int zr = 2 * (zb >> 3), zc = 2 * (zb & 7);
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;  // mma fragment coordinates
+  const int rr = tid / kBC, ss = tid % kBC;  // (row, column) of the C x C steps
+  // accumulators over the passes: dQb, dKh, dGK (channels 16 warp .. + 15, two n-tiles), dT_b or dA (warps 4-7)
+  float accQ[2][4] = {}, accH[2][4] = {}, accG[2][4] = {}, accTA[4] = {};
+  float accGam = 0.f;
   const size_t sh = (size_t)slot * H + h;
   const float *Sg = a.Sent + sh * dk * dv, *dSg = a.dSx + sh * dk * dv;
-  // A pass's inputs are copied into the staging area one pass ahead, so that
+  // A pass's inputs are copied into a staging buffer one pass ahead, so that
   // their global-memory latency overlaps the previous pass: S and dS' columns
   // (64 bytes of each of dk rows) and the C rows of V and dO (kGradDvt
   // elements each, rows past the chunk's end zero-filled).
@@ -488,121 +526,127 @@ __global__ void __launch_bounds__(kBThreads, 2) bwd_grads_kernel(BwdArgs a) {
   const int vrow = vpiece ? tid >> vsh : opiece ? (tid - 128) >> osh : 0;
   const int vpc = vpiece ? tid & ((1 << vsh) - 1) : opiece ? (tid - 128) & ((1 << osh) - 1) : 0;
   const size_t vrow_off = ((size_t)(t0 + (vrow < len ? vrow : 0)) * H + h) * dv;  // (in range when zero-filled)
-  auto fetch = [&](int c0) {
+  auto fetch = [&](int c0, int bi) {
+    float *sS = Sb + bi * 2 * dk * lr, *sD = sS + dk * lr;
+    char *vb = reinterpret_cast<char *>(Vb + bi * 512);
     for (int e = tid; e < dk * 4; e += kBThreads) {  // row e / 4, columns 4 (e % 4) .. + 3
-      const size_t go = (size_t)(e >> 2) * dv + c0 + 4 * (e & 3);
-      cp_async16(Sst + 4 * e, Sg + go, 16);
-      cp_async16(dSst + 4 * e, dSg + go, 16);
+      const int i = e >> 2, q = 4 * (e & 3);
+      const size_t go = (size_t)i * dv + c0 + q;
+      cp_async16(sS + i * lr + q, Sg + go, 16);
+      cp_async16(sD + i * lr + q, dSg + go, 16);
     }
     if (vpiece)
-      cp_async16(reinterpret_cast<char *>(Vst) + 16 * tid,
-                 reinterpret_cast<const char *>(a.v) + (vrow_off + c0) * vsz + 16 * vpc, vrow < len ? 16 : 0);
+      cp_async16(vb + 16 * tid, reinterpret_cast<const char *>(a.v) + (vrow_off + c0) * vsz + 16 * vpc,
+                 vrow < len ? 16 : 0);
     if (opiece)
-      cp_async16(reinterpret_cast<char *>(dOst) + 16 * (tid - 128),
+      cp_async16(vb + 1024 + 16 * (tid - 128),
                  reinterpret_cast<const char *>(a.dO) + (vrow_off + c0) * osz + 16 * vpc, vrow < len ? 16 : 0);
     cp_async_commit();
   };
-  const int vr = tid / kGradDvt, vc = tid % kGradDvt;  // kBThreads == C * kGradDvt
-  fetch(0);
-  for (int c0 = 0; c0 < dv; c0 += kGradDvt) {
+  fetch(0, 0);
+  for (int c0 = 0, bi = 0; c0 < dv; c0 += kGradDvt, bi ^= 1) {
+    const float *sS = Sb + bi * 2 * dk * lr, *sD = sS + dk * lr;
+    const char *vb = reinterpret_cast<const char *>(Vb + bi * 512);
     cp_async_wait_all();
-    __syncthreads();  // this pass's staging has landed; the previous pass is done with the column buffers
-    for (int e = tid; e < 2 * dk; e += kBThreads) {  // S, dS' columns, transposed in 4 x 4 blocks
-      const int w = e >= dk, b = w ? e - dk : e;  // array, then block b < dk: rows 4 (b / 4).., columns 4 (b % 4)..
-      const int i0 = 4 * (b >> 2), cq = 4 * (b & 3);
-      const float *src = (w ? dSst : Sst) + i0 * kGradDvt + cq;
-      float *dst = (w ? dSt : St) + cq * ld + i0;
-      const float4 r0 = *reinterpret_cast<const float4 *>(src), r1 = *reinterpret_cast<const float4 *>(src + kGradDvt),
-                   r2 = *reinterpret_cast<const float4 *>(src + 2 * kGradDvt),
-                   r3 = *reinterpret_cast<const float4 *>(src + 3 * kGradDvt);
-      *reinterpret_cast<float4 *>(dst) = make_float4(r0.x, r1.x, r2.x, r3.x);
-      *reinterpret_cast<float4 *>(dst + ld) = make_float4(r0.y, r1.y, r2.y, r3.y);
-      *reinterpret_cast<float4 *>(dst + 2 * ld) = make_float4(r0.z, r1.z, r2.z, r3.z);
-      *reinterpret_cast<float4 *>(dst + 3 * ld) = make_float4(r0.w, r1.w, r2.w, r3.w);
+    __syncthreads();  // this pass's staging has landed; the previous pass is done with every pass array
+    {  // V and dO rows, widened to fp32 (one element per thread: kBThreads == C * kGradDvt)
+      const int o = rr * kGradDvt + ss;
+      Pr[rr * lr + ss] = vsz == 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(vb)[o])
+                                  : reinterpret_cast<const float *>(vb)[o];
+      dOr[rr * lr + ss] = osz == 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(vb + 1024)[o])
+                                   : reinterpret_cast<const float *>(vb + 1024)[o];
     }
-    {  // V rows (P = V - GK S after the next step) and dO rows, widened to fp32
-      const int o = vr * kGradDvt + vc;
-      Pt[vc * lw + vr] = vsz == 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(Vst)[o]) : Vst[o];
-      dOt[vc * lw + vr] = osz == 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dOst)[o]) : dOst[o];
-    }
-    __syncthreads();  // the staging area is free for the next pass
-    if (c0 + kGradDvt < dv) fetch(c0 + kGradDvt);
-    {  // partial Z = GK S (zp = 0) or Y = Kh dS' (zp = 1) over half of dk, 2 x 2 outputs
-      const float *Mm = zp ? c.Kh : c.GK;
-      const float *Vm = zp ? dSt : St;
-      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-      const int half = dk / 2, ia = zq * half;
-#pragma unroll 2
-      for (int i = ia; i < ia + half; i += 4) {
-        const float4 m0 = *reinterpret_cast<const float4 *>(Mm + zr * ld + i);
-        const float4 m1 = *reinterpret_cast<const float4 *>(Mm + (zr + 1) * ld + i);
-        const float4 v0 = *reinterpret_cast<const float4 *>(Vm + zc * ld + i);
-        const float4 v1 = *reinterpret_cast<const float4 *>(Vm + (zc + 1) * ld + i);
-        a00 = fmaf(m0.x, v0.x, fmaf(m0.y, v0.y, fmaf(m0.z, v0.z, fmaf(m0.w, v0.w, a00))));
-        a01 = fmaf(m0.x, v1.x, fmaf(m0.y, v1.y, fmaf(m0.z, v1.z, fmaf(m0.w, v1.w, a01))));
-        a10 = fmaf(m1.x, v0.x, fmaf(m1.y, v0.y, fmaf(m1.z, v0.z, fmaf(m1.w, v0.w, a10))));
-        a11 = fmaf(m1.x, v1.x, fmaf(m1.y, v1.y, fmaf(m1.z, v1.z, fmaf(m1.w, v1.w, a11))));
+    if (c0 + kGradDvt < dv) fetch(c0 + kGradDvt, bi ^ 1);
+    {  // partial Z = GK S (zp = 0) or Y = Kh dS' (zp = 1) over half of dk: warp (zp, column tile, half)
+      const int zp = warp >> 2, n0 = 8 * ((warp >> 1) & 1), half = dk / 2, ka = (warp & 1) * half;
+      const float *Am = zp ? c.Kh : c.GK, *Bm = zp ? sD : sS;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k0 = ka; k0 < ka + half; k0 += 8) {
+        const float av[4] = {Am[g * ld + k0 + t], Am[(g + 8) * ld + k0 + t], Am[g * ld + k0 + t + 4],
+                             Am[(g + 8) * ld + k0 + t + 4]};
+        const float bv[2] = {Bm[(k0 + t) * lr + n0 + g], Bm[(k0 + t + 4) * lr + n0 + g]};
+        mma_3xtf32(d, av, bv);
       }
-      float *rd = red + (zp * 2 + zq) * kBC * kBC;
-      rd[zr * kBC + zc] = a00;
-      rd[zr * kBC + zc + 1] = a01;
-      rd[(zr + 1) * kBC + zc] = a10;
-      rd[(zr + 1) * kBC + zc + 1] = a11;
+      float *rd = red + (zp * 2 + (warp & 1)) * kBC * kBC + n0 + 2 * t;
+      *reinterpret_cast<float2 *>(rd + g * kBC) = make_float2(d[0], d[1]);
+      *reinterpret_cast<float2 *>(rd + (g + 8) * kBC) = make_float2(d[2], d[3]);
     }
     __syncthreads();
     {  // P = V - Z;  dV~ = Y + A^T dO   (thread = (row rr, column ss))
       const float z = red[rr * kBC + ss] + red[kBC * kBC + rr * kBC + ss];
       float y = red[2 * kBC * kBC + rr * kBC + ss] + red[3 * kBC * kBC + rr * kBC + ss];
-      for (int s2 = rr; s2 < kBC; ++s2) y += c.A[s2 * kBC + rr] * dOt[ss * lw + s2];
-      Pt[ss * lw + rr] -= z;
-      dVtt[ss * lw + rr] = y;
+      for (int s2 = rr; s2 < kBC; ++s2) y += c.A[s2 * kBC + rr] * dOr[s2 * lr + ss];
+      Pr[rr * lr + ss] -= z;
+      dVtr[rr * lr + ss] = y;
     }
     __syncthreads();
     {  // V~ = T_b P;  dV = T_b^T dV~
       float y = 0.f, d = 0.f;
-      for (int s2 = 0; s2 <= rr; ++s2) y += c.T[rr * kBC + s2] * c.beta[s2] * Pt[ss * lw + s2];
-      for (int s2 = rr; s2 < kBC; ++s2) d += c.T[s2 * kBC + rr] * dVtt[ss * lw + s2];
+      for (int s2 = 0; s2 <= rr; ++s2) y += c.T[rr * kBC + s2] * c.beta[s2] * Pr[s2 * lr + ss];
+      for (int s2 = rr; s2 < kBC; ++s2) d += c.T[s2 * kBC + rr] * dVtr[s2 * lr + ss];
       d *= c.beta[rr];
-      Vtt[ss * lw + rr] = y;
-      dVv[ss * lw + rr] = d;
+      Vtr[rr * lr + ss] = y;
+      dVr[rr * lr + ss] = d;
       if (rr < len) a.gv[((size_t)(t0 + rr) * H + h) * dv + c0 + ss] = d;
     }
     __syncthreads();
-    if (own) {  // dQb += dO S^T, dKh += V~ dS'^T, dGK -= dV S^T on this thread's 4 x 2 block
-#pragma unroll 4
-      for (int cc = 0; cc < kGradDvt; ++cc) {
-        const float4 o4 = *reinterpret_cast<const float4 *>(dOt + cc * lw + rb);
-        const float4 v4 = *reinterpret_cast<const float4 *>(Vtt + cc * lw + rb);
-        const float4 d4 = *reinterpret_cast<const float4 *>(dVv + cc * lw + rb);
-        const float2 s2 = *reinterpret_cast<const float2 *>(St + cc * ld + ip);
-        const float2 ds2 = *reinterpret_cast<const float2 *>(dSt + cc * ld + ip);
-        const float oo[4] = {o4.x, o4.y, o4.z, o4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w},
-                    dd[4] = {d4.x, d4.y, d4.z, d4.w};
+    if (16 * warp < dk) {  // dQb += dO S^T, dKh += V~ dS'^T, dGK -= dV S^T on channels 16 warp .. + 15
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          aQ[q][0] += oo[q] * s2.x; aQ[q][1] += oo[q] * s2.y;
-          aH[q][0] += vv[q] * ds2.x; aH[q][1] += vv[q] * ds2.y;
-          aG[q][0] -= dd[q] * s2.x; aG[q][1] -= dd[q] * s2.y;
+      for (int k0 = 0; k0 < kGradDvt; k0 += 8) {
+        const int ra = g * lr + k0 + t, rb = (g + 8) * lr + k0 + t;  // A fragment: rows g, g + 8
+        uint32_t oh[4], ol[4], vh[4], vl[4], dh[4], dl[4];
+        split_frag(oh, ol, dOr[ra], dOr[rb], dOr[ra + 4], dOr[rb + 4]);
+        split_frag(vh, vl, Vtr[ra], Vtr[rb], Vtr[ra + 4], Vtr[rb + 4]);
+        split_frag(dh, dl, -dVr[ra], -dVr[rb], -dVr[ra + 4], -dVr[rb + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {  // B(k = column, n = channel) = S[channel][column]
+          const int cb = (16 * warp + 8 * nt + g) * lr + k0 + t;
+          uint32_t sh2[2], sl2[2], dsh[2], dsl[2];
+          split_frag(sh2, sl2, sS[cb], sS[cb + 4]);
+          split_frag(dsh, dsl, sD[cb], sD[cb + 4]);
+          mma_3xtf32(accQ[nt], oh, ol, sh2, sl2);
+          mma_3xtf32(accH[nt], vh, vl, dsh, dsl);
+          mma_3xtf32(accG[nt], dh, dl, sh2, sl2);
         }
       }
     }
-    for (int cc = 0; cc < kGradDvt; ++cc) {  // dT_b += dV~ P^T, dA += dO V~^T
-      accTb += dVtt[cc * lw + rr] * Pt[cc * lw + ss];
-      accA += dOt[cc * lw + rr] * Vtt[cc * lw + ss];
+    if (warp >= 4) {  // dT_b += dV~ P^T (warps 4, 5), dA += dO V~^T (warps 6, 7): one 8-column tile each
+      const bool isA = warp >= 6;
+      const float *Am = isA ? dOr : dVtr, *Bm = isA ? Vtr : Pr;
+      const int n0 = 8 * (warp & 1);
+#pragma unroll
+      for (int k0 = 0; k0 < kGradDvt; k0 += 8) {
+        const int ra = g * lr + k0 + t, rb = (g + 8) * lr + k0 + t, cb = (n0 + g) * lr + k0 + t;
+        const float av[4] = {Am[ra], Am[rb], Am[ra + 4], Am[rb + 4]};
+        const float bv[2] = {Bm[cb], Bm[cb + 4]};
+        mma_3xtf32(accTA, av, bv);
+      }
+    } else if (tid < dk) {  // dgamma_i += sum over the pass's columns of dS'[i][c] S[i][c]
+#pragma unroll
+      for (int q = 0; q < kGradDvt; q += 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(sS + tid * lr + q);
+        const float4 y = *reinterpret_cast<const float4 *>(sD + tid * lr + q);
+        accGam += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+      }
     }
-    if (tid < dk)
-      for (int cc = 0; cc < kGradDvt; ++cc) accGam += dSt[cc * ld + tid] * St[cc * ld + tid];
   }
   __syncthreads();  // the pass buffers become dQb, dKb, dGK, dKh
-  if (own)
+  if (16 * warp < dk)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      dQb[(rb + q) * ld + ip] = aQ[q][0]; dQb[(rb + q) * ld + ip + 1] = aQ[q][1];
-      dKh[(rb + q) * ld + ip] = aH[q][0]; dKh[(rb + q) * ld + ip + 1] = aH[q][1];
-      dGK[(rb + q) * ld + ip] = aG[q][0]; dGK[(rb + q) * ld + ip + 1] = aG[q][1];
+    for (int nt = 0; nt < 2; ++nt) {  // D fragment: rows g, g + 8; columns 2t, 2t + 1 of the tile
+      const int o = g * ld + 16 * warp + 8 * nt + 2 * t, o8 = o + 8 * ld;
+      *reinterpret_cast<float2 *>(dQb + o) = make_float2(accQ[nt][0], accQ[nt][1]);
+      *reinterpret_cast<float2 *>(dQb + o8) = make_float2(accQ[nt][2], accQ[nt][3]);
+      *reinterpret_cast<float2 *>(dKh + o) = make_float2(accH[nt][0], accH[nt][1]);
+      *reinterpret_cast<float2 *>(dKh + o8) = make_float2(accH[nt][2], accH[nt][3]);
+      *reinterpret_cast<float2 *>(dGK + o) = make_float2(accG[nt][0], accG[nt][1]);
+      *reinterpret_cast<float2 *>(dGK + o8) = make_float2(accG[nt][2], accG[nt][3]);
     }
-  dTb[tid] = accTb;
-  dA[tid] = accA;
+  if (warp >= 4) {
+    float *dst = (warp >= 6 ? dA : dTb) + g * kBC + 8 * (warp & 1) + 2 * t;
+    *reinterpret_cast<float2 *>(dst) = make_float2(accTA[0], accTA[1]);
+    *reinterpret_cast<float2 *>(dst + 8 * kBC) = make_float2(accTA[2], accTA[3]);
+  }
   if (tid < dk) dgam[tid] = accGam;
   __syncthreads();
   // through T_b = T diag(beta) and T = (I + L)^-1:  X = T^T (dT_b diag(beta))
@@ -705,9 +749,8 @@ __global__ void __launch_bounds__(kBThreads, 2) bwd_grads_kernel(BwdArgs a) {
 }
 
 size_t grads_smem_bytes(int dk) {
-  const size_t ld = (size_t)dk + 4, lw = kBC + 4;
-  const size_t pass = 2 * kGradDvt * ld + 5 * kGradDvt * lw + 4 * kBC * kBC + 2 * (size_t)dk * kGradDvt +
-                      2 * kBC * kGradDvt;
+  const size_t ld = (size_t)dk + 4, lr = kGradDvt + 4;
+  const size_t pass = 5 * kBC * lr + 4 * kBC * kBC + 4 * (size_t)dk * lr + 2 * 512;
   const size_t tail = 4 * kBC * ld;
   return sizeof(float) * (5 * kBC * ld + 6 * kBC * kBC + kBC + 2 * 128 + (pass > tail ? pass : tail));
 }
