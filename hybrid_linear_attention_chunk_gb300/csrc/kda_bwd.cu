@@ -221,15 +221,15 @@ __device__ void setup_chunk(const BwdArgs &a, const ChunkSm &c, int t0, int len,
     c.gam[tid] = expf(acc);
   }
   __syncthreads();
-  for (int e = tid; e < kBC * dk; e += kBThreads) {
+  for (int e = tid; e < kBC * dk; e += kBThreads) {  // (Kh = K e^{G_C - G} = Kb gamma)
     const int r = e / dk, i = e % dk;
-    const float G = c.G[r * ld + i], Gl = c.G[(kBC - 1) * ld + i];
+    const float G = c.G[r * ld + i];
     const float kv = c.Kb[r * ld + i];
-    const float eg = expf(G);
+    const float eg = expf(G), kb = kv * expf(-G);
     c.Qb[r * ld + i] *= eg;
     c.GK[r * ld + i] = kv * eg;
-    c.Kb[r * ld + i] = kv * expf(-G);
-    c.Kh[r * ld + i] = kv * expf(Gl - G);
+    c.Kb[r * ld + i] = kb;
+    c.Kh[r * ld + i] = kb * c.gam[i];
   }
   __syncthreads();
   {  // one thread per (r, s): A and M, four channels per 128-bit load
@@ -725,8 +725,8 @@ __global__ void __launch_bounds__(kBThreads, 2) bwd_grads_kernel(BwdArgs a) {
   // elementwise to q, k and the cumulative log-decay G (dG in dKb's place)
   for (int e = tid; e < kBC * dk; e += kBThreads) {
     const int r = e / dk, i = e % dk;
-    const float G = c.G[r * ld + i], Gl = c.G[(kBC - 1) * ld + i];
-    const float eg = expf(G), ei = expf(-G), eh = expf(Gl - G);
+    const float G = c.G[r * ld + i];
+    const float eg = expf(G), ei = expf(-G), eh = ei * c.gam[i];  // e^{G_C - G}
     const float q = dQb[r * ld + i], kb = dKb[r * ld + i], gk = dGK[r * ld + i], kh = dKh[r * ld + i];
     if (r < len) {
       const size_t idx = ((size_t)(t0 + r) * H + h) * dk + i;
