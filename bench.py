@@ -499,7 +499,7 @@ def time_backward(kda, x, w, steps, ms_headline, dev, stream, world):
     torch.cuda.synchronize(dev)
     ms = reduce_max(ev0.elapsed_time(ev1) / steps, world, dev)
     tok = w.B * w.T
-    res = {"workload": w.name, "api": "kda_chunk_bwd (fp32 CUDA-core kernels, 16-token chunks)", "steps": steps,
+    res = {"workload": w.name, "api": "kda_chunk_bwd (fp32, 16-token chunks; gradient products on mma.sync split-tf32)", "steps": steps,
            "ms_per_step": round(ms, 3), "tokens_per_s": round(world * tok / (ms * 1e-3), 1),
            "time_vs_forward": round(ms / ms_headline, 3), "workspace_bytes": int(ws_bytes),
            "launches_per_step": 4}
