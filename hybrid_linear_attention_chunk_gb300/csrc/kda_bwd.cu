@@ -108,6 +108,10 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_b
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(kPending) : "memory");
+}
 
 // fp32 products on the tensor cores: mma.sync m16n8k8 with tf32 operands,
 // each operand x split as hi = tf32(x), lo = tf32(x - hi) and the product
@@ -308,6 +312,12 @@ __global__ void __launch_bounds__(kBThreads) bwd_prep_kernel(BwdArgs a) {
 // update takes 4 x 4 outputs per thread from 128-bit shared loads.  The
 // [C][dk] operands keep 16-byte-padded rows so that the row pairs a warp
 // reads fall in distinct banks.
+// A step's operands arrive by cp.async while the previous step runs, each as
+// soon as its buffer is free: forward, W after the product, and X = V, T_b,
+// Kh and gamma after the reduction (Kh and gamma into the buffer the update
+// does not read); reverse, Kh after the product, and Qb, A, gamma and X = dO
+// after the reduction, during which Qb^T dO is already added, so the last
+// phase reads only W (fetched at the step's start) and V~-gradient rows.
 constexpr int kSP = kScanDvt + 4;  // row stride of the [.][dvt] arrays (16-byte rows)
 
 template <bool kReverse>
@@ -321,16 +331,18 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
   const int nblk = 8 * ncb;                  // (row pair, column block) tasks of the C x dvt product
   const int nsplit = kBThreads / nblk;       // dk split of that product
   const int ilen = dk / nsplit;
-  float *S = smem;                     // [dk][kSP]
-  float *X = S + dk * kSP;             // [C][kSP]: V or dO rows
-  float *red = X + kBC * kSP;          // [nsplit][C][kSP]: partial sums
-  float *Y = red;                      // [C][kSP]: V~ or dV~, over the first partial sums
-  const int ldm = dk + 4;              // row stride of the [C][dk] operands
-  float *Wm = red + nsplit * kBC * kSP;  // [C][ldm]
-  float *Km = Wm + kBC * ldm;          // [C][ldm]: Kh
-  float *Qm = Km + kBC * ldm;          // [C][ldm]: Qb (reverse only)
-  float *Cm = Qm + (kReverse ? kBC * ldm : 0);  // [C][C]: T_b (forward) or A (reverse)
-  float *gm = Cm + kBC * kBC;          // [dk]
+  const int ldm = dk + 4;                    // row stride of the [C][dk] operands
+  const kda_dtype xt = kReverse ? a.out : a.qkv;  // X rows: dO (reverse) or V (forward)
+  const int xsz = xt == KDA_BF16 ? 2 : 4;
+  float *S = smem;                       // [dk][kSP]
+  float *red = S + dk * kSP;             // [nsplit][C][kSP]: partial sums
+  float *Y = red;                        // [C][kSP]: V~ or dV~, over the first partial sums
+  float *Xr = red + nsplit * kBC * kSP;  // [C][dvt] X rows in their dtype (2 KB)
+  float *Wm = Xr + kBC * kScanDvt;       // [C][ldm]: W
+  float *Km = Wm + kBC * ldm;            // [C][ldm]: Kh (forward: two buffers)
+  float *Qm = Km + (kReverse ? 1 : 2) * kBC * ldm;  // [C][ldm]: Qb (reverse only)
+  float *Cm = Qm + (kReverse ? kBC * ldm : 0);       // [C][C]: T_b (forward) or A (reverse)
+  float *gm = Cm + kBC * kBC;            // [dk]: gamma (forward: two buffers)
   int bos, eos;
   bounds(a, n, bos, eos);
   const int nch = (eos - bos + kBC - 1) / kBC;
@@ -341,6 +353,56 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
     const float *src = kReverse ? a.dST : a.s0;
     S[i * kSP + cc] = src ? src[soff + (size_t)i * dv + c0g + cc] : 0.f;
   }
+  // asynchronous copies of chunk j's operands (all sizes powers of two)
+  const int q4sh = __ffs(dk / 4) - 1;                    // log2 of the 16-byte pieces of a [dk] row
+  const int xsh = __ffs(dvt * xsz / 16) - 1;             // log2 of the pieces of an X row
+  auto chunk_at = [&](int j, int &t0, int &len, size_t &sh) {
+    j = kReverse ? nch - 1 - j : j;
+    t0 = bos + j * kBC;
+    len = min(kBC, eos - t0);
+    sh = (size_t)(base + j) * H + h;
+  };
+  auto fetch_rows = [&](float *dst, const float *src) {  // [C][dk] workspace rows -> [C][ldm]
+    for (int e = tid; e < (kBC << q4sh); e += kBThreads)
+      cp_async16(dst + (e >> q4sh) * ldm + 4 * (e & ((1 << q4sh) - 1)), src + 4 * e, 16);
+  };
+  auto fetch_small = [&](int jj, float *g_dst) {  // X rows, the C x C matrix and gamma of step jj
+    int t0, len;
+    size_t sh;
+    chunk_at(jj, t0, len, sh);
+    const char *xg = reinterpret_cast<const char *>(kReverse ? a.dO : a.v);
+    for (int e = tid; e < (kBC << xsh); e += kBThreads) {
+      const int r = e >> xsh, pc = e & ((1 << xsh) - 1);
+      const size_t row = (size_t)(t0 + (r < len ? r : 0)) * H + h;  // (in range when zero-filled)
+      cp_async16(reinterpret_cast<char *>(Xr) + r * dvt * xsz + 16 * pc, xg + (row * dv + c0g) * xsz + 16 * pc,
+                 r < len ? 16 : 0);
+    }
+    if (tid < kBC * kBC / 4) cp_async16(Cm + 4 * tid, (kReverse ? a.A : a.Tb) + sh * kBC * kBC + 4 * tid, 16);
+    if (tid < dk / 4) cp_async16(g_dst + 4 * tid, a.gam + sh * dk + 4 * tid, 16);
+  };
+  auto xval = [&](int r, int cc) -> float {
+    return xsz == 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(Xr)[r * dvt + cc])
+                    : Xr[r * dvt + cc];
+  };
+  auto xval4 = [&](int r, int cc) -> float4 {
+    if (xsz == 2) {
+      const uint2 u = *reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(Xr) + r * dvt + cc);
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+      return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    return *reinterpret_cast<const float4 *>(Xr + r * dvt + cc);
+  };
+  if (nch > 0) {  // the first step's operands (the reverse scan's W comes at each step's start)
+    int t0, len;
+    size_t sh;
+    chunk_at(0, t0, len, sh);
+    if (!kReverse) fetch_rows(Wm, a.W + sh * kBC * dk);
+    fetch_rows(Km, a.Kh + sh * kBC * dk);
+    if (kReverse) fetch_rows(Qm, a.Qb + sh * kBC * dk);
+    fetch_small(0, gm);
+    cp_async_commit();
+  }
   // tasks: the C x dvt product (row pair rp, column block cb, dk split sp) and
   // the dk x dvt update (rows i0..i0+3, columns c0..c0+3)
   const int blk = tid % nblk, sp = tid / nblk;
@@ -348,42 +410,26 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
   const int ib = tid / ncb, i0 = 4 * ib, cu0 = 4 * (tid % ncb);
   const bool upd = i0 < dk;
   for (int jj = 0; jj < nch; ++jj) {
-    const int j = kReverse ? nch - 1 - jj : jj;
-    const int t0 = bos + j * kBC, len = min(kBC, eos - t0);
-    const size_t sh = (size_t)(base + j) * H + h;
-    __syncthreads();  // S final for this chunk; the previous chunk's operands are consumed
+    int t0, len;
+    size_t sh;
+    chunk_at(jj, t0, len, sh);
+    const bool more = jj + 1 < nch;
+    const int buf = kReverse ? 0 : (jj & 1);  // forward: Kh and gamma buffers alternate
+    const float *Kc = Km + buf * kBC * ldm, *gc = gm + buf * dk;
+    cp_async_wait_all();
+    __syncthreads();  // this step's operands have landed; S is final for this chunk
+    if (kReverse) {   // W of this step, needed only by the last phase
+      fetch_rows(Wm, a.W + sh * kBC * dk);
+      cp_async_commit();
+    }
     float *rec = (kReverse ? a.dSx : a.Sent) + sh * dk * dv;
     if (upd)
 #pragma unroll
       for (int r = 0; r < 4; ++r)
         *reinterpret_cast<float4 *>(rec + (size_t)(i0 + r) * dv + c0g + cu0) =
             *reinterpret_cast<const float4 *>(S + (i0 + r) * kSP + cu0);
-    for (int e = tid; e < kBC * dvt; e += kBThreads) {
-      const int r = e / dvt, cc = e % dvt;
-      float x = 0.f;
-      if (r < len) {
-        const size_t idx = ((size_t)(t0 + r) * H + h) * dv + c0g + cc;
-        x = kReverse ? ld_elem(a.dO, idx, a.out) : ld_elem(a.v, idx, a.qkv);
-      }
-      X[r * kSP + cc] = x;
-    }
-    {
-      const float4 *w4 = reinterpret_cast<const float4 *>(a.W + sh * kBC * dk);
-      const float4 *k4 = reinterpret_cast<const float4 *>(a.Kh + sh * kBC * dk);
-      const float4 *q4 = reinterpret_cast<const float4 *>(a.Qb + sh * kBC * dk);
-      const int q4r = dk / 4;
-      for (int e = tid; e < kBC * q4r; e += kBThreads) {
-        const int o = (e / q4r) * ldm + 4 * (e % q4r);
-        *reinterpret_cast<float4 *>(Wm + o) = w4[e];
-        *reinterpret_cast<float4 *>(Km + o) = k4[e];
-        if (kReverse) *reinterpret_cast<float4 *>(Qm + o) = q4[e];
-      }
-    }
-    Cm[tid] = kReverse ? a.A[sh * kBC * kBC + tid] : a.Tb[sh * kBC * kBC + tid];  // kBThreads == C * C
-    for (int i = tid; i < dk; i += kBThreads) gm[i] = a.gam[sh * dk + i];
-    __syncthreads();
     {  // partial (W S) or (Kh S) over this thread's slice of dk
-      const float *m0p = (kReverse ? Km : Wm) + r0 * ldm, *m1p = m0p + ldm;
+      const float *m0p = (kReverse ? Kc : Wm) + r0 * ldm, *m1p = m0p + ldm;
       float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
       const int ia = sp * ilen, ie = ia + ilen;
       int i = ia;
@@ -408,50 +454,83 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
       *reinterpret_cast<float4 *>(red + (sp * kBC + r0) * kSP + cy) = acc0;
       *reinterpret_cast<float4 *>(red + (sp * kBC + r0 + 1) * kSP + cy) = acc1;
     }
-    __syncthreads();
+    __syncthreads();  // partial sums complete; the product's operand buffer is free
+    if (more) {
+      int t1, l1;
+      size_t sh1;
+      chunk_at(jj + 1, t1, l1, sh1);
+      fetch_rows(kReverse ? Km : Wm, (kReverse ? a.Kh : a.W) + sh1 * kBC * dk);
+      cp_async_commit();
+    }
     for (int e = tid; e < kBC * dvt; e += kBThreads) {  // (each (r, cc) is read and then written by one thread)
       const int r = e / dvt, cc = e % dvt;
       float part = 0.f;
       for (int q = 0; q < nsplit; ++q) part += red[(q * kBC + r) * kSP + cc];
       float y = 0.f;
       if (!kReverse) {  // V~ = T_b V - W S
-        for (int s = 0; s <= r; ++s) y += Cm[r * kBC + s] * X[s * kSP + cc];
+        for (int s = 0; s <= r; ++s) y += Cm[r * kBC + s] * xval(s, cc);
         y -= part;
       } else {          // dV~ = A^T dO + Kh dS
-        for (int s = r; s < kBC; ++s) y += Cm[s * kBC + r] * X[s * kSP + cc];
+        for (int s = r; s < kBC; ++s) y += Cm[s * kBC + r] * xval(s, cc);
         y += part;
       }
       Y[r * kSP + cc] = y;
     }
-    __syncthreads();
-    if (upd) {  // rows i0..i0+3, columns cu0..cu0+3 of the new S
-      float4 sv[4];
+    float4 sv[4];
+    if (upd) {  // rows i0..i0+3, columns cu0..cu0+3 of the new S: diag(gamma) S (+ Qb^T dO, reverse)
       float g4[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         sv[q] = *reinterpret_cast<const float4 *>(S + (i0 + q) * kSP + cu0);
-        g4[q] = gm[i0 + q];
+        g4[q] = gc[i0 + q];
         sv[q].x *= g4[q]; sv[q].y *= g4[q]; sv[q].z *= g4[q]; sv[q].w *= g4[q];
       }
+      if (kReverse) {
+#pragma unroll 4
+        for (int r = 0; r < kBC; ++r) {
+          const float4 o4 = xval4(r, cu0);
+          const float4 q4 = *reinterpret_cast<const float4 *>(Qm + r * ldm + i0);
+          const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            sv[q].x += qq[q] * o4.x; sv[q].y += qq[q] * o4.y; sv[q].z += qq[q] * o4.z; sv[q].w += qq[q] * o4.w;
+          }
+        }
+      }
+    }
+    if (kReverse) {
+      if (more) cp_async_wait_group<1>();  // this step's W (the next step's Kh may stay in flight)
+      else cp_async_wait_all();
+    }
+    __syncthreads();  // Y complete; X, the C x C matrix, gamma (and Qb) are free
+    if (more) {
+      fetch_small(jj + 1, kReverse ? gm : gm + (buf ^ 1) * dk);
+      if (kReverse) {
+        int t1, l1;
+        size_t sh1;
+        chunk_at(jj + 1, t1, l1, sh1);
+        fetch_rows(Qm, a.Qb + sh1 * kBC * dk);
+      } else {
+        int t1, l1;
+        size_t sh1;
+        chunk_at(jj + 1, t1, l1, sh1);
+        fetch_rows(Km + (buf ^ 1) * kBC * ldm, a.Kh + sh1 * kBC * dk);
+      }
+      cp_async_commit();
+    }
+    if (upd) {  // + Kh^T Y (forward) or - W^T dV~ (reverse)
+      const float *Mu = kReverse ? Wm : Kc;
 #pragma unroll 4
       for (int r = 0; r < kBC; ++r) {
         const float4 y4 = *reinterpret_cast<const float4 *>(Y + r * kSP + cu0);
-        if (!kReverse) {
-          const float4 k4 = *reinterpret_cast<const float4 *>(Km + r * ldm + i0);
-          const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+        const float4 m4 = *reinterpret_cast<const float4 *>(Mu + r * ldm + i0);
+        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            sv[q].x += kk[q] * y4.x; sv[q].y += kk[q] * y4.y; sv[q].z += kk[q] * y4.z; sv[q].w += kk[q] * y4.w;
-          }
-        } else {
-          const float4 o4 = *reinterpret_cast<const float4 *>(X + r * kSP + cu0);
-          const float4 q4 = *reinterpret_cast<const float4 *>(Qm + r * ldm + i0);
-          const float4 w4 = *reinterpret_cast<const float4 *>(Wm + r * ldm + i0);
-          const float qq[4] = {q4.x, q4.y, q4.z, q4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            sv[q].x += qq[q] * o4.x - ww[q] * y4.x; sv[q].y += qq[q] * o4.y - ww[q] * y4.y;
-            sv[q].z += qq[q] * o4.z - ww[q] * y4.z; sv[q].w += qq[q] * o4.w - ww[q] * y4.w;
+        for (int q = 0; q < 4; ++q) {
+          if (kReverse) {
+            sv[q].x -= mm[q] * y4.x; sv[q].y -= mm[q] * y4.y; sv[q].z -= mm[q] * y4.z; sv[q].w -= mm[q] * y4.w;
+          } else {
+            sv[q].x += mm[q] * y4.x; sv[q].y += mm[q] * y4.y; sv[q].z += mm[q] * y4.z; sv[q].w += mm[q] * y4.w;
           }
         }
       }
@@ -470,8 +549,8 @@ __global__ void __launch_bounds__(kBThreads, 4) bwd_scan_kernel(BwdArgs a) {
 
 size_t scan_smem_bytes(bool reverse, int dk, int dv) {
   const int ncb = (dv < kScanDvt ? dv : kScanDvt) / 4, nsplit = kBThreads / (8 * ncb);
-  return sizeof(float) * ((size_t)dk * kSP + kBC * kSP + (size_t)nsplit * kBC * kSP +
-                          (reverse ? 3 : 2) * kBC * ((size_t)dk + 4) + kBC * kBC + dk);
+  return sizeof(float) * ((size_t)dk * kSP + (size_t)nsplit * kBC * kSP + kBC * kScanDvt +
+                          3 * kBC * ((size_t)dk + 4) + kBC * kBC + (reverse ? 1 : 2) * (size_t)dk);
 }
 
 // Gradients of one chunk's rows, from its entry state and the state gradient
