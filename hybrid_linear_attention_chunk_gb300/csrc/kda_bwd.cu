@@ -651,22 +651,63 @@ __global__ void __launch_bounds__(kBThreads, 2) bwd_grads_kernel(BwdArgs a) {
       *reinterpret_cast<float2 *>(rd + (g + 8) * kBC) = make_float2(d[2], d[3]);
     }
     __syncthreads();
-    {  // P = V - Z;  dV~ = Y + A^T dO   (thread = (row rr, column ss))
-      const float z = red[rr * kBC + ss] + red[kBC * kBC + rr * kBC + ss];
-      float y = red[2 * kBC * kBC + rr * kBC + ss] + red[3 * kBC * kBC + rr * kBC + ss];
-      for (int s2 = rr; s2 < kBC; ++s2) y += c.A[s2 * kBC + rr] * dOr[s2 * lr + ss];
-      Pr[rr * lr + ss] -= z;
-      dVtr[rr * lr + ss] = y;
+    Pr[rr * lr + ss] -= red[rr * kBC + ss] + red[kBC * kBC + rr * kBC + ss];  // P = V - Z
+    if (warp < 2) {  // dV~ = Y + A^T dO on the tensor cores: warp = 8-column tile
+      const int n0 = 8 * warp, o = g * kBC + n0 + 2 * t, o8 = o + 8 * kBC;
+      const float *ry = red + 2 * kBC * kBC;
+      float d[4] = {ry[o] + ry[kBC * kBC + o], ry[o + 1] + ry[kBC * kBC + o + 1], ry[o8] + ry[kBC * kBC + o8],
+                    ry[o8 + 1] + ry[kBC * kBC + o8 + 1]};
+#pragma unroll
+      for (int k0 = 0; k0 < kBC; k0 += 8) {  // A(r, s) = A^T[r][s] = A[s][r]; B(s, c) = dO[s][c]
+        const float av[4] = {c.A[(k0 + t) * kBC + g], c.A[(k0 + t) * kBC + g + 8], c.A[(k0 + t + 4) * kBC + g],
+                             c.A[(k0 + t + 4) * kBC + g + 8]};
+        const float bv[2] = {dOr[(k0 + t) * lr + n0 + g], dOr[(k0 + t + 4) * lr + n0 + g]};
+        mma_3xtf32(d, av, bv);
+      }
+      *reinterpret_cast<float2 *>(dVtr + g * lr + n0 + 2 * t) = make_float2(d[0], d[1]);
+      *reinterpret_cast<float2 *>(dVtr + (g + 8) * lr + n0 + 2 * t) = make_float2(d[2], d[3]);
     }
     __syncthreads();
-    {  // V~ = T_b P;  dV = T_b^T dV~
-      float y = 0.f, d = 0.f;
-      for (int s2 = 0; s2 <= rr; ++s2) y += c.T[rr * kBC + s2] * c.beta[s2] * Pr[s2 * lr + ss];
-      for (int s2 = rr; s2 < kBC; ++s2) d += c.T[s2 * kBC + rr] * dVtr[s2 * lr + ss];
-      d *= c.beta[rr];
-      Vtr[rr * lr + ss] = y;
-      dVr[rr * lr + ss] = d;
-      if (rr < len) a.gv[((size_t)(t0 + rr) * H + h) * dv + c0 + ss] = d;
+    if (warp < 4) {  // V~ = T_b P (warps 0, 1);  dV = T_b^T dV~ = diag(beta) T^T dV~ (warps 2, 3)
+      const bool isD = warp >= 2;
+      const int n0 = 8 * (warp & 1);
+      const float *Bm = isD ? dVtr : Pr;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k0 = 0; k0 < kBC; k0 += 8) {
+        const int s0 = k0 + t, s4 = k0 + t + 4;
+        float av[4];
+        if (isD) {  // A(r, s) = T[s][r]
+          av[0] = c.T[s0 * kBC + g]; av[1] = c.T[s0 * kBC + g + 8];
+          av[2] = c.T[s4 * kBC + g]; av[3] = c.T[s4 * kBC + g + 8];
+        } else {    // A(r, s) = T[r][s] beta_s
+          av[0] = c.T[g * kBC + s0] * c.beta[s0]; av[1] = c.T[(g + 8) * kBC + s0] * c.beta[s0];
+          av[2] = c.T[g * kBC + s4] * c.beta[s4]; av[3] = c.T[(g + 8) * kBC + s4] * c.beta[s4];
+        }
+        const float bv[2] = {Bm[s0 * lr + n0 + g], Bm[s4 * lr + n0 + g]};
+        mma_3xtf32(d, av, bv);
+      }
+      const int col = n0 + 2 * t;
+      if (isD) {
+        const float b0 = c.beta[g], b8 = c.beta[g + 8];
+        d[0] *= b0; d[1] *= b0; d[2] *= b8; d[3] *= b8;
+        *reinterpret_cast<float2 *>(dVr + g * lr + col) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2 *>(dVr + (g + 8) * lr + col) = make_float2(d[2], d[3]);
+        // (the gradient outputs are only 4-byte aligned: scalar stores)
+        if (g < len) {
+          float *o = a.gv + ((size_t)(t0 + g) * H + h) * dv + c0 + col;
+          o[0] = d[0];
+          o[1] = d[1];
+        }
+        if (g + 8 < len) {
+          float *o = a.gv + ((size_t)(t0 + g + 8) * H + h) * dv + c0 + col;
+          o[0] = d[2];
+          o[1] = d[3];
+        }
+      } else {
+        *reinterpret_cast<float2 *>(Vtr + g * lr + col) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2 *>(Vtr + (g + 8) * lr + col) = make_float2(d[2], d[3]);
+      }
     }
     __syncthreads();
     if (16 * warp < dk) {  // dQb += dO S^T, dKh += V~ dS'^T, dGK -= dV S^T on channels 16 warp .. + 15
