@@ -116,10 +116,12 @@ def test_bwd_matches_forward_differences(kda):
     assert abs(fd - an) <= 2e-3 * max(abs(an), 1.0), (fd, an)
 
 
-@pytest.mark.parametrize("dk,dv", [(32, 16), (16, 64), (128, 32), (64, 128)])
+@pytest.mark.parametrize("dk,dv", [(32, 16), (16, 64), (16, 16), (128, 32), (64, 128)])
 def test_bwd_shapes_fp32(kda, dk, dv):
-    """Other head sizes (the scans' 16-column tiling at dv = 16, a dk split of
-    two channels per thread group at dk = 16), packed ragged sequences."""
+    """Other head sizes (the scans' 16-column tiling at dv = 16; at dk = dv = 16
+    the scans' dk split leaves two channels per thread group, below one 128-bit
+    load; at dk = 16 one warp holds all gradient channels), packed ragged
+    sequences."""
     lens = np.array([50, 17, 33])
     w = inputs.scaled(inputs.TINY_FP32, H=3, dk=dk, dv=dv, varlen_seqs=len(lens), random_initial_state=True)
     x = inputs.make_prefill(w, device=DEV, lengths=lens)
