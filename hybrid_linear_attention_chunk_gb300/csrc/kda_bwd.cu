@@ -273,7 +273,7 @@ __device__ void setup_chunk(const BwdArgs &a, const ChunkSm &c, int t0, int len,
 // ------------------------------------------------------------------ kernels
 
 __global__ void __launch_bounds__(kBThreads) bwd_prep_kernel(BwdArgs a) {
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) float smem[];  // (the set-up stores 128-bit rows)
   const int slot = blockIdx.x, h = blockIdx.y;
   int n, j;
   if (!locate(a, slot, n, j)) return;
