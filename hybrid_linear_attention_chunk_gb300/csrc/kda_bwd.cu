@@ -26,11 +26,14 @@
 // reference for every tile ([K3-notes §2.2, Fig. 3]) and all factors stay
 // within e^{+-80} in fp32.
 //
-// Four launches, fp32 on CUDA cores:
+// Four launches, all in fp32 arithmetic:
 //   bwd_prep   (every chunk in parallel)  Qb, Kh, W, A, T_b, gamma of each chunk
 //   bwd_scan<forward>  (per sequence, head, 32 dv columns)  the entry state of every chunk
 //   bwd_scan<reverse>  (same, last chunk first)  the state gradient after every chunk; dS_0
 //   bwd_grads  (every chunk in parallel)  dq, dk, dv, dg, dbeta of the chunk's rows
+// The prep kernel and the scans run on CUDA cores; the gradient kernel's
+// products run on mma.sync with operands split into two tf32 parts (see
+// mma_3xtf32), the rest of it on CUDA cores.
 #include "kda_internal.cuh"
 
 namespace kda {
