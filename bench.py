@@ -263,7 +263,7 @@ def run_gpu(args):
         hq, hk, hv, hg, hb = (t.cpu().pin_memory() for t in (q, k, v, g, beta))
         ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         hs = torch.empty(sT.shape, dtype=sT.dtype).pin_memory()
-        e2e_steps = max(3, min(20, args.steps // 20))
+        e2e_steps = max(20, min(50, args.steps // 20))  # a timed region of ~0.15 s or more
 
         # The batch goes through in P token ranges of every sequence: range p
         # of all B sequences is one kda_chunk_fwd call that resumes from the
@@ -430,6 +430,8 @@ def run_gpu(args):
         }
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, x, seconds=args.cpu_seconds)
+            if dec is not None:
+                line["decode"]["cpu_baseline"] = cpu_baseline_decode(inputs.DECODE_N256, dev)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -639,10 +641,53 @@ def cpu_baseline(w, x, seconds=12.0):
         nchains = (nchains // w.H) * w.H
     dt = run_chains(nchains)
     tok_equiv = nchains * T / w.H  # tokens (all heads) of work done
-    return {"value": round(tok_equiv / dt, 2), "unit": "tokens/s", "cores": min(cores, nchains),
+    res = {"value": round(tok_equiv / dt, 2), "unit": "tokens/s", "cores": min(cores, nchains),
+           "kind": "oracle",
+           "sample": f"{nchains} of {w.B * w.H} (sequence, head) chains of {w.name}, full length {T}; "
+                     f"value = chains*T/H tokens per second; {dt:.1f} s"}
+    # the same oracle on one thread: the first L tokens of one chain
+    h1 = {name: inputs.host_f32(x[name][:T, :1].contiguous()) for name in ("q", "k", "v", "log_alpha", "beta")}
+
+    def one_thread(L):
+        t0 = time.perf_counter()
+        oracle.recurrent(*(h1[n][:L] for n in ("q", "k", "v", "log_alpha", "beta")), None,
+                         np.array([0, L], dtype=np.int64), nthreads=1)
+        return time.perf_counter() - t0
+
+    L = min(T, max(64, int(512 * min(4.0, seconds / 3) / max(one_thread(512), 1e-4))))
+    d1 = one_thread(L)
+    res["one_thread"] = {"value": round(L / w.H / d1, 2), "unit": "tokens/s", "cores": 1,
+                         "sample": f"tokens [0, {L}) of chain (0, 0) on one thread; value = L/H tokens per second; "
+                                   f"{d1:.1f} s"}
+    return res
+
+
+def cpu_baseline_decode(dw, dev, seconds=8.0):
+    """The fp64 oracle's decode step on host cores over the whole decode state
+    (N=256, H=32, d=128, every head), for as many consecutive steps as fill
+    about `seconds`."""
+    import numpy as np
+    import oracle
+    from hybrid_linear_attention_chunk_gb300 import inputs
+
+    cores = os.cpu_count() or 1
+    K = 64
+    dx = inputs.make_decode(dw, steps=K, device=dev)
+    names = ("q", "k", "v", "log_alpha", "beta")
+    S = inputs.host_f32(dx["state"]).astype(np.float64)
+    steps = [[inputs.host_f32(dx[n][t]) for n in names] for t in range(K)]
+    del dx
+    t0 = time.perf_counter()
+    done = 0
+    while done < K and (done < 2 or time.perf_counter() - t0 < seconds):
+        _, S = oracle.decode_step(*steps[done], S, nthreads=cores)
+        done += 1
+    dt = time.perf_counter() - t0
+    per = dt / done
+    return {"value": round(dw.N / per, 2), "unit": "seq*steps/s",
+            "state_gbs": round(decode_bytes(dw.N, dw.H, dw.dk, dw.dv) / per / 1e9, 3), "cores": cores,
             "kind": "oracle",
-            "sample": f"{nchains} of {w.B * w.H} (sequence, head) chains of {w.name}, full length {T}; "
-                      f"value = chains*T/H tokens per second; {dt:.1f} s"}
+            "sample": f"{done} consecutive steps of {dw.name} over all {dw.N * dw.H} heads; {dt:.1f} s"}
 
 
 def run_reference(args):

@@ -2,8 +2,6 @@
 // device memory (see include/kda.h).  The workspace of the long-sequence
 // plan comes from a fixed array compiled into the library instead of from
 // cudaMallocAsync or from the caller.
-#include <mutex>
-
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -12,23 +10,16 @@ namespace {
 // Held by every GPU that loads the library, until the process exits.
 static __device__ __align__(256) unsigned char g_static_ws[KDA_STATIC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_ws_mutex;
-void *g_ws_ptr[kMaxDevices] = {};
-
-// Device address of g_static_ws on the current device.  In host code the name
-// g_static_ws is only a host-side stand-in, so the address is looked up once
-// per device, with that device current, and cached.
+// Device address of g_static_ws in the current device's context.  In host
+// code the name g_static_ws is only a host-side stand-in, so the address is
+// looked up with that device current.  It is looked up on every call and not
+// cached: a context that is destroyed and created again (cudaDeviceReset, a
+// primary context released and retained) loads the module again, and the
+// array may then sit at another address.  The lookup allocates nothing.
 kda_status static_ws_address(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_ws_mutex);
-  if (!g_ws_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return KDA_ERR_CUDA;
-    g_ws_ptr[dev] = p;
-  }
-  *out = g_ws_ptr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return KDA_ERR_CUDA;
+  *out = p;
   return KDA_OK;
 }
 

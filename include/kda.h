@@ -346,18 +346,21 @@ kda_status kda_device_watchdog(unsigned int *flags, int clear);
  * is unusable whenever its planner splits long sequences, because it then
  * allocates a stream-ordered workspace, and kda_chunk_fwd_ex needs a buffer they
  * may have no way to provide.  This entry point takes the same arguments as
- * kda_chunk_fwd and computes the same results, but takes its workspace from a
- * fixed array inside the library (KDA_STATIC_WORKSPACE_BYTES); it never calls
- * cudaMalloc, cudaMallocAsync, cudaFree or any other allocating routine.  The
- * caller still passes every input and output buffer.
+ * kda_chunk_fwd (with desc->validate = 0) and computes the same results, but
+ * takes its workspace from a fixed array inside the library
+ * (KDA_STATIC_WORKSPACE_BYTES); it never calls cudaMalloc, cudaMallocAsync,
+ * cudaFree or any other allocating routine.  The caller still passes every
+ * input and output buffer.
  *
  * - A call whose plan needs more scratch than KDA_STATIC_WORKSPACE_BYTES (see
  *   kda_chunk_fwd_workspace_size) returns KDA_ERR_SCRATCH_LIMIT before launching
  *   anything.  Validate mode needs an allocation and is refused with
  *   KDA_ERR_UNSUPPORTED.
- * - The first call on a device (the current device at call time) looks up the
- *   array's device address once for that device; make that first call before
- *   any stream capture.
+ * - Every call looks up the array's address in the current device's context
+ *   (cudaGetSymbolAddress, which allocates nothing), so the address stays
+ *   right after that context is destroyed and created again.  The first call
+ *   in a context may load the library's device code into it; make that first
+ *   call before any stream capture.
  * - All calls in the process share the one array, and it keeps whatever the
  *   previous call left in it (every call writes all the scratch it reads, so
  *   nothing has to start at zero).  Calls whose work overlaps on the GPU (on

@@ -438,3 +438,20 @@ def test_resume_from_checkpoint_matches_full_run():
         o2, s2 = oracle.recurrent(q[cut:], k[cut:], v[cut:], g[cut:], beta[cut:], initial_state=ck[j - 1:j])
         np.testing.assert_allclose(o2, o[cut:], rtol=0, atol=1e-10)
         np.testing.assert_allclose(s2, sf, rtol=0, atol=1e-10)
+
+
+def test_state_columns_split_equals_full_run():
+    """Column j of the state is written by entry j of v alone ([K3-notes §2.2]:
+    the erase and the decay act on S from the left), so running a head as
+    independent chains of a few state columns gives the full run exactly.
+    The long-context parity test relies on this to spread one 2^20-token head
+    over several host cores."""
+    from _helpers import oracle_heads_by_columns
+    from hybrid_linear_attention_chunk_gb300 import inputs
+    w = inputs.scaled(inputs.LONG_T1M, B=1, T=0, H=3, dk=16, dv=16, varlen_seqs=3, len_lo=20, len_hi=90)
+    x = inputs.make_prefill(w, lengths=np.array([70, 0, 45]))
+    h = {n: inputs.host_f32(x[n]) for n in ("q", "k", "v", "log_alpha", "beta", "initial_state")}
+    cu = x["cu_seqlens"].numpy()
+    o, s = oracle.recurrent(h["q"], h["k"], h["v"], h["log_alpha"], h["beta"], h["initial_state"], cu)
+    o2, s2 = oracle_heads_by_columns(x, [2, 0], width=4, workers=3)
+    assert np.array_equal(o2, o[:, [2, 0]]) and np.array_equal(s2, s[:, [2, 0]])

@@ -19,6 +19,35 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
+def _pool_watch():
+    """Reset and read the high-water mark of memory in use from the current
+    device's memory pool, the pool that stream-ordered allocations
+    (cudaMallocAsync) draw from; torch's caching allocator does not use it."""
+    rt = None
+    for name in ("libcudart.so.13", "libcudart.so", "/usr/local/cuda/lib64/libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    if rt is None:
+        pytest.fail("libcudart not found")
+    used_mem_high = 8  # cudaMemPoolAttrUsedMemHigh
+    pool = ctypes.c_void_p()
+    assert rt.cudaDeviceGetMemPool(ctypes.byref(pool), torch.cuda.current_device()) == 0
+
+    def reset():
+        zero = ctypes.c_uint64(0)
+        assert rt.cudaMemPoolSetAttribute(pool, used_mem_high, ctypes.byref(zero)) == 0
+
+    def high():
+        v = ctypes.c_uint64(0)
+        assert rt.cudaMemPoolGetAttribute(pool, used_mem_high, ctypes.byref(v)) == 0
+        return v.value
+
+    return reset, high
+
+
 def _split_inputs(T, H, seed):
     w = inputs.scaled(inputs.LONG_T1M, B=1, T=T, H=H)
     return inputs.make_prefill(w, device=DEV, seed=seed)
@@ -32,13 +61,23 @@ def test_noalloc_matches_kda_chunk_fwd_on_two_calls_in_a_row(kda):
         d = kda.chunk_desc(x["q"], x["v"], gate_dtype=0, segments=4, B=1)
         need = kda.kda_chunk_fwd_workspace_size(d)
         assert 0 < need <= (32 << 20)
+        reset, high = _pool_watch()
+        torch.cuda.synchronize()
+        reset()
         o_ref, s_ref = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
                                          x["initial_state"], None, B=1, segments=4)
         o = torch.empty_like(o_ref)
         s = torch.empty_like(s_ref)
+        torch.cuda.synchronize()
+        # the watch sees the workspace kda_chunk_fwd takes from the pool ...
+        assert high() >= need
+        reset()
+        base = high()  # what the pool still had in use at the reset (normally 0)
         kda.kda_chunk_fwd_noalloc(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["initial_state"],
                                   None, o, s, B=1, segments=4)
         torch.cuda.synchronize()
+        # ... and nothing from the allocation-free call
+        assert high() == base, "kda_chunk_fwd_noalloc took memory from the stream-ordered pool"
         assert_close(to_np(o), to_np(o_ref), TOL_BF16_FRO, TOL_BF16_MAXN, what=f"o call {call}")
         assert_close(to_np(s), to_np(s_ref), TOL_BF16_FRO, TOL_BF16_MAXN, what=f"S call {call}")
 
