@@ -8,15 +8,21 @@
 //
 // One CTA walks the chunks of one (sequence, head) chain.  With Q, K, V the
 // chunk's rows, G the within-chunk cumulative log-decay (row r includes token
-// r), Gamma = exp(G) and gamma_C = exp(G_C) ([K3-notes §2.2, chunkwise form]):
-//   M1  [A ; L''] = [Q o Gamma ; Gamma o K] (K / Gamma)^T      (M=128 N=64 K=128)
-//   A  = Tril_incl(A), L = StrictTril(diag(beta) L'')
-//   T_b = (I + L)^{-1} diag(beta)   blocked substitution: CUDA cores (fp32), last level tf32 MMA
-//   M2  U^T = V^T T_b^T                                          (M=128 N=64 K=64)
-//   M3  W^T = (Gamma o K)^T T_b^T                                (M=128 N=64 K=64)
-//   M4  V~^T = U^T - S^T W^T ;  O^T = S^T (Q o Gamma)^T          (M=128 N=64 K=128, twice)
-//   M5  O^T += V~^T A^T                                          (M=128 N=64 K=64)
-//   M6  S^T <- (S^T + V~^T (K / Gamma)) Diag(gamma_C)            (M=128 N=128 K=64)
+// r), Gamma = exp(G), gamma_C = exp(G_C) and N = -beta o Gamma o K
+// ([K3-notes §2.2, chunkwise form]):
+//   M1  [A ; -L] = [Q o Gamma ; N] (K / Gamma)^T                 (M=128 N=64 K=128)
+//   A  = Tril_incl(A), L strictly lower
+//   T  = (I + L)^{-1}   blocked substitution: CUDA cores (fp32), last level tf32 MMA
+//   X  := (beta o V)^T                   written into TMEM in fp32 by the state group
+//   M4  X += S^T N^T,  so X = R^T with R = beta o (V - (Gamma o K) S)   (M=128 N=64 K=128)
+//       O^T = S^T (Q o Gamma)^T                                   (M=128 N=64 K=128)
+//   M7  V~^T = R^T T^T   tf32: A = R^T read from TMEM, B = T fp32   (M=128 N=64 K=64)
+//   M5  O^T += V~^T A^T                                           (M=128 N=64 K=64)
+//   M6  S^T <- (S^T + V~^T (K / Gamma)) Diag(gamma_C)              (M=128 N=128 K=64)
+// The page leaves the WY factors out; with T_b = T diag(beta) they are
+// U = T_b V and W = T_b (Gamma o K), and V~ = U - W S = T R, so neither U nor W
+// is formed: the state chain needs R (one product into an accumulator that
+// already holds beta o V) and T, which the solve leaves in fp32.
 // (fp32 master state in TMEM; the Diag(gamma_C) scaling is applied to the
 // accumulated state in the same TMEM pass that refreshes its bf16 copy, and
 // K / Gamma doubles as M1's key operand.  When the chunk took the per-tile
@@ -24,18 +30,20 @@
 // takes K o gamma_C / Gamma, as S^T <- S^T Diag(gamma_C) + V~^T (K o gamma_C / Gamma).)
 // Every product is computed transposed so that M = 128 (dv or dk) and the
 // tensor core runs at full width; TMEM lane j holds row j of the result.
-// M4 reads its A operand, the bf16 copy of S^T, straight from TMEM.
+// M4 and O read their A operand, the bf16 copy of S^T, straight from TMEM,
+// M7 reads R^T (fp32) and M5/M6 read bf16 V~^T from TMEM as well.
 //
 // Two warp groups overlap consecutive chunks.  The chunk group (warps 0-7)
-// runs one chunk ahead: decay prologue, M1, the UT solve, M2/M3, and the TMA
-// loads of q, k, log-decay and v.  q and k land in the buffers that become
-// the chunk's Q o Gamma and K o gamma_C / Gamma operands, which are then
-// scaled in place.  M2/M3 complete asynchronously: their completion is what
-// hands the chunk to the state group.  The state group (warps 8-11) runs the
-// serial state chain: -W staging, M4, V~ staging, M5/M6, the gamma scaling,
-// the bf16 state copy and the output.  Operands the state group still reads
-// while the chunk group prepares the next chunk are double-buffered by chunk
-// parity.  Thread 0 of each group issues that group's MMAs.
+// runs one chunk ahead: decay prologue, the operands, M1 and the UT solve, and
+// the TMA loads of q, k and log-decay.  q and k land in the buffers that
+// become the chunk's Q o Gamma and K / Gamma operands, which are then scaled
+// in place.  The state group (warps 8-11) runs the serial state chain: M4/O,
+// M7, the bf16 copy of V~, M5/M6, the gamma scaling, the bf16 state copy and
+// the output; it also brings in v by TMA and writes the next chunk's X while
+// M5/M6 run.  Operands the state group still reads while the chunk group
+// prepares the next chunk are double-buffered by chunk parity; T is
+// single-buffered, and the solve waits for the previous chunk's M7 before it
+// writes L.  Thread 0 of each group issues that group's MMAs.
 //
 // Range guard ([K3-notes §2.2, Eq. 5 and Fig. 3]): with log-decay >= -5 a
 // 16-token tile sums to >= -80.  If every channel's chunk total G_C is >= -80
@@ -79,44 +87,48 @@ constexpr float kSingleRefBound2 = kSingleRefBound * kLog2e;  // the -80 bound i
 
 // Shared-memory map (byte offsets from a 1024-aligned base).  "x2" buffers
 // are indexed by chunk parity.
-constexpr uint32_t OFF_QG = 0;        // 48 KB: per 64-column K-half (stride KHALF):
-                                      //   [Q o Gamma, even chunks | Gamma o K | Q o Gamma, odd chunks]
-constexpr uint32_t KHALF = 24576;
-constexpr uint32_t OFF_KB = 49152;    // 16 KB: K / Gamma -> L, then T over it (fp32 64x64)
-constexpr uint32_t OFF_TF = 65536;    // 16 KB: solve scratch: T_[01][01]^T and X^T (tf32 B operands of
-                                      //   the level-2 products, 4 KB each), level-1 products (2 KB)
-constexpr uint32_t OFF_KH = 81920;    // x2 16 KB: K / Gamma (B of M1, MN-major B of M6), or
+constexpr uint32_t OFF_QG = 0;        // 64 KB: per 64-column K-half (stride KHALF), per parity (16 KB):
+                                      //   [Q o Gamma | N], the 128 rows of M1's A operand
+constexpr uint32_t KHALF = 32768;
+constexpr uint32_t OFF_KB = 65536;    // 16 KB: L, then T over it (fp32 64x64, tf32 operand layout);
+                                      //   B of M7, kept until that product is done
+constexpr uint32_t OFF_TF = 81920;    // 16 KB: solve scratch: T_[01][01]^T and X^T (tf32 B operands of
+                                      //   the level-2 products, 4 KB each), level-1 products (2 KB),
+                                      //   decay prologue sums (4 KB at OFF_PRO); on the per-tile range
+                                      //   path, M1's key operand of one tile (all 16 KB)
+constexpr uint32_t OFF_KH = 98304;    // x2 16 KB: K / Gamma (B of M1, MN-major B of M6), or
                                       //   K o gamma_C / Gamma after the per-tile range path
-constexpr uint32_t OFF_AM = 114688;   // x2 8 KB: A bf16, 64 rows x 64
-constexpr uint32_t OFF_ZT = 131072;   // 8 KB: T_b bf16 (read by M2/M3)
-constexpr uint32_t OFF_V = 139264;    // 16 KB: v tile (TMA), two 64-column boxes
-constexpr uint32_t OFF_GS = 155648;   // 32 KB: log-decay tile (TMA), fp32 [64][128]
-constexpr uint32_t OFF_VT = 188416;   // 16 KB: -W^T (MN-major), then V~^T, then the output tile
-constexpr uint32_t OFF_PRO = 204800;  // 5 KB: decay prologue sums (written while M2/M3 may still run)
-constexpr uint32_t OFF_CTL = 209920;  // 4 KB control block
+constexpr uint32_t OFF_AM = 131072;   // x2 8 KB: A bf16, 64 rows x 64
+constexpr uint32_t OFF_V = 147456;    // 16 KB: v tile (TMA), two 64-column boxes
+constexpr uint32_t OFF_GS = 163840;   // 32 KB: log-decay tile (TMA), fp32 [64][128]; with decay logits
+                                      //   (bf16, 16 KB) the out_gate tile sits in the second half
+constexpr uint32_t OFF_OG = OFF_GS + 16384;
+constexpr uint32_t OFF_VT = 196608;   // 16 KB: output tile
+constexpr uint32_t OFF_CTL = 212992;  // 4 KB control block
+constexpr uint32_t OFF_PRO = OFF_TF + 12288;
 constexpr uint32_t SMEM_USED = OFF_CTL + 4096;
-constexpr uint32_t OFF_OG = SMEM_USED;  // 16 KB, output-gate variant only: out_gate tile (TMA), bf16 [64][128]
-// + 1024 bytes of alignment slack
-constexpr uint32_t smem_bytes(bool og) { return (og ? OFF_OG + 16384 : SMEM_USED) + 1024; }
-static_assert(smem_bytes(true) <= 232448, "shared memory per CTA");
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 // TMEM columns (512 allocated).
-constexpr uint32_t TM_D1 = 0;     // M1 result (chunk group)
-constexpr uint32_t TM_W = 64;     // M3 result W^T (read by the state group)
-constexpr uint32_t TM_U = 128;    // x2 64: U^T, V~^T after M4 (by chunk parity)
+constexpr uint32_t TM_D1 = 0;     // M1 result, level-2 products (chunk group)
+constexpr uint32_t TM_X = 64;     // (beta o V)^T, then R^T after M4 (fp32; A operand of M7)
+constexpr uint32_t TM_Y = 128;    // V~^T (fp32, M7 result)
+constexpr uint32_t TM_YB = 192;   // bf16 V~^T, two values per column (A operand of M5/M6), 32 columns
 constexpr uint32_t TM_O = 256;    // O^T accumulator
-constexpr uint32_t TM_STB = 320;  // bf16 S^T, two values per column (A operand of M4)
+constexpr uint32_t TM_STB = 320;  // bf16 S^T, two values per column (A operand of M4 and O)
 constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
-  B_M1 = 0, B_M23, B_VFULL, B_GFULL, B_QK0, B_QK1, B_TB, B_M4,
+  B_M1 = 0, B_M7, B_VFULL, B_GFULL, B_QK0, B_QK1, B_TB, B_M4,
   B_M56, B_L2, B_TD_C, B_TD_S, B_OG, B_COUNT
 };
 
 struct Ctl {
   uint64_t bar[16];
   float gam[2][128];     // gamma_C per channel, by chunk parity
-  float bs[64];          // beta of the chunk's rows (0 past the end)
+  float bs[64];          // beta of the chunk's rows (0 past the end), chunk group
+  float bsx[64];         // beta of the rows of the chunk whose X the state group writes next
   alignas(16) float nw[128];  // RMSNorm weight (output-gate variant), read as float4
   uint32_t tmem_slot;
   int abort;             // any thread gave up
@@ -188,12 +200,6 @@ __device__ __forceinline__ void st_row16_bf16(uint8_t *tile, uint32_t row, uint3
                pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
   st_shared_v4(tile + sw128_offset(row, c0 + 8), pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]),
                pack_bf16(v[12], v[13]), pack_bf16(v[14], v[15]));
-}
-
-// Stores 4 fp32 values as bf16 at columns [c0, c0+4) of a 128-byte-swizzled
-// tile (c0 a multiple of 4).
-__device__ __forceinline__ void st_row4_bf16(uint8_t *tile, uint32_t row, uint32_t c0, const float4 &v) {
-  *reinterpret_cast<uint2 *>(tile + sw128_offset(row, c0)) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
 }
 
 __device__ __forceinline__ void sts64(uint8_t *p, uint2 v) { *reinterpret_cast<uint2 *>(p) = v; }
@@ -275,11 +281,14 @@ __device__ __forceinline__ int tt_idx(int n, int k) { return (n << 5) + ((((k >>
 // A group-wide view of an mbarrier wait: the group's thread 0 waits, the
 // group synchronises, and every thread gets the same verdict (so no thread
 // can leave while others sit in a group barrier).
+// A second barrier b2 (>= 0) is waited for after the first, with parity p2.
 template <bool kChunkGroup>
-__device__ __forceinline__ bool group_wait(Ctl *ctl, int b, uint32_t parity, int gtid, int &seq, unsigned int *err) {
+__device__ __forceinline__ bool group_wait(Ctl *ctl, int b, uint32_t parity, int gtid, int &seq, unsigned int *err,
+                                           int b2 = -1, uint32_t p2 = 0) {
   int *go = kChunkGroup ? ctl->go_c : ctl->go_s;
   if (gtid == 0) {
-    const bool ok = mbar_wait(smem_u32(&ctl->bar[b]), parity, &ctl->abort, err, 1u << b);
+    bool ok = mbar_wait(smem_u32(&ctl->bar[b]), parity, &ctl->abort, err, 1u << b);
+    if (ok && b2 >= 0) ok = mbar_wait(smem_u32(&ctl->bar[b2]), p2 & 1u, &ctl->abort, err, 1u << b2);
     go[seq & 1] = ok && !ctl->abort;
   }
   if (kChunkGroup) bar_chunk(); else bar_state();
@@ -398,55 +407,59 @@ __device__ __forceinline__ void issue_qk(const TcMaps *maps, Ctl *ctl, uint32_t 
 
 // ------------------------------------------------------------- MMA batches
 
+// M1 of the chunk of parity par: A = the 128 rows [Q o Gamma ; N] of that
+// parity (contiguous within each K-half), B = the keys kb.
 __device__ __forceinline__ void issue_m1(uint32_t tbase, uint32_t qg, uint32_t kb, int par, bool acc_first) {
   constexpr uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
-  // A = 128 consecutive rows: [Q o Gamma ; Gamma o K] for even chunks,
-  // [Gamma o K ; Q o Gamma] for odd ones (so the solve swaps lane roles)
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t ka = (kk >> 2) * KHALF + par * 8192 + (kk & 3) * 32;
+    const uint32_t ka = (kk >> 2) * KHALF + par * 16384 + (kk & 3) * 32;
     const uint32_t kbo = (kk >> 2) * 8192 + (kk & 3) * 32;
     mma_bf16_ss(tbase + TM_D1, smem_desc_sw128(qg + ka, 16, 1024), smem_desc_sw128(kb + kbo, 16, 1024), id,
                 (kk > 0 || acc_first) ? 1u : 0u);
   }
 }
 
-__device__ __forceinline__ void issue_m23(uint32_t tbase, uint32_t v, uint32_t qg, uint32_t zt, uint32_t tm_u) {
-  constexpr uint32_t id = idesc_bf16_f32(128, 64, 1, 0);
+// M4: X += S^T N^T (A = bf16 S^T in TMEM, B = N, K-major).
+__device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t qg, int par) {
+  constexpr uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)  // U^T = V^T T_b^T   (A = V, MN-major: 2 blocks of 64 columns)
-    mma_bf16_ss(tbase + tm_u, smem_desc_sw128(v + kk * 2048, 8192, 1024), smem_desc_sw128(zt + kk * 32, 16, 1024),
-                id, kk > 0 ? 1u : 0u);
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk)  // W^T = (Gamma o K)^T T_b^T   (A = the Gamma o K blocks, MN-major)
-    mma_bf16_ss(tbase + TM_W, smem_desc_sw128(qg + 8192 + kk * 2048, KHALF, 1024),
-                smem_desc_sw128(zt + kk * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
-}
-
-__device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t vt, uint32_t qg, int par, uint32_t tm_u) {
-  constexpr uint32_t id_w = idesc_bf16_f32(128, 64, 0, 1);
-  constexpr uint32_t id_q = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk)  // V~^T = U^T + S^T (-W)^T     (B = -W^T, MN-major, in the V~ buffer)
-    mma_bf16_ts(tbase + tm_u, tbase + TM_STB + kk * 8, smem_desc_sw128(vt + kk * 2048, 8192, 1024), id_w, 1u);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {  // O^T = S^T (Q o Gamma)^T
-    const uint32_t kb = (kk >> 2) * KHALF + par * 16384 + (kk & 3) * 32;
-    mma_bf16_ts(tbase + TM_O, tbase + TM_STB + kk * 8, smem_desc_sw128(qg + kb, 16, 1024), id_q, kk > 0 ? 1u : 0u);
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t kb = (kk >> 2) * KHALF + par * 16384 + 8192 + (kk & 3) * 32;
+    mma_bf16_ts(tbase + TM_X, tbase + TM_STB + kk * 8, smem_desc_sw128(qg + kb, 16, 1024), id, 1u);
   }
 }
 
-__device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t vt, uint32_t am, uint32_t kh) {
+// O^T = S^T (Q o Gamma)^T (A = bf16 S^T in TMEM, B = Q o Gamma, K-major).
+__device__ __forceinline__ void issue_o(uint32_t tbase, uint32_t qg, int par) {
+  constexpr uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t kb = (kk >> 2) * KHALF + par * 16384 + (kk & 3) * 32;
+    mma_bf16_ts(tbase + TM_O, tbase + TM_STB + kk * 8, smem_desc_sw128(qg + kb, 16, 1024), id, kk > 0 ? 1u : 0u);
+  }
+}
+
+// M7: V~^T = R^T T^T in tf32 (A = R^T fp32 in TMEM, one K element per
+// column; B = T fp32 in the two 32-column K-halves of the solve's buffer).
+__device__ __forceinline__ void issue_m7(uint32_t tbase, uint32_t tt) {
+  constexpr uint32_t id = idesc_tf32_f32(128, 64);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_tf32_ts(tbase + TM_Y, tbase + TM_X + kk * 8,
+                smem_desc_sw128(tt + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
+}
+
+// M6 then M5 (A = bf16 V~^T in TMEM).
+__device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t am, uint32_t kh) {
   constexpr uint32_t id5 = idesc_bf16_f32(128, 64, 0, 0);
   constexpr uint32_t id6 = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)  // O^T += V~^T A^T
-    mma_bf16_ss(tbase + TM_O, smem_desc_sw128(vt + kk * 32, 16, 1024), smem_desc_sw128(am + kk * 32, 16, 1024),
-                id5, 1u);
+  for (int kk = 0; kk < 4; ++kk)  // S^T += V~^T (K / Gamma)   (B MN-major)
+    mma_bf16_ts(tbase + TM_S, tbase + TM_YB + kk * 8, smem_desc_sw128(kh + kk * 2048, 8192, 1024), id6, 1u);
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)  // S^T += V~^T (K o gamma_C / Gamma)   (B MN-major)
-    mma_bf16_ss(tbase + TM_S, smem_desc_sw128(vt + kk * 32, 16, 1024),
-                smem_desc_sw128(kh + kk * 2048, 8192, 1024), id6, 1u);
+  for (int kk = 0; kk < 4; ++kk)  // O^T += V~^T A^T
+    mma_bf16_ts(tbase + TM_O, tbase + TM_YB + kk * 8, smem_desc_sw128(am + kk * 32, 16, 1024), id5, 1u);
 }
 
 // The sequence of rank r when N packed sequences are ordered by length,
@@ -527,6 +540,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   tc_fence_after();
   const uint32_t tbase = ctl->tmem_slot;
   const uint32_t sm_base = smem_u32(sm);
+  const float *betap = reinterpret_cast<const float *>(a.beta);
 
   if (tid < kChunkThreads) {
     // =========================================================== chunk group
@@ -539,7 +553,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     // 64-column K-half, and a thread's rows lie in one 16-token tile, t8 / 2
     const int p4 = ctid & 31, t8 = ctid >> 5;
     int seq = 0;
-    uint32_t ph_m1 = 0, ph_m23 = 0, ph_g = 0, ph_l2 = 0;
+    uint32_t ph_m1 = 0, ph_g = 0, ph_l2 = 0;
     Loader ld{&maps, ctl, sm_base, h, 0, 0, (uint32_t)(kC * kD * (kZ ? 2 : 4))};
     // decay gate (Eq. 5) in log2 units: g log2(e) = zg_min / (1 + 2^(zs z))
     const float zs = kZ ? -expf(a.A_log[h]) * kLog2e : 0.f;
@@ -547,28 +561,16 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     if (ctid == 0 && nchunks > 0) {
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
-      tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.g);
       ld.g(bos);
       // q and k of the first two chunks; later ones are issued by the state
       // group as it frees each parity's buffers
       issue_qk(&maps, ctl, sm_base, h, bos, 0);
       if (nchunks > 1) issue_qk(&maps, ctl, sm_base, h, bos + kC, 1);
-      if (!zero_v) issue_v(&maps, ctl, sm_base, h, bos);
-    }
-    if (zero_v)  // the v tile stays zero for the whole item
-      for (int e = ctid; e < 16384 / 16; e += kChunkThreads)
-        reinterpret_cast<uint4 *>(sm + OFF_V)[e] = make_uint4(0u, 0u, 0u, 0u);
-    for (int e = ctid; e < 8192 / 16; e += kChunkThreads)  // T_b above the diagonal: zero for good
-      reinterpret_cast<uint4 *>(sm + OFF_ZT)[e] = make_uint4(0u, 0u, 0u, 0u);
-    if (ctid < 64) {  // T_01^T in the transposed copy of T_[01][01]: zero for good
-      const int n = 16 + (ctid >> 2), k0 = 4 * (ctid & 3);
-      *reinterpret_cast<float4 *>(reinterpret_cast<float *>(sm + OFF_TF) + tt_idx(n, k0)) =
-          make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float beta_next = 0.f;
-    if (ctid < kC && ctid < eos - bos) beta_next = __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(bos + ctid) * H + h);
-    float *tot = reinterpret_cast<float *>(sm + OFF_PRO);  // [4][128] per-tile decay sums
+    if (ctid < kC && ctid < eos - bos) beta_next = __ldg(betap + (size_t)(bos + ctid) * H + h);
+    float *tot = reinterpret_cast<float *>(sm + OFF_PRO);  // [8][128] per-row-group decay sums
     const float *gs = reinterpret_cast<const float *>(sm + OFF_GS);
     uint8_t *qg = sm + OFF_QG;
     bool alive = true;
@@ -626,22 +628,16 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       }
       const float4 gam = make_float4(ex2(tc.x), ex2(tc.y), ex2(tc.z), ex2(tc.w));
       const bool vote = fminf(fminf(tc.x, tc.y), fminf(tc.z, tc.w)) < kSingleRefBound2;
+      float nb[8];  // -beta of the thread's rows (N = -beta o Gamma o K)
+#pragma unroll
+      for (int r = 0; r < 8; ++r) nb[r] = -ctl->bs[8 * t8 + r];
       if (ctid < kC)  // beta of the next chunk's rows, 0 past the end
-        beta_next = ctid < eos - (t0 + kC)
-                        ? __ldg(reinterpret_cast<const float *>(a.beta) + (size_t)(t0 + kC + ctid) * H + h)
-                        : 0.f;
-      // The previous chunk's M2/M3 must be done with Gamma o K and T_b before
-      // this chunk overwrites them; this chunk's q and k have landed.
+        beta_next = ctid < eos - (t0 + kC) ? __ldg(betap + (size_t)(t0 + kC + ctid) * H + h) : 0.f;
+      // This chunk's q and k have landed (the copy was issued once the state
+      // group was done with this parity's buffers, two chunks back).
       if (ctid == 0) {
-        bool ok = true;
-        if (m >= 1) {
-          ok = solo_wait(ctl, B_M23, ph_m23, A.err);
-          ph_m23 ^= 1u;
-        }
-        if (ok) {
-          ok = solo_wait(ctl, B_QK0 + par, (m >> 1) & 1, A.err);
-          if (ok) ++ctl->qk_lnd[par];
-        }
+        const bool ok = solo_wait(ctl, B_QK0 + par, (m >> 1) & 1, A.err);
+        if (ok) ++ctl->qk_lnd[par];
         ctl->go_c[seq & 1] = ok && !ctl->abort;
       }
       // the barrier also closes the range-guard vote
@@ -656,9 +652,9 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // operand tiles: channel quad p4 sits in K-half p4 / 16 at column 4 p4 mod 64
       const uint32_t half = (uint32_t)(p4 >> 4), col = (uint32_t)(4 * p4) & 63u;
       uint8_t *qb_h = qg + half * KHALF + par * 16384;  // q -> Q o Gamma (in place)
-      uint8_t *gk_h = qg + half * KHALF + 8192;         // Gamma o K
-      uint8_t *kb_h = sm + OFF_KB + half * 8192;        // K / Gamma
-      uint8_t *kh_h = kh + half * 8192;                 // k -> K o gamma_C / Gamma (in place)
+      uint8_t *nb_h = qb_h + 8192;                      // N = -beta o Gamma o K
+      uint8_t *kb_h = sm + OFF_TF + half * 8192;        // a tile's keys (per-tile range path)
+      uint8_t *kh_h = kh + half * 8192;                 // k -> K / Gamma (in place)
       float4 qv[8], kv[8];
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
@@ -672,8 +668,9 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         for (int r = 0; r < 8; ++r) {  // K / Gamma in place of k: M1's keys and M6's operand
           const uint32_t off = sw128_offset(8 * t8 + r, col);
           const float4 e = ex2_4(Gl[r]), i = ex2_4(neg4(Gl[r]));
+          const float4 ge = mul4(kv[r], e);
           sts64(qb_h + off, pack4_bf16(mul4(qv[r], e)));
-          sts64(gk_h + off, pack4_bf16(mul4(kv[r], e)));
+          sts64(nb_h + off, pack4_bf16(make_float4(nb[r] * ge.x, nb[r] * ge.y, nb[r] * ge.z, nb[r] * ge.w)));
           sts64(kh_h + off, pack4_bf16(mul4(kv[r], i)));
         }
         group_publish<true>();
@@ -681,7 +678,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           issue_m1(tbase, smem_u32(qg), sm_base + OFF_KH + par * 16384, par, false);
           mma_commit(smem_u32(&ctl->bar[B_M1]));
         }
-        alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
+        // M1 done, and the previous chunk's M7 done with T (L is written over it below)
+        alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err, m > 0 ? B_M7 : -1, (m - 1) & 1);
         ph_m1 ^= 1u;
       } else {
         // M1 in four accumulating rounds, one per 16-token key tile b, with
@@ -703,12 +701,12 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
             }
             if (tile == b) fb = mul4(kv[r], ex2_4(sub4(rb, Gl[r])));
             sts64(qb_h + off, pack4_bf16(fq));
-            sts64(gk_h + off, pack4_bf16(fk));
+            sts64(nb_h + off, pack4_bf16(make_float4(nb[r] * fk.x, nb[r] * fk.y, nb[r] * fk.z, nb[r] * fk.w)));
             sts64(kb_h + off, pack4_bf16(fb));
           }
           group_publish<true>();
           if (ctid == 0) {
-            issue_m1(tbase, smem_u32(qg), sm_base + OFF_KB, par, b > 0);
+            issue_m1(tbase, smem_u32(qg), sm_base + OFF_TF, par, b > 0);
             mma_commit(smem_u32(&ctl->bar[B_M1]));
           }
           alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
@@ -720,24 +718,27 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         for (int r = 0; r < 8; ++r) {
           const uint32_t off = sw128_offset(8 * t8 + r, col);
           const float4 e = ex2_4(Gl[r]);
+          const float4 ge = mul4(kv[r], e);
           sts64(qb_h + off, pack4_bf16(mul4(qv[r], e)));
-          sts64(gk_h + off, pack4_bf16(mul4(kv[r], e)));
+          sts64(nb_h + off, pack4_bf16(make_float4(nb[r] * ge.x, nb[r] * ge.y, nb[r] * ge.z, nb[r] * ge.w)));
           sts64(kh_h + off, pack4_bf16(mul4(kv[r], ex2_4(sub4(tc, Gl[r])))));
         }
+        // the previous chunk's M7 is done with T (L is written over it below)
+        if (m > 0) alive = group_wait<true>(ctl, B_M7, (m - 1) & 1, ctid, seq, A.err);
       }
       if (!alive) break;
 
-      // ---------------- masks, L, and T_b = (I + L)^{-1} diag(beta)
+      // ---------------- masks, L, and T = (I + L)^{-1}
       // L is stored with zeros on and above its diagonal and T is computed in
       // place over it: T is zero above the diagonal too, so the zeros L leaves
       // there are already T's.
       {
-        float *Lf = reinterpret_cast<float *>(sm + OFF_KB);  // K / Gamma is dead once M1 is done
+        float *Lf = reinterpret_cast<float *>(sm + OFF_KB);
         float *TTf = reinterpret_cast<float *>(sm + OFF_TF);      // T_[01][01]^T, [32][32] K-major
         float *XTf = TTf + 1024;                                  // X^T of level 2, [32][32] K-major
         float *Xf = TTf + 2048;                                   // level-1 products
-        // even chunks: TMEM lanes 0..63 hold A's rows, 64..127 L''; odd chunks the reverse
-        const bool a_rows = (qw < 2) == (par == 0);
+        // TMEM lanes 0..63 hold A's rows, 64..127 the rows of -L (N (K / Gamma)^T)
+        const bool a_rows = qw < 2;
         const int r = 32 * (qw & 1) + lane;
         float v[32];  // row r, columns [32 ch, 32 ch + 32) of the Gram product
         tmem_ld32(tmem_addr(tbase, 32 * qw, TM_D1 + 32 * ch), v);
@@ -749,9 +750,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           st_row16_bf16(sm + OFF_AM + par * 8192, r, s0, v);
           st_row16_bf16(sm + OFF_AM + par * 8192, r, s0 + 16, v + 16);
         } else {
-          const float br = ctl->bs[r];
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) v[cc] = (s0 + cc < r) ? br * v[cc] : 0.f;
+          for (int cc = 0; cc < 32; ++cc) v[cc] = (s0 + cc < r) ? -v[cc] : 0.f;
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4)
             *reinterpret_cast<float4 *>(Lf + lt_idx(r, s0 + 4 * c4)) =
@@ -791,6 +791,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
             for (int j = 0; j < 4; ++j)
               *reinterpret_cast<float4 *>(TTf + tt_idx(base + cc, base + 4 * j)) =
                   make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+        } else if (ctid < 128) {
+          // T_01^T of the transposed copy is zero (the per-tile range path may
+          // have used this buffer for its key operand)
+          const int e = ctid - 64;
+          *reinterpret_cast<float4 *>(TTf + tt_idx(16 + (e >> 2), 4 * (e & 3))) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         bar_chunk();
         // Off-diagonal blocks in two levels of the 2x2 block inverse
@@ -798,12 +803,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         //   level 1 (16-row blocks): T_10 and T_32;
         //   level 2 (32-row blocks): T_[23][01].
         // Each output is X = R P^-1, then -Q^-1 X.  Level 1 runs on CUDA cores
-        // (fp32); level 2 on the tensor core (tf32, below).  Every block of
-        // T_b = T diag(beta) is written as soon as its T block is final, the
-        // product outputs straight from registers or TMEM; T_b's blocks above
-        // the diagonal stay zero from the start.
-        const float4 *bs4 = reinterpret_cast<const float4 *>(ctl->bs);
-        uint8_t *zt = sm + OFF_ZT;
+        // (fp32); level 2 on the tensor core (tf32, below).
         if (ctid < 128) {
           // level 1: two 16x16 outputs, 128 tasks of (row, 4 columns)
           const int blk = ctid >> 6, rr = (ctid >> 2) & 15, q4 = ctid & 3;
@@ -832,27 +832,14 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           }
           acc = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
           *reinterpret_cast<float4 *>(Lf + lt_idx(rb + rr, cb + 4 * q4)) = acc;
-          st_row4_bf16(zt, rb + rr, cb + 4 * q4, mul4(acc, bs4[cb / 4 + q4]));
           if (blk == 0) {  // T_10 into the transposed copy
             TTf[tt_idx(4 * q4, 16 + rr)] = acc.x;
             TTf[tt_idx(4 * q4 + 1, 16 + rr)] = acc.y;
             TTf[tt_idx(4 * q4 + 2, 16 + rr)] = acc.z;
             TTf[tt_idx(4 * q4 + 3, 16 + rr)] = acc.w;
           }
-        } else if (ctid < 192) {
-          // T_b of the diagonal blocks: row rr of block db, its 16 columns
-          const int e = ctid - 128, db = e >> 4, rr = e & 15;
-          const int row = 16 * db + rr, c0 = 16 * db;
-          float v[16];
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 tv = mul4(lds128(Lf + lt_idx(row, c0 + 4 * c4)), bs4[c0 / 4 + c4]);
-            v[4 * c4] = tv.x; v[4 * c4 + 1] = tv.y; v[4 * c4 + 2] = tv.z; v[4 * c4 + 3] = tv.w;
-          }
-          st_row16_bf16(zt, row, c0, v);
         }
-        // level 2 on the tensor core (tf32; the level-2 block of T is small
-        // beside the diagonal, and T_b is rounded to bf16 after it):
+        // level 2 on the tensor core (tf32):
         //   X = L_[23][01] T_[01][01], then T_[23][01] = -T_[23][23] X.
         // M = 128 rows of the row-major operand (rows 0-31 and 64-127 of the
         // product are not used), N = 32, K = 32; D in the M1 result's columns.
@@ -886,20 +873,19 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
         if (!(alive = group_wait<true>(ctl, B_L2, ph_l2, ctid, seq, A.err))) break;
         ph_l2 ^= 1u;
-        if ((warp & 3) == 1) {  // rows 32-63: T_[23][23] X = -T_[23][01]  ->  T_b
+        if ((warp & 3) == 1) {  // rows 32-63: T_[23][23] X = -T_[23][01]
           const int n0 = 16 * (warp >> 2);
           float y[16];
           tmem_ld16(tmem_addr(tbase, 32, TM_D1 + 32 + n0), y);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) y[i] *= -ctl->bs[n0 + i];
-          st_row16_bf16(zt, 32 + lane, n0, y);
+          for (int i = 0; i < 16; ++i) Lf[lt_idx(32 + lane, n0 + i)] = -y[i];
         }
       }
       if (ctid == 0) ctl->slow[par] = slow;
       group_publish<true>();
-      // ---------------- hand the chunk to the state group, which issues M2/M3
-      // (the arrive releases the chunk's shared-memory state to it)
+      // ---------------- hand the chunk to the state group (the arrive releases
+      // the chunk's operands, A, T and gamma_C to it)
       if (ctid == 0) mbar_arrive(smem_u32(&ctl->bar[B_TB]));
     }
     if (ctid == 0) {
@@ -917,7 +903,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     int seq = 0;
     uint32_t ph_m4 = 0, ph_m56 = 0;
     uint8_t *vt = sm + OFF_VT;
-    if (kOG && stid == 0) tma_prefetch_desc(&maps.og);
+    if (stid == 0 && nchunks > 0) {
+      tma_prefetch_desc(&maps.v);
+      if (kOG) tma_prefetch_desc(&maps.og);
+      if (!zero_v) issue_v(&maps, ctl, sm_base, h, bos);
+    }
     // entry state -> TMEM: fp32 master and the bf16 copy M4 reads (S^T row j;
     // the identity for a transition item, zero without an initial state)
 #pragma unroll 1
@@ -930,61 +920,81 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0 + 16), *reinterpret_cast<float(*)[16]>(s + 16));
       tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_STB + i0 / 2), s);
     }
-    tmem_wait_st();
-    group_publish<false>();
+    if (stid < kC) ctl->bsx[stid] = stid < eos - bos ? __ldg(betap + (size_t)(bos + stid) * H + h) : 0.f;
+    // X of chunk c := (beta o V)^T in fp32: thread j writes column j of V
+    // times beta (v of rows past the end has beta = 0).  Every state thread
+    // has passed a barrier since bsx was written.
+    auto fill_x = [&](int c) -> bool {
+      if (!zero_v) {
+        if (!group_wait<false>(ctl, B_VFULL, c & 1, stid, seq, A.err)) return false;
+        if (stid == 0) ++ctl->v_lnd;
+      } else {
+        bar_state();
+      }
+      const uint8_t *vb = sm + OFF_V + (j >> 6) * 8192;
+      const uint32_t jc = (uint32_t)j & 63u;
+#pragma unroll 1
+      for (int s0 = 0; s0 < kC; s0 += 32) {
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float vv = zero_v ? 0.f
+                                  : __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                        vb + sw128_offset((uint32_t)(s0 + i), jc)));
+          x[i] = ctl->bsx[s0 + i] * vv;
+        }
+        tmem_st16(tmem_addr(tbase, 32 * qw, TM_X + s0), *reinterpret_cast<float(*)[16]>(x));
+        tmem_st16(tmem_addr(tbase, 32 * qw, TM_X + s0 + 16), *reinterpret_cast<float(*)[16]>(x + 16));
+      }
+      return true;
+    };
     bool alive = true;
+    if (nchunks > 0) {
+      bar_state();  // bsx
+      alive = fill_x(0);
+      tmem_wait_st();
+      tc_fence_before();
+      bar_state();  // every thread has read the v tile of chunk 0
+      if (stid == 0 && !zero_v && nchunks > 1) issue_v(&maps, ctl, sm_base, h, bos + kC);
+    } else {
+      tmem_wait_st();
+      tc_fence_before();
+    }
     for (int c = 0; c < nchunks && alive; ++c) {
       const int par = c & 1;
       const int t0 = bos + c * kC;
       const int len = min(kC, eos - t0);
-      const uint32_t tm_u = TM_U + par * 64;
-      // ---------------- M2/M3: U^T and W^T, once the chunk group has T_b
+      // beta of the next chunk's rows (for its X), fetched early
+      float bnext = 0.f;
+      if (stid < kC && c + 1 < nchunks && t0 + kC + stid < eos) bnext = __ldg(betap + (size_t)(t0 + kC + stid) * H + h);
+      // ---------------- M4 and O once the chunk group has handed the chunk over
       if (!(alive = group_wait<false>(ctl, B_TB, c & 1, stid, seq, A.err))) break;
       // (every thread is past the previous chunk's reads of the out_gate tile)
       if (kOG && stid == 0) issue_og(&maps, ctl, sm_base, h, t0);
       if (stid == 0) {
-        bool ok = true;
-        if (!zero_v) {
-          ok = solo_wait(ctl, B_VFULL, c & 1, A.err);
-          if (ok) ++ctl->v_lnd;
-        }
-        if (ok) {
-          issue_m23(tbase, sm_base + OFF_V, sm_base + OFF_QG, sm_base + OFF_ZT, tm_u);
-          mma_commit(smem_u32(&ctl->bar[B_M23]));
-        }
-      }
-      if (!(alive = group_wait<false>(ctl, B_M23, c & 1, stid, seq, A.err))) break;
-      if (stid == 0 && !zero_v && c + 1 < nchunks) issue_v(&maps, ctl, sm_base, h, t0 + kC);  // M2 is done with v
-
-      // ---------------- -W^T (TMEM) -> MN-major operand in the V~ buffer
-      {
-        float v[64];
-        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_W), *reinterpret_cast<float(*)[32]>(v));
-        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_W + 32), *reinterpret_cast<float(*)[32]>(v + 32));
-        tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < 64; ++cc) v[cc] = -v[cc];
-#pragma unroll
-        for (int r0 = 0; r0 < 64; r0 += 16) st_row16_bf16(vt, j, r0, v + r0);
-      }
-      group_publish<false>();
-      if (stid == 0) {
-        issue_m4(tbase, sm_base + OFF_VT, sm_base + OFF_QG, par, tm_u);
+        issue_m4(tbase, sm_base + OFF_QG, par);
         mma_commit(smem_u32(&ctl->bar[B_M4]));
+        issue_o(tbase, sm_base + OFF_QG, par);
+        // M7 once M4 has completed R (M7 reads it from TMEM)
+        if (solo_wait(ctl, B_M4, ph_m4, A.err)) {
+          issue_m7(tbase, sm_base + OFF_KB);
+          mma_commit(smem_u32(&ctl->bar[B_M7]));
+        }
       }
-      if (!(alive = group_wait<false>(ctl, B_M4, ph_m4, stid, seq, A.err))) break;
       ph_m4 ^= 1u;
+      if (!(alive = group_wait<false>(ctl, B_M7, c & 1, stid, seq, A.err))) break;
 
-      // ---------------- V~^T -> bf16 operand; after the per-tile range path,
-      // S^T <- S^T Diag(gamma_C) before M6 (else the scaling follows M6)
+      // ---------------- V~^T -> bf16 A operand of M5/M6; after the per-tile
+      // range path, S^T <- S^T Diag(gamma_C) before M6 (else the scaling follows M6)
       const bool slow = ctl->slow[par] != 0;
       {
-        float v[64];
-        tmem_ld32(tmem_addr(tbase, 32 * qw, tm_u), *reinterpret_cast<float(*)[32]>(v));
-        tmem_ld32(tmem_addr(tbase, 32 * qw, tm_u + 32), *reinterpret_cast<float(*)[32]>(v + 32));
+        float y[32];
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_Y), y);
         tmem_wait_ld();
-#pragma unroll
-        for (int r0 = 0; r0 < 64; r0 += 16) st_row16_bf16(vt, j, r0, v + r0);
+        tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_YB), y);
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_Y + 32), y);
+        tmem_wait_ld();
+        tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_YB + 16), y);
       }
       if (slow) {
         const float *gam = ctl->gam[par];
@@ -998,15 +1008,22 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), *reinterpret_cast<float(*)[16]>(s));
           tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0 + 16), *reinterpret_cast<float(*)[16]>(s + 16));
         }
-        tmem_wait_st();
       }
+      if (stid < kC) ctl->bsx[stid] = bnext;
+      tmem_wait_st();
       group_publish<false>();
       if (stid == 0) {
-        issue_m56(tbase, sm_base + OFF_VT, sm_base + OFF_AM + par * 8192, sm_base + OFF_KH + par * 16384);
+        issue_m56(tbase, sm_base + OFF_AM + par * 8192, sm_base + OFF_KH + par * 16384);
         mma_commit(smem_u32(&ctl->bar[B_M56]));
       }
+      // ---------------- X of the next chunk while M5/M6 run (M7 has read X)
+      if (c + 1 < nchunks && !(alive = fill_x(c + 1))) break;
+      tmem_wait_st();
+      tc_fence_before();
       if (!(alive = group_wait<false>(ctl, B_M56, ph_m56, stid, seq, A.err))) break;
       ph_m56 ^= 1u;
+      // every thread has read the v tile of chunk c + 1: chunk c + 2's may land
+      if (stid == 0 && !zero_v && c + 2 < nchunks) issue_v(&maps, ctl, sm_base, h, t0 + 2 * kC);
 
       // ---------------- S^T <- S^T Diag(gamma_C) (unless done before M6), the
       // bf16 copy of the new state (and a checkpoint of the fp32 state when
@@ -1048,10 +1065,10 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       } else {
         bar_state();
       }
-      // This parity's operand buffers are free (M4-M6 have completed and every
+      // This parity's operand buffers are free (M4-M7 have completed and every
       // state thread has read gamma_C): q and k of the chunk two ahead land in
-      // them; its A tile, gamma_C and TMEM U^T are written only after that
-      // copy has been waited for.
+      // them; its N and A tiles and gamma_C are written only after that copy
+      // has been waited for.
       if (stid == 0 && c + 2 < nchunks) issue_qk(&maps, ctl, sm_base, h, t0 + 2 * kC, par);
       if (a.o) {  // segment passes of the long-sequence plan write no output
         const uint4 *src = reinterpret_cast<const uint4 *>(vt);
@@ -1163,7 +1180,7 @@ CUresult encode_tok_head(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, 
 
 template <bool kZ, bool kOG>
 cudaError_t launch_variant(const TcMaps &maps, const TcArgs &args, int grid, cudaStream_t s) {
-  constexpr uint32_t bytes = smem_bytes(kOG);
+  constexpr uint32_t bytes = SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<kZ, kOG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)bytes);
   if (e != cudaSuccess) return e;
@@ -1198,7 +1215,10 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
   TcArgs args{a, reinterpret_cast<unsigned int *>(wd)};
   const int grid = a.N * a.nseg * a.H * a.kinds;
   if (z) return og ? launch_variant<true, true>(maps, args, grid, s) : launch_variant<true, false>(maps, args, grid, s);
-  return og ? launch_variant<false, true>(maps, args, grid, s) : launch_variant<false, false>(maps, args, grid, s);
+  // the output gate comes with the layer form, whose decay is given as logits
+  // (the out_gate tile shares the decay tile's buffer, half of which bf16 logits use)
+  if (og) return cudaErrorInvalidValue;
+  return launch_variant<false, false>(maps, args, grid, s);
 }
 
 cudaError_t read_tc_watchdog(unsigned int *flags, bool clear) {
