@@ -13,7 +13,7 @@
 //   M1  [A ; -L] = [Q o Gamma ; N] (K / Gamma)^T                 (M=128 N=64 K=128)
 //   A  = Tril_incl(A), L strictly lower
 //   T  = (I + L)^{-1}   blocked substitution: CUDA cores (fp32), last level tf32 MMA
-//   X  := (beta o V)^T                   written into TMEM in fp32 by the state group
+//   M3  X  = V^T Diag(beta)              (M=128 N=64 K=64; beta rounded to bf16)
 //   M4  X += S^T N^T,  so X = R^T with R = beta o (V - (Gamma o K) S)   (M=128 N=64 K=128)
 //       O^T = S^T (Q o Gamma)^T                                   (M=128 N=64 K=128)
 //   M7  V~^T = R^T T^T   tf32: A = R^T read from TMEM, B = T fp32   (M=128 N=64 K=64)
@@ -39,8 +39,7 @@
 // become the chunk's Q o Gamma and K / Gamma operands, which are then scaled
 // in place.  The state group (warps 8-11) runs the serial state chain: M4/O,
 // M7, the bf16 copy of V~, M5/M6, the gamma scaling, the bf16 state copy and
-// the output; it also brings in v by TMA and writes the next chunk's X while
-// M5/M6 run.  Operands the state group still reads while the chunk group
+// the output; it also brings in v by TMA and writes Diag(beta) for M3.  Operands the state group still reads while the chunk group
 // prepares the next chunk are double-buffered by chunk parity; T is
 // single-buffered, and the solve waits for the previous chunk's M7 before it
 // writes L.  Thread 0 of each group issues that group's MMAs.
@@ -93,7 +92,7 @@ constexpr uint32_t KHALF = 32768;
 constexpr uint32_t OFF_KB = 65536;    // 16 KB: L, then T over it (fp32 64x64, tf32 operand layout);
                                       //   B of M7, kept until that product is done
 constexpr uint32_t OFF_TF = 81920;    // 16 KB: solve scratch: T_[01][01]^T and X^T (tf32 B operands of
-                                      //   the level-2 products, 4 KB each), level-1 products (2 KB),
+                                      //   the level-64 products, 4 KB each), 16- and 32-row level products (3 KB),
                                       //   decay prologue sums (4 KB at OFF_PRO); on the per-tile range
                                       //   path, M1's key operand of one tile (all 16 KB)
 constexpr uint32_t OFF_KH = 98304;    // x2 16 KB: K / Gamma (B of M1, MN-major B of M6), or
@@ -104,7 +103,8 @@ constexpr uint32_t OFF_GS = 163840;   // 32 KB: log-decay tile (TMA), fp32 [64][
                                       //   (bf16, 16 KB) the out_gate tile sits in the second half
 constexpr uint32_t OFF_OG = OFF_GS + 16384;
 constexpr uint32_t OFF_VT = 196608;   // 16 KB: output tile
-constexpr uint32_t OFF_CTL = 212992;  // 4 KB control block
+constexpr uint32_t OFF_DB = 212992;   // 8 KB: Diag(beta) in bf16, K-major 64 x 64 (B operand of M3)
+constexpr uint32_t OFF_CTL = 221184;  // 4 KB control block
 constexpr uint32_t OFF_PRO = OFF_TF + 12288;
 constexpr uint32_t SMEM_USED = OFF_CTL + 4096;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
@@ -112,7 +112,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 // TMEM columns (512 allocated).
 constexpr uint32_t TM_D1 = 0;     // M1 result, level-2 products (chunk group)
-constexpr uint32_t TM_X = 64;     // (beta o V)^T, then R^T after M4 (fp32; A operand of M7)
+constexpr uint32_t TM_X = 64;     // (beta o V)^T after M3, R^T after M4 (fp32; A operand of M7)
 constexpr uint32_t TM_Y = 128;    // V~^T (fp32, M7 result)
 constexpr uint32_t TM_YB = 192;   // bf16 V~^T, two values per column (A operand of M5/M6), 32 columns
 constexpr uint32_t TM_O = 256;    // O^T accumulator
@@ -121,14 +121,18 @@ constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
   B_M1 = 0, B_M7, B_VFULL, B_GFULL, B_QK0, B_QK1, B_TB, B_M4,
-  B_M56, B_L2, B_TD_C, B_TD_S, B_OG, B_COUNT
+  B_M56, B_L2, B_TD_C, B_TD_S, B_OG, B_OPS0, B_OPS1, B_COUNT
 };
+// B_OPS0 + (c & 1): chunk c's operands are in place (arrived once per chunk of
+// that parity, so a barrier runs at most one phase ahead of its waiter: the
+// next arrival on it needs the q/k copy the state group issues after chunk
+// c's products)
 
 struct Ctl {
   uint64_t bar[16];
-  float gam[2][128];     // gamma_C per channel, by chunk parity
-  float bs[64];          // beta of the chunk's rows (0 past the end), chunk group
-  float bsx[64];         // beta of the rows of the chunk whose X the state group writes next
+  float gam[3][128];     // gamma_C per channel, by chunk index mod 3
+  alignas(16) float bsb[2][64];  // beta of a chunk's rows (0 past the end), by chunk parity: chunk group
+  alignas(16) float bsx[2][64];  // the same, state group (for X)
   alignas(16) float nw[128];  // RMSNorm weight (output-gate variant), read as float4
   uint32_t tmem_slot;
   int abort;             // any thread gave up
@@ -139,7 +143,8 @@ struct Ctl {
   int og_iss, og_lnd;        // out_gate copies issued and waited for (state group)
   int slow[2];               // the chunk took the per-tile range path (by chunk parity)
 };
-static_assert(offsetof(Ctl, nw) % 16 == 0 && offsetof(Ctl, gam) % 16 == 0, "vector reads of the control block");
+static_assert(offsetof(Ctl, nw) % 16 == 0 && offsetof(Ctl, gam) % 16 == 0 && offsetof(Ctl, bsb) % 16 == 0,
+              "vector reads of the control block");
 static_assert(sizeof(Ctl) <= 4096, "control block");
 
 struct TcArgs {
@@ -204,6 +209,24 @@ __device__ __forceinline__ void st_row16_bf16(uint8_t *tile, uint32_t row, uint3
 
 __device__ __forceinline__ void sts64(uint8_t *p, uint2 v) { *reinterpret_cast<uint2 *>(p) = v; }
 
+// beta of row `row` of the chunk at t0 into dst[row]: an asynchronous 4-byte
+// copy (a plain load would hold up the next barrier until it returned), or 0
+// past the end of the range.  The copy is waited for with cp_async_wait_all.
+__device__ __forceinline__ void beta_async(float *dst, const float *beta, int t0, int row, int eos, int H, int h) {
+  if (t0 + row < eos) {
+    asm volatile(
+        "{\n\t.reg .u64 g;\n\tcvta.to.global.u64 g, %1;\n\t"
+        "cp.async.ca.shared.global [%0], [g], 4;\n\t}" ::"r"(smem_u32(dst + row)),
+        "l"(beta + (size_t)(t0 + row) * H + h)
+        : "memory");
+  } else {
+    dst[row] = 0.f;
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ float4 unpack4_bf16(uint2 u) {
   const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y);
   return make_float4(a.x, a.y, b.x, b.y);
@@ -249,22 +272,6 @@ __device__ __forceinline__ float4 sub4(const float4 &a, const float4 &b) {
 __device__ __forceinline__ float4 neg4(const float4 &a) { return make_float4(-a.x, -a.y, -a.z, -a.w); }
 __device__ __forceinline__ float4 ex2_4(const float4 &a) { return make_float4(ex2(a.x), ex2(a.y), ex2(a.z), ex2(a.w)); }
 
-
-// acc += l[k0 + i] * t[i] for i < 8 (l: the left factor's row, four per float4)
-__device__ __forceinline__ void fma8(float4 &acc, const float4 *l, int k0, const float4 (&t)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float lv = f4c(l[(k0 + i) >> 2], (k0 + i) & 3);
-    acc.x += lv * t[i].x; acc.y += lv * t[i].y; acc.z += lv * t[i].z; acc.w += lv * t[i].w;
-  }
-}
-
-
-// Named barrier over the first n threads of the chunk group.
-__device__ __forceinline__ void bar_sync_n(int id, int n) {
-  __syncwarp();
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 // fp32 64x64 matrices of the solve (L, T) are stored as two 32-column halves
 // of 64 rows x 128 bytes whose 16-byte chunks are XORed with (row & 7): the
@@ -420,6 +427,16 @@ __device__ __forceinline__ void issue_m1(uint32_t tbase, uint32_t qg, uint32_t k
   }
 }
 
+// M3: X = V^T Diag(beta) (A = the v tile, MN-major: two blocks of 64
+// columns; B = Diag(beta), K-major).
+__device__ __forceinline__ void issue_m3(uint32_t tbase, uint32_t v, uint32_t db) {
+  constexpr uint32_t id = idesc_bf16_f32(128, 64, 1, 0);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_bf16_ss(tbase + TM_X, smem_desc_sw128(v + kk * 2048, 8192, 1024), smem_desc_sw128(db + kk * 32, 16, 1024),
+                id, kk > 0 ? 1u : 0u);
+}
+
 // M4: X += S^T N^T (A = bf16 S^T in TMEM, B = N, K-major).
 __device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t qg, int par) {
   constexpr uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
@@ -568,8 +585,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       issue_qk(&maps, ctl, sm_base, h, bos, 0);
       if (nchunks > 1) issue_qk(&maps, ctl, sm_base, h, bos + kC, 1);
     }
-    float beta_next = 0.f;
-    if (ctid < kC && ctid < eos - bos) beta_next = __ldg(betap + (size_t)(bos + ctid) * H + h);
+    if (ctid < kC && nchunks > 0) beta_async(ctl->bsb[0], betap, bos, ctid, eos, H, h);
     float *tot = reinterpret_cast<float *>(sm + OFF_PRO);  // [8][128] per-row-group decay sums
     const float *gs = reinterpret_cast<const float *>(sm + OFF_GS);
     uint8_t *qg = sm + OFF_QG;
@@ -585,6 +601,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // registers; the row groups' totals meet in shared memory to give every
       // row group its offset and every 16-token tile its reference (the
       // cumulative decay before its first row).
+      cp_async_wait_all();  // this chunk's beta
       if (!(alive = group_wait<true>(ctl, B_GFULL, ph_g, ctid, seq, A.err))) break;
       ph_g ^= 1u;
       if (ctid == 0) ld.landed = ld.issued;
@@ -609,10 +626,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           Gl[r] = run;
         }
         *reinterpret_cast<float4 *>(tot + t8 * 128 + 4 * p4) = run;
-        if (ctid < kC) ctl->bs[ctid] = beta_next;
       }
       bar_chunk();
       if (ctid == 0 && m + 1 < nchunks) ld.g(t0 + kC);  // the log-decay tile has been consumed
+      // beta of the next chunk (its buffer was last read in the previous chunk)
+      if (ctid < kC && m + 1 < nchunks) beta_async(ctl->bsb[par ^ 1], betap, t0 + kC, ctid, eos, H, h);
       float4 ref[4], tc = make_float4(0.f, 0.f, 0.f, 0.f);  // tile references; chunk total G_C
       {
         float4 off = tc;
@@ -629,10 +647,12 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       const float4 gam = make_float4(ex2(tc.x), ex2(tc.y), ex2(tc.z), ex2(tc.w));
       const bool vote = fminf(fminf(tc.x, tc.y), fminf(tc.z, tc.w)) < kSingleRefBound2;
       float nb[8];  // -beta of the thread's rows (N = -beta o Gamma o K)
-#pragma unroll
-      for (int r = 0; r < 8; ++r) nb[r] = -ctl->bs[8 * t8 + r];
-      if (ctid < kC)  // beta of the next chunk's rows, 0 past the end
-        beta_next = ctid < eos - (t0 + kC) ? __ldg(betap + (size_t)(t0 + kC + ctid) * H + h) : 0.f;
+      {
+        const float4 b0 = *reinterpret_cast<const float4 *>(&ctl->bsb[par][8 * t8]);
+        const float4 b1 = *reinterpret_cast<const float4 *>(&ctl->bsb[par][8 * t8 + 4]);
+        nb[0] = -b0.x; nb[1] = -b0.y; nb[2] = -b0.z; nb[3] = -b0.w;
+        nb[4] = -b1.x; nb[5] = -b1.y; nb[6] = -b1.z; nb[7] = -b1.w;
+      }
       // This chunk's q and k have landed (the copy was issued once the state
       // group was done with this parity's buffers, two chunks back).
       if (ctid == 0) {
@@ -645,10 +665,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       alive = ctl->go_c[seq & 1] != 0;
       ++seq;
       if (!alive) break;
-      // gamma_C of this parity is free only now: the q/k copy just waited for
-      // was issued after the state group's last read of it (two chunks back);
-      // the state group reads it after the hand-off below
-      if (t8 == 0) *reinterpret_cast<float4 *>(&ctl->gam[par][4 * p4]) = gam;
+      // gamma_C goes to slot m mod 3: the state group may still be reading
+      // slot (m - 2) mod 3 (the q/k copy just waited for is issued as soon as
+      // chunk m - 2's products are done, before that chunk's state refresh);
+      // it reads this slot after the hand-off below
+      if (t8 == 0) *reinterpret_cast<float4 *>(&ctl->gam[m % 3][4 * p4]) = gam;
       // operand tiles: channel quad p4 sits in K-half p4 / 16 at column 4 p4 mod 64
       const uint32_t half = (uint32_t)(p4 >> 4), col = (uint32_t)(4 * p4) & 63u;
       uint8_t *qb_h = qg + half * KHALF + par * 16384;  // q -> Q o Gamma (in place)
@@ -677,6 +698,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         if (ctid == 0) {
           issue_m1(tbase, smem_u32(qg), sm_base + OFF_KH + par * 16384, par, false);
           mma_commit(smem_u32(&ctl->bar[B_M1]));
+          // the state group may start M4 and O (behind M1 in the tensor pipe)
+          mbar_arrive(smem_u32(&ctl->bar[B_OPS0 + par]));
         }
         // M1 done, and the previous chunk's M7 done with T (L is written over it below)
         alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err, m > 0 ? B_M7 : -1, (m - 1) & 1);
@@ -723,6 +746,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           sts64(nb_h + off, pack4_bf16(make_float4(nb[r] * ge.x, nb[r] * ge.y, nb[r] * ge.z, nb[r] * ge.w)));
           sts64(kh_h + off, pack4_bf16(mul4(kv[r], ex2_4(sub4(tc, Gl[r])))));
         }
+        group_publish<true>();
+        if (ctid == 0) mbar_arrive(smem_u32(&ctl->bar[B_OPS0 + par]));  // the state group may start M4 and O
         // the previous chunk's M7 is done with T (L is written over it below)
         if (m > 0) alive = group_wait<true>(ctl, B_M7, (m - 1) & 1, ctid, seq, A.err);
       }
@@ -736,7 +761,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         float *Lf = reinterpret_cast<float *>(sm + OFF_KB);
         float *TTf = reinterpret_cast<float *>(sm + OFF_TF);      // T_[01][01]^T, [32][32] K-major
         float *XTf = TTf + 1024;                                  // X^T of level 2, [32][32] K-major
-        float *Xf = TTf + 2048;                                   // level-1 products
+        float *Xf = TTf + 2048;                                   // 16- and 32-row level products (3 KB)
         // TMEM lanes 0..63 hold A's rows, 64..127 the rows of -L (N (K / Gamma)^T)
         const bool a_rows = qw < 2;
         const int r = 32 * (qw & 1) + lane;
@@ -758,85 +783,102 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
                 make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
         }
         bar_chunk();
-        // Diagonal 16x16 blocks: one column of T per thread, rows in groups of
-        // four (left-looking).  A group first takes the contributions of the
-        // rows already solved, then is solved within itself; the sum of row r
-        // adds the x[r-1] term last, so consecutive rows are one multiply-add
-        // apart on the dependent chain.
+        // T = (I + L)^{-1} by recursive 2x2 block inversion,
+        //   [[P, 0], [R, Q]]^{-1} = [[P^-1, 0], [-Q^-1 R P^-1, Q^-1]],
+        // from the 8x8 diagonal blocks up: blocks of 8 by substitution, the
+        // 16- and 32-row levels as X = R P^-1 then -Q^-1 X on CUDA cores (fp32,
+        // every chunk-group thread), the 64-row level on the tensor core (tf32,
+        // below).  Every T block is written in place over L as soon as it is
+        // final; the blocks of T_[01][01] also go, transposed, into the B
+        // operand of the first level-64 product.
+        // 8x8 diagonal blocks: one column per thread; a block's eight threads
+        // share a warp, so the warp is done reading the block's L before any
+        // of them writes T over it.  Threads 64..159 meanwhile write the zero
+        // blocks of the transposed copy.
         if (ctid < 64) {
-          const int base = 16 * (ctid >> 4), cc = ctid & 15;
-          float x[16];
+          const int base = 8 * (ctid >> 3), cc = ctid & 7;
+          float4 lr[8][2];
 #pragma unroll
-          for (int R = 0; R < 4; ++R) {
-            float4 lr[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int q = 0; q <= R; ++q)
-                lr[i][q] = *reinterpret_cast<const float4 *>(Lf + lt_idx(base + 4 * R + i, base + 4 * q));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int rr = 4 * R + i;
-              float acc = rr == cc ? 1.f : 0.f;
-#pragma unroll
-              for (int mm = 0; mm < rr; ++mm) acc -= f4c(lr[i][mm >> 2], mm & 3) * x[mm];
-              x[rr] = acc;
-            }
+          for (int r = 1; r < 8; ++r) {
+            lr[r][0] = lds128(Lf + lt_idx(base + r, base));
+            lr[r][1] = lds128(Lf + lt_idx(base + r, base + 4));
           }
-          bar_sync_n(3, 64);  // the block's L is read in full before T overwrites it
+          float x[8];
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) Lf[lt_idx(base + rr, base + cc)] = x[rr];
-          if (base < 32)  // column cc of T_00 / T_11 is row cc of the transposed copy
+          for (int r = 0; r < 8; ++r) {
+            float acc = r == cc ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<float4 *>(TTf + tt_idx(base + cc, base + 4 * j)) =
-                  make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-        } else if (ctid < 128) {
-          // T_01^T of the transposed copy is zero (the per-tile range path may
-          // have used this buffer for its key operand)
-          const int e = ctid - 64;
-          *reinterpret_cast<float4 *>(TTf + tt_idx(16 + (e >> 2), 4 * (e & 3))) = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < r; ++s) acc = fmaf(-f4c(lr[r][s >> 2], s & 3), x[s], acc);
+            x[r] = acc;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int r = 0; r < 8; ++r) Lf[lt_idx(base + r, base + cc)] = x[r];
+          if (base < 32) {  // column cc of the block is row base + cc of the transposed copy
+            *reinterpret_cast<float4 *>(TTf + tt_idx(base + cc, base)) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4 *>(TTf + tt_idx(base + cc, base + 4)) = make_float4(x[4], x[5], x[6], x[7]);
+          }
+        } else if (ctid < 160) {
+          // zeros of T_[01][01]^T: (n 8..15, k 0..7), (n 24..31, k 16..23), (n 16..31, k 0..15)
+          const int e = ctid - 64;  // 96 float4
+          int n, k;
+          if (e < 16) { n = 8 + (e >> 1); k = 4 * (e & 1); }
+          else if (e < 32) { n = 24 + ((e - 16) >> 1); k = 16 + 4 * (e & 1); }
+          else { n = 16 + ((e - 32) >> 2); k = 4 * (e & 3); }
+          *reinterpret_cast<float4 *>(TTf + tt_idx(n, k)) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         bar_chunk();
-        // Off-diagonal blocks in two levels of the 2x2 block inverse
-        // [[P, 0], [R, Q]]^{-1} = [[P^-1, 0], [-Q^-1 R P^-1, Q^-1]]:
-        //   level 1 (16-row blocks): T_10 and T_32;
-        //   level 2 (32-row blocks): T_[23][01].
-        // Each output is X = R P^-1, then -Q^-1 X.  Level 1 runs on CUDA cores
-        // (fp32); level 2 on the tensor core (tf32, below).
-        if (ctid < 128) {
-          // level 1: two 16x16 outputs, 128 tasks of (row, 4 columns)
-          const int blk = ctid >> 6, rr = (ctid >> 2) & 15, q4 = ctid & 3;
-          const int rb = 16 * (2 * blk + 1), cb = 16 * (2 * blk);  // output block (rb, cb)
-          float *X1 = Xf + blk * 256;                              // [16][16]
-          float4 l[4], t[8];
+        // 16-row level: four blocks, one (row i, column jj) of the output per thread
+        {
+          const int b = ctid >> 6, i = (ctid >> 3) & 7, jj = ctid & 7, o = 16 * b;
+          float *Xb = Xf + 64 * b;  // [8][8]
+          const float4 r0 = lds128(Lf + lt_idx(o + 8 + i, o)), r1 = lds128(Lf + lt_idx(o + 8 + i, o + 4));
+          float acc = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc = fmaf(f4c(k < 4 ? r0 : r1, k & 3), Lf[lt_idx(o + k, o + jj)], acc);
+          Xb[8 * i + jj] = acc;
+          bar_chunk();
+          const float4 q0 = lds128(Lf + lt_idx(o + 8 + i, o + 8)), q1 = lds128(Lf + lt_idx(o + 8 + i, o + 12));
+          float t = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) t = fmaf(f4c(k < 4 ? q0 : q1, k & 3), Xb[8 * k + jj], t);
+          Lf[lt_idx(o + 8 + i, o + jj)] = -t;
+          if (o < 32) TTf[tt_idx(o + jj, o + 8 + i)] = -t;
+        }
+        bar_chunk();
+        // 32-row level: T_10 and T_32 of the 16-row blocks, two adjacent
+        // columns of one row per thread
+        {
+          const int blk = ctid >> 7, rr = (ctid >> 3) & 15, c2 = 2 * (ctid & 7);
+          const int rb = 16 * (2 * blk + 1), cb = 32 * blk;  // output block (rb, cb)
+          float *X1 = Xf + 256 + 256 * blk;                   // [16][16]
+          float4 l[4];
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) l[c4] = lds128(Lf + lt_idx(rb + rr, cb + 4 * c4));  // row of L_(rb, cb)
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int k0 = 0; k0 < 16; k0 += 8) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) t[i] = lds128(Lf + lt_idx(cb + k0 + i, cb + 4 * q4));
-            fma8(acc, l, k0, t);
+          for (int k = 0; k < 16; ++k) {
+            const float2 tv = *reinterpret_cast<const float2 *>(Lf + lt_idx(cb + k, cb + c2));
+            const float lk = f4c(l[k >> 2], k & 3);
+            acc.x = fmaf(lk, tv.x, acc.x);
+            acc.y = fmaf(lk, tv.y, acc.y);
           }
-          *reinterpret_cast<float4 *>(X1 + rr * 16 + 4 * q4) = acc;
-          bar_sync_n(3, 128);
+          *reinterpret_cast<float2 *>(X1 + 16 * rr + c2) = acc;
+          bar_chunk();
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) l[c4] = lds128(Lf + lt_idx(rb + rr, rb + 4 * c4));  // row of T_(rb, rb)
-          acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          acc = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int k0 = 0; k0 < 16; k0 += 8) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) t[i] = lds128(X1 + (k0 + i) * 16 + 4 * q4);
-            fma8(acc, l, k0, t);
+          for (int k = 0; k < 16; ++k) {
+            const float2 xv = *reinterpret_cast<const float2 *>(X1 + 16 * k + c2);
+            const float lk = f4c(l[k >> 2], k & 3);
+            acc.x = fmaf(lk, xv.x, acc.x);
+            acc.y = fmaf(lk, xv.y, acc.y);
           }
-          acc = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-          *reinterpret_cast<float4 *>(Lf + lt_idx(rb + rr, cb + 4 * q4)) = acc;
+          *reinterpret_cast<float2 *>(Lf + lt_idx(rb + rr, cb + c2)) = make_float2(-acc.x, -acc.y);
           if (blk == 0) {  // T_10 into the transposed copy
-            TTf[tt_idx(4 * q4, 16 + rr)] = acc.x;
-            TTf[tt_idx(4 * q4 + 1, 16 + rr)] = acc.y;
-            TTf[tt_idx(4 * q4 + 2, 16 + rr)] = acc.z;
-            TTf[tt_idx(4 * q4 + 3, 16 + rr)] = acc.w;
+            TTf[tt_idx(c2, 16 + rr)] = -acc.x;
+            TTf[tt_idx(c2 + 1, 16 + rr)] = -acc.y;
           }
         }
         // level 2 on the tensor core (tf32):
@@ -888,6 +930,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // the chunk's operands, A, T and gamma_C to it)
       if (ctid == 0) mbar_arrive(smem_u32(&ctl->bar[B_TB]));
     }
+    cp_async_wait_all();
     if (ctid == 0) {
       ld.drain(A.err);
       volatile int no_abort = 0;
@@ -920,66 +963,53 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0 + 16), *reinterpret_cast<float(*)[16]>(s + 16));
       tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_STB + i0 / 2), s);
     }
-    if (stid < kC) ctl->bsx[stid] = stid < eos - bos ? __ldg(betap + (size_t)(bos + stid) * H + h) : 0.f;
-    // X of chunk c := (beta o V)^T in fp32: thread j writes column j of V
-    // times beta (v of rows past the end has beta = 0).  Every state thread
-    // has passed a barrier since bsx was written.
-    auto fill_x = [&](int c) -> bool {
-      if (!zero_v) {
-        if (!group_wait<false>(ctl, B_VFULL, c & 1, stid, seq, A.err)) return false;
-        if (stid == 0) ++ctl->v_lnd;
-      } else {
-        bar_state();
-      }
-      const uint8_t *vb = sm + OFF_V + (j >> 6) * 8192;
-      const uint32_t jc = (uint32_t)j & 63u;
-#pragma unroll 1
-      for (int s0 = 0; s0 < kC; s0 += 32) {
-        float x[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float vv = zero_v ? 0.f
-                                  : __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                        vb + sw128_offset((uint32_t)(s0 + i), jc)));
-          x[i] = ctl->bsx[s0 + i] * vv;
-        }
-        tmem_st16(tmem_addr(tbase, 32 * qw, TM_X + s0), *reinterpret_cast<float(*)[16]>(x));
-        tmem_st16(tmem_addr(tbase, 32 * qw, TM_X + s0 + 16), *reinterpret_cast<float(*)[16]>(x + 16));
-      }
-      return true;
-    };
+    // Diag(beta): zero off the diagonal for good (and the v tile of a
+    // transition item, whose v is zero); the diagonal of chunk 0
+    for (int e = stid; e < 8192 / 16; e += kStateThreads)
+      reinterpret_cast<uint4 *>(sm + OFF_DB)[e] = make_uint4(0u, 0u, 0u, 0u);
+    if (zero_v)
+      for (int e = stid; e < 16384 / 16; e += kStateThreads)
+        reinterpret_cast<uint4 *>(sm + OFF_V)[e] = make_uint4(0u, 0u, 0u, 0u);
+    bar_state();  // the zeros are written before the diagonal goes over them
+    if (stid < kC)
+      *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_DB + sw128_offset(stid, stid)) =
+          __float2bfloat16_rn(stid < eos - bos ? __ldg(betap + (size_t)(bos + stid) * H + h) : 0.f);
+    tmem_wait_st();
+    group_publish<false>();
     bool alive = true;
-    if (nchunks > 0) {
-      bar_state();  // bsx
-      alive = fill_x(0);
-      tmem_wait_st();
-      tc_fence_before();
-      bar_state();  // every thread has read the v tile of chunk 0
-      if (stid == 0 && !zero_v && nchunks > 1) issue_v(&maps, ctl, sm_base, h, bos + kC);
-    } else {
-      tmem_wait_st();
-      tc_fence_before();
-    }
     for (int c = 0; c < nchunks && alive; ++c) {
       const int par = c & 1;
       const int t0 = bos + c * kC;
       const int len = min(kC, eos - t0);
-      // beta of the next chunk's rows (for its X), fetched early
-      float bnext = 0.f;
-      if (stid < kC && c + 1 < nchunks && t0 + kC + stid < eos) bnext = __ldg(betap + (size_t)(t0 + kC + stid) * H + h);
-      // ---------------- M4 and O once the chunk group has handed the chunk over
+      // beta of the next chunk's rows (for its Diag(beta))
+      if (stid < kC && c + 1 < nchunks) beta_async(ctl->bsx[par ^ 1], betap, t0 + kC, stid, eos, H, h);
+      // ---------------- M3, M4 and O as soon as the chunk's operands are in
+      // place (the chunk group may still be solving for T) and v has landed;
+      // the bf16 state and Diag(beta) were written before the barrier that
+      // ended the previous iteration
+      if (stid == 0) {
+        bool ok = solo_wait(ctl, B_OPS0 + par, (c >> 1) & 1, A.err);
+        if (ok && !zero_v) {
+          ok = solo_wait(ctl, B_VFULL, c & 1, A.err);
+          if (ok) ++ctl->v_lnd;
+        }
+        if (ok) {
+          issue_m3(tbase, sm_base + OFF_V, sm_base + OFF_DB);
+          issue_m4(tbase, sm_base + OFF_QG, par);
+          mma_commit(smem_u32(&ctl->bar[B_M4]));
+          issue_o(tbase, sm_base + OFF_QG, par);
+        }
+      }
+      // ---------------- M7 once the chunk group has handed T over and M4 has
+      // completed R (M7 reads it from TMEM)
       if (!(alive = group_wait<false>(ctl, B_TB, c & 1, stid, seq, A.err))) break;
       // (every thread is past the previous chunk's reads of the out_gate tile)
       if (kOG && stid == 0) issue_og(&maps, ctl, sm_base, h, t0);
-      if (stid == 0) {
-        issue_m4(tbase, sm_base + OFF_QG, par);
-        mma_commit(smem_u32(&ctl->bar[B_M4]));
-        issue_o(tbase, sm_base + OFF_QG, par);
-        // M7 once M4 has completed R (M7 reads it from TMEM)
-        if (solo_wait(ctl, B_M4, ph_m4, A.err)) {
-          issue_m7(tbase, sm_base + OFF_KB);
-          mma_commit(smem_u32(&ctl->bar[B_M7]));
-        }
+      if (stid == 0 && solo_wait(ctl, B_M4, ph_m4, A.err)) {
+        issue_m7(tbase, sm_base + OFF_KB);
+        mma_commit(smem_u32(&ctl->bar[B_M7]));
+        // M3 has read the v tile: the next chunk's may land
+        if (!zero_v && c + 1 < nchunks) issue_v(&maps, ctl, sm_base, h, t0 + kC);
       }
       ph_m4 ^= 1u;
       if (!(alive = group_wait<false>(ctl, B_M7, c & 1, stid, seq, A.err))) break;
@@ -997,7 +1027,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_YB + 16), y);
       }
       if (slow) {
-        const float *gam = ctl->gam[par];
+        const float *gam = ctl->gam[c % 3];
 #pragma unroll 1
         for (int i0 = 0; i0 < kD; i0 += 32) {
           float s[32];
@@ -1009,28 +1039,31 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0 + 16), *reinterpret_cast<float(*)[16]>(s + 16));
         }
       }
-      if (stid < kC) ctl->bsx[stid] = bnext;
+      // Diag(beta) of the next chunk (M3 of this chunk is done: M7 has completed)
+      if (stid < kC && c + 1 < nchunks) {
+        cp_async_wait_all();
+        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_DB + sw128_offset(stid, stid)) =
+            __float2bfloat16_rn(ctl->bsx[par ^ 1][stid]);
+      }
       tmem_wait_st();
       group_publish<false>();
       if (stid == 0) {
         issue_m56(tbase, sm_base + OFF_AM + par * 8192, sm_base + OFF_KH + par * 16384);
         mma_commit(smem_u32(&ctl->bar[B_M56]));
       }
-      // ---------------- X of the next chunk while M5/M6 run (M7 has read X)
-      if (c + 1 < nchunks && !(alive = fill_x(c + 1))) break;
-      tmem_wait_st();
-      tc_fence_before();
       if (!(alive = group_wait<false>(ctl, B_M56, ph_m56, stid, seq, A.err))) break;
       ph_m56 ^= 1u;
-      // every thread has read the v tile of chunk c + 1: chunk c + 2's may land
-      if (stid == 0 && !zero_v && c + 2 < nchunks) issue_v(&maps, ctl, sm_base, h, t0 + 2 * kC);
+      // This parity's operand buffers are free (every product of chunk c has
+      // completed): q and k of the chunk two ahead land in them; its N and A
+      // tiles are written only after that copy has been waited for.
+      if (stid == 0 && c + 2 < nchunks) issue_qk(&maps, ctl, sm_base, h, t0 + 2 * kC, par);
 
       // ---------------- S^T <- S^T Diag(gamma_C) (unless done before M6), the
       // bf16 copy of the new state (and a checkpoint of the fp32 state when
       // one ends this chunk); the output rows
       float *cp = ckpt_ptr(a, n, h, t0 + len - seq_bos);
       {
-        const float *gam = ctl->gam[par];
+        const float *gam = ctl->gam[c % 3];
 #pragma unroll 1
         for (int i0 = 0; i0 < kD; i0 += 32) {
           float s[32];
@@ -1065,11 +1098,6 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       } else {
         bar_state();
       }
-      // This parity's operand buffers are free (M4-M7 have completed and every
-      // state thread has read gamma_C): q and k of the chunk two ahead land in
-      // them; its N and A tiles and gamma_C are written only after that copy
-      // has been waited for.
-      if (stid == 0 && c + 2 < nchunks) issue_qk(&maps, ctl, sm_base, h, t0 + 2 * kC, par);
       if (a.o) {  // segment passes of the long-sequence plan write no output
         const uint4 *src = reinterpret_cast<const uint4 *>(vt);
         uint4 *o = reinterpret_cast<uint4 *>(a.o);
@@ -1123,6 +1151,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         for (int cc = 0; cc < 32; ++cc) s_out[(size_t)(i0 + cc) * kD + j] = s[cc];
       }
     }
+    cp_async_wait_all();
     if (stid == 0) {
       volatile int no_abort = 0;
       mma_commit(smem_u32(&ctl->bar[B_TD_S]));
