@@ -13,9 +13,9 @@
 //   M1  [A ; -L] = [Q o Gamma ; N] (K / Gamma)^T                 (M=128 N=64 K=128)
 //   A  = Tril_incl(A), L strictly lower
 //   T  = (I + L)^{-1}   blocked substitution: CUDA cores (fp32), last level tf32 MMA
-//   M3  X  = V^T Diag(beta)              (M=128 N=64 K=64; beta rounded to bf16)
-//   M4  X += S^T N^T,  so X = R^T with R = beta o (V - (Gamma o K) S)   (M=128 N=64 K=128)
-//       O^T = S^T (Q o Gamma)^T                                   (M=128 N=64 K=128)
+//   M4  [O^T | X] = S^T [Q o Gamma ; N]^T                        (M=128 N=128 K=128)
+//   M3  X += V^T Diag(beta), so X = R^T with R = beta o (V - (Gamma o K) S)
+//                                        (M=128 N=64 K=64; beta rounded to bf16)
 //   M7  V~^T = R^T T^T   tf32: A = R^T read from TMEM, B = T fp32   (M=128 N=64 K=64)
 //   M5  O^T += V~^T A^T                                           (M=128 N=64 K=64)
 //   M6  S^T <- (S^T + V~^T (K / Gamma)) Diag(gamma_C)              (M=128 N=128 K=64)
@@ -112,11 +112,11 @@ static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 // TMEM columns (512 allocated).
 constexpr uint32_t TM_D1 = 0;     // M1 result, level-2 products (chunk group)
-constexpr uint32_t TM_X = 64;     // (beta o V)^T after M3, R^T after M4 (fp32; A operand of M7)
-constexpr uint32_t TM_Y = 128;    // V~^T (fp32, M7 result)
-constexpr uint32_t TM_YB = 192;   // bf16 V~^T, two values per column (A operand of M5/M6), 32 columns
-constexpr uint32_t TM_O = 256;    // O^T accumulator
-constexpr uint32_t TM_STB = 320;  // bf16 S^T, two values per column (A operand of M4 and O)
+constexpr uint32_t TM_Y = 64;     // V~^T (fp32, M7 result)
+constexpr uint32_t TM_YB = 128;   // bf16 V~^T, two values per column (A operand of M5/M6), 32 columns
+constexpr uint32_t TM_O = 192;    // O^T accumulator; with TM_X the 128 columns of one M4 product
+constexpr uint32_t TM_X = 256;    // S^T N^T after M4, then R^T after M3 (fp32; A operand of M7)
+constexpr uint32_t TM_STB = 320;  // bf16 S^T, two values per column (A operand of M4)
 constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
@@ -427,34 +427,26 @@ __device__ __forceinline__ void issue_m1(uint32_t tbase, uint32_t qg, uint32_t k
   }
 }
 
-// M3: X = V^T Diag(beta) (A = the v tile, MN-major: two blocks of 64
+// M4: [O^T | X] = S^T [Q o Gamma ; N]^T, one N = 128 product (A = bf16
+// S^T in TMEM; B = the 128 rows [Q o Gamma ; N] of the chunk's parity, K-major,
+// contiguous within each K-half like M1's A operand).
+__device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t qg, int par) {
+  constexpr uint32_t id = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t kb = (kk >> 2) * KHALF + par * 16384 + (kk & 3) * 32;
+    mma_bf16_ts(tbase + TM_O, tbase + TM_STB + kk * 8, smem_desc_sw128(qg + kb, 16, 1024), id, kk > 0 ? 1u : 0u);
+  }
+}
+
+// M3: X += V^T Diag(beta) (A = the v tile, MN-major: two blocks of 64
 // columns; B = Diag(beta), K-major).
 __device__ __forceinline__ void issue_m3(uint32_t tbase, uint32_t v, uint32_t db) {
   constexpr uint32_t id = idesc_bf16_f32(128, 64, 1, 0);
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)
     mma_bf16_ss(tbase + TM_X, smem_desc_sw128(v + kk * 2048, 8192, 1024), smem_desc_sw128(db + kk * 32, 16, 1024),
-                id, kk > 0 ? 1u : 0u);
-}
-
-// M4: X += S^T N^T (A = bf16 S^T in TMEM, B = N, K-major).
-__device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t qg, int par) {
-  constexpr uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t kb = (kk >> 2) * KHALF + par * 16384 + 8192 + (kk & 3) * 32;
-    mma_bf16_ts(tbase + TM_X, tbase + TM_STB + kk * 8, smem_desc_sw128(qg + kb, 16, 1024), id, 1u);
-  }
-}
-
-// O^T = S^T (Q o Gamma)^T (A = bf16 S^T in TMEM, B = Q o Gamma, K-major).
-__device__ __forceinline__ void issue_o(uint32_t tbase, uint32_t qg, int par) {
-  constexpr uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t kb = (kk >> 2) * KHALF + par * 16384 + (kk & 3) * 32;
-    mma_bf16_ts(tbase + TM_O, tbase + TM_STB + kk * 8, smem_desc_sw128(qg + kb, 16, 1024), id, kk > 0 ? 1u : 0u);
-  }
+                id, 1u);
 }
 
 // M7: V~^T = R^T T^T in tf32 (A = R^T fp32 in TMEM, one K element per
@@ -983,7 +975,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       const int len = min(kC, eos - t0);
       // beta of the next chunk's rows (for its Diag(beta))
       if (stid < kC && c + 1 < nchunks) beta_async(ctl->bsx[par ^ 1], betap, t0 + kC, stid, eos, H, h);
-      // ---------------- M3, M4 and O as soon as the chunk's operands are in
+      // ---------------- M4 (with O) and M3 as soon as the chunk's operands are in
       // place (the chunk group may still be solving for T) and v has landed;
       // the bf16 state and Diag(beta) were written before the barrier that
       // ended the previous iteration
@@ -994,10 +986,9 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           if (ok) ++ctl->v_lnd;
         }
         if (ok) {
-          issue_m3(tbase, sm_base + OFF_V, sm_base + OFF_DB);
           issue_m4(tbase, sm_base + OFF_QG, par);
+          issue_m3(tbase, sm_base + OFF_V, sm_base + OFF_DB);
           mma_commit(smem_u32(&ctl->bar[B_M4]));
-          issue_o(tbase, sm_base + OFF_QG, par);
         }
       }
       // ---------------- M7 once the chunk group has handed T over and M4 has
