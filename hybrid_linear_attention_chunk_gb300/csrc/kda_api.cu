@@ -216,7 +216,7 @@ kda_status run_prefill(const kda_chunk_desc *d, const PrefillArgs &a, cudaStream
   if (d->kernel == KDA_KERNEL_TC && !tc) return KDA_ERR_UNSUPPORTED;
   const bool use_tc = d->kernel != KDA_KERNEL_SIMT && tc;
   if (d->segments > 1 && (!use_tc || a.cu)) return KDA_ERR_UNSUPPORTED;
-  const SegPlan pl = use_tc ? plan_segments(a, d->segments) : SegPlan{1, 0, 0};
+  const SegPlan pl = use_tc ? plan_segments(a, d->segments) : SegPlan{1, 0, 0, 0};
   if (pl.P > 1 && ws_mode == 1) {
     if (!ws) return KDA_ERR_NULL;
     if (ws_bytes < pl.ws_bytes) return KDA_ERR_SHAPE;

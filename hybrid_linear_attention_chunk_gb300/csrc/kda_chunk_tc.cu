@@ -501,34 +501,77 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   const PrefillArgs &a = A.a;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H;
-  // work item: (sequence n, segment, head h, kind) -- see PrefillArgs
-  int item = blockIdx.x;
-  const int kind = item % a.kinds;
-  item /= a.kinds;
-  const int h = item % H;
-  item /= H;
-  const int seg = item % a.nseg;
-  int n = item / a.nseg;
-  // Packed sequences run longest first: work items are handed to SMs in
-  // index order, so a long sequence that came late would finish last.
-  if (a.cu && a.N > 1 && a.N <= kLongestFirstMax)
-    n = longest_first(a.cu, a.N, n, reinterpret_cast<int *>(sm + OFF_TF), tid);
-  int bos, eos;
-  seq_range(a, n, bos, eos);
-  const int seq_bos = bos;  // checkpoints count tokens from the sequence start
-  if (a.seg_tokens > 0) {
-    const int sb = min(eos, bos + seg * a.seg_tokens);
-    eos = min(eos, sb + a.seg_tokens);
+  // work item -- see PrefillArgs
+  constexpr size_t DD = (size_t)kD * kD;
+  int n, h, kind = 0, bos, eos, seq_bos;
+  const float *s_in = nullptr;  // entry state (null: zero, or the identity for kind 1)
+  float *s_out = nullptr;       // where the final state goes (nullable)
+  bool out_item;                // writes outputs (and checkpoints)
+  if (a.plan == 0) {
+    int item = blockIdx.x;
+    kind = item % a.kinds;
+    item /= a.kinds;
+    h = item % H;
+    item /= H;
+    const int seg = item % a.nseg;
+    n = item / a.nseg;
+    // Packed sequences run longest first: work items are handed to SMs in
+    // index order, so a long sequence that came late would finish last.
+    if (a.cu && a.N > 1 && a.N <= kLongestFirstMax)
+      n = longest_first(a.cu, a.N, n, reinterpret_cast<int *>(sm + OFF_TF), tid);
+    seq_range(a, n, bos, eos);
+    seq_bos = bos;  // checkpoints count tokens from the sequence start
+    if (a.seg_tokens > 0) {
+      const int sb = min(eos, bos + seg * a.seg_tokens);
+      eos = min(eos, sb + a.seg_tokens);
+      bos = sb;
+    }
+    if (kind == 0 && a.s0) s_in = a.s0 + (((size_t)n * a.nseg + seg) * H + h) * DD;
+    if (a.sT) {
+      if (a.kinds == 2) s_out = a.sT + ((((size_t)kind * a.N + n) * a.nseg + seg) * H + h) * DD;
+      else if (seg == a.nseg - 1) s_out = a.sT + ((size_t)n * H + h) * DD;
+    }
+    out_item = a.o != nullptr;
+  } else {
+    // the long-sequence plan: segment 0 items first (the longest), then the rest
+    const int NH = a.N * H;
+    int item = blockIdx.x, seg = 0;
+    if (a.plan == 1 && item < NH) {
+      n = item / H;
+      h = item % H;
+    } else {
+      if (a.plan == 1) {
+        item -= NH;
+        kind = item % 2;
+        item /= 2;
+      }
+      h = item % H;
+      item /= H;
+      const int nsegs = a.plan == 1 ? a.P - 2 : a.P - 1;
+      seg = 1 + item % nsegs;
+      n = item / nsegs;
+    }
+    seq_range(a, n, bos, eos);
+    seq_bos = bos;
+    const int sb = seg == 0 ? bos : min(eos, bos + a.seg0 + (seg - 1) * a.seg_tokens);
+    eos = min(eos, seg == 0 ? bos + a.seg0 : sb + a.seg_tokens);
     bos = sb;
+    const size_t nh = (size_t)n * H + h;
+    if (a.plan == 1 && seg == 0) {
+      s_in = a.s0 ? a.s0 + nh * DD : nullptr;
+      s_out = a.E + ((size_t)n * (a.P - 1) * H + h) * DD;
+      out_item = true;
+    } else if (a.plan == 1) {
+      s_out = a.pairs + ((((size_t)kind * a.N + n) * (a.P - 2) + (seg - 1)) * H + h) * DD;
+      out_item = false;
+    } else {
+      s_in = a.E + (((size_t)n * (a.P - 1) + (seg - 1)) * H + h) * DD;
+      if (seg == a.P - 1 && a.sT) s_out = a.sT + nh * DD;
+      out_item = true;
+    }
   }
   const int nchunks = (eos - bos + kC - 1) / kC;
   const bool zero_v = kind == 1;  // transition pass: v = 0, identity entry state
-  const float *s_in = (kind == 0 && a.s0) ? a.s0 + (((size_t)n * a.nseg + seg) * H + h) * kD * kD : nullptr;
-  float *s_out = nullptr;
-  if (a.sT) {
-    if (a.kinds == 2) s_out = a.sT + ((((size_t)kind * a.N + n) * a.nseg + seg) * H + h) * kD * kD;
-    else if (seg == a.nseg - 1) s_out = a.sT + ((size_t)n * H + h) * kD * kD;
-  }
 
   if (warp == 0) {
     tmem_alloc(smem_u32(&ctl->tmem_slot), 512);
@@ -995,7 +1038,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // completed R (M7 reads it from TMEM)
       if (!(alive = group_wait<false>(ctl, B_TB, c & 1, stid, seq, A.err))) break;
       // (every thread is past the previous chunk's reads of the out_gate tile)
-      if (kOG && stid == 0) issue_og(&maps, ctl, sm_base, h, t0);
+      if (kOG && out_item && stid == 0) issue_og(&maps, ctl, sm_base, h, t0);
       if (stid == 0 && solo_wait(ctl, B_M4, ph_m4, A.err)) {
         issue_m7(tbase, sm_base + OFF_KB);
         mma_commit(smem_u32(&ctl->bar[B_M7]));
@@ -1052,7 +1095,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // ---------------- S^T <- S^T Diag(gamma_C) (unless done before M6), the
       // bf16 copy of the new state (and a checkpoint of the fp32 state when
       // one ends this chunk); the output rows
-      float *cp = ckpt_ptr(a, n, h, t0 + len - seq_bos);
+      float *cp = out_item ? ckpt_ptr(a, n, h, t0 + len - seq_bos) : nullptr;
       {
         const float *gam = ctl->gam[c % 3];
 #pragma unroll 1
@@ -1083,13 +1126,13 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       }
       tmem_wait_st();
       tc_fence_before();
-      if constexpr (kOG) {  // the barrier also waits for this chunk's out_gate tile
+      if (kOG && out_item) {  // the barrier also waits for this chunk's out_gate tile
         if (!(alive = group_wait<false>(ctl, B_OG, c & 1, stid, seq, A.err))) break;
         if (stid == 0) ++ctl->og_lnd;
       } else {
         bar_state();
       }
-      if (a.o) {  // segment passes of the long-sequence plan write no output
+      if (out_item) {  // (the pair items of the long-sequence plan write no output)
         const uint4 *src = reinterpret_cast<const uint4 *>(vt);
         uint4 *o = reinterpret_cast<uint4 *>(a.o);
         float w8[8];
@@ -1233,7 +1276,8 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
   cudaError_t e = cudaGetSymbolAddress(&wd, g_tc_watchdog);
   if (e != cudaSuccess) return e;
   TcArgs args{a, reinterpret_cast<unsigned int *>(wd)};
-  const int grid = a.N * a.nseg * a.H * a.kinds;
+  const int NH = a.N * a.H;
+  const int grid = a.plan == 1 ? NH + 2 * NH * (a.P - 2) : a.plan == 2 ? NH * (a.P - 1) : NH * a.nseg * a.kinds;
   if (z) return og ? launch_variant<true, true>(maps, args, grid, s) : launch_variant<true, false>(maps, args, grid, s);
   // the output gate comes with the layer form, whose decay is given as logits
   // (the out_gate tile shares the decay tile's buffer, half of which bf16 logits use)

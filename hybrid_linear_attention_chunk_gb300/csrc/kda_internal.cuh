@@ -43,6 +43,20 @@ struct PrefillArgs {
   int seg_tokens = 0;        // 0: the whole sequence is one segment
   int nseg = 1;
   int kinds = 1;
+  // Passes of the long-sequence plan (tensor-core kernel, B x T batches
+  // only); plan 0 is the layout above.  Sequence n is cut into P segments:
+  // segment 0 of seg0 tokens, then segments of seg_tokens.
+  //   plan 1 (pass 1): one work item per (n, h) runs segment 0 from s0 with
+  //     outputs and writes its final state to E[n][0][h]; then every segment
+  //     1 .. P-2 runs as kind 0 (zero state, v) and kind 1 (identity, v = 0)
+  //     into pairs[kind][n][segment - 1][h], without outputs.
+  //   plan 2 (pass 3): segment p = 1 .. P-1 runs from E[n][p - 1][h] with
+  //     outputs; the last one writes sT[n][h].
+  int plan = 0;
+  int P = 1;
+  int seg0 = 0;
+  float *pairs = nullptr;    // [2][N][P-2][H][dk][dv]
+  float *E = nullptr;        // [N][P-1][H][dk][dv]: entry states of segments 1 .. P-1
   // State checkpoints (nullable ck): the state after every ck_every tokens of
   // a sequence (a multiple of the chunk) goes to slot first + j - 1 of ck
   // [slots][H][dk][dv], first = ck_cu[n] when ck_cu is given, else
@@ -116,8 +130,9 @@ cudaError_t launch_chunk_bwd(const PrefillArgs &p, const BwdIo &io, void *ws, cu
 // Segment plan for long sequences (kda_cp.cu).
 struct SegPlan {
   int P;              // segments per sequence (1: no split)
-  int seg_tokens;     // tokens per segment (a multiple of the chunk)
-  size_t ws_bytes;    // device workspace: (3P - 2) x N x H fp32 dk x dv states
+  int seg_tokens;     // tokens of segments 1 .. P-1 (a multiple of the chunk; the last may be shorter)
+  size_t ws_bytes;    // device workspace: (3P - 5) x N x H fp32 dk x dv states
+  int seg0;           // tokens of segment 0 (a multiple of the chunk)
 };
 SegPlan plan_segments(const PrefillArgs &a, int requested);
 cudaError_t launch_chunk_tc_segmented(const PrefillArgs &a, const SegPlan &pl, void *ws, cudaStream_t s);

@@ -123,7 +123,7 @@ def test_segment_planner_sizes(lib):
     assert n.value == 0
     forced = _desc(B=1, T=4096, H=2, dk=128, dv=128, segments=4)
     assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(forced), ctypes.byref(n)) == 0
-    assert n.value == (3 * 4 - 2) * 2 * 128 * 128 * 4
+    assert n.value == (3 * 4 - 5) * 2 * 128 * 128 * 4  # P-2 pairs and P-1 entry states per chain
     varlen_split = _desc(B=1, T=4096, H=2, dk=128, dv=128, num_seqs=2, segments=4)
     assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(varlen_split), ctypes.byref(n)) == -7
 

@@ -50,7 +50,7 @@ def test_caller_workspace_equals_stream_ordered(kda):
     w, x = long_inputs(1, 3000, 2)
     d = kda.chunk_desc(x["q"], x["v"], gate_dtype=0, segments=4, B=1)
     nbytes = kda.kda_chunk_fwd_workspace_size(d)
-    assert nbytes == (3 * 4 - 2) * 1 * 2 * 128 * 128 * 4
+    assert nbytes == (3 * 4 - 5) * 1 * 2 * 128 * 128 * 4  # P-2 pairs and P-1 entry states per chain
     ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
     o1, s1 = run(kda, x, 1, segments=4)
     o2, s2 = run(kda, x, 1, segments=4, workspace=ws)

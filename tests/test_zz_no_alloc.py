@@ -97,7 +97,7 @@ def test_noalloc_unsplit_call_matches(kda):
 
 def test_noalloc_rejects_plans_beyond_the_static_scratch(kda):
     """Two sequences of 2^20 tokens and 16 heads cut into 16 segments each
-    need 96 MiB of scratch, more than the 32 MiB array: the call is refused
+    need 86 MiB of scratch, more than the 32 MiB array: the call is refused
     before any launch."""
     lib = kda.load()
     d = kda.KdaChunkDesc()
