@@ -543,12 +543,23 @@ def time_backward(kda, x, w, steps, ms_headline, dev, stream, world):
         step()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = reduce_max(ev0.elapsed_time(ev1) / steps, world, dev)
+    ms_local = ev0.elapsed_time(ev1) / steps
+    ms = reduce_max(ms_local, world, dev)
     tok = w.B * w.T
+    # algorithmic bytes: the forward's inputs and dO read once, the five fp32
+    # gradients written once (no initial state, no final-state gradient here)
+    th = tok * w.H
+    qkv_b = x["q"].element_size()
+    alg = th * ((2 * w.dk + w.dv) * qkv_b + w.dk * 4 + 4 + w.dv * dO.element_size()) \
+        + th * ((2 * w.dk + w.dv + w.dk) * 4 + 4)
+    gbs = alg / (ms_local * 1e-3) / 1e9
     res = {"workload": w.name, "api": "kda_chunk_bwd (fp32, 16-token chunks; gradient products on mma.sync split-tf32)", "steps": steps,
            "ms_per_step": round(ms, 3), "tokens_per_s": round(world * tok / (ms * 1e-3), 1),
            "time_vs_forward": round(ms / ms_headline, 3), "workspace_bytes": int(ws_bytes),
-           "launches_per_step": 4}
+           "launches_per_step": 4,
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": load_peaks()[0], "unit": "GB/s",
+                        "frac": round(gbs / load_peaks()[0], 4), "algorithmic_bytes_per_step": int(alg),
+                        "note": "the per-chunk states the backward keeps (workspace) are not algorithmic bytes"}}
     del dO, ws, grads
     torch.cuda.empty_cache()
     return res
