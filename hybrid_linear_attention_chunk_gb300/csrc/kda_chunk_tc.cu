@@ -12,11 +12,15 @@
 // ([K3-notes §2.2, chunkwise form]):
 //   M1  [A ; -L] = [Q o Gamma ; N] (K / Gamma)^T                 (M=128 N=64 K=128)
 //   A  = Tril_incl(A), L strictly lower
-//   T  = (I + L)^{-1}   blocked substitution: CUDA cores (fp32), last level tf32 MMA
+//   T  = (I + L)^{-1} up to its 32-row diagonal blocks: recursive block inversion on CUDA cores (fp32);
+//        with the output gate (kOG) also its 64-row level, as two tf32 products (M=128 N=32 K=32)
 //   M4  [O^T | X] = S^T [Q o Gamma ; N]^T                        (M=128 N=128 K=128)
 //   M3  X += V^T Diag(beta), so X = R^T with R = beta o (V - (Gamma o K) S)
 //                                        (M=128 N=64 K=64; beta rounded to bf16)
-//   M7  V~^T = R^T T^T   tf32: A = R^T read from TMEM, B = T fp32   (M=128 N=64 K=64)
+//   M7  V~ = T R by block substitution over 32-row halves, tf32 (A read from TMEM):
+//         V~_0 = T_00 R_0,  R_1 -= L_10 V~_0,  V~_1 = T_11 R_1        (M=128 N=32 K=32, three steps)
+//       with kOG, whose state group carries the gate's epilogue, one product with the full T
+//                                                                     (M=128 N=64 K=64)
 //   M5  O^T += V~^T A^T                                           (M=128 N=64 K=64)
 //   M6  S^T <- (S^T + V~^T (K / Gamma)) Diag(gamma_C)              (M=128 N=128 K=64)
 // The page leaves the WY factors out; with T_b = T diag(beta) they are
@@ -121,7 +125,7 @@ constexpr uint32_t TM_S = 384;    // fp32 master state S^T (128 columns)
 
 enum Bar : int {
   B_M1 = 0, B_M7, B_VFULL, B_GFULL, B_QK0, B_QK1, B_TB, B_M4,
-  B_M56, B_L2, B_TD_C, B_TD_S, B_OG, B_OPS0, B_OPS1, B_COUNT
+  B_M56, B_M7S, B_L2, B_TD_C, B_TD_S, B_OG, B_OPS0, B_OPS1, B_COUNT
 };
 // B_OPS0 + (c & 1): chunk c's operands are in place (arrived once per chunk of
 // that parity, so a barrier runs at most one phase ahead of its waiter: the
@@ -449,9 +453,28 @@ __device__ __forceinline__ void issue_m3(uint32_t tbase, uint32_t v, uint32_t db
                 id, 1u);
 }
 
-// M7: V~^T = R^T T^T in tf32 (A = R^T fp32 in TMEM, one K element per
-// column; B = T fp32 in the two 32-column K-halves of the solve's buffer).
-__device__ __forceinline__ void issue_m7(uint32_t tbase, uint32_t tt) {
+// M7 in three steps over the two 32-row halves of the chunk (tf32; A from
+// TMEM, one K element per column; B from the solve's buffer tt, whose
+// 32-row diagonal blocks hold T_00 and T_11 and whose lower-left block holds
+// -L_10):
+//   step 0:  V~_0^T  = R_0^T T_00^T
+//   step 1:  R_1^T  += V~_0^T (-L_10)^T
+//   step 2:  V~_1^T  = R_1^T T_11^T
+__device__ __forceinline__ void issue_m7_step(uint32_t tbase, uint32_t tt, int step) {
+  constexpr uint32_t id = idesc_tf32_f32(128, 32);
+  // (D, A column offsets; B = rows [32 (step > 0), +32) of K-half (step == 2))
+  const uint32_t d = step == 0 ? TM_Y : step == 1 ? TM_X + 32 : TM_Y + 32;
+  const uint32_t a = step == 0 ? TM_X : step == 1 ? TM_Y : TM_X + 32;
+  const uint32_t b = tt + (step == 2 ? 8192u : 0u) + (step > 0 ? 4096u : 0u);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_tf32_ts(tbase + d, tbase + a + kk * 8, smem_desc_sw128(b + kk * 32, 16, 1024), id,
+                (kk > 0 || step == 1) ? 1u : 0u);
+}
+
+// M7 as one product, V~^T = R^T T^T, with the full T in the solve's buffer
+// (its two 32-column K-halves).
+__device__ __forceinline__ void issue_m7_full(uint32_t tbase, uint32_t tt) {
   constexpr uint32_t id = idesc_tf32_f32(128, 64);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
@@ -494,6 +517,12 @@ template <bool kZ, bool kOG>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   extern __shared__ uint8_t smem_raw[];
+  // Where the 64-row level of T's solve runs: in the chunk group on the
+  // tensor core (the full T, one M7 product), or folded into a three-step M7
+  // in the state group.  The output gate's epilogue makes the state group the
+  // longer of the two per chunk, so that variant keeps the level in the chunk
+  // group; without it the chunk group is the longer one.
+  constexpr bool kL64 = kOG;
   // 1024-aligned base by pointer arithmetic on the shared array, so that the
   // compiler keeps every access through `sm` in the shared address space
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -794,8 +823,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // there are already T's.
       {
         float *Lf = reinterpret_cast<float *>(sm + OFF_KB);
-        float *TTf = reinterpret_cast<float *>(sm + OFF_TF);      // T_[01][01]^T, [32][32] K-major
-        float *XTf = TTf + 1024;                                  // X^T of level 2, [32][32] K-major
+        float *TTf = reinterpret_cast<float *>(sm + OFF_TF);      // kL64: T_[01][01]^T, [32][32] K-major
+        float *XTf = TTf + 1024;                                  // kL64: X^T of level 2, [32][32] K-major
         float *Xf = TTf + 2048;                                   // 16- and 32-row level products (3 KB)
         // TMEM lanes 0..63 hold A's rows, 64..127 the rows of -L (N (K / Gamma)^T)
         const bool a_rows = qw < 2;
@@ -810,26 +839,32 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           st_row16_bf16(sm + OFF_AM + par * 8192, r, s0, v);
           st_row16_bf16(sm + OFF_AM + par * 8192, r, s0 + 16, v + 16);
         } else {
+          // L below the diagonal; without kL64 its lower-left 32 x 32 block is
+          // kept as -L (the state group's M7 subtracts L_10 V~_0 with it)
+          const float sg = (!kL64 && r >= 32 && s0 < 32) ? 1.f : -1.f;
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) v[cc] = (s0 + cc < r) ? -v[cc] : 0.f;
+          for (int cc = 0; cc < 32; ++cc) v[cc] = (s0 + cc < r) ? sg * v[cc] : 0.f;
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4)
             *reinterpret_cast<float4 *>(Lf + lt_idx(r, s0 + 4 * c4)) =
                 make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
         }
         bar_chunk();
-        // T = (I + L)^{-1} by recursive 2x2 block inversion,
+        // The 32-row diagonal blocks of T = (I + L)^{-1} by recursive 2x2
+        // block inversion,
         //   [[P, 0], [R, Q]]^{-1} = [[P^-1, 0], [-Q^-1 R P^-1, Q^-1]],
         // from the 8x8 diagonal blocks up: blocks of 8 by substitution, the
         // 16- and 32-row levels as X = R P^-1 then -Q^-1 X on CUDA cores (fp32,
-        // every chunk-group thread), the 64-row level on the tensor core (tf32,
-        // below).  Every T block is written in place over L as soon as it is
-        // final; the blocks of T_[01][01] also go, transposed, into the B
-        // operand of the first level-64 product.
+        // every chunk-group thread).  Every T block is written in place over L
+        // as soon as it is final.  Without kL64 the 64-row level is not
+        // formed: the state group's M7 applies it by substitution over the two
+        // 32-row halves, with -L_10 from the lower-left block.  With kL64 it is
+        // formed on the tensor core (tf32, below), and the blocks of T_[01][01]
+        // also go, transposed, into the B operand of its first product.
         // 8x8 diagonal blocks: one column per thread; a block's eight threads
         // share a warp, so the warp is done reading the block's L before any
-        // of them writes T over it.  Threads 64..159 meanwhile write the zero
-        // blocks of the transposed copy.
+        // of them writes T over it.  With kL64, threads 64..159 meanwhile
+        // write the zero blocks of the transposed copy.
         if (ctid < 64) {
           const int base = 8 * (ctid >> 3), cc = ctid & 7;
           float4 lr[8][2];
@@ -849,11 +884,11 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           __syncwarp();
 #pragma unroll
           for (int r = 0; r < 8; ++r) Lf[lt_idx(base + r, base + cc)] = x[r];
-          if (base < 32) {  // column cc of the block is row base + cc of the transposed copy
+          if (kL64 && base < 32) {  // column cc of the block is row base + cc of the transposed copy
             *reinterpret_cast<float4 *>(TTf + tt_idx(base + cc, base)) = make_float4(x[0], x[1], x[2], x[3]);
             *reinterpret_cast<float4 *>(TTf + tt_idx(base + cc, base + 4)) = make_float4(x[4], x[5], x[6], x[7]);
           }
-        } else if (ctid < 160) {
+        } else if (kL64 && ctid < 160) {
           // zeros of T_[01][01]^T: (n 8..15, k 0..7), (n 24..31, k 16..23), (n 16..31, k 0..15)
           const int e = ctid - 64;  // 96 float4
           int n, k;
@@ -878,7 +913,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) t = fmaf(f4c(k < 4 ? q0 : q1, k & 3), Xb[8 * k + jj], t);
           Lf[lt_idx(o + 8 + i, o + jj)] = -t;
-          if (o < 32) TTf[tt_idx(o + jj, o + 8 + i)] = -t;
+          if (kL64 && o < 32) TTf[tt_idx(o + jj, o + 8 + i)] = -t;
         }
         bar_chunk();
         // 32-row level: T_10 and T_32 of the 16-row blocks, two adjacent
@@ -911,52 +946,54 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
             acc.y = fmaf(lk, xv.y, acc.y);
           }
           *reinterpret_cast<float2 *>(Lf + lt_idx(rb + rr, cb + c2)) = make_float2(-acc.x, -acc.y);
-          if (blk == 0) {  // T_10 into the transposed copy
+          if (kL64 && blk == 0) {  // T_10 into the transposed copy
             TTf[tt_idx(c2, 16 + rr)] = -acc.x;
             TTf[tt_idx(c2 + 1, 16 + rr)] = -acc.y;
           }
         }
-        // level 2 on the tensor core (tf32):
-        //   X = L_[23][01] T_[01][01], then T_[23][01] = -T_[23][23] X.
-        // M = 128 rows of the row-major operand (rows 0-31 and 64-127 of the
-        // product are not used), N = 32, K = 32; D in the M1 result's columns.
-        group_publish<true>();
-        if (ctid == 0) {
-          constexpr uint32_t id = idesc_tf32_f32(128, 32);
+        if constexpr (kL64) {
+          // level 2 on the tensor core (tf32):
+          //   X = L_[23][01] T_[01][01], then T_[23][01] = -T_[23][23] X.
+          // M = 128 rows of the row-major operand (rows 0-31 and 64-127 of the
+          // product are not used), N = 32, K = 32; D in the M1 result's columns.
+          group_publish<true>();
+          if (ctid == 0) {
+            constexpr uint32_t id = idesc_tf32_f32(128, 32);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_tf32_ss(tbase + TM_D1, smem_desc_sw128(sm_base + OFF_KB + kk * 32, 16, 1024),
-                        smem_desc_sw128(sm_base + OFF_TF + kk * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
-          mma_commit(smem_u32(&ctl->bar[B_L2]));
-        }
-        if (!(alive = group_wait<true>(ctl, B_L2, ph_l2, ctid, seq, A.err))) break;
-        ph_l2 ^= 1u;
-        if ((warp & 3) == 1) {  // rows 32-63 of the product: X (TMEM lanes 32-63) -> X^T
-          const int n0 = 16 * (warp >> 2);
-          float x[16];
-          tmem_ld16(tmem_addr(tbase, 32, TM_D1 + n0), x);
-          tmem_wait_ld();
+            for (int kk = 0; kk < 4; ++kk)
+              mma_tf32_ss(tbase + TM_D1, smem_desc_sw128(sm_base + OFF_KB + kk * 32, 16, 1024),
+                          smem_desc_sw128(sm_base + OFF_TF + kk * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&ctl->bar[B_L2]));
+          }
+          if (!(alive = group_wait<true>(ctl, B_L2, ph_l2, ctid, seq, A.err))) break;
+          ph_l2 ^= 1u;
+          if ((warp & 3) == 1) {  // rows 32-63 of the product: X (TMEM lanes 32-63) -> X^T
+            const int n0 = 16 * (warp >> 2);
+            float x[16];
+            tmem_ld16(tmem_addr(tbase, 32, TM_D1 + n0), x);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) XTf[tt_idx(n0 + i, lane)] = x[i];
-        }
-        group_publish<true>();
-        if (ctid == 0) {
-          constexpr uint32_t id = idesc_tf32_f32(128, 32);
+            for (int i = 0; i < 16; ++i) XTf[tt_idx(n0 + i, lane)] = x[i];
+          }
+          group_publish<true>();
+          if (ctid == 0) {
+            constexpr uint32_t id = idesc_tf32_f32(128, 32);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_tf32_ss(tbase + TM_D1 + 32, smem_desc_sw128(sm_base + OFF_KB + 8192 + kk * 32, 16, 1024),
-                        smem_desc_sw128(sm_base + OFF_TF + 4096 + kk * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
-          mma_commit(smem_u32(&ctl->bar[B_L2]));
-        }
-        if (!(alive = group_wait<true>(ctl, B_L2, ph_l2, ctid, seq, A.err))) break;
-        ph_l2 ^= 1u;
-        if ((warp & 3) == 1) {  // rows 32-63: T_[23][23] X = -T_[23][01]
-          const int n0 = 16 * (warp >> 2);
-          float y[16];
-          tmem_ld16(tmem_addr(tbase, 32, TM_D1 + 32 + n0), y);
-          tmem_wait_ld();
+            for (int kk = 0; kk < 4; ++kk)
+              mma_tf32_ss(tbase + TM_D1 + 32, smem_desc_sw128(sm_base + OFF_KB + 8192 + kk * 32, 16, 1024),
+                          smem_desc_sw128(sm_base + OFF_TF + 4096 + kk * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&ctl->bar[B_L2]));
+          }
+          if (!(alive = group_wait<true>(ctl, B_L2, ph_l2, ctid, seq, A.err))) break;
+          ph_l2 ^= 1u;
+          if ((warp & 3) == 1) {  // rows 32-63: T_[23][23] X = -T_[23][01]
+            const int n0 = 16 * (warp >> 2);
+            float y[16];
+            tmem_ld16(tmem_addr(tbase, 32, TM_D1 + 32 + n0), y);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) Lf[lt_idx(32 + lane, n0 + i)] = -y[i];
+            for (int i = 0; i < 16; ++i) Lf[lt_idx(32 + lane, n0 + i)] = -y[i];
+          }
         }
       }
       if (ctid == 0) ctl->slow[par] = slow;
@@ -979,7 +1016,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     const int qw = warp & 3;                // lane quarter, = stid >> 5
     const int j = stid;
     int seq = 0;
-    uint32_t ph_m4 = 0, ph_m56 = 0;
+    uint32_t ph_m4 = 0, ph_m56 = 0, ph_m7s = 0;
     uint8_t *vt = sm + OFF_VT;
     if (stid == 0 && nchunks > 0) {
       tma_prefetch_desc(&maps.v);
@@ -1040,10 +1077,23 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // (every thread is past the previous chunk's reads of the out_gate tile)
       if (kOG && out_item && stid == 0) issue_og(&maps, ctl, sm_base, h, t0);
       if (stid == 0 && solo_wait(ctl, B_M4, ph_m4, A.err)) {
-        issue_m7(tbase, sm_base + OFF_KB);
-        mma_commit(smem_u32(&ctl->bar[B_M7]));
+        if constexpr (kL64) {
+          issue_m7_full(tbase, sm_base + OFF_KB);
+          mma_commit(smem_u32(&ctl->bar[B_M7]));
+        }
         // M3 has read the v tile: the next chunk's may land
         if (!zero_v && c + 1 < nchunks) issue_v(&maps, ctl, sm_base, h, t0 + kC);
+        // the three M7 steps, each reading from TMEM what the one before wrote
+        bool ok = !kL64;
+        for (int step = 0; step < 3 && ok; ++step) {
+          issue_m7_step(tbase, sm_base + OFF_KB, step);
+          if (step < 2) {
+            mma_commit(smem_u32(&ctl->bar[B_M7S]));
+            ok = solo_wait(ctl, B_M7S, ph_m7s, A.err);
+            ph_m7s ^= 1u;
+          }
+        }
+        if (ok) mma_commit(smem_u32(&ctl->bar[B_M7]));
       }
       ph_m4 ^= 1u;
       if (!(alive = group_wait<false>(ctl, B_M7, c & 1, stid, seq, A.err))) break;
