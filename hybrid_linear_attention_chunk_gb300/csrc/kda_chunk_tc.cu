@@ -157,7 +157,7 @@ struct TcArgs {
 };
 
 struct TcMaps {
-  CUtensorMap q, k, v, g, og;
+  CUtensorMap q, k, v, g, og, o;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -494,6 +494,26 @@ __device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t am, uint32_t 
     mma_bf16_ts(tbase + TM_O, tbase + TM_YB + kk * 8, smem_desc_sw128(am + kk * 32, 16, 1024), id5, 1u);
 }
 
+// M4 (with O) and M3 of chunk c, by the state group's thread 0, once the
+// chunk's operands are in place (the chunk group may still be solving for T)
+// and its v tile has landed.  The bf16 state, Diag(beta) and the previous
+// chunk's reads of O were ordered before this by the barrier that ended the
+// previous chunk.
+__device__ __forceinline__ bool issue_m43(const TcArgs &A, Ctl *ctl, uint32_t tbase, uint32_t sm_base, int c,
+                                          bool zero_v) {
+  bool ok = solo_wait(ctl, B_OPS0 + (c & 1), (c >> 1) & 1, A.err);
+  if (ok && !zero_v) {
+    ok = solo_wait(ctl, B_VFULL, c & 1, A.err);
+    if (ok) ++ctl->v_lnd;
+  }
+  if (ok) {
+    issue_m4(tbase, sm_base + OFF_QG, c & 1);
+    issue_m3(tbase, sm_base + OFF_V, sm_base + OFF_DB);
+    mma_commit(smem_u32(&ctl->bar[B_M4]));
+  }
+  return ok;
+}
+
 // The sequence of rank r when N packed sequences are ordered by length,
 // longest first (ties by index).  Every thread of the CTA calls it; s holds
 // N + 1 ints of shared scratch.
@@ -589,14 +609,14 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     if (a.plan == 1 && seg == 0) {
       s_in = a.s0 ? a.s0 + nh * DD : nullptr;
       s_out = a.E + ((size_t)n * (a.P - 1) * H + h) * DD;
-      out_item = true;
+      out_item = a.o != nullptr;
     } else if (a.plan == 1) {
       s_out = a.pairs + ((((size_t)kind * a.N + n) * (a.P - 2) + (seg - 1)) * H + h) * DD;
       out_item = false;
     } else {
       s_in = a.E + (((size_t)n * (a.P - 1) + (seg - 1)) * H + h) * DD;
       if (seg == a.P - 1 && a.sT) s_out = a.sT + nh * DD;
-      out_item = true;
+      out_item = a.o != nullptr;
     }
   }
   const int nchunks = (eos - bos + kC - 1) / kC;
@@ -1055,22 +1075,10 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       const int len = min(kC, eos - t0);
       // beta of the next chunk's rows (for its Diag(beta))
       if (stid < kC && c + 1 < nchunks) beta_async(ctl->bsx[par ^ 1], betap, t0 + kC, stid, eos, H, h);
-      // ---------------- M4 (with O) and M3 as soon as the chunk's operands are in
-      // place (the chunk group may still be solving for T) and v has landed;
-      // the bf16 state and Diag(beta) were written before the barrier that
-      // ended the previous iteration
-      if (stid == 0) {
-        bool ok = solo_wait(ctl, B_OPS0 + par, (c >> 1) & 1, A.err);
-        if (ok && !zero_v) {
-          ok = solo_wait(ctl, B_VFULL, c & 1, A.err);
-          if (ok) ++ctl->v_lnd;
-        }
-        if (ok) {
-          issue_m4(tbase, sm_base + OFF_QG, par);
-          issue_m3(tbase, sm_base + OFF_V, sm_base + OFF_DB);
-          mma_commit(smem_u32(&ctl->bar[B_M4]));
-        }
-      }
+      // M4 and M3 (issued here rather than right after the previous chunk's
+      // state refresh: there they met the chunk group's operand pass in the
+      // shared-memory pipe, and the step took ~10 % longer)
+      if (stid == 0) issue_m43(A, ctl, tbase, sm_base, c, zero_v);
       // ---------------- M7 once the chunk group has handed T over and M4 has
       // completed R (M7 reads it from TMEM)
       if (!(alive = group_wait<false>(ctl, B_TB, c & 1, stid, seq, A.err))) break;
@@ -1134,6 +1142,9 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       if (stid == 0) {
         issue_m56(tbase, sm_base + OFF_AM + par * 8192, sm_base + OFF_KH + par * 16384);
         mma_commit(smem_u32(&ctl->bar[B_M56]));
+        // the previous chunk's output store has read the staging tile (it is
+        // written again after the barrier below)
+        tma_store_wait_read();
       }
       if (!(alive = group_wait<false>(ctl, B_M56, ph_m56, stid, seq, A.err))) break;
       ph_m56 ^= 1u;
@@ -1142,9 +1153,23 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // tiles are written only after that copy has been waited for.
       if (stid == 0 && c + 2 < nchunks) issue_qk(&maps, ctl, sm_base, h, t0 + 2 * kC, par);
 
+      // ---------------- the output rows of the chunk to the staging tile (O is
+      // read before the next chunk's M4 overwrites it): before the state
+      // refresh, or after it with the output gate (each order measured the
+      // faster one for its variant)
+      auto stage_o = [&]() {
+        __nv_bfloat16 *ostage = reinterpret_cast<__nv_bfloat16 *>(vt);
+        float v[64];
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_O), *reinterpret_cast<float(*)[32]>(v));
+        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_O + 32), *reinterpret_cast<float(*)[32]>(v + 32));
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 64; ++cc) ostage[cc * kD + j] = __float2bfloat16_rn(v[cc]);
+      };
+      if constexpr (!kOG) stage_o();
       // ---------------- S^T <- S^T Diag(gamma_C) (unless done before M6), the
       // bf16 copy of the new state (and a checkpoint of the fp32 state when
-      // one ends this chunk); the output rows
+      // one ends this chunk)
       float *cp = out_item ? ckpt_ptr(a, n, h, t0 + len - seq_bos) : nullptr;
       {
         const float *gam = ctl->gam[c % 3];
@@ -1165,24 +1190,25 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
             for (int cc = 0; cc < 32; ++cc) cp[(size_t)(i0 + cc) * kD + j] = s[cc];
         }
       }
-      {
-        __nv_bfloat16 *ostage = reinterpret_cast<__nv_bfloat16 *>(vt);
-        float v[64];
-        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_O), *reinterpret_cast<float(*)[32]>(v));
-        tmem_ld32(tmem_addr(tbase, 32 * qw, TM_O + 32), *reinterpret_cast<float(*)[32]>(v + 32));
-        tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < 64; ++cc) ostage[cc * kD + j] = __float2bfloat16_rn(v[cc]);
-      }
+      if constexpr (kOG) stage_o();
+      // A whole chunk without the output gate leaves by one TMA store of the
+      // staging tile; a chunk cut short by the end of its sequence (whose
+      // neighbour's rows the box would cover) and the gated rows by plain stores.
+      const bool tma_out = !kOG && out_item && len == kC;
       tmem_wait_st();
       tc_fence_before();
+      if (tma_out) fence_proxy_async_smem();
       if (kOG && out_item) {  // the barrier also waits for this chunk's out_gate tile
         if (!(alive = group_wait<false>(ctl, B_OG, c & 1, stid, seq, A.err))) break;
         if (stid == 0) ++ctl->og_lnd;
       } else {
         bar_state();
       }
-      if (out_item) {  // (the pair items of the long-sequence plan write no output)
+      if (tma_out && stid == 0) {
+        tma_store_3d(&maps.o, sm_base + OFF_VT, 0, h, t0);
+        tma_store_commit();
+      }
+      if (out_item && !tma_out) {  // (the pair items of the long-sequence plan write no output)
         const uint4 *src = reinterpret_cast<const uint4 *>(vt);
         uint4 *o = reinterpret_cast<uint4 *>(a.o);
         float w8[8];
@@ -1222,8 +1248,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           }
         }
       }
-      // (the next chunk's first group wait orders these reads of the staging
-      // tile before it is written again)
+      // (the next chunk's group waits order these reads of the staging tile
+      // before it is written again)
     }
     if (alive && s_out) {
 #pragma unroll 1
@@ -1237,6 +1263,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
     }
     cp_async_wait_all();
     if (stid == 0) {
+      tma_store_wait_all();
       volatile int no_abort = 0;
       mma_commit(smem_u32(&ctl->bar[B_TD_S]));
       mbar_wait(smem_u32(&ctl->bar[B_TD_S]), 0, &no_abort, A.err, 1u << 24);
@@ -1320,7 +1347,8 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
       encode_tok_head(encode, &maps.k, a.k, a.T_total, a.H, false, true) != CUDA_SUCCESS ||
       encode_tok_head(encode, &maps.v, a.v, a.T_total, a.H, false, true) != CUDA_SUCCESS ||
       encode_tok_head(encode, &maps.g, a.g, a.T_total, a.H, !z, false) != CUDA_SUCCESS ||
-      (og && encode_tok_head(encode, &maps.og, a.og, a.T_total, a.H, false, false) != CUDA_SUCCESS))
+      (og && encode_tok_head(encode, &maps.og, a.og, a.T_total, a.H, false, false) != CUDA_SUCCESS) ||
+      (a.o && encode_tok_head(encode, &maps.o, a.o, a.T_total, a.H, false, false) != CUDA_SUCCESS))
     return cudaErrorInvalidValue;
   void *wd = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&wd, g_tc_watchdog);
