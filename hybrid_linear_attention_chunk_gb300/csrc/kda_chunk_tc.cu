@@ -750,9 +750,9 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       ++seq;
       if (!alive) break;
       // gamma_C goes to slot m mod 3: the state group may still be reading
-      // slot (m - 2) mod 3 (the q/k copy just waited for is issued as soon as
-      // chunk m - 2's products are done, before that chunk's state refresh);
-      // it reads this slot after the hand-off below
+      // slot (m - 2) mod 3 (the q/k copy just waited for was issued once
+      // chunk m - 2's M5/M6 were done, before that chunk's state refresh),
+      // but it is past chunk m - 3's; it reads this slot after the hand-off below
       if (t8 == 0) *reinterpret_cast<float4 *>(&ctl->gam[m % 3][4 * p4]) = gam;
       // operand tiles: channel quad p4 sits in K-half p4 / 16 at column 4 p4 mod 64
       const uint32_t half = (uint32_t)(p4 >> 4), col = (uint32_t)(4 * p4) & 63u;
@@ -780,13 +780,19 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
         group_publish<true>();
         if (ctid == 0) {
-          issue_m1(tbase, smem_u32(qg), sm_base + OFF_KH + par * 16384, par, false);
-          mma_commit(smem_u32(&ctl->bar[B_M1]));
-          // the state group may start M4 and O (behind M1 in the tensor pipe)
+          // the state group may start M4 and O; M1 goes in only after the
+          // previous chunk's M7 (which M1 would otherwise hold up in the
+          // tensor pipe, and whose T the L written below replaces)
           mbar_arrive(smem_u32(&ctl->bar[B_OPS0 + par]));
+          const bool ok =
+              m == 0 || mbar_wait(smem_u32(&ctl->bar[B_M7]), (m - 1) & 1, &ctl->abort, A.err, 1u << B_M7);
+          tc_fence_after();
+          if (ok) {
+            issue_m1(tbase, smem_u32(qg), sm_base + OFF_KH + par * 16384, par, false);
+            mma_commit(smem_u32(&ctl->bar[B_M1]));
+          }
         }
-        // M1 done, and the previous chunk's M7 done with T (L is written over it below)
-        alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err, m > 0 ? B_M7 : -1, (m - 1) & 1);
+        alive = group_wait<true>(ctl, B_M1, ph_m1, ctid, seq, A.err);
         ph_m1 ^= 1u;
       } else {
         // M1 in four accumulating rounds, one per 16-token key tile b, with
@@ -1017,6 +1023,13 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
       }
       if (ctid == 0) ctl->slow[par] = slow;
+      // q and k of chunk m + 1 go into the buffers of chunk m - 1 once its M5
+      // and M6 are done (the state group completes them while this chunk's
+      // solve runs; issuing here keeps the copy off the state group's path).
+      // B_M56 cannot be a phase ahead: chunk m's M5/M6 wait for the hand-off below.
+      if (ctid == 0 && m >= 1 && m + 1 < nchunks &&
+          mbar_wait(smem_u32(&ctl->bar[B_M56]), (m - 1) & 1, &ctl->abort, A.err, 1u << B_M56))
+        issue_qk(&maps, ctl, sm_base, h, t0 + kC, par ^ 1);
       group_publish<true>();
       // ---------------- hand the chunk to the state group (the arrive releases
       // the chunk's operands, A, T and gamma_C to it)
@@ -1148,11 +1161,8 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       }
       if (!(alive = group_wait<false>(ctl, B_M56, ph_m56, stid, seq, A.err))) break;
       ph_m56 ^= 1u;
-      // This parity's operand buffers are free (every product of chunk c has
-      // completed): q and k of the chunk two ahead land in them; its N and A
-      // tiles are written only after that copy has been waited for.
-      if (stid == 0 && c + 2 < nchunks) issue_qk(&maps, ctl, sm_base, h, t0 + 2 * kC, par);
-
+      // (this parity's operand buffers are now free: the chunk group loads q
+      // and k of the chunk two ahead into them)
       // ---------------- the output rows of the chunk to the staging tile (O is
       // read before the next chunk's M4 overwrites it): before the state
       // refresh, or after it with the output gate (each order measured the
