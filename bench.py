@@ -403,6 +403,8 @@ def run_gpu(args):
         if nsteps > 0:
             extra[key] = time_prefill_workload(kda, inputs, wl, nsteps, dev, stream, world, rank, hbm_peak)
 
+    if world > 1 and args.cp_steps > 0:
+        extra["cp"] = time_cp(kda, inputs, args.cp_steps, dev, world, rank)
     if args.ckpt_steps > 0:
         extra["checkpoints"] = time_checkpoints(kda, x, w, args.ckpt_steps, 512, ms_step, dev, stream, world)
     if args.bwd_steps > 0:
@@ -479,6 +481,72 @@ def time_prefill_workload(kda, inputs, w, steps, dev, stream, world, rank, hbm_p
                         "frac": round(gbs / hbm_peak, 4), "algorithmic_bytes_per_step": int(alg)}}
     del x, out, sT
     torch.cuda.empty_cache()
+    return res
+
+
+def time_cp(kda, inputs, steps, dev, world, rank, w=None, backend=None, all_gather=None, seed_base=None):
+    """The long-context workload over the ranks by tokens, through the
+    context-parallel path (kda_chunk_fwd_cp): rank r holds tokens
+    [r L, (r + 1) L) of every sequence, forms its affine pair, one all-gather
+    moves every rank's pair (and rank 0's initial state), the entry states are
+    composed and the local segment rerun.  Total work is fixed (strong
+    scaling); the pairs are the only data that crosses devices.  `backend` and
+    `all_gather` default to the library and torch.distributed; on a CPU device
+    the steps are timed with the host clock."""
+    import time
+    import torch
+    from hybrid_linear_attention_chunk_gb300.cp import LibraryBackend, kda_chunk_fwd_cp
+
+    w = w or inputs.LONG_T1M
+    if w.T % world:
+        return {"workload": w.name, "skipped": f"{w.T} tokens do not split evenly over {world} ranks"}
+    L = w.T // world
+    wl = inputs.scaled(w, T=L)
+    seed = (inputs.SEED_BASE if seed_base is None else seed_base) + w.seed_index + 1000 * rank
+    x = inputs.make_prefill(wl, device=dev, seed=seed)
+    s0 = x["initial_state"] if rank == 0 else None
+    backend = backend or LibraryBackend(kda)
+
+    def step():
+        return kda_chunk_fwd_cp(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], s0, rank=rank, world=world,
+                                B=w.B, all_gather=all_gather, backend=backend)
+
+    cuda = dev.type == "cuda"
+    sync = (lambda: torch.cuda.synchronize(dev)) if cuda else (lambda: None)
+    step()
+    sync()
+    barrier(world, dev if cuda else None)
+    if cuda:
+        stream = torch.cuda.current_stream(dev)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        sync()
+        ms_local = ev0.elapsed_time(ev1) / steps
+    else:
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            step()
+        ms_local = (time.perf_counter() - t0) * 1e3 / steps
+    per_rank = [ms_local]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+        parts = [torch.zeros_like(t) for _ in range(world)]
+        dist.all_gather(parts, t)
+        per_rank = [float(p.item()) for p in parts]
+    ms = max(per_rank)
+    tokens = w.B * w.T
+    pair_bytes = 3 * w.B * w.H * w.dk * w.dv * 4
+    res = {"workload": w.name, "path": "kda_chunk_fwd_cp", "ranks": world, "tokens_per_rank": L,
+           "steps": steps, "ms_per_step": round(ms, 3), "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+           "scaling": "strong", "per_rank_ms": [round(v, 3) for v in per_rank],
+           "allgather_bytes_per_rank": pair_bytes}
+    del x
+    if cuda:
+        torch.cuda.empty_cache()
     return res
 
 
@@ -765,6 +833,9 @@ def main(argv=None):
                     help="steps of the headline batch in the layer form (0: skip)")
     ap.add_argument("--ckpt-steps", type=int, default=100,
                     help="steps of the headline batch with 512-token state checkpoints (0: skip)")
+    ap.add_argument("--cp-steps", type=int, default=3,
+                    help="with N > 1: steps of the 2^20-token workload split over the ranks by tokens "
+                         "(context-parallel path; 0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -127,3 +127,42 @@ def test_single_rank_is_the_plain_call():
     o, s = kda_chunk_fwd_cp(q, k, v, g, beta, s0, rank=0, world=1, B=1, backend=OracleBackend())
     o_ref, s_ref = oracle.recurrent(q.numpy(), k.numpy(), v.numpy(), g.numpy(), beta.numpy(), s0.numpy())
     assert np.array_equal(o.numpy(), o_ref) and np.array_equal(s.numpy(), s_ref)
+
+
+def _bench_rank_main(rank, world, port, results):
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    sys.path.insert(0, os.path.join(root, "tests"))
+    import torch.distributed as dist
+    import bench
+    from hybrid_linear_attention_chunk_gb300 import inputs
+    from test_cp_cpu import OracleBackend
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = inputs.scaled(inputs.LONG_T1M, T=48, H=2, dk=8, dv=8, qkv_dtype=torch.float32,
+                          out_dtype=torch.float32)
+        results[rank] = bench.time_cp(None, inputs, 2, torch.device("cpu"), world, rank, w=w,
+                                      backend=OracleBackend())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_bench_cp_leg_on_gloo_ranks():
+    """bench.py's context-parallel leg (run under torchrun with N > 1): every
+    rank times the same schedule on its token segment, and the line carries
+    every rank's time, the max over ranks and the bytes each rank sends."""
+    world = 2
+    port = _free_port()
+    with mp.Manager() as mgr:
+        results = mgr.dict()
+        mp.spawn(_bench_rank_main, args=(world, port, results), nprocs=world, join=True)
+        res = dict(results)
+    for r in range(world):
+        e = res[r]
+        assert e["path"] == "kda_chunk_fwd_cp" and e["ranks"] == world and e["tokens_per_rank"] == 24
+        assert len(e["per_rank_ms"]) == world and e["per_rank_ms"] == res[0]["per_rank_ms"]
+        assert e["ms_per_step"] == round(max(e["per_rank_ms"]), 3) and e["ms_per_step"] > 0
+        assert e["allgather_bytes_per_rank"] == 3 * 1 * 2 * 8 * 8 * 4
+        assert e["scaling"] == "strong" and e["tokens_per_s"] > 0
