@@ -434,8 +434,20 @@ __device__ __forceinline__ void issue_m1(uint32_t tbase, uint32_t qg, uint32_t k
 // M4: [O^T | X] = S^T [Q o Gamma ; N]^T, one N = 128 product (A = bf16
 // S^T in TMEM; B = the 128 rows [Q o Gamma ; N] of the chunk's parity, K-major,
 // contiguous within each K-half like M1's A operand).
-__device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t qg, int par) {
+// With x_only (a work item that writes no output) only X = S^T N^T, from
+// the N rows (the second 64 of each K-half's 128).
+__device__ __forceinline__ void issue_m4(uint32_t tbase, uint32_t qg, int par, bool x_only) {
   constexpr uint32_t id = idesc_bf16_f32(128, 128, 0, 0);
+  constexpr uint32_t idx = idesc_bf16_f32(128, 64, 0, 0);
+  if (x_only) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t kb = (kk >> 2) * KHALF + par * 16384 + 8192 + (kk & 3) * 32;
+      mma_bf16_ts(tbase + TM_X, tbase + TM_STB + kk * 8, smem_desc_sw128(qg + kb, 16, 1024), idx,
+                  kk > 0 ? 1u : 0u);
+    }
+    return;
+  }
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t kb = (kk >> 2) * KHALF + par * 16384 + (kk & 3) * 32;
@@ -482,13 +494,14 @@ __device__ __forceinline__ void issue_m7_full(uint32_t tbase, uint32_t tt) {
                 smem_desc_sw128(tt + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
 }
 
-// M6 then M5 (A = bf16 V~^T in TMEM).
-__device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t am, uint32_t kh) {
+// M6 then, for a work item that writes output, M5 (A = bf16 V~^T in TMEM).
+__device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t am, uint32_t kh, bool with_o) {
   constexpr uint32_t id5 = idesc_bf16_f32(128, 64, 0, 0);
   constexpr uint32_t id6 = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)  // S^T += V~^T (K / Gamma)   (B MN-major)
     mma_bf16_ts(tbase + TM_S, tbase + TM_YB + kk * 8, smem_desc_sw128(kh + kk * 2048, 8192, 1024), id6, 1u);
+  if (!with_o) return;
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)  // O^T += V~^T A^T
     mma_bf16_ts(tbase + TM_O, tbase + TM_YB + kk * 8, smem_desc_sw128(am + kk * 32, 16, 1024), id5, 1u);
@@ -499,16 +512,18 @@ __device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t am, uint32_t 
 // and its v tile has landed.  The bf16 state, Diag(beta) and the previous
 // chunk's reads of O were ordered before this by the barrier that ended the
 // previous chunk.
+// A transition item (zero_v: v = 0) skips M3, whose product is zero, and an
+// item without output (with_o false) forms X alone.
 __device__ __forceinline__ bool issue_m43(const TcArgs &A, Ctl *ctl, uint32_t tbase, uint32_t sm_base, int c,
-                                          bool zero_v) {
+                                          bool zero_v, bool with_o) {
   bool ok = solo_wait(ctl, B_OPS0 + (c & 1), (c >> 1) & 1, A.err);
   if (ok && !zero_v) {
     ok = solo_wait(ctl, B_VFULL, c & 1, A.err);
     if (ok) ++ctl->v_lnd;
   }
   if (ok) {
-    issue_m4(tbase, sm_base + OFF_QG, c & 1);
-    issue_m3(tbase, sm_base + OFF_V, sm_base + OFF_DB);
+    issue_m4(tbase, sm_base + OFF_QG, c & 1, !with_o);
+    if (!zero_v) issue_m3(tbase, sm_base + OFF_V, sm_base + OFF_DB);
     mma_commit(smem_u32(&ctl->bar[B_M4]));
   }
   return ok;
@@ -1091,7 +1106,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       // M4 and M3 (issued here rather than right after the previous chunk's
       // state refresh: there they met the chunk group's operand pass in the
       // shared-memory pipe, and the step took ~10 % longer)
-      if (stid == 0) issue_m43(A, ctl, tbase, sm_base, c, zero_v);
+      if (stid == 0) issue_m43(A, ctl, tbase, sm_base, c, zero_v, out_item);
       // ---------------- M7 once the chunk group has handed T over and M4 has
       // completed R (M7 reads it from TMEM)
       if (!(alive = group_wait<false>(ctl, B_TB, c & 1, stid, seq, A.err))) break;
@@ -1153,7 +1168,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
       tmem_wait_st();
       group_publish<false>();
       if (stid == 0) {
-        issue_m56(tbase, sm_base + OFF_AM + par * 8192, sm_base + OFF_KH + par * 16384);
+        issue_m56(tbase, sm_base + OFF_AM + par * 8192, sm_base + OFF_KH + par * 16384, out_item);
         mma_commit(smem_u32(&ctl->bar[B_M56]));
         // the previous chunk's output store has read the staging tile (it is
         // written again after the barrier below)
@@ -1176,7 +1191,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
 #pragma unroll
         for (int cc = 0; cc < 64; ++cc) ostage[cc * kD + j] = __float2bfloat16_rn(v[cc]);
       };
-      if constexpr (!kOG) stage_o();
+      if (!kOG && out_item) stage_o();
       // ---------------- S^T <- S^T Diag(gamma_C) (unless done before M6), the
       // bf16 copy of the new state (and a checkpoint of the fp32 state when
       // one ends this chunk)
@@ -1200,7 +1215,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
             for (int cc = 0; cc < 32; ++cc) cp[(size_t)(i0 + cc) * kD + j] = s[cc];
         }
       }
-      if constexpr (kOG) stage_o();
+      if (kOG && out_item) stage_o();
       // A whole chunk without the output gate leaves by one TMA store of the
       // staging tile; a chunk cut short by the end of its sequence (whose
       // neighbour's rows the box would cover) and the gated rows by plain stores.
