@@ -129,8 +129,8 @@ enum Bar : int {
 };
 // B_OPS0 + (c & 1): chunk c's operands are in place (arrived once per chunk of
 // that parity, so a barrier runs at most one phase ahead of its waiter: the
-// next arrival on it needs the q/k copy the state group issues after chunk
-// c's products)
+// next arrival on it needs the q/k copy that is issued only once chunk c's
+// M5/M6 are done)
 
 struct Ctl {
   uint64_t bar[16];
