@@ -401,7 +401,8 @@ def run_gpu(args):
     for key, wl, nsteps in (("long_context", inputs.LONG_T1M, args.long_steps),
                             ("varlen", inputs.VARLEN_64, args.varlen_steps)):
         if nsteps > 0:
-            extra[key] = time_prefill_workload(kda, inputs, wl, nsteps, dev, stream, world, rank, hbm_peak)
+            extra[key] = time_prefill_workload(kda, inputs, wl, nsteps, dev, stream, world, rank, hbm_peak,
+                                               0.0 if args.no_cpu_baseline else args.cpu_seconds / 2)
 
     if world > 1 and args.cp_steps > 0:
         extra["cp"] = time_cp(kda, inputs, args.cp_steps, dev, world, rank)
@@ -440,8 +441,9 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def time_prefill_workload(kda, inputs, w, steps, dev, stream, world, rank, hbm_peak):
-    """Times one more prefill workload (one kda_chunk_fwd call per step)."""
+def time_prefill_workload(kda, inputs, w, steps, dev, stream, world, rank, hbm_peak, cpu_seconds=0.0):
+    """Times one more prefill workload (one kda_chunk_fwd call per step); with
+    cpu_seconds > 0 (rank 0) the oracle is timed beside it on a bounded sample."""
     import numpy as np
     import torch
     x = inputs.make_prefill(w, device=dev, seed=inputs.SEED_BASE + w.seed_index + 1000 * rank)
@@ -479,6 +481,8 @@ def time_prefill_workload(kda, inputs, w, steps, dev, stream, world, rank, hbm_p
            "split_workspace_bytes": int(ws_bytes),
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                         "frac": round(gbs / hbm_peak, 4), "algorithmic_bytes_per_step": int(alg)}}
+    if cpu_seconds > 0 and rank == 0:
+        res["cpu_baseline"] = cpu_baseline_sample(w, x, cpu_seconds)
     del x, out, sT
     torch.cuda.empty_cache()
     return res
@@ -739,6 +743,36 @@ def cpu_baseline(w, x, seconds=12.0):
                          "sample": f"tokens [0, {L}) of chain (0, 0) on one thread; value = L/H tokens per second; "
                                    f"{d1:.1f} s"}
     return res
+
+
+def cpu_baseline_sample(w, x, seconds=6.0):
+    """The fp64 oracle (as it stands) on host cores over a bounded sample of a
+    prefill workload: the first L tokens of sequence 0, every head in parallel,
+    from the sequence's initial state, L calibrated to about `seconds`."""
+    import numpy as np
+    import oracle
+    from hybrid_linear_attention_chunk_gb300 import inputs
+
+    cores = os.cpu_count() or 1
+    names = ("q", "k", "v", "log_alpha", "beta")
+    len0 = int(x["lengths"][0])
+    s0 = x["initial_state"]
+    s0h = None if s0 is None else inputs.host_f32(s0[:1])
+
+    def run(L):
+        hs = [inputs.host_f32(x[n][:L]) for n in names]
+        t0 = time.perf_counter()
+        oracle.recurrent(*hs, s0h, np.array([0, L], dtype=np.int64), nthreads=cores, want_o=True)
+        return time.perf_counter() - t0
+
+    L0 = min(len0, 256)
+    t_cal = run(L0)
+    L = int(min(len0, max(L0, L0 * seconds / max(t_cal, 1e-4))))
+    dt = run(L)
+    return {"value": round(L / dt, 2), "unit": "tokens/s", "cores": min(cores, w.H), "kind": "oracle",
+            "sample": f"tokens [0, {L}) of sequence 0 of {w.name}, all {w.H} heads in parallel"
+                      f"{'' if s0 is None else ' from its initial state'}; value = tokens (every head) per "
+                      f"second; {dt:.1f} s"}
 
 
 def cpu_baseline_decode(dw, dev, seconds=8.0):

@@ -45,3 +45,19 @@ def test_two_gloo_ranks_reduce_max():
 def test_single_rank_is_identity():
     import bench
     assert bench.reduce_max(2.25, 1) == 2.25
+
+
+def test_cpu_baseline_sample_legs():
+    """The oracle legs timed beside the long-context and varlen workloads: a
+    bounded prefix of sequence 0 over every head, from its initial state, on
+    host cores (small shapes here, so the leg runs in well under a second)."""
+    import torch
+    import bench
+    from hybrid_linear_attention_chunk_gb300 import inputs
+    for base in (inputs.LONG_T1M, inputs.VARLEN_64):
+        kw = dict(H=2, dk=16, dv=16, qkv_dtype=torch.float32, out_dtype=torch.float32)
+        w = inputs.scaled(base, T=512, **kw) if base.varlen_seqs == 0 else inputs.scaled(base, varlen_seqs=3, **kw)
+        x = inputs.make_prefill(w, device="cpu")
+        r = bench.cpu_baseline_sample(w, x, seconds=0.2)
+        assert r["kind"] == "oracle" and r["unit"] == "tokens/s" and r["value"] > 0
+        assert 1 <= r["cores"] <= w.H and "initial state" in r["sample"]
