@@ -494,6 +494,24 @@ __device__ __forceinline__ void issue_m7_full(uint32_t tbase, uint32_t tt) {
                 smem_desc_sw128(tt + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
 }
 
+// M6 then, for a work item that writes output, M5, over the tokens of one
+// 32-row half of the chunk (K-steps 2 half and 2 half + 1).
+__device__ __forceinline__ void issue_m56_half(uint32_t tbase, uint32_t am, uint32_t kh, bool with_o, int half) {
+  constexpr uint32_t id5 = idesc_bf16_f32(128, 64, 0, 0);
+  constexpr uint32_t id6 = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+  for (int k2 = 0; k2 < 2; ++k2) {
+    const int kk = 2 * half + k2;
+    mma_bf16_ts(tbase + TM_S, tbase + TM_YB + kk * 8, smem_desc_sw128(kh + kk * 2048, 8192, 1024), id6, 1u);
+  }
+  if (!with_o) return;
+#pragma unroll
+  for (int k2 = 0; k2 < 2; ++k2) {
+    const int kk = 2 * half + k2;
+    mma_bf16_ts(tbase + TM_O, tbase + TM_YB + kk * 8, smem_desc_sw128(am + kk * 32, 16, 1024), id5, 1u);
+  }
+}
+
 // M6 then, for a work item that writes output, M5 (A = bf16 V~^T in TMEM).
 __device__ __forceinline__ void issue_m56(uint32_t tbase, uint32_t am, uint32_t kh, bool with_o) {
   constexpr uint32_t id5 = idesc_bf16_f32(128, 64, 0, 0);
@@ -548,7 +566,9 @@ __device__ int longest_first(const int32_t *cu, int N, int r, int *s, int tid) {
   return n;
 }
 
-template <bool kZ, bool kOG>
+// kSplit: M7's last two steps overlap the bf16 staging of V~'s first half
+// and M5/M6 over the first 32 tokens (see the state group); chosen per launch.
+template <bool kZ, bool kOG, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
   extern __shared__ uint8_t smem_raw[];
@@ -1119,24 +1139,94 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
         // M3 has read the v tile: the next chunk's may land
         if (!zero_v && c + 1 < nchunks) issue_v(&maps, ctl, sm_base, h, t0 + kC);
-        // the three M7 steps, each reading from TMEM what the one before wrote
-        bool ok = !kL64;
-        for (int step = 0; step < 3 && ok; ++step) {
-          issue_m7_step(tbase, sm_base + OFF_KB, step);
-          if (step < 2) {
-            mma_commit(smem_u32(&ctl->bar[B_M7S]));
-            ok = solo_wait(ctl, B_M7S, ph_m7s, A.err);
-            ph_m7s ^= 1u;
+        if constexpr (!kL64) {
+          // the three M7 steps, each reading from TMEM what the one before
+          // wrote; with kSplit only the first here, the other two below
+          bool ok = true;
+          for (int step = 0; step < (kSplit ? 1 : 3) && ok; ++step) {
+            issue_m7_step(tbase, sm_base + OFF_KB, step);
+            if (step < 2) {
+              mma_commit(smem_u32(&ctl->bar[B_M7S]));
+              if constexpr (!kSplit) {
+                ok = solo_wait(ctl, B_M7S, ph_m7s, A.err);
+                ph_m7s ^= 1u;
+              }
+            }
           }
+          if (ok && !kSplit) mma_commit(smem_u32(&ctl->bar[B_M7]));
         }
-        if (ok) mma_commit(smem_u32(&ctl->bar[B_M7]));
       }
       ph_m4 ^= 1u;
+      const bool slow = ctl->slow[par] != 0;
+      if constexpr (!kL64 && kSplit) {
+        // Steps 1 and 2 of M7.  While they run, the group turns V~_0 (step
+        // 0's result) into bf16, so that M6/M5 over the first 32 tokens follow
+        // step 2 in the pipe and only the second half remains after it.  This
+        // pays when the state group sets the pace (one chain per SM); when
+        // the chunk group does (many chains, the long-sequence plan), the
+        // later M7 costs more than it saves and the plain order is used.
+        if (!(alive = group_wait<false>(ctl, B_M7S, ph_m7s, stid, seq, A.err))) break;
+        ph_m7s ^= 1u;
+        if (stid == 0) {
+          issue_m7_step(tbase, sm_base + OFF_KB, 1);
+          mma_commit(smem_u32(&ctl->bar[B_M7S]));
+        }
+        {
+          float y[32];
+          tmem_ld32(tmem_addr(tbase, 32 * qw, TM_Y), y);
+          tmem_wait_ld();
+          tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_YB), y);
+        }
+        // after the per-tile range path, S^T <- S^T Diag(gamma_C) before M6
+        // (else the scaling follows M6)
+        if (slow) {
+          const float *gam = ctl->gam[c % 3];
+#pragma unroll 1
+          for (int i0 = 0; i0 < kD; i0 += 32) {
+            float sv[32];
+            tmem_ld32(tmem_addr(tbase, 32 * qw, TM_S + i0), sv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) sv[cc] *= gam[i0 + cc];
+            tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0), *reinterpret_cast<float(*)[16]>(sv));
+            tmem_st16(tmem_addr(tbase, 32 * qw, TM_S + i0 + 16), *reinterpret_cast<float(*)[16]>(sv + 16));
+          }
+        }
+        // Diag(beta) of the next chunk (M3 of this chunk is done)
+        if (stid < kC && c + 1 < nchunks) {
+          cp_async_wait_all();
+          *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_DB + sw128_offset(stid, stid)) =
+              __float2bfloat16_rn(ctl->bsx[par ^ 1][stid]);
+        }
+        tmem_wait_st();
+        group_publish<false>();
+        if (stid == 0 && solo_wait(ctl, B_M7S, ph_m7s, A.err)) {
+          issue_m7_step(tbase, sm_base + OFF_KB, 2);
+          mma_commit(smem_u32(&ctl->bar[B_M7]));
+          issue_m56_half(tbase, sm_base + OFF_AM + par * 8192, sm_base + OFF_KH + par * 16384, out_item, 0);
+        }
+        ph_m7s ^= 1u;
+        if (!(alive = group_wait<false>(ctl, B_M7, c & 1, stid, seq, A.err))) break;
+        {
+          float y[32];
+          tmem_ld32(tmem_addr(tbase, 32 * qw, TM_Y + 32), y);
+          tmem_wait_ld();
+          tmem_st_bf16x32(tmem_addr(tbase, 32 * qw, TM_YB + 16), y);
+        }
+        tmem_wait_st();
+        group_publish<false>();
+        if (stid == 0) {
+          issue_m56_half(tbase, sm_base + OFF_AM + par * 8192, sm_base + OFF_KH + par * 16384, out_item, 1);
+          mma_commit(smem_u32(&ctl->bar[B_M56]));
+          // the previous chunk's output store has read the staging tile (it is
+          // written again after the barrier below)
+          tma_store_wait_read();
+        }
+      } else {
       if (!(alive = group_wait<false>(ctl, B_M7, c & 1, stid, seq, A.err))) break;
 
       // ---------------- V~^T -> bf16 A operand of M5/M6; after the per-tile
       // range path, S^T <- S^T Diag(gamma_C) before M6 (else the scaling follows M6)
-      const bool slow = ctl->slow[par] != 0;
       {
         float y[32];
         tmem_ld32(tmem_addr(tbase, 32 * qw, TM_Y), y);
@@ -1173,6 +1263,7 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         // the previous chunk's output store has read the staging tile (it is
         // written again after the barrier below)
         tma_store_wait_read();
+      }
       }
       if (!(alive = group_wait<false>(ctl, B_M56, ph_m56, stid, seq, A.err))) break;
       ph_m56 ^= 1u;
@@ -1343,13 +1434,13 @@ CUresult encode_tok_head(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <bool kZ, bool kOG>
+template <bool kZ, bool kOG, bool kSplit>
 cudaError_t launch_variant(const TcMaps &maps, const TcArgs &args, int grid, cudaStream_t s) {
   constexpr uint32_t bytes = SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<kZ, kOG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)bytes);
+  cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<kZ, kOG, kSplit>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  chunk_tc_kernel<kZ, kOG><<<grid, kThreads, bytes, s>>>(maps, args);
+  chunk_tc_kernel<kZ, kOG, kSplit><<<grid, kThreads, bytes, s>>>(maps, args);
   return cudaGetLastError();
 }
 
@@ -1378,14 +1469,26 @@ cudaError_t launch_chunk_tc(const PrefillArgs &a, cudaStream_t s) {
   void *wd = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&wd, g_tc_watchdog);
   if (e != cudaSuccess) return e;
-  TcArgs args{a, reinterpret_cast<unsigned int *>(wd)};
   const int NH = a.N * a.H;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    sms = 0;
+  // split M7 for an unsplit launch with at most one chain per SM (measured:
+  // batch prefill 0.570 -> 0.555 ms; varlen and the long-sequence plan slower)
+  const bool split = a.plan == 0 && a.kinds == 1 && a.nseg == 1 && NH <= sms;
+  TcArgs args{a, reinterpret_cast<unsigned int *>(wd)};
   const int grid = a.plan == 1 ? NH + 2 * NH * (a.P - 2) : a.plan == 2 ? NH * (a.P - 1) : NH * a.nseg * a.kinds;
-  if (z) return og ? launch_variant<true, true>(maps, args, grid, s) : launch_variant<true, false>(maps, args, grid, s);
+  if (z) {
+    if (og) return launch_variant<true, true, false>(maps, args, grid, s);
+    return split ? launch_variant<true, false, true>(maps, args, grid, s)
+                 : launch_variant<true, false, false>(maps, args, grid, s);
+  }
   // the output gate comes with the layer form, whose decay is given as logits
   // (the out_gate tile shares the decay tile's buffer, half of which bf16 logits use)
   if (og) return cudaErrorInvalidValue;
-  return launch_variant<false, false>(maps, args, grid, s);
+  return split ? launch_variant<false, false, true>(maps, args, grid, s)
+               : launch_variant<false, false, false>(maps, args, grid, s);
 }
 
 cudaError_t read_tc_watchdog(unsigned int *flags, bool clear) {
