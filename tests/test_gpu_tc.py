@@ -187,3 +187,36 @@ def test_tc_many_packed_sequences(kda, nseq):
     o_ref, s_ref = oracle_prefill(x)
     assert_close(to_np(o), o_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="o")
     assert_close(to_np(s), s_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="S")
+
+
+@pytest.mark.parametrize("decay", ["workload", "alternating_floor"])
+def test_tc_split_and_plain_orders_agree_bitwise(kda, decay):
+    """The kernel runs its state group in one of two orders, chosen at launch:
+    with at most one (sequence, head) chain per SM, V~'s first half and its
+    M5/M6 overlap M7's last steps; otherwise the plain order.  Both form the
+    same products with the same accumulation order, so B=5 x H=32 chains
+    (more than the SMs: plain) and their first 4 sequences alone (128 chains:
+    split) give bitwise equal outputs and states, ragged last chunk and
+    (with the alternating floor) the per-tile range path included.  The
+    batch is also checked against the oracle on a few chains."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    w = inputs.scaled(inputs.PREFILL_B4_T8K, B=5, T=300, random_initial_state=True)
+    assert w.B * w.H > sms >= (w.B - 1) * w.H
+    x = inputs.make_prefill(w, device=DEV)
+    if decay == "alternating_floor":
+        x["log_alpha"].view(w.B, w.T, w.H, w.dk)[:, 64:128] = -5.0
+    o5, s5 = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["initial_state"], None,
+                               B=w.B)
+    n4 = (w.B - 1) * w.T
+    sub = {n: x[n][:n4].contiguous() for n in ("q", "k", "v", "log_alpha", "beta")}
+    o4, s4 = kda.kda_chunk_fwd(sub["q"], sub["k"], sub["v"], sub["log_alpha"], sub["beta"],
+                               x["initial_state"][: w.B - 1].contiguous(), None, B=w.B - 1)
+    torch.cuda.synchronize()
+    assert torch.equal(o4, o5[:n4]) and torch.equal(s4, s5[: w.B - 1])
+    chains = [0, 33, 4 * 32 + 7]
+    o_ref, s_ref = oracle_prefill(x, chains=chains)
+    for c in chains:
+        n, h = divmod(c, w.H)
+        sl = slice(n * w.T, (n + 1) * w.T)
+        assert_close(to_np(o5[sl, h]), o_ref[sl, h], TOL_BF16_FRO, TOL_BF16_MAXN, what=f"o chain {c}")
+        assert_close(to_np(s5[n, h]), s_ref[n, h], TOL_BF16_FRO, TOL_BF16_MAXN, what=f"S chain {c}")
