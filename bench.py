@@ -97,8 +97,16 @@ def load_peaks():
 
 
 def source_sha(path: str) -> str:
+    """sha256[:16] of a source file's code: line comments and blank lines are
+    left out, so that a comment edit does not void a capture of the same code."""
     with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+        lines = f.read().decode("utf-8").splitlines()
+    code = []
+    for ln in lines:
+        cut = ln.split("//", 1)[0].rstrip()
+        if cut:
+            code.append(cut)
+    return hashlib.sha256("\n".join(code).encode("utf-8")).hexdigest()[:16]
 
 
 def profiled_traffic():

@@ -43,10 +43,16 @@
 // become the chunk's Q o Gamma and K / Gamma operands, which are then scaled
 // in place.  The state group (warps 8-11) runs the serial state chain: M4/O,
 // M7, the bf16 copy of V~, M5/M6, the gamma scaling, the bf16 state copy and
-// the output; it also brings in v by TMA and writes Diag(beta) for M3.  Operands the state group still reads while the chunk group
-// prepares the next chunk are double-buffered by chunk parity; T is
-// single-buffered, and the solve waits for the previous chunk's M7 before it
-// writes L.  Thread 0 of each group issues that group's MMAs.
+// the output (one TMA store of the staging tile for a whole chunk); it also
+// brings in v by TMA and writes Diag(beta) for M3.  Operands the state group
+// still reads while the chunk group prepares the next chunk are
+// double-buffered by chunk parity; T is single-buffered, and M1 (then the
+// solve) waits for the previous chunk's M7 before L is written over T.
+// Thread 0 of each group issues that group's MMAs.  With kSplit (chosen at
+// launch when every chain has an SM of its own, so that the state group sets
+// the pace) V~'s first half is staged in bf16, and its M5/M6 queued, while
+// M7's last two steps run.  Work items that write no output (the
+// long-sequence plan's pairs) form X alone and skip M5 and the staging.
 //
 // Range guard ([K3-notes §2.2, Eq. 5 and Fig. 3]): with log-decay >= -5 a
 // 16-token tile sums to >= -80.  If every channel's chunk total G_C is >= -80
