@@ -963,6 +963,14 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
           else if (e < 32) { n = 24 + ((e - 16) >> 1); k = 16 + 4 * (e & 1); }
           else { n = 16 + ((e - 32) >> 2); k = 4 * (e & 3); }
           *reinterpret_cast<float4 *>(TTf + tt_idx(n, k)) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if (ctid == 160 && m >= 1 && m + 1 < nchunks &&
+                   mbar_wait(smem_u32(&ctl->bar[B_M56]), (m - 1) & 1, &ctl->abort, A.err, 1u << B_M56)) {
+          // q and k of chunk m + 1 go into the buffers of chunk m - 1, whose
+          // M5/M6 the state group has finished by now (this thread is idle in
+          // this phase; issued a whole solve earlier than at the hand-off, the
+          // copy lands before the next chunk's operand pass needs it).  B_M56
+          // cannot be a phase ahead: chunk m's M5/M6 wait for this chunk's hand-off.
+          issue_qk(&maps, ctl, sm_base, h, t0 + kC, par ^ 1);
         }
         bar_chunk();
         // 16-row level: four blocks, one (row i, column jj) of the output per thread
@@ -1064,13 +1072,6 @@ chunk_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs A) {
         }
       }
       if (ctid == 0) ctl->slow[par] = slow;
-      // q and k of chunk m + 1 go into the buffers of chunk m - 1 once its M5
-      // and M6 are done (the state group completes them while this chunk's
-      // solve runs; issuing here keeps the copy off the state group's path).
-      // B_M56 cannot be a phase ahead: chunk m's M5/M6 wait for the hand-off below.
-      if (ctid == 0 && m >= 1 && m + 1 < nchunks &&
-          mbar_wait(smem_u32(&ctl->bar[B_M56]), (m - 1) & 1, &ctl->abort, A.err, 1u << B_M56))
-        issue_qk(&maps, ctl, sm_base, h, t0 + kC, par ^ 1);
       group_publish<true>();
       // ---------------- hand the chunk to the state group (the arrive releases
       // the chunk's operands, A, T and gamma_C to it)
