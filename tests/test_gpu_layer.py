@@ -157,3 +157,33 @@ def test_layer_validate_rejects_bad_values(kda):
         kda.kda_layer_fwd(x["q"], x["k"], x["v"], gt["z"], x["beta"], gt["A_log"], g_min=-5.5,
                           cu_seqlens=x["cu_seqlens"])
     assert e.value.status == -5
+
+
+def test_layer_many_chains_plain_and_split_orders_agree(kda):
+    """Decay logits without the output gate, on more (sequence, head) chains
+    than the GPU has SMs (80 packed sequences x 2 heads: the plain
+    state-group order) against the oracle, and the first 8 of those sequences
+    alone (16 chains: the split order) bitwise equal to their rows of the
+    large call.  Lengths 1..200, so most sequences end in a ragged chunk."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(11)
+    lens = rng.integers(1, 201, size=80)
+    w = inputs.scaled(inputs.VARLEN_64, H=2)
+    assert len(lens) * w.H > sms
+    x = inputs.make_prefill(w, device=DEV, lengths=lens)
+    gt = inputs.make_layer_gates(x["T_total"], w.H, w.dk, w.dv, w.qkv_dtype, device=DEV)
+    o, s = run_layer(kda, x, gt, False, 0.0, kernel="tc")
+    o_ref, s_ref = oracle_layer(x, gt, False, 0.0)
+    torch.cuda.synchronize()
+    assert_close(to_np(o), o_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="o")
+    assert_close(to_np(s), s_ref, TOL_BF16_FRO, TOL_BF16_MAXN, what="S")
+    k = 8
+    cu = x["cu_seqlens"].cpu().numpy()
+    end = int(cu[k])
+    sub = {n: x[n][:end].contiguous() for n in ("q", "k", "v", "beta")}
+    sub["initial_state"] = x["initial_state"][:k].contiguous()
+    sub["cu_seqlens"] = x["cu_seqlens"][: k + 1].contiguous()
+    gsub = {"z": gt["z"][:end].contiguous(), "A_log": gt["A_log"]}
+    o8, s8 = run_layer(kda, sub, gsub, False, 0.0, kernel="tc")
+    torch.cuda.synchronize()
+    assert torch.equal(o8, o[:end]) and torch.equal(s8, s[:k])
